@@ -1,0 +1,137 @@
+/*
+ * moe_oracle.h -- plain, slow, fp64 CPU oracle of the top-k SwiGLU
+ * mixture-of-experts layer (forward + backward), its device-side schedule
+ * tables and the MXFP8 (E4M3 + E8M0, 1x32 blocks) weight quantiser.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or
+ * call this library: only the tests, the smoke check and the CPU-baseline leg
+ * of the benchmark use it. It shares no code, header, table or helper with
+ * the CUDA library.
+ *
+ * What it follows (page titles as cited throughout this directory):
+ *  - "Mixture-of-Kittens: Cursor open-sources an MoE training megakernel"
+ *    (clip, key-points bullets 2-5 and the key flowchart): the router picks
+ *    top-k experts; tokens are dispatched to experts with per-expert counts
+ *    and no token dropping; each expert is a SwiGLU FFN (gate/up, silu*mul,
+ *    down); the combine forms the routing-weighted sum; the backward runs the
+ *    mirrored reverse-combine / reverse-dispatch; reductions run in a fixed
+ *    order so results are bitwise reproducible.
+ *  - "Mixture-of-Kittens (MoK)" project summary, "core concepts" table:
+ *    MXFP8 weight format, weights pre-quantised by a quantise op.
+ *  - OCP Microscaling Formats (MX) v1.0 for the E8M0 shared-scale rule and
+ *    the OFP8 E4M3 element format (public definitions; the pages only name
+ *    the format).
+ *
+ * Every floating-point quantity below is computed in fp64 from the exact
+ * values of the inputs, with no intermediate rounding, except where a step
+ * is defined in fp32 (the router add, fl32(logit + bias), which the GPU
+ * performs identically so that the selection is comparable bit for bit).
+ *
+ * Conventions: row-major arrays; bf16 arrays are passed as their uint16 bit
+ * patterns. Return value 0 = OK, nonzero = error (see ORC_ERR_*).
+ */
+#ifndef MOE_ORACLE_H
+#define MOE_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORC_OK = 0, ORC_ERR_ARG = 1, ORC_ERR_NAN = 2 };
+
+/* Top-k routing. z[t,e] = fl32(logits[t,e] + bias[e]) (bias may be NULL).
+ * ids[t,0..k) = the k experts with the largest z, ordered by (z descending,
+ * expert index ascending). w[t,j] = softmax over the k selected z (equal to
+ * the softmax over all E renormalised on the selected k). Any NaN in z ->
+ * ORC_ERR_NAN. */
+int orc_route_topk(int64_t N, int32_t E, int32_t k, const float* logits,
+                   const float* bias, int32_t* ids, double* w);
+
+/* Schedule tables for the expert-grouped token buffer.
+ *  counts[e]          number of assignments (t,j) with ids[t,j] == e
+ *  offsets[0..E]      exclusive prefix sum of counts (offsets[E] = N*k)
+ *  pad_offsets[0..E]  exclusive prefix sum of counts rounded up to tile_m
+ *  slot_of[t*k+j]     pad_offsets[e] + #{t' < t routed to e}: the row of the
+ *                     expert-grouped buffer that holds assignment (t,j)
+ *  src_of_row[r]      inverse map, r < pad_offsets[E]: t*k+j, or -1 for the
+ *                     padding rows that round each segment up to tile_m
+ *  tiles[3*i..]       (expert, first row, valid rows) of each tile_m-row tile
+ *                     in row order; *n_tiles = pad_offsets[E] / tile_m
+ * rows_cap / tiles_cap bound the output arrays (ORC_ERR_ARG if too small). */
+int orc_build_schedule(int64_t N, int32_t k, int32_t E, int32_t tile_m,
+                       const int32_t* ids, int32_t* counts, int32_t* offsets,
+                       int32_t* pad_offsets, int32_t* slot_of,
+                       int32_t* src_of_row, int64_t rows_cap, int32_t* tiles,
+                       int64_t tiles_cap, int32_t* n_tiles);
+
+/* Layer forward. Inputs either all fp64 (the *_f64 entry points, used for
+ * finite differences) or bf16 bit patterns (x, wg, wu, wd).
+ *   x [N,H], wg [E,I,H], wu [E,I,H], wd [E,H,I], ids [N,k], w [N,k]
+ *   y [N,H] = sum_j w[t,j] * Wd[e] (silu(Wg[e] x_t) * (Wu[e] x_t)),
+ *   accumulated over j = 0..k-1 in order.
+ * ye_out (optional, may be NULL) [N*k, H] receives each assignment's expert
+ * output, indexed by t*k+j. threads <= 0 -> hardware concurrency. */
+int orc_forward_f64(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k,
+                    const double* x, const double* wg, const double* wu,
+                    const double* wd, const int32_t* ids, const double* w,
+                    double* y, double* ye_out, int threads);
+int orc_forward_bf16(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k,
+                     const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
+                     const uint16_t* wd, const int32_t* ids, const double* w,
+                     double* y, double* ye_out, int threads);
+
+/* Layer backward for the loss L = <dy, y> with the routing held fixed.
+ * Outputs: dx [N,H], dwg [E,I,H], dwu [E,I,H], dwd [E,H,I], dw [N,k]
+ * (dw[t,j] = dL/dw[t,j] = <dy_t, ye_{t,j}>). Weight gradients sum the
+ * assignments of each expert in ascending token order. */
+int orc_backward_f64(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k,
+                     const double* x, const double* wg, const double* wu,
+                     const double* wd, const int32_t* ids, const double* w,
+                     const double* dy, double* dx, double* dwg, double* dwu,
+                     double* dwd, double* dw, int threads);
+int orc_backward_bf16(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k,
+                      const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
+                      const uint16_t* wd, const int32_t* ids, const double* w,
+                      const uint16_t* dy, double* dx, double* dwg, double* dwu,
+                      double* dwd, double* dw, int threads);
+
+/* Sampled forms for workloads too large to run whole on a CPU.
+ * orc_tokens_bf16: y, dx rows [n_tok,H] and dw [n_tok,k] for the listed
+ * tokens only (each needs only its own k assignments).
+ * orc_expert_wgrad_bf16: the weight gradients of expert e restricted to the
+ * listed rows: dwg_rows/dwu_rows [n_i,H] hold dWg[e][i_list[r]][:],
+ * dwd_rows [n_h,I] hold dWd[e][h_list[r]][:]; every assignment routed to e
+ * contributes, in ascending token order. */
+int orc_tokens_bf16(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k,
+                    const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
+                    const uint16_t* wd, const int32_t* ids, const double* w,
+                    const uint16_t* dy, int64_t n_tok, const int64_t* tok,
+                    double* y, double* dx, double* dw, int threads);
+int orc_expert_wgrad_bf16(int64_t N, int32_t H, int32_t I, int32_t E,
+                          int32_t k, const uint16_t* x, const uint16_t* wg,
+                          const uint16_t* wu, const uint16_t* wd,
+                          const int32_t* ids, const double* w,
+                          const uint16_t* dy, int32_t e, int64_t n_i,
+                          const int32_t* i_list, int64_t n_h,
+                          const int32_t* h_list, double* dwg_rows,
+                          double* dwu_rows, double* dwd_rows, int threads);
+
+/* MXFP8 quantiser (OCP MX v1.0, MXFP8 E4M3): for each block of 32
+ * consecutive values along a row, X = 2^(floor(log2(amax)) - 8) (8 = the
+ * largest E4M3 exponent), scale code = that exponent + 127 clamped to
+ * [0, 254] (an all-zero block gets code 0); each element is V / 2^(code-127)
+ * rounded to the nearest E4M3 value, ties to even, magnitudes above 448
+ * saturating to 448. src [rows, cols] bf16, cols % 32 == 0;
+ * q [rows, cols], scale [rows, cols/32]. */
+int orc_mxfp8_quantize(int64_t rows, int64_t cols, const uint16_t* src,
+                       uint8_t* q, uint8_t* scale);
+/* Element rule alone: E4M3 code of v (double), RNE, saturating. */
+uint8_t orc_e4m3_encode(double v);
+/* Exact value of an E4M3 code (NaN codes return NaN). */
+double orc_e4m3_decode(uint8_t code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
