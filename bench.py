@@ -1,0 +1,406 @@
+#!/usr/bin/env python
+"""MoE layer forward+backward tokens/s on one GB300 (the layer's hot path).
+
+One step = route (top-k) -> schedule -> dispatch -> gate/up GEMM + SwiGLU ->
+down GEMM -> combine -> reverse-combine (+ d routing weights) -> down
+dgrad (+ SwiGLU backward) -> down wgrad -> gate/up dgrad -> gate/up wgrad ->
+reverse-dispatch, on one batch of seeded synthetic input already resident in
+HBM. Default workload: N=16384 tokens, H=4096, I=1536, E=128 experts, top-8,
+bf16, router logits plus a Zipf(1.2) per-expert bias (skewed expert loads).
+
+Multi-GPU (torchrun, N ranks): replicas only -- every rank runs its own batch
+with no collective on the data path ("scaling": "weak"); the barrier and the
+max over ranks of the timed region stay.
+
+--impl reference times the CPU oracle (fp64 C++, all host cores) on a
+bounded sample of the same workload; it is a deliberately slow correctness
+reference, not a tuned competitor.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer fwd+bwd tokens/s on 1 GB300; GEMM TFLOP/s as % of tensor peak"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=None, help="workload name (default: skewed fwd+bwd)")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=0,
+                    help="oracle sample size in tokens (0 = sized for ~15 s)")
+    ap.add_argument("--phase-report", action="store_true", help="print per-phase timings")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def phase_flops(shape):
+    """Algorithmic flops of each GEMM phase (padding rows excluded)."""
+    A, H, I = shape.N * shape.k, shape.H, shape.I
+    return {"gate_up": 4 * A * H * I, "down": 2 * A * H * I, "down_dgrad": 2 * A * H * I,
+            "down_wgrad": 2 * A * H * I, "gate_up_dgrad": 4 * A * H * I,
+            "gate_up_wgrad": 4 * A * H * I}
+
+
+def phase_bytes(shape, R):
+    """Algorithmic HBM bytes of the data-movement phases."""
+    N, A, H, E, k = shape.N, shape.N * shape.k, shape.H, shape.E, shape.k
+    return {"route": 4 * N * E + 8 * N * k, "dispatch": 2 * N * H + 2 * A * H + 4 * A,
+            "combine": 2 * A * H + 8 * A + 2 * N * H,
+            "reverse_combine": 2 * N * H + 2 * A * H + 8 * A + 2 * A * H + 4 * A,
+            "reverse_dispatch": 2 * A * H + 4 * A + 2 * N * H}
+
+
+def run_ours(args, ws_, rank, local):
+    import torch
+    from mixture_experts_layer_schedule_gb300 import MoELayer, _lib, inputs
+
+    shape = inputs.ALL[args.config] if args.config else inputs.SKEWED
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inp = inputs.make_inputs(shape, seed=rank, device=dev)
+    layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev)
+    p, wsb = layer.p, layer.ws
+    w = _lib.weights(inp["wg"], inp["wu"], inp["wd"])
+    sv = layer.saved_tensors()
+    g = layer.grads
+    dyxe = torch.empty((layer.R, shape.H), dtype=torch.bfloat16, device=dev)
+    dgb = torch.empty((layer.R, shape.I), dtype=torch.bfloat16, device=dev)
+    dub = torch.empty((layer.R, shape.I), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    backward = shape.backward
+
+    phases = ["route", "schedule", "dispatch", "gate_up", "down", "combine"]
+    if backward:
+        phases += ["reverse_combine", "down_dgrad", "down_wgrad", "gate_up_dgrad",
+                   "gate_up_wgrad", "reverse_dispatch"]
+    calls = {
+        "route": lambda: _lib.moe_route_topk(p, inp["logits"], inp["bias"], layer.topk_ids,
+                                             layer.topk_w, wsb),
+        "schedule": lambda: _lib.moe_build_schedule(p, layer.topk_ids, wsb),
+        "dispatch": lambda: _lib.moe_dispatch(p, wsb, inp["x"], sv["xe"]),
+        "gate_up": lambda: _lib.moe_expert_gate_up(p, wsb, sv["xe"], w, sv["g"], sv["u"],
+                                                   sv["act"]),
+        "down": lambda: _lib.moe_expert_down(p, wsb, sv["act"], w, sv["ye"]),
+        "combine": lambda: _lib.moe_combine(p, wsb, sv["ye"], layer.topk_w, layer.y),
+        "reverse_combine": lambda: _lib.moe_reverse_combine(p, wsb, inp["dy"], sv["ye"],
+                                                            layer.topk_w, dyxe, g.d_topk_w),
+        "down_dgrad": lambda: _lib.moe_expert_down_dgrad(p, wsb, dyxe, sv["g"], sv["u"], w, dgb,
+                                                         dub),
+        "down_wgrad": lambda: _lib.moe_expert_down_wgrad(p, wsb, dyxe, sv["act"], g.dw_down),
+        "gate_up_dgrad": lambda: _lib.moe_expert_gate_up_dgrad(p, wsb, dgb, dub, w, dyxe),
+        "gate_up_wgrad": lambda: _lib.moe_expert_gate_up_wgrad(p, wsb, dgb, dub, sv["xe"],
+                                                               g.dw_gate, g.dw_up),
+        "reverse_dispatch": lambda: _lib.moe_reverse_dispatch(p, wsb, dyxe, g.dx),
+    }
+
+    def step(events=None):
+        for i, ph in enumerate(phases):
+            if events is not None:
+                events[i].record(stream)
+            calls[ph]()
+        if events is not None:
+            events[len(phases)].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0, "device error during warm-up"
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)] for _ in range(K)]
+    n0 = _lib.moe_launch_count()
+    clk = ClockSampler(local)
+    clk.start()
+    if ws_ > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(K):
+        step(ev[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if ws_ > 1:
+        torch.distributed.barrier()
+    clocks = clk.stop()
+    launches = _lib.moe_launch_count() - n0
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if ws_ > 1:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ph_ms = {ph: statistics.mean(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(K))
+             for i, ph in enumerate(phases)}
+    assert layer.device_error() == 0, "device error in the timed region"
+
+    # ---- end to end through the public API with host buffers ----
+    pin = {k: inp[k].cpu().pin_memory() for k in ("x", "logits", "dy") if inp.get(k) is not None}
+    out_y = torch.empty((shape.N, shape.H), dtype=torch.bfloat16).pin_memory()
+    out_dx = torch.empty((shape.N, shape.H), dtype=torch.bfloat16).pin_memory()
+    dx_in = {k: torch.empty_like(v, device=dev) for k, v in pin.items()}
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = out_y.numel() * 2 + (out_dx.numel() * 2 if backward else 0)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        for k, v in pin.items():
+            dx_in[k].copy_(v, non_blocking=True)
+        layer.step(dx_in["x"], dx_in["logits"], inp["bias"], inp["wg"], inp["wu"], inp["wd"],
+                   dx_in.get("dy"), backward=backward)
+        out_y.copy_(layer.y, non_blocking=True)
+        if backward:
+            out_dx.copy_(g.dx, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if ws_ > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # ---- roofline of the dominant kernel ----
+    peaks = load_peaks()
+    fl = phase_flops(shape)
+    by = phase_bytes(shape, layer.R)
+    dominant = max(ph_ms, key=ph_ms.get)
+    if dominant in fl:
+        achieved = fl[dominant] / (ph_ms[dominant] * 1e-3) / 1e12
+        roof = {"kernel": dominant, "bound": "tensor", "achieved": round(achieved, 1),
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                "peak_kind": f"{peaks['source']} bf16 sustained", "traffic": None}
+    else:
+        achieved = by[dominant] / (ph_ms[dominant] * 1e-3) / 1e9
+        roof = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_kind": peaks["source"],
+                "traffic": None}
+    gemm_ms = sum(ph_ms[k] for k in fl if k in ph_ms)
+    gemm_flops = sum(fl[k] for k in fl if k in ph_ms)
+    phase_report = {}
+    for ph in phases:
+        d = {"ms": round(ph_ms[ph], 4)}
+        if ph in fl:
+            tf = fl[ph] / (ph_ms[ph] * 1e-3) / 1e12
+            d.update(tflops=round(tf, 1), frac=round(tf / peaks["bf16_tflops_sustained"], 3))
+        elif ph in by:
+            gb = by[ph] / (ph_ms[ph] * 1e-3) / 1e9
+            d.update(gbs=round(gb, 1), frac=round(gb / peaks["hbm_gbs"], 3))
+        phase_report[ph] = d
+
+    step_ms = elapsed_ms / K
+    value = shape.N * K * ws_ / (elapsed_ms * 1e-3)
+    rec = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws_, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Gaussian inputs and random-init expert weights)",
+        "config": {"workload": shape.name, "N": shape.N, "H": shape.H, "I": shape.I,
+                   "E": shape.E, "k": shape.k, "zipf_bias": shape.zipf_s,
+                   "passes": "fwd+bwd" if backward else "fwd",
+                   "l2": "inputs larger than L2 (expert weights alone "
+                         f"{3 * shape.E * shape.H * shape.I * 2 / 1e9:.2f} GB)",
+                   "parallelism": f"replicas x{ws_}"},
+        "gemm_tflops": round(gemm_flops / (gemm_ms * 1e-3) / 1e12, 1),
+        "gemm_frac_of_peak": round(gemm_flops / (gemm_ms * 1e-3) / 1e12 /
+                                   peaks["bf16_tflops_sustained"], 4),
+        "roofline": roof,
+        "e2e": {"value": round(shape.N * ws_ / (e2e_ms * 1e-3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "phases": phase_report,
+    }
+    return rec, shape, inp
+
+
+def cpu_sample(shape, inp, n_tok, threads):
+    """Run the oracle on the first n_tok tokens of the workload (fwd+bwd with
+    weight gradients). Returns (seconds, tokens)."""
+    import numpy as np
+
+    import oracle
+    logits = inp["logits"][:n_tok].cpu().numpy()
+    bias = None if inp["bias"] is None else inp["bias"].cpu().numpy()
+    x = oracle.as_bf16_bits(inp["x"][:n_tok])
+    dy = oracle.as_bf16_bits(inp["dy"][:n_tok]) if inp.get("dy") is not None else None
+    wg, wu, wd = (oracle.as_bf16_bits(inp[k]) for k in ("wg", "wu", "wd"))
+    t0 = time.perf_counter()
+    ids, w = oracle.route_topk(logits, bias, shape.k)
+    oracle.build_schedule(ids, shape.E)
+    if shape.backward:
+        oracle.forward_bf16(x, wg, wu, wd, ids, w, threads=threads)
+        oracle.backward_bf16(x, wg, wu, wd, ids, w, dy, threads=threads)
+    else:
+        oracle.forward_bf16(x, wg, wu, wd, ids, w, threads=threads)
+    return time.perf_counter() - t0, n_tok
+
+
+def run_reference(args, ws_, rank):
+    """The oracle, timed on the host cores, on bounded samples of the workload."""
+    if rank != 0:
+        return None
+    import torch
+
+    from mixture_experts_layer_schedule_gb300 import inputs
+    shape = inputs.ALL[args.config] if args.config else inputs.SKEWED
+    threads = os.cpu_count() or 1
+    n_tok = args.cpu_tokens or 32
+    small = shape.with_(N=max(n_tok, 1))
+    inp = inputs.make_inputs(shape.with_(N=n_tok), seed=0, device="cpu")
+    for _ in range(args.warmup):
+        cpu_sample(shape, inp, n_tok, threads)
+    times = [cpu_sample(shape, inp, n_tok, threads)[0] for _ in range(args.steps)]
+    tot = sum(times)
+    value = n_tok * args.steps / tot
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded Gaussian inputs and random-init expert weights)",
+        "config": {"workload": shape.name, "N": shape.N, "H": shape.H, "I": shape.I,
+                   "E": shape.E, "k": shape.k, "zipf_bias": shape.zipf_s,
+                   "passes": "fwd+bwd" if shape.backward else "fwd"},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"first {n_tok} tokens of the workload per step "
+                                   f"(full expert weights, fwd+bwd with weight gradients)"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    ws_, rank, local = dist_env()
+    if ws_ > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+    if args.impl == "reference":
+        rec = run_reference(args, ws_, rank)
+        if rec is not None:
+            print(json.dumps(rec), flush=True)
+        return
+    rec, shape, inp = run_ours(args, ws_, rank, local)
+    if rank == 0 and ws_ == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        n_tok = args.cpu_tokens or 256
+        secs, n = cpu_sample(shape, inp, n_tok, threads)
+        rec["cpu_baseline"] = {"value": round(n / secs, 3), "unit": UNIT, "cores": threads,
+                               "kind": "oracle",
+                               "sample": f"first {n} tokens of the workload (full expert "
+                                         f"weights, fwd+bwd with weight gradients), "
+                                         f"{secs:.1f} s"}
+    if rank == 0:
+        if not args.phase_report:
+            rec.pop("phases", None)
+        print(json.dumps(rec), flush=True)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

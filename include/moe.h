@@ -1,0 +1,232 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) deterministic top-k SwiGLU
+ * mixture-of-experts layer: routing, device-side schedule, dispatch, grouped
+ * expert FFN, combine, their backward, and the MXFP8 quantiser.
+ *
+ * Sources of the operations (page title, section):
+ *  [MoK]  "Mixture-of-Kittens (MoK)" project summary -- "use the functional
+ *         API" (workspace created once per model, build_schedule from the
+ *         router's top-k experts, forward -> (out, ctx), backward(ctx) ->
+ *         grads) and "core concepts" (the ops layer leaves every tensor to the
+ *         caller; MXFP8 weights are pre-quantised by a quantise op).
+ *  [Clip] "Mixture-of-Kittens: Cursor open-sources an MoE training
+ *         megakernel" -- key points 2-5 (pull dispatch / push combine and the
+ *         mirrored backward rounds; minibatch granularity; ring token buffer
+ *         and schedule built on the GPU with no host sync and no token
+ *         dropping; SwiGLU expert FFN; bitwise determinism) and the key
+ *         flowchart (router top-k -> dispatch -> expert FFN + SwiGLU ->
+ *         combine -> weighted-sum output).
+ *
+ * General rules for every entry point:
+ *  - Ownership: the caller allocates and frees every buffer (device memory
+ *    unless stated otherwise). The library never allocates, frees or
+ *    synchronises; each call only enqueues kernels on `stream` (a
+ *    cudaStream_t, NULL = legacy default stream) and returns.
+ *  - Errors detectable on the host (NULL pointer, unsupported size,
+ *    misaligned pointer) return a moe_status immediately and enqueue nothing.
+ *    Errors found by the kernels (expert id out of range, NaN router logit,
+ *    a barrier wait that exceeded its time limit) are recorded in a sticky
+ *    device error word inside the workspace; read it with
+ *    moe_get_device_error after synchronising the stream.
+ *  - Determinism: identical inputs give bitwise-identical outputs. No
+ *    floating-point atomics are used; every reduction has a fixed order.
+ *  - Pointers to device buffers must be 16-byte aligned; row-major layouts.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* NULL / inconsistent / misaligned argument */
+  MOE_ERR_UNSUPPORTED = 2, /* size or dtype outside what the kernels support */
+  MOE_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
+  MOE_ERR_DEVICE = 4       /* reserved: device error word was set */
+} moe_status;
+
+/* Codes of the device error word (first error wins). */
+enum {
+  MOE_DEVERR_NONE = 0,
+  MOE_DEVERR_BAD_EXPERT = 1, /* a top-k id outside [0, E) reached the schedule */
+  MOE_DEVERR_NAN_LOGIT = 2,  /* a router logit (+ bias) was NaN */
+  MOE_DEVERR_TIMEOUT = 3     /* a kernel's barrier wait ran out of time */
+};
+
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_dtype;
+
+/* Problem size. N tokens, H hidden, I expert intermediate, E experts,
+ * k experts per token. Supported: N >= 0, 1 <= k <= min(E, 32), E <= 1024,
+ * H and I multiples of 256. dtype: MOE_BF16 (MOE_MXFP8 weights are produced
+ * by mxfp8_quantize; the layer entry points take MOE_BF16). */
+typedef struct {
+  int64_t N;
+  int32_t H, I, E, k;
+  int32_t dtype;
+} moe_problem;
+
+/* Expert weights, bf16, K dimension contiguous:
+ *   w_gate [E][I][H], w_up [E][I][H], w_down [E][H][I]. */
+typedef struct {
+  const void* w_gate;
+  const void* w_up;
+  const void* w_down;
+} moe_weights;
+
+/* Rows of every expert-grouped buffer: each expert's segment of the buffer is
+ * rounded up to a multiple of 128 rows (the tile height), so the buffer needs
+ * at most N*k + E*127 rows, rounded up to 128. Padding rows hold zeros. */
+int64_t moe_grouped_rows(const moe_problem* p);
+
+/* Bytes of the workspace (schedule tables, scratch, backward buffers, device
+ * error word). Created once per problem size and reused across calls. */
+moe_status moe_workspace_bytes(const moe_problem* p, size_t* bytes);
+
+/* Bytes of the forward context ("fwd_ctx" of [MoK]) that moe_forward fills
+ * and moe_backward reads: Xe [R,H], G [R,I], U [R,I], Act [R,I], Ye [R,H],
+ * all bf16, R = moe_grouped_rows(p), in that order, each 256-byte aligned. */
+moe_status moe_saved_bytes(const moe_problem* p, size_t* bytes);
+
+typedef struct {
+  void *xe, *g, *u, *act, *ye;
+} moe_saved_view;
+moe_status moe_saved_layout(const moe_problem* p, void* saved, moe_saved_view* out);
+
+/* Device pointers to the schedule tables inside a workspace (host-side
+ * address arithmetic only; nothing is launched):
+ *  counts[E]        assignments per expert
+ *  offsets[E+1]     exclusive prefix sum of counts (offsets[E] = N*k)
+ *  pad_offsets[E+1] exclusive prefix sum of counts rounded up to 128
+ *  slot_of[N*k]     row of the expert-grouped buffer holding assignment
+ *                   (t, j) = pad_offsets[e] + #{t' < t routed to e}
+ *  src_of_row[R]    t*k + j of the assignment in row r, -1 on padding rows
+ *                   (valid for r < pad_offsets[E])
+ *  tiles[R/128][3]  (expert, first row, valid rows) of each 128-row tile
+ *  n_tiles[1]       number of tiles = pad_offsets[E] / 128 */
+typedef struct {
+  int32_t *counts, *offsets, *pad_offsets, *slot_of, *src_of_row, *tiles, *n_tiles;
+} moe_schedule;
+moe_status moe_schedule_view(const moe_problem* p, void* ws, moe_schedule* out);
+
+/* [Clip] flowchart "Router picks top-k experts". logits fp32 [N,E], bias fp32
+ * [E] or NULL. z = fl32(logit + bias); topk_ids int32 [N,k] = the k largest z
+ * ordered by (z descending, expert index ascending); topk_w fp32 [N,k] =
+ * softmax of the selected z (the full softmax renormalised over the top-k).
+ * A NaN z sets MOE_DEVERR_NAN_LOGIT. ws is needed only for the error word. */
+moe_status moe_route_topk(const moe_problem* p, const float* logits, const float* bias,
+                          int32_t* topk_ids, float* topk_w, void* ws, void* stream);
+
+/* [Clip] key point 4 / [MoK] build_schedule: per-expert counts, exclusive
+ * prefix sums, token->row permutation and tile list, built on the device from
+ * topk_ids int32 [N,k] with no host synchronisation and no token dropping.
+ * Writes the tables of moe_schedule_view into ws. Ids outside [0,E) set
+ * MOE_DEVERR_BAD_EXPERT (the tables are then unspecified). */
+moe_status moe_build_schedule(const moe_problem* p, const int32_t* topk_ids, void* ws,
+                              void* stream);
+
+/* ---- forward phases (the ws must hold the schedule of this call) ---- */
+
+/* Dispatch ([Clip] key point 2, pull dispatch; on one GPU an HBM copy):
+ * xe[slot_of[t,j]] = x[t] for every assignment, padding rows = 0.
+ * x bf16 [N,H] -> xe bf16 [R,H]. */
+moe_status moe_dispatch(const moe_problem* p, const void* ws, const void* x, void* xe,
+                        void* stream);
+
+/* Expert gate/up GEMM with the SwiGLU epilogue ([Clip] key point 5): per
+ * expert e and its rows, G = Xe Wg[e]^T, U = Xe Wu[e]^T (fp32 accumulation on
+ * the tensor cores), Act = silu(G) * U. Writes G, U, Act bf16 [R,I]. */
+moe_status moe_expert_gate_up(const moe_problem* p, const void* ws, const void* xe,
+                              const moe_weights* w, void* g, void* u, void* act, void* stream);
+
+/* Expert down GEMM: Ye = Act Wd[e]^T, bf16 [R,H]. */
+moe_status moe_expert_down(const moe_problem* p, const void* ws, const void* act,
+                           const moe_weights* w, void* ye, void* stream);
+
+/* Combine ([Clip] key point 2 push combine; flowchart "weighted-sum output"):
+ * y[t] = sum_{j=0..k-1} topk_w[t,j] * ye[slot_of[t,j]], accumulated in fp32
+ * in ascending j, rounded once to bf16. y bf16 [N,H]. */
+moe_status moe_combine(const moe_problem* p, const void* ws, const void* ye, const float* topk_w,
+                       void* y, void* stream);
+
+/* Whole forward: dispatch, gate/up, down, combine; saved = forward context. */
+moe_status moe_forward(const moe_problem* p, const void* x, const moe_weights* w,
+                       const float* topk_w, void* y, void* saved, void* ws, void* stream);
+
+/* ---- backward phases ([Clip] key point 2: pull reverse-combine, push
+ *      reverse-dispatch), for the loss gradient dy with routing held fixed */
+
+/* Reverse-combine: dye[slot_of[t,j]] = bf16(topk_w[t,j] * dy[t]); padding
+ * rows = 0; d_topk_w[t,j] = <dy[t], ye[slot_of[t,j]]> (fp32, fixed-order
+ * reduction). dy bf16 [N,H], ye bf16 [R,H] -> dye bf16 [R,H], fp32 [N,k]. */
+moe_status moe_reverse_combine(const moe_problem* p, const void* ws, const void* dy,
+                               const void* ye, const float* topk_w, void* dye, float* d_topk_w,
+                               void* stream);
+
+/* Down backward, data gradient, with the SwiGLU backward epilogue:
+ * dAct = dYe Wd[e]; s = sigmoid(G); dG = dAct * U * s * (1 + G (1 - s));
+ * dU = dAct * G * s. dye, g, u bf16 [R,H] / [R,I] -> dg, du bf16 [R,I]. */
+moe_status moe_expert_down_dgrad(const moe_problem* p, const void* ws, const void* dye,
+                                 const void* g, const void* u, const moe_weights* w, void* dg,
+                                 void* du, void* stream);
+
+/* Down backward, weight gradient: dw_down[e] = dYe_e^T Act_e summed over the
+ * expert's rows (fp32 [E][H][I]; experts without tokens get zeros). */
+moe_status moe_expert_down_wgrad(const moe_problem* p, const void* ws, const void* dye,
+                                 const void* act, float* dw_down, void* stream);
+
+/* Gate/up backward, data gradient: dXe = dG Wg[e] + dU Wu[e] (bf16 [R,H]). */
+moe_status moe_expert_gate_up_dgrad(const moe_problem* p, const void* ws, const void* dg,
+                                    const void* du, const moe_weights* w, void* dxe,
+                                    void* stream);
+
+/* Gate/up backward, weight gradients: dw_gate[e] = dG_e^T Xe_e and
+ * dw_up[e] = dU_e^T Xe_e (fp32 [E][I][H]; experts without tokens get 0). */
+moe_status moe_expert_gate_up_wgrad(const moe_problem* p, const void* ws, const void* dg,
+                                    const void* du, const void* xe, float* dw_gate,
+                                    float* dw_up, void* stream);
+
+/* Reverse-dispatch: dx[t] = sum_{j=0..k-1} dxe[slot_of[t,j]] (fp32, ascending
+ * j, rounded once to bf16). dxe bf16 [R,H] -> dx bf16 [N,H]. */
+moe_status moe_reverse_dispatch(const moe_problem* p, const void* ws, const void* dxe, void* dx,
+                                void* stream);
+
+/* Whole backward from the forward context. Outputs dx bf16 [N,H], dw_gate,
+ * dw_up fp32 [E][I][H], dw_down fp32 [E][H][I], d_topk_w fp32 [N,k]. Uses
+ * the workspace for dYe/dXe (shared buffer), dG and dU. */
+moe_status moe_backward(const moe_problem* p, const void* saved, const moe_weights* w,
+                        const float* topk_w, const void* dy, void* dx, float* dw_gate,
+                        float* dw_up, float* dw_down, float* d_topk_w, void* ws, void* stream);
+
+/* [MoK] core concepts, MXFP8 row: quantise bf16 [rows, cols] (cols % 32 == 0)
+ * to MXFP8 along each row: per 1x32 block, E8M0 scale code =
+ * clamp(floor(log2(amax)) - 8 + 127, 0, 254) (0 for an all-zero block), and
+ * E4M3 elements = round-to-nearest-even(v / 2^(code-127)), saturating to
+ * +-448 (OCP Microscaling Formats v1.0). q u8 [rows, cols], scale u8
+ * [rows, cols/32]. */
+moe_status mxfp8_quantize(const void* src_bf16, int64_t rows, int64_t cols, uint8_t* q_e4m3,
+                          uint8_t* scale_e8m0, void* stream);
+
+/* Enqueue an asynchronous copy of the device error word of `ws` into
+ * *code_out (host memory; pinned memory keeps the copy asynchronous). The
+ * value is valid after the caller synchronises the stream. */
+moe_status moe_get_device_error(const moe_problem* p, const void* ws, int32_t* code_out,
+                                void* stream);
+/* Enqueue a reset of the device error word to MOE_DEVERR_NONE. */
+moe_status moe_clear_device_error(const moe_problem* p, void* ws, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* moe_status_string(moe_status s);
+
+/* Number of kernels this library has launched in the calling process (all
+ * devices, all streams); for launch accounting in benchmarks. */
+uint64_t moe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

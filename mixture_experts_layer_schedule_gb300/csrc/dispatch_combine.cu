@@ -1,0 +1,172 @@
+// dispatch_combine.cu -- the HBM-bound data-movement phases of the layer.
+//
+// On one GPU the pages' NVLink rounds ("Mixture-of-Kittens: Cursor
+// open-sources an MoE training megakernel", key point 2: pull dispatch, push
+// combine, pull reverse-combine, push reverse-dispatch) become copies between
+// the token-ordered tensors and the expert-grouped buffer:
+//   dispatch         xe[slot(t,j)] = x[t]
+//   combine          y[t] = sum_j w[t,j] * ye[slot(t,j)]           (fp32, j order)
+//   reverse-combine  dye[slot(t,j)] = w[t,j] * dy[t];  dw[t,j] = <dy[t], ye[slot(t,j)]>
+//   reverse-dispatch dx[t] = sum_j dxe[slot(t,j)]                  (fp32, j order)
+// Each CTA owns one token and walks its row in 16-byte vectors, so every row
+// of x / dy / y / dx is read or written exactly once and each expert row is
+// touched by exactly one CTA. Extra CTAs (one per expert) zero the padding
+// rows that round each expert segment up to the tile height. Slots are
+// bounds-checked: an unplaced assignment (bad expert id) is skipped.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+  f[4] = bf16lo(v.z); f[5] = bf16hi(v.z); f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+// Zero the padding rows of expert e's segment (CTA index >= N).
+__device__ __forceinline__ void zero_padding(int e, const int32_t* __restrict__ counts,
+                                             const int32_t* __restrict__ pad_offsets,
+                                             int64_t R, int hv, uint4* __restrict__ buf) {
+  const int64_t r0 = static_cast<int64_t>(pad_offsets[e]) + counts[e];
+  const int64_t r1 = pad_offsets[e + 1];
+  for (int64_t r = r0; r < r1 && r < R; ++r)
+    for (int v = threadIdx.x; v < hv; v += blockDim.x) buf[r * hv + v] = make_uint4(0, 0, 0, 0);
+}
+
+__global__ void __launch_bounds__(kThreads) dispatch_kernel(
+    const uint4* __restrict__ x, const int32_t* __restrict__ slot_of,
+    const int32_t* __restrict__ counts, const int32_t* __restrict__ pad_offsets, int64_t N, int k,
+    int hv, int64_t R, uint4* __restrict__ xe) {
+  const int64_t t = blockIdx.x;
+  if (t >= N) {
+    zero_padding(static_cast<int>(t - N), counts, pad_offsets, R, hv, xe);
+    return;
+  }
+  __shared__ int32_t slots[kMaxK];
+  if (threadIdx.x < k) slots[threadIdx.x] = slot_of[t * k + threadIdx.x];
+  __syncthreads();
+  for (int v = threadIdx.x; v < hv; v += blockDim.x) {
+    const uint4 val = x[t * hv + v];
+    for (int j = 0; j < k; ++j)
+      if (slots[j] >= 0 && slots[j] < R) xe[static_cast<int64_t>(slots[j]) * hv + v] = val;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) combine_kernel(
+    const uint4* __restrict__ ye, const float* __restrict__ w, const int32_t* __restrict__ slot_of,
+    int64_t N, int k, int hv, int64_t R, uint4* __restrict__ y) {
+  const int64_t t = blockIdx.x;
+  __shared__ int32_t slots[kMaxK];
+  __shared__ float wt[kMaxK];
+  if (threadIdx.x < k) {
+    slots[threadIdx.x] = slot_of[t * k + threadIdx.x];
+    wt[threadIdx.x] = w ? w[t * k + threadIdx.x] : 1.0f;
+  }
+  __syncthreads();
+  for (int v = threadIdx.x; v < hv; v += blockDim.x) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int j = 0; j < k; ++j) {
+      if (slots[j] < 0 || slots[j] >= R) continue;
+      float f[8];
+      unpack8(ye[static_cast<int64_t>(slots[j]) * hv + v], f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = fmaf(wt[j], f[q], acc[q]);
+    }
+    y[t * hv + v] = pack8(acc);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) reverse_combine_kernel(
+    const uint4* __restrict__ dy, const uint4* __restrict__ ye, const float* __restrict__ w,
+    const int32_t* __restrict__ slot_of, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ pad_offsets, int64_t N, int k, int hv, int64_t R,
+    uint4* __restrict__ dye, float* __restrict__ dw) {
+  __shared__ float red[kThreads / 32][kMaxK];
+  const int64_t t = blockIdx.x;
+  if (t >= N) {
+    zero_padding(static_cast<int>(t - N), counts, pad_offsets, R, hv, dye);
+    return;
+  }
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  for (int j = 0; j < k; ++j) {
+    const int32_t slot = slot_of[t * k + j];
+    const bool ok = slot >= 0 && slot < R;
+    const float wj = w[t * k + j];
+    float part = 0.0f;
+    for (int v = threadIdx.x; v < hv; v += blockDim.x) {
+      float g[8];
+      unpack8(dy[t * hv + v], g);
+      if (ok) {
+        float s[8], e8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) s[q] = wj * g[q];
+        dye[static_cast<int64_t>(slot) * hv + v] = pack8(s);
+        unpack8(ye[static_cast<int64_t>(slot) * hv + v], e8);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) part = fmaf(g[q], e8[q], part);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_down_sync(0xffffffffu, part, off);
+    if (lane == 0) red[wib][j] = part;
+  }
+  __syncthreads();
+  if (threadIdx.x < k) {
+    float s = 0.0f;
+    for (int q = 0; q < kThreads / 32; ++q) s += red[q][threadIdx.x];  // fixed order
+    dw[t * k + threadIdx.x] = s;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const Layout& L, const void* ws, const void* x, void* xe,
+                            cudaStream_t s) {
+  const int64_t blocks = L.N + L.E;
+  dispatch_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
+      static_cast<const uint4*>(x), at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.counts),
+      at<int32_t>(ws, L.pad_offsets), L.N, L.k, L.H / 8, L.R, static_cast<uint4*>(xe));
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const Layout& L, const void* ws, const void* ye, const float* w,
+                           void* y, cudaStream_t s) {
+  if (L.N == 0) return cudaSuccess;
+  combine_kernel<<<static_cast<unsigned>(L.N), kThreads, 0, s>>>(
+      static_cast<const uint4*>(ye), w, at<int32_t>(ws, L.slot_of), L.N, L.k, L.H / 8, L.R,
+      static_cast<uint4*>(y));
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reverse_combine(const Layout& L, const void* ws, const void* dy,
+                                   const void* ye, const float* w, void* dye, float* dw,
+                                   cudaStream_t s) {
+  const int64_t blocks = L.N + L.E;
+  reverse_combine_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
+      static_cast<const uint4*>(dy), static_cast<const uint4*>(ye), w,
+      at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.pad_offsets), L.N,
+      L.k, L.H / 8, L.R, static_cast<uint4*>(dye), dw);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reverse_dispatch(const Layout& L, const void* ws, const void* dxe, void* dx,
+                                    cudaStream_t s) {
+  if (L.N == 0) return cudaSuccess;
+  combine_kernel<<<static_cast<unsigned>(L.N), kThreads, 0, s>>>(
+      static_cast<const uint4*>(dxe), nullptr, at<int32_t>(ws, L.slot_of), L.N, L.k, L.H / 8, L.R,
+      static_cast<uint4*>(dx));
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

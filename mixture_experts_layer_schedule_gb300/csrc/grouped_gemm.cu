@@ -1,0 +1,592 @@
+// grouped_gemm.cu -- the expert FFN GEMMs of the layer on the 5th-generation
+// tensor cores (tcgen05, accumulators in TMEM), with their epilogues fused.
+//
+// The expert FFN is a grouped GEMM with a SwiGLU activation (gate/up, then
+// silu * mul, then down) run per minibatch of tokens ("Mixture-of-Kittens:
+// Cursor open-sources an MoE training megakernel", key points 3 and 5 and the
+// key flowchart node "expert FFN + SwiGLU"). The backward rounds (key point
+// 2) need the matching data-gradient and weight-gradient GEMMs.
+//
+// One persistent kernel template serves every GEMM of the layer. Each CTA
+// (one per SM) runs three roles that hand work over through mbarriers:
+//   warp 0      TMA producer: streams 64-wide K slices of the A and B tiles
+//               into a ring of shared-memory stages (128-byte swizzle);
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256,
+//               K=16) into one of two TMEM accumulators, and commits each
+//               stage back to the producer when the tensor core is done;
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (one TMEM lane quadrant
+//               per warp, one output row per thread), apply the fused
+//               epilogue, store to global memory, release the accumulator.
+// The two accumulators let the epilogue of tile i overlap the MMAs of tile
+// i+1. Every wait is bounded; a timeout records MOE_DEVERR_TIMEOUT, drains
+// the copies and MMAs in flight, frees TMEM and returns.
+//
+// Modes (rows of the expert-grouped buffer are padded per expert to 128, and
+// padding rows hold zeros, so every tile is a full 128-row tile of one
+// expert):
+//   GATE_UP  G|U = Xe . [Wg[e]; Wu[e]]^T   -> G, U, Act = silu(G) * U (bf16)
+//   DOWN     Ye  = Act . Wd[e]^T            -> bf16
+//   DACT     dAct = dYe . Wd[e]             -> dG, dU via the SwiGLU backward (bf16)
+//   DXE      dXe = dG . Wg[e] + dU . Wu[e]  -> bf16 (two K phases)
+//   WGRAD    dW[e] = P_e^T . Q_e over the expert's rows (K = tokens) -> fp32,
+//            for up to two problems per launch (dWg and dWu share Q = Xe).
+#include <algorithm>
+#include <mutex>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, kStages = 4;
+constexpr int kABytes = BM * BK * 2;  // 16 KB
+constexpr int kBBytes = BN * BK * 2;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+constexpr int kGemmThreads = 192;
+constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
+
+enum Mode { GATE_UP = 0, DOWN = 1, DACT = 2, DXE = 3, WGRAD = 4 };
+
+struct Maps {
+  CUtensorMap a0, a1, b0, b1;
+};
+
+struct Args {
+  const int32_t* tiles;        // [n][3] (expert, row0, valid) of the 128-row tiles
+  const int32_t* n_tiles;      // device count of those tiles
+  const int32_t* pad_offsets;  // [E+1] padded segment starts (WGRAD K ranges)
+  int32_t* err;
+  int max_mtiles;              // host bound on *n_tiles (R / 128)
+  int64_t rows;                // rows of the expert-grouped buffers (R)
+  int n_nt;                    // N tiles per M tile
+  int kb1, kb2;                // K blocks of phase 1 and 2
+  int b_rows;                  // rows per expert in B's 2-D view
+  int E, w_mt, w_nt, n_probs;  // WGRAD tiling
+  int ld_out;                  // output row length (elements)
+  void *out0, *out1, *out2;
+  const void *in0, *in1;
+};
+
+template <int MODE>
+struct Traits {
+  static constexpr bool a_mn = (MODE == WGRAD);
+  static constexpr bool b_mn = (MODE == DACT || MODE == DXE || MODE == WGRAD);
+};
+
+__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, int32_t* err) {
+  int no_abort = 0;  // drain waits do not stop at the abort flag
+  return mbar_wait(bar, parity, &no_abort, err);
+}
+
+struct TileInfo {
+  int e, row0, mt, nt, prob, kstart, nkb;
+  bool skip;
+};
+
+template <int MODE>
+__device__ __forceinline__ TileInfo decode_tile(const Args& a, int64_t t) {
+  TileInfo ti;
+  if constexpr (MODE == WGRAD) {
+    const int64_t per_prob = static_cast<int64_t>(a.E) * a.w_mt * a.w_nt;
+    ti.prob = static_cast<int>(t / per_prob);
+    int64_t r = t % per_prob;
+    ti.e = static_cast<int>(r / (a.w_mt * a.w_nt));
+    r %= (a.w_mt * a.w_nt);
+    ti.mt = static_cast<int>(r / a.w_nt);
+    ti.nt = static_cast<int>(r % a.w_nt);
+    ti.kstart = a.pad_offsets[ti.e];
+    ti.nkb = (a.pad_offsets[ti.e + 1] - ti.kstart) / BK;
+    ti.row0 = 0;
+    ti.skip = false;
+    if (ti.kstart < 0 || ti.nkb < 0 || ti.kstart + static_cast<int64_t>(ti.nkb) * BK > a.rows) {
+      ti.nkb = 0;  // corrupt schedule: compute nothing, store nothing
+      ti.skip = true;
+    }
+  } else {
+    const int mtile = static_cast<int>(t / a.n_nt);
+    ti.nt = static_cast<int>(t % a.n_nt);
+    ti.mt = mtile;
+    ti.e = a.tiles[3 * mtile + 0];
+    ti.row0 = a.tiles[3 * mtile + 1];
+    ti.prob = 0;
+    ti.kstart = 0;
+    ti.nkb = a.kb1 + a.kb2;
+    ti.skip = false;
+    if (ti.e < 0 || ti.e >= a.E || ti.row0 < 0 || ti.row0 > a.rows - BM) {
+      ti.e = 0;  // corrupt schedule: compute nothing, store nothing
+      ti.row0 = 0;
+      ti.nkb = 0;
+      ti.skip = true;
+    }
+  }
+  return ti;
+}
+
+template <int MODE>
+__device__ __forceinline__ int64_t total_tiles(const Args& a) {
+  if constexpr (MODE == WGRAD) {
+    return static_cast<int64_t>(a.n_probs) * a.E * a.w_mt * a.w_nt;
+  } else {
+    int n = *a.n_tiles;
+    n = n < 0 ? 0 : (n > a.max_mtiles ? a.max_mtiles : n);
+    return static_cast<int64_t>(n) * a.n_nt;
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ void issue_loads(const Maps& m, const Args& a, const TileInfo& ti,
+                                            int kb, uint8_t* sA, uint8_t* sB, uint64_t* bar) {
+  if constexpr (MODE == GATE_UP) {
+    tma_load_2d(sA, &m.a0, bar, kb * BK, ti.row0);
+    const int brow = ti.e * a.b_rows + ti.nt * (BN / 2);
+    tma_load_2d(sB, &m.b0, bar, kb * BK, brow);
+    tma_load_2d(sB + kBBytes / 2, &m.b1, bar, kb * BK, brow);
+  } else if constexpr (MODE == DOWN) {
+    tma_load_2d(sA, &m.a0, bar, kb * BK, ti.row0);
+    tma_load_2d(sB, &m.b0, bar, kb * BK, ti.e * a.b_rows + ti.nt * BN);
+  } else if constexpr (MODE == DACT || MODE == DXE) {
+    const bool second = (MODE == DXE) && kb >= a.kb1;
+    const int kk = second ? kb - a.kb1 : kb;
+    tma_load_2d(sA, second ? &m.a1 : &m.a0, bar, kk * BK, ti.row0);
+    const CUtensorMap* mb = second ? &m.b1 : &m.b0;
+#pragma unroll
+    for (int c = 0; c < BN / 64; ++c)
+      tma_load_2d(sB + c * (64 * BK * 2), mb, bar, ti.nt * BN + c * 64, ti.e * a.b_rows + kk * BK);
+  } else {  // WGRAD
+    const CUtensorMap* ma = ti.prob ? &m.a1 : &m.a0;
+    const CUtensorMap* mb = ti.prob ? &m.b1 : &m.b0;
+    const int krow = ti.kstart + kb * BK;
+#pragma unroll
+    for (int c = 0; c < BM / 64; ++c)
+      tma_load_2d(sA + c * (64 * BK * 2), ma, bar, ti.mt * BM + c * 64, krow);
+#pragma unroll
+    for (int c = 0; c < BN / 64; ++c)
+      tma_load_2d(sB + c * (64 * BK * 2), mb, bar, ti.nt * BN + c * 64, krow);
+  }
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+template <int MODE>
+__device__ __forceinline__ void epilogue(const Args& a, const TileInfo& ti, uint32_t tmem_acc,
+                                         int quad, int lane) {
+  const int rit = quad * 32 + lane;  // row within the tile
+  const uint32_t taddr = tmem_acc + (static_cast<uint32_t>(quad * 32) << 16);
+  if constexpr (MODE == GATE_UP) {
+    const int64_t row = ti.row0 + rit;
+    const int64_t o = row * a.ld_out + ti.nt * (BN / 2);
+    for (int c = 0; c < BN / 2; c += 32) {
+      uint32_t g[32], u[32];
+      tmem_ld32(taddr + c, g);
+      tmem_ld32(taddr + BN / 2 + c, u);
+      tmem_ld_wait();
+      uint4* pg = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out0) + o + c);
+      uint4* pu = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out1) + o + c);
+      uint4* pa = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out2) + o + c);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        uint32_t wg[4], wu[4], wa[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float g0 = __uint_as_float(g[8 * v + 2 * q]), g1 = __uint_as_float(g[8 * v + 2 * q + 1]);
+          const float u0 = __uint_as_float(u[8 * v + 2 * q]), u1 = __uint_as_float(u[8 * v + 2 * q + 1]);
+          wg[q] = pack_bf16x2(g0, g1);
+          wu[q] = pack_bf16x2(u0, u1);
+          wa[q] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
+        }
+        pg[v] = make_uint4(wg[0], wg[1], wg[2], wg[3]);
+        pu[v] = make_uint4(wu[0], wu[1], wu[2], wu[3]);
+        pa[v] = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+      }
+    }
+  } else if constexpr (MODE == DOWN || MODE == DXE) {
+    const int64_t row = ti.row0 + rit;
+    const int64_t o = row * a.ld_out + ti.nt * BN;
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t d[32];
+      tmem_ld32(taddr + c, d);
+      tmem_ld_wait();
+      uint4* p = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out0) + o + c);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          w4[q] = pack_bf16x2(__uint_as_float(d[8 * v + 2 * q]), __uint_as_float(d[8 * v + 2 * q + 1]));
+        p[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+    }
+  } else if constexpr (MODE == DACT) {
+    const int64_t row = ti.row0 + rit;
+    const int64_t o = row * a.ld_out + ti.nt * BN;
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t d[32];
+      tmem_ld32(taddr + c, d);
+      const uint4* pg = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.in0) + o + c);
+      const uint4* pu = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.in1) + o + c);
+      uint4 gv[4], uv[4];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        gv[v] = pg[v];
+        uv[v] = pu[v];
+      }
+      tmem_ld_wait();
+      uint4* pdg = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out0) + o + c);
+      uint4* pdu = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out1) + o + c);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint32_t gw[4] = {gv[v].x, gv[v].y, gv[v].z, gv[v].w};
+        const uint32_t uw[4] = {uv[v].x, uv[v].y, uv[v].z, uv[v].w};
+        uint32_t og[4], ou[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float dg2[2], du2[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float da = __uint_as_float(d[8 * v + 2 * q + h]);
+            const float g = h ? bf16hi(gw[q]) : bf16lo(gw[q]);
+            const float u = h ? bf16hi(uw[q]) : bf16lo(uw[q]);
+            const float s = 1.0f / (1.0f + expf(-g));
+            dg2[h] = da * u * s * (1.0f + g * (1.0f - s));
+            du2[h] = da * g * s;
+          }
+          og[q] = pack_bf16x2(dg2[0], dg2[1]);
+          ou[q] = pack_bf16x2(du2[0], du2[1]);
+        }
+        pdg[v] = make_uint4(og[0], og[1], og[2], og[3]);
+        pdu[v] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+      }
+    }
+  } else {  // WGRAD: fp32 rows of dW[e]
+    const int64_t M_total = static_cast<int64_t>(a.w_mt) * BM;
+    float* out = static_cast<float*>(ti.prob ? a.out1 : a.out0);
+    const int64_t o = (static_cast<int64_t>(ti.e) * M_total + ti.mt * BM + rit) * a.ld_out + ti.nt * BN;
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t d[32];
+      if (ti.nkb > 0) {
+        tmem_ld32(taddr + c, d);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) d[q] = 0u;
+      }
+      uint4* p = reinterpret_cast<uint4*>(out + o + c);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) p[v] = make_uint4(d[4 * v], d[4 * v + 1], d[4 * v + 2], d[4 * v + 3]);
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ Maps maps, const Args args) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], drain_bar;
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ int abort_flag;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 128);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.a0);
+    tma_prefetch_desc(&maps.b0);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_slot;
+  volatile int* abortp = &abort_flag;
+  const int64_t total = total_tiles<MODE>(args);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile<MODE>(args, t);
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, args.err)) { ok = false; break; }
+          uint8_t* sA = smem + stage * kStageBytes;
+          mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
+          issue_loads<MODE>(maps, args, ti, kb, sA, sA + kABytes, &full_bar[stage]);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // Every issued copy must land before the CTA may exit.
+      for (int s = 0; s < kStages; ++s)
+        if ((issued_mask >> s) & 1u) wait_drain(&full_bar[s], (issued_parity >> s) & 1u, args.err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t idesc = idesc_bf16(BM, BN, Traits<MODE>::a_mn, Traits<MODE>::b_mn);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile<MODE>(args, t);
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abortp, args.err)) break;
+        tc_fence_after();
+        const uint32_t dtmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abortp, args.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
+          const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks) {
+            uint64_t ad, bd;
+            if constexpr (Traits<MODE>::a_mn) ad = sdesc_sw128(a_addr + ks * 2048, 64 * BK * 2, 1024);
+            else ad = sdesc_sw128(a_addr + ks * 32, 16, 1024);
+            if constexpr (Traits<MODE>::b_mn) bd = sdesc_sw128(b_addr + ks * 2048, 64 * BK * 2, 1024);
+            else bd = sdesc_sw128(b_addr + ks * 32, 16, 1024);
+            umma_bf16(dtmem, ad, bd, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty_bar[stage]);  // stage free once these MMAs retire
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(&tfull_bar[acc]);  // accumulator ready (immediate if no MMA)
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      umma_commit(&drain_bar);
+      wait_drain(&drain_bar, 0, args.err);
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 ----------------
+    const int quad = warp & 3;  // TMEM lanes this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+      const TileInfo ti = decode_tile<MODE>(args, t);
+      if (!mbar_wait(&tfull_bar[acc], acc_phase, abortp, args.err)) break;
+      tc_fence_after();
+      if (!ti.skip) epilogue<MODE>(args, ti, tmem_base + acc * BN, quad, lane);
+      else if (lane == 0) set_dev_error(args.err, MOE_DEVERR_BAD_EXPERT);
+      tc_fence_before();
+      mbar_arrive(&tempty_bar[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps and launches.
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 view [outer][inner] (inner contiguous), box 64 x box_outer,
+// 128-byte swizzle. Returns false on failure.
+bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || outer <= 0 || inner <= 0) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (inner * 2) % 16 != 0) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner * 2)};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_outer)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+template <int MODE>
+moe_status launch(const Maps& maps, const Args& args, int64_t tiles_upper, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
+  if (tiles_upper <= 0) return MOE_OK;
+  const int grid = static_cast<int>(std::min<int64_t>(sm_count(), tiles_upper));
+  grouped_gemm_kernel<MODE><<<grid, kGemmThreads, kSmemBytes, s>>>(maps, args);
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+Args base_args(const Layout& L, const void* ws) {
+  Args a{};
+  a.tiles = at<int32_t>(ws, L.tiles);
+  a.n_tiles = at<int32_t>(ws, L.n_tiles);
+  a.pad_offsets = at<int32_t>(ws, L.pad_offsets);
+  a.err = const_cast<int32_t*>(at<int32_t>(ws, L.err));
+  a.max_mtiles = static_cast<int>(L.R / BM);
+  a.rows = L.R;
+  a.E = L.E;
+  return a;
+}
+
+}  // namespace
+
+moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const void* wg,
+                        const void* wu, void* g, void* u, void* act, cudaStream_t s) {
+  Maps m{};
+  if (!make_map(&m.a0, xe, L.H, L.R, BM) ||
+      !make_map(&m.b0, wg, L.H, static_cast<int64_t>(L.E) * L.I, BN / 2) ||
+      !make_map(&m.b1, wu, L.H, static_cast<int64_t>(L.E) * L.I, BN / 2))
+    return MOE_ERR_CUDA;
+  m.a1 = m.a0;
+  Args a = base_args(L, ws);
+  a.n_nt = L.I / (BN / 2);
+  a.kb1 = L.H / BK;
+  a.kb2 = 0;
+  a.b_rows = L.I;
+  a.ld_out = L.I;
+  a.out0 = g;
+  a.out1 = u;
+  a.out2 = act;
+  return launch<GATE_UP>(m, a, static_cast<int64_t>(a.max_mtiles) * a.n_nt, s);
+}
+
+moe_status gemm_down(const Layout& L, const void* ws, const void* act, const void* wd, void* ye,
+                     cudaStream_t s) {
+  Maps m{};
+  if (!make_map(&m.a0, act, L.I, L.R, BM) ||
+      !make_map(&m.b0, wd, L.I, static_cast<int64_t>(L.E) * L.H, BN))
+    return MOE_ERR_CUDA;
+  m.a1 = m.a0;
+  m.b1 = m.b0;
+  Args a = base_args(L, ws);
+  a.n_nt = L.H / BN;
+  a.kb1 = L.I / BK;
+  a.kb2 = 0;
+  a.b_rows = L.H;
+  a.ld_out = L.H;
+  a.out0 = ye;
+  return launch<DOWN>(m, a, static_cast<int64_t>(a.max_mtiles) * a.n_nt, s);
+}
+
+moe_status gemm_down_dgrad(const Layout& L, const void* ws, const void* dye, const void* g,
+                           const void* u, const void* wd, void* dg, void* du, cudaStream_t s) {
+  Maps m{};
+  if (!make_map(&m.a0, dye, L.H, L.R, BM) ||
+      !make_map(&m.b0, wd, L.I, static_cast<int64_t>(L.E) * L.H, 64))
+    return MOE_ERR_CUDA;
+  m.a1 = m.a0;
+  m.b1 = m.b0;
+  Args a = base_args(L, ws);
+  a.n_nt = L.I / BN;
+  a.kb1 = L.H / BK;
+  a.kb2 = 0;
+  a.b_rows = L.H;
+  a.ld_out = L.I;
+  a.out0 = dg;
+  a.out1 = du;
+  a.in0 = g;
+  a.in1 = u;
+  return launch<DACT>(m, a, static_cast<int64_t>(a.max_mtiles) * a.n_nt, s);
+}
+
+moe_status gemm_down_wgrad(const Layout& L, const void* ws, const void* dye, const void* act,
+                           float* dw_down, cudaStream_t s) {
+  Maps m{};
+  if (!make_map(&m.a0, dye, L.H, L.R, 64) || !make_map(&m.b0, act, L.I, L.R, 64))
+    return MOE_ERR_CUDA;
+  m.a1 = m.a0;
+  m.b1 = m.b0;
+  Args a = base_args(L, ws);
+  a.w_mt = L.H / BM;
+  a.w_nt = L.I / BN;
+  a.n_probs = 1;
+  a.ld_out = L.I;
+  a.out0 = dw_down;
+  a.out1 = dw_down;
+  return launch<WGRAD>(m, a, static_cast<int64_t>(L.E) * a.w_mt * a.w_nt, s);
+}
+
+moe_status gemm_gate_up_dgrad(const Layout& L, const void* ws, const void* dg, const void* du,
+                              const void* wg, const void* wu, void* dxe, cudaStream_t s) {
+  Maps m{};
+  if (!make_map(&m.a0, dg, L.I, L.R, BM) || !make_map(&m.a1, du, L.I, L.R, BM) ||
+      !make_map(&m.b0, wg, L.H, static_cast<int64_t>(L.E) * L.I, 64) ||
+      !make_map(&m.b1, wu, L.H, static_cast<int64_t>(L.E) * L.I, 64))
+    return MOE_ERR_CUDA;
+  Args a = base_args(L, ws);
+  a.n_nt = L.H / BN;
+  a.kb1 = L.I / BK;
+  a.kb2 = L.I / BK;
+  a.b_rows = L.I;
+  a.ld_out = L.H;
+  a.out0 = dxe;
+  return launch<DXE>(m, a, static_cast<int64_t>(a.max_mtiles) * a.n_nt, s);
+}
+
+moe_status gemm_gate_up_wgrad(const Layout& L, const void* ws, const void* dg, const void* du,
+                              const void* xe, float* dw_gate, float* dw_up, cudaStream_t s) {
+  Maps m{};
+  if (!make_map(&m.a0, dg, L.I, L.R, 64) || !make_map(&m.a1, du, L.I, L.R, 64) ||
+      !make_map(&m.b0, xe, L.H, L.R, 64))
+    return MOE_ERR_CUDA;
+  m.b1 = m.b0;
+  Args a = base_args(L, ws);
+  a.w_mt = L.I / BM;
+  a.w_nt = L.H / BN;
+  a.n_probs = 2;
+  a.ld_out = L.H;
+  a.out0 = dw_gate;
+  a.out1 = dw_up;
+  return launch<WGRAD>(m, a, 2LL * L.E * a.w_mt * a.w_nt, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,325 @@
+// moe_api.cu -- the C ABI (include/moe.h): argument validation, workspace and
+// forward-context layout, and the order of the phases of the layer.
+//
+// The shape of the interface follows the functional API described in the
+// project summary "Mixture-of-Kittens (MoK)" (section "use the functional
+// API"): a workspace created once per model, build_schedule from the router's
+// top-k experts, forward returning the output and a context, backward taking
+// that context; and its ops layer, where the caller owns every tensor.
+#include <algorithm>
+#include <atomic>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+moe_status make_layout(const moe_problem* p, Layout* L) {
+  if (!p || !L) return MOE_ERR_INVALID_ARG;
+  if (p->N < 0 || p->H <= 0 || p->I <= 0 || p->E <= 0 || p->k <= 0) return MOE_ERR_INVALID_ARG;
+  if (p->k > p->E) return MOE_ERR_INVALID_ARG;
+  if (p->E > kMaxE || p->k > kMaxK) return MOE_ERR_UNSUPPORTED;
+  if (p->H % 256 != 0 || p->I % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  if (p->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const int64_t A = p->N * p->k;
+  const int64_t R = (A + static_cast<int64_t>(p->E) * (kTileM - 1) + kTileM - 1) / kTileM * kTileM;
+  if (R >= (1LL << 31) - 1 || p->N > (1LL << 31) / p->k) return MOE_ERR_UNSUPPORTED;
+  L->N = p->N;
+  L->A = A;
+  L->R = R;
+  L->H = p->H;
+  L->I = p->I;
+  L->E = p->E;
+  L->k = p->k;
+  L->n_warps = (A + kSchedSub - 1) / kSchedSub;
+  size_t o = 0;
+  auto take = [&o](size_t bytes) {
+    const size_t here = o;
+    o = align256(o + bytes);
+    return here;
+  };
+  L->err = take(sizeof(int32_t));
+  L->counts = take(sizeof(int32_t) * p->E);
+  L->offsets = take(sizeof(int32_t) * (p->E + 1));
+  L->pad_offsets = take(sizeof(int32_t) * (p->E + 1));
+  L->slot_of = take(sizeof(int32_t) * std::max<int64_t>(A, 1));
+  L->src_of_row = take(sizeof(int32_t) * R);
+  L->tiles = take(sizeof(int32_t) * 3 * (R / kTileM));
+  L->n_tiles = take(sizeof(int32_t));
+  L->warp_counts = take(sizeof(int32_t) * p->E * std::max<int64_t>(L->n_warps, 1));
+  L->dyxe = take(static_cast<size_t>(R) * p->H * 2);
+  L->dg = take(static_cast<size_t>(R) * p->I * 2);
+  L->du = take(static_cast<size_t>(R) * p->I * 2);
+  L->ws_bytes = o;
+  o = 0;
+  L->xe = take(static_cast<size_t>(R) * p->H * 2);
+  L->g = take(static_cast<size_t>(R) * p->I * 2);
+  L->u = take(static_cast<size_t>(R) * p->I * 2);
+  L->act = take(static_cast<size_t>(R) * p->I * 2);
+  L->ye = take(static_cast<size_t>(R) * p->H * 2);
+  L->saved_bytes = o;
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+inline bool aligned(const void* p, uintptr_t a) {
+  return p != nullptr && (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+inline cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
+inline moe_status cu(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                      \
+  do {                                     \
+    moe_status st_ = (expr);               \
+    if (st_ != MOE_OK) return st_;         \
+  } while (0)
+
+moe_status prep(const moe_problem* p, const void* ws, Layout* L) {
+  MOE_TRY(make_layout(p, L));
+  if (!aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+bool weights_ok(const moe_weights* w) {
+  return w && aligned(w->w_gate, 16) && aligned(w->w_up, 16) && aligned(w->w_down, 16);
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t moe_grouped_rows(const moe_problem* p) {
+  Layout L;
+  return make_layout(p, &L) == MOE_OK ? L.R : -1;
+}
+
+moe_status moe_workspace_bytes(const moe_problem* p, size_t* bytes) {
+  Layout L;
+  MOE_TRY(make_layout(p, &L));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = L.ws_bytes;
+  return MOE_OK;
+}
+
+moe_status moe_saved_bytes(const moe_problem* p, size_t* bytes) {
+  Layout L;
+  MOE_TRY(make_layout(p, &L));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = L.saved_bytes;
+  return MOE_OK;
+}
+
+moe_status moe_saved_layout(const moe_problem* p, void* saved, moe_saved_view* out) {
+  Layout L;
+  MOE_TRY(make_layout(p, &L));
+  if (!aligned(saved, 256) || !out) return MOE_ERR_INVALID_ARG;
+  out->xe = at<char>(saved, L.xe);
+  out->g = at<char>(saved, L.g);
+  out->u = at<char>(saved, L.u);
+  out->act = at<char>(saved, L.act);
+  out->ye = at<char>(saved, L.ye);
+  return MOE_OK;
+}
+
+moe_status moe_schedule_view(const moe_problem* p, void* ws, moe_schedule* out) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (!out) return MOE_ERR_INVALID_ARG;
+  out->counts = at<int32_t>(ws, L.counts);
+  out->offsets = at<int32_t>(ws, L.offsets);
+  out->pad_offsets = at<int32_t>(ws, L.pad_offsets);
+  out->slot_of = at<int32_t>(ws, L.slot_of);
+  out->src_of_row = at<int32_t>(ws, L.src_of_row);
+  out->tiles = at<int32_t>(ws, L.tiles);
+  out->n_tiles = at<int32_t>(ws, L.n_tiles);
+  return MOE_OK;
+}
+
+moe_status moe_route_topk(const moe_problem* p, const float* logits, const float* bias,
+                          int32_t* topk_ids, float* topk_w, void* ws, void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (L.N > 0 && (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4)))
+    return MOE_ERR_INVALID_ARG;
+  if (bias && !aligned(bias, 4)) return MOE_ERR_INVALID_ARG;
+  return cu(launch_route_topk(L, logits, bias, topk_ids, topk_w, at<int32_t>(ws, L.err), S(stream)));
+}
+
+moe_status moe_build_schedule(const moe_problem* p, const int32_t* topk_ids, void* ws,
+                              void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (L.N > 0 && !aligned(topk_ids, 4)) return MOE_ERR_INVALID_ARG;
+  return cu(launch_build_schedule(L, topk_ids, ws, S(stream)));
+}
+
+moe_status moe_dispatch(const moe_problem* p, const void* ws, const void* x, void* xe,
+                        void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if ((L.N > 0 && !aligned(x, 16)) || !aligned(xe, 16)) return MOE_ERR_INVALID_ARG;
+  return cu(launch_dispatch(L, ws, x, xe, S(stream)));
+}
+
+moe_status moe_expert_gate_up(const moe_problem* p, const void* ws, const void* xe,
+                              const moe_weights* w, void* g, void* u, void* act, void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (!aligned(xe, 16) || !weights_ok(w) || !aligned(g, 16) || !aligned(u, 16) ||
+      !aligned(act, 16))
+    return MOE_ERR_INVALID_ARG;
+  return gemm_gate_up(L, ws, xe, w->w_gate, w->w_up, g, u, act, S(stream));
+}
+
+moe_status moe_expert_down(const moe_problem* p, const void* ws, const void* act,
+                           const moe_weights* w, void* ye, void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (!aligned(act, 16) || !weights_ok(w) || !aligned(ye, 16)) return MOE_ERR_INVALID_ARG;
+  return gemm_down(L, ws, act, w->w_down, ye, S(stream));
+}
+
+moe_status moe_combine(const moe_problem* p, const void* ws, const void* ye, const float* topk_w,
+                       void* y, void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (L.N > 0 && (!aligned(ye, 16) || !aligned(topk_w, 4) || !aligned(y, 16)))
+    return MOE_ERR_INVALID_ARG;
+  return cu(launch_combine(L, ws, ye, topk_w, y, S(stream)));
+}
+
+moe_status moe_forward(const moe_problem* p, const void* x, const moe_weights* w,
+                       const float* topk_w, void* y, void* saved, void* ws, void* stream) {
+  moe_saved_view v;
+  MOE_TRY(moe_saved_layout(p, saved, &v));
+  MOE_TRY(moe_dispatch(p, ws, x, v.xe, stream));
+  MOE_TRY(moe_expert_gate_up(p, ws, v.xe, w, v.g, v.u, v.act, stream));
+  MOE_TRY(moe_expert_down(p, ws, v.act, w, v.ye, stream));
+  return moe_combine(p, ws, v.ye, topk_w, y, stream);
+}
+
+moe_status moe_reverse_combine(const moe_problem* p, const void* ws, const void* dy,
+                               const void* ye, const float* topk_w, void* dye, float* d_topk_w,
+                               void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (!aligned(ye, 16) || !aligned(dye, 16)) return MOE_ERR_INVALID_ARG;
+  if (L.N > 0 && (!aligned(dy, 16) || !aligned(topk_w, 4) || !aligned(d_topk_w, 4)))
+    return MOE_ERR_INVALID_ARG;
+  return cu(launch_reverse_combine(L, ws, dy, ye, topk_w, dye, d_topk_w, S(stream)));
+}
+
+moe_status moe_expert_down_dgrad(const moe_problem* p, const void* ws, const void* dye,
+                                 const void* g, const void* u, const moe_weights* w, void* dg,
+                                 void* du, void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (!aligned(dye, 16) || !aligned(g, 16) || !aligned(u, 16) || !weights_ok(w) ||
+      !aligned(dg, 16) || !aligned(du, 16))
+    return MOE_ERR_INVALID_ARG;
+  return gemm_down_dgrad(L, ws, dye, g, u, w->w_down, dg, du, S(stream));
+}
+
+moe_status moe_expert_down_wgrad(const moe_problem* p, const void* ws, const void* dye,
+                                 const void* act, float* dw_down, void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (!aligned(dye, 16) || !aligned(act, 16) || !aligned(dw_down, 16))
+    return MOE_ERR_INVALID_ARG;
+  return gemm_down_wgrad(L, ws, dye, act, dw_down, S(stream));
+}
+
+moe_status moe_expert_gate_up_dgrad(const moe_problem* p, const void* ws, const void* dg,
+                                    const void* du, const moe_weights* w, void* dxe,
+                                    void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (!aligned(dg, 16) || !aligned(du, 16) || !weights_ok(w) || !aligned(dxe, 16))
+    return MOE_ERR_INVALID_ARG;
+  return gemm_gate_up_dgrad(L, ws, dg, du, w->w_gate, w->w_up, dxe, S(stream));
+}
+
+moe_status moe_expert_gate_up_wgrad(const moe_problem* p, const void* ws, const void* dg,
+                                    const void* du, const void* xe, float* dw_gate,
+                                    float* dw_up, void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (!aligned(dg, 16) || !aligned(du, 16) || !aligned(xe, 16) || !aligned(dw_gate, 16) ||
+      !aligned(dw_up, 16))
+    return MOE_ERR_INVALID_ARG;
+  return gemm_gate_up_wgrad(L, ws, dg, du, xe, dw_gate, dw_up, S(stream));
+}
+
+moe_status moe_reverse_dispatch(const moe_problem* p, const void* ws, const void* dxe, void* dx,
+                                void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (L.N > 0 && (!aligned(dxe, 16) || !aligned(dx, 16))) return MOE_ERR_INVALID_ARG;
+  return cu(launch_reverse_dispatch(L, ws, dxe, dx, S(stream)));
+}
+
+moe_status moe_backward(const moe_problem* p, const void* saved, const moe_weights* w,
+                        const float* topk_w, const void* dy, void* dx, float* dw_gate,
+                        float* dw_up, float* dw_down, float* d_topk_w, void* ws, void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  moe_saved_view v;
+  MOE_TRY(moe_saved_layout(p, const_cast<void*>(saved), &v));
+  void* dyxe = at<char>(ws, L.dyxe);
+  void* dg = at<char>(ws, L.dg);
+  void* du = at<char>(ws, L.du);
+  MOE_TRY(moe_reverse_combine(p, ws, dy, v.ye, topk_w, dyxe, d_topk_w, stream));
+  MOE_TRY(moe_expert_down_dgrad(p, ws, dyxe, v.g, v.u, w, dg, du, stream));
+  MOE_TRY(moe_expert_down_wgrad(p, ws, dyxe, v.act, dw_down, stream));
+  // dXe overwrites dYe in the shared buffer: dYe's last reader ran above.
+  MOE_TRY(moe_expert_gate_up_dgrad(p, ws, dg, du, w, dyxe, stream));
+  MOE_TRY(moe_expert_gate_up_wgrad(p, ws, dg, du, v.xe, dw_gate, dw_up, stream));
+  return moe_reverse_dispatch(p, ws, dyxe, dx, stream);
+}
+
+moe_status mxfp8_quantize(const void* src_bf16, int64_t rows, int64_t cols, uint8_t* q_e4m3,
+                          uint8_t* scale_e8m0, void* stream) {
+  if (rows < 0 || cols < 0 || cols % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (rows * cols == 0) return MOE_OK;
+  if (!aligned(src_bf16, 16) || !aligned(q_e4m3, 16) || !scale_e8m0) return MOE_ERR_INVALID_ARG;
+  return cu(launch_mxfp8_quantize(src_bf16, rows, cols, q_e4m3, scale_e8m0, S(stream)));
+}
+
+moe_status moe_get_device_error(const moe_problem* p, const void* ws, int32_t* code_out,
+                                void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (!code_out) return MOE_ERR_INVALID_ARG;
+  return cu(cudaMemcpyAsync(code_out, at<int32_t>(ws, L.err), sizeof(int32_t),
+                            cudaMemcpyDeviceToHost, S(stream)));
+}
+
+moe_status moe_clear_device_error(const moe_problem* p, void* ws, void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  return cu(cudaMemsetAsync(at<int32_t>(ws, L.err), 0, sizeof(int32_t), S(stream)));
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size or dtype";
+    case MOE_ERR_CUDA: return "CUDA runtime or driver error";
+    case MOE_ERR_DEVICE: return "device error word set";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// moe_internal.h -- host-side layout of the workspace and forward context,
+// and the kernel launchers shared between the translation units of the CUDA
+// library. Not part of the public ABI (see include/moe.h).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kTileM = 128;          // rows per expert tile (tcgen05 M)
+constexpr int kSchedSub = 256;       // assignments per warp in the schedule scans
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+  int64_t N, A, R;        // tokens, assignments, expert-grouped rows
+  int32_t H, I, E, k;
+  int64_t n_warps;        // schedule warps = ceil(A / kSchedSub)
+  // workspace byte offsets
+  size_t err, counts, offsets, pad_offsets, slot_of, src_of_row, tiles, n_tiles, warp_counts,
+      dyxe, dg, du, ws_bytes;
+  // forward-context byte offsets
+  size_t xe, g, u, act, ye, saved_bytes;
+};
+
+// Validates the problem (sizes the kernels support) and fills the layout.
+moe_status make_layout(const moe_problem* p, Layout* L);
+
+template <class T>
+inline T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+template <class T>
+inline const T* at(const void* base, size_t off) {
+  return reinterpret_cast<const T*>(static_cast<const char*>(base) + off);
+}
+
+// ---- launchers (return the launch error, if any) ----
+cudaError_t launch_route_topk(const Layout& L, const float* logits, const float* bias,
+                              int32_t* ids, float* w, int32_t* err, cudaStream_t s);
+cudaError_t launch_build_schedule(const Layout& L, const int32_t* ids, void* ws, cudaStream_t s);
+cudaError_t launch_build_schedule_with_scratch(const Layout& L, const int32_t* ids, void* ws,
+                                               int32_t* warp_counts, cudaStream_t s);
+cudaError_t launch_dispatch(const Layout& L, const void* ws, const void* x, void* xe,
+                            cudaStream_t s);
+cudaError_t launch_combine(const Layout& L, const void* ws, const void* ye, const float* w,
+                           void* y, cudaStream_t s);
+cudaError_t launch_reverse_combine(const Layout& L, const void* ws, const void* dy,
+                                   const void* ye, const float* w, void* dye, float* dw,
+                                   cudaStream_t s);
+cudaError_t launch_reverse_dispatch(const Layout& L, const void* ws, const void* dxe, void* dx,
+                                    cudaStream_t s);
+cudaError_t launch_mxfp8_quantize(const void* src, int64_t rows, int64_t cols, uint8_t* q,
+                                  uint8_t* scale, cudaStream_t s);
+
+// Grouped GEMMs (tcgen05). Return MOE_ERR_CUDA on a driver/launch failure.
+moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const void* wg,
+                        const void* wu, void* g, void* u, void* act, cudaStream_t s);
+moe_status gemm_down(const Layout& L, const void* ws, const void* act, const void* wd, void* ye,
+                     cudaStream_t s);
+moe_status gemm_down_dgrad(const Layout& L, const void* ws, const void* dye, const void* g,
+                           const void* u, const void* wd, void* dg, void* du, cudaStream_t s);
+moe_status gemm_down_wgrad(const Layout& L, const void* ws, const void* dye, const void* act,
+                           float* dw_down, cudaStream_t s);
+moe_status gemm_gate_up_dgrad(const Layout& L, const void* ws, const void* dg, const void* du,
+                              const void* wg, const void* wu, void* dxe, cudaStream_t s);
+moe_status gemm_gate_up_wgrad(const Layout& L, const void* ws, const void* dg, const void* du,
+                              const void* xe, float* dw_gate, float* dw_up, cudaStream_t s);
+
+// Launch accounting (every kernel launch of the library calls note_launch).
+void note_launch();
+
+}  // namespace moe

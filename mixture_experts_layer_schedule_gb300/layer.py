@@ -1,0 +1,109 @@
+"""Functional front end over the C ABI: workspace once per problem size,
+schedule from the router's top-k experts, forward -> (y, context), backward
+-> gradients. This mirrors the functional API described in the project
+summary "Mixture-of-Kittens (MoK)" (section "use the functional API"). torch
+only allocates device memory and supplies the stream; every step of the
+layer runs in the CUDA library.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+
+
+@dataclass
+class Grads:
+    dx: torch.Tensor
+    dw_gate: torch.Tensor
+    dw_up: torch.Tensor
+    dw_down: torch.Tensor
+    d_topk_w: torch.Tensor
+
+
+class MoELayer:
+    """Buffers of one problem size on one device, reused across calls."""
+
+    def __init__(self, N, H, I, E, k, device="cuda", allocate_grads=True):
+        self.N, self.H, self.I, self.E, self.k = int(N), int(H), int(I), int(E), int(k)
+        self.device = torch.device(device)
+        self.p = _lib.problem(N, H, I, E, k)
+        self.R = _lib.moe_grouped_rows(self.p)
+        dev = self.device
+        self.ws = torch.empty(_lib.moe_workspace_bytes(self.p), dtype=torch.uint8, device=dev)
+        self.saved = torch.empty(_lib.moe_saved_bytes(self.p), dtype=torch.uint8, device=dev)
+        self.ws.zero_()  # clears the device error word
+        self.topk_ids = torch.empty((N, k), dtype=torch.int32, device=dev)
+        self.topk_w = torch.empty((N, k), dtype=torch.float32, device=dev)
+        self.y = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        self.grads = None
+        if allocate_grads:
+            self.grads = Grads(
+                dx=torch.empty((N, H), dtype=torch.bfloat16, device=dev),
+                dw_gate=torch.empty((E, I, H), dtype=torch.float32, device=dev),
+                dw_up=torch.empty((E, I, H), dtype=torch.float32, device=dev),
+                dw_down=torch.empty((E, H, I), dtype=torch.float32, device=dev),
+                d_topk_w=torch.empty((N, k), dtype=torch.float32, device=dev))
+
+    # -- views -------------------------------------------------------------
+    def saved_tensors(self) -> dict:
+        v = _lib.moe_saved_layout(self.p, self.saved)
+        base = self.saved.data_ptr()
+        out = {}
+        for name, cols in (("xe", self.H), ("g", self.I), ("u", self.I), ("act", self.I),
+                           ("ye", self.H)):
+            off = getattr(v, name) - base
+            nbytes = self.R * cols * 2
+            out[name] = self.saved[off:off + nbytes].view(torch.bfloat16).view(self.R, cols)
+        return out
+
+    def schedule_tensors(self) -> dict:
+        s = _lib.moe_schedule_view(self.p, self.ws)
+        base = self.ws.data_ptr()
+        sizes = dict(counts=self.E, offsets=self.E + 1, pad_offsets=self.E + 1,
+                     slot_of=self.N * self.k, src_of_row=self.R, tiles=3 * (self.R // 128),
+                     n_tiles=1)
+        out = {}
+        for name, n in sizes.items():
+            off = getattr(s, name) - base
+            out[name] = self.ws[off:off + 4 * n].view(torch.int32)
+        return out
+
+    # -- steps -------------------------------------------------------------
+    def route(self, logits, bias=None, stream=None):
+        _lib.moe_route_topk(self.p, logits, bias, self.topk_ids, self.topk_w, self.ws, stream)
+        return self.topk_ids, self.topk_w
+
+    def build_schedule(self, topk_ids=None, stream=None):
+        _lib.moe_build_schedule(self.p, self.topk_ids if topk_ids is None else topk_ids, self.ws,
+                                stream)
+
+    def forward(self, x, wg, wu, wd, topk_w=None, stream=None):
+        w = _lib.weights(wg, wu, wd)
+        _lib.moe_forward(self.p, x, w, self.topk_w if topk_w is None else topk_w, self.y,
+                         self.saved, self.ws, stream)
+        return self.y
+
+    def backward(self, dy, wg, wu, wd, topk_w=None, stream=None) -> Grads:
+        g = self.grads
+        w = _lib.weights(wg, wu, wd)
+        _lib.moe_backward(self.p, self.saved, w, self.topk_w if topk_w is None else topk_w, dy,
+                          g.dx, g.dw_gate, g.dw_up, g.dw_down, g.d_topk_w, self.ws, stream)
+        return g
+
+    def step(self, x, logits, bias, wg, wu, wd, dy, stream=None, backward=True):
+        """Route, schedule, forward and (optionally) backward: one layer pass."""
+        self.route(logits, bias, stream)
+        self.build_schedule(None, stream)
+        y = self.forward(x, wg, wu, wd, None, stream)
+        if backward:
+            self.backward(dy, wg, wu, wd, None, stream)
+        return y
+
+    def device_error(self, stream=None) -> int:
+        return _lib.moe_get_device_error(self.p, self.ws, stream)
+
+    def clear_device_error(self, stream=None):
+        _lib.moe_clear_device_error(self.p, self.ws, stream)

@@ -1,0 +1,69 @@
+"""The C-ABI library loads and exports every entry point include/moe.h
+declares; host-only entry points (sizes, validation) behave as documented.
+No compute call is made, so this runs without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_layer_schedule_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text,
+                                 flags=re.M)))
+
+
+def test_header_declares_the_binding_names():
+    declared = _header_functions()
+    assert "moe_forward" in declared and "mxfp8_quantize" in declared
+    assert sorted(declared) == sorted(_lib.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_sizes_and_validation(lib):
+    p = _lib.problem(256, 256, 512, 8, 2)
+    assert _lib.moe_grouped_rows(p) == ((512 + 8 * 127 + 127) // 128) * 128
+    ws = _lib.moe_workspace_bytes(p)
+    sv = _lib.moe_saved_bytes(p)
+    R = _lib.moe_grouped_rows(p)
+    assert sv >= R * (2 * 256 + 3 * 512) * 2 and sv % 256 == 0
+    assert ws >= R * (256 + 2 * 512) * 2
+    for bad, status in (((256, 200, 512, 8, 2), _lib.MOE_ERR_UNSUPPORTED),
+                        ((256, 256, 512, 8, 9), _lib.MOE_ERR_INVALID_ARG),
+                        ((256, 256, 512, 2048, 2), _lib.MOE_ERR_UNSUPPORTED),
+                        ((-1, 256, 512, 8, 2), _lib.MOE_ERR_INVALID_ARG)):
+        with pytest.raises(_lib.MoEError) as ei:
+            _lib.moe_workspace_bytes(_lib.problem(*bad))
+        assert ei.value.status == status
+    with pytest.raises(_lib.MoEError) as ei:
+        _lib.moe_workspace_bytes(_lib.problem(256, 256, 512, 8, 2, dtype=_lib.MOE_MXFP8))
+    assert ei.value.status == _lib.MOE_ERR_UNSUPPORTED
+
+
+def test_null_and_misaligned_pointers_are_rejected_before_any_launch(lib):
+    p = _lib.problem(64, 256, 256, 4, 2)
+    st = lib.moe_build_schedule(ctypes.byref(p), None, None, None)
+    assert st == _lib.MOE_ERR_INVALID_ARG
+    st = lib.moe_dispatch(ctypes.byref(p), 256, 16, 0, None)  # xe NULL
+    assert st == _lib.MOE_ERR_INVALID_ARG
+    st = lib.moe_dispatch(ctypes.byref(p), 256 + 8, 16, 16, None)  # ws misaligned
+    assert st == _lib.MOE_ERR_INVALID_ARG
+    st = lib.mxfp8_quantize(16, 4, 48, 16, 16, None)  # cols not a multiple of 32
+    assert st == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_status_string(_lib.MOE_ERR_CUDA) == b"CUDA runtime or driver error"

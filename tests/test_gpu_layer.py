@@ -1,0 +1,220 @@
+"""GPU layer parity.
+
+1. Each phase kernel against a plain PyTorch fp32 reference of the same op,
+   computed from the kernel's own inputs (isolates each GEMM mode).
+2. The whole forward + backward against the fp64 oracle, element by element,
+   max|err| <= 2e-2 * max|ref| per tensor, on sizes spanning several tiles
+   with ragged tails and empty experts.
+3. Identity experts (expert output := expert input), and bitwise-identical
+   reruns (clip "Mixture-of-Kittens: Cursor open-sources an MoE training
+   megakernel", key point 5 and "how to" item 6: fixed accumulation order).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_layer_schedule_gb300 import MoELayer, _lib, inputs
+
+from gpu_helpers import BF16_TOL, assert_close, custom_shape, dev, max_rel, run_layer, to_dev
+
+pytestmark = pytest.mark.gpu
+
+RAGGED = custom_shape(300, 512, 768, 16, 4, zipf_s=1.2, name="ragged_skewed")
+
+
+def _phase_setup(shape, seed=0):
+    inp = to_dev(inputs.make_inputs(shape, seed=seed, device="cpu"))
+    layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev())
+    layer.route(inp["logits"], inp["bias"])
+    layer.build_schedule()
+    return inp, layer
+
+
+def _segments(layer):
+    s = {k: v.cpu().numpy() for k, v in layer.schedule_tensors().items()}
+    return [(e, int(s["pad_offsets"][e]), int(s["counts"][e])) for e in range(layer.E)], s
+
+
+@pytest.mark.parametrize("shape", [inputs.TINY, RAGGED], ids=lambda s: s.name)
+def test_phases_match_torch_fp32(shape):
+    inp, layer = _phase_setup(shape)
+    p, ws = layer.p, layer.ws
+    w = _lib.weights(inp["wg"], inp["wu"], inp["wd"])
+    sv = layer.saved_tensors()
+    xe, g, u, act, ye = sv["xe"], sv["g"], sv["u"], sv["act"], sv["ye"]
+    sv["xe"].fill_(7.0)  # poison: padding rows must come back zero
+    _lib.moe_dispatch(p, ws, inp["x"], xe)
+    torch.cuda.synchronize()
+    segs, s = _segments(layer)
+    slot_of = s["slot_of"].reshape(shape.N, shape.k)
+    x = inp["x"]
+    # dispatch: exact copies, zero padding
+    np.testing.assert_array_equal(
+        xe[torch.as_tensor(slot_of.ravel(), device=dev()).long()].view(torch.int16).cpu().numpy(),
+        x.repeat_interleave(shape.k, 0).view(torch.int16).cpu().numpy())
+    for e, r0, c in segs:
+        pad_rows = xe[r0 + c: int(s["pad_offsets"][e + 1])]
+        assert torch.all(pad_rows == 0)
+
+    _lib.moe_expert_gate_up(p, ws, xe, w, g, u, act)
+    _lib.moe_expert_down(p, ws, act, w, ye)
+    torch.cuda.synchronize()
+    wg, wu, wd = (inp[k].float() for k in ("wg", "wu", "wd"))
+    for e, r0, c in segs:
+        if c == 0:
+            continue
+        rows = slice(r0, r0 + c)
+        G = xe[rows].float() @ wg[e].T
+        U = xe[rows].float() @ wu[e].T
+        assert_close(f"G[{e}]", g[rows], G.double().cpu().numpy(), 1e-2)
+        assert_close(f"U[{e}]", u[rows], U.double().cpu().numpy(), 1e-2)
+        A = torch.nn.functional.silu(G) * U
+        assert_close(f"Act[{e}]", act[rows], A.double().cpu().numpy(), 1e-2)
+        Y = act[rows].float() @ wd[e].T
+        assert_close(f"Ye[{e}]", ye[rows], Y.double().cpu().numpy(), 1e-2)
+
+    # combine
+    _lib.moe_combine(p, ws, ye, layer.topk_w, layer.y)
+    torch.cuda.synchronize()
+    sl = torch.as_tensor(slot_of, device=dev()).long()
+    yref = (layer.topk_w.unsqueeze(-1) * ye[sl].float()).sum(1)
+    assert_close("y", layer.y, yref.double().cpu().numpy(), 1e-2)
+
+    # backward phases
+    dy = inp["dy"]
+    dye = torch.empty_like(ye)
+    dye.fill_(3.0)
+    dtw = torch.empty_like(layer.topk_w)
+    _lib.moe_reverse_combine(p, ws, dy, ye, layer.topk_w, dye, dtw)
+    torch.cuda.synchronize()
+    dye_ref = (layer.topk_w.unsqueeze(-1) * dy.float().unsqueeze(1)).bfloat16()
+    assert torch.equal(dye[sl], dye_ref)
+    for e, r0, c in segs:
+        assert torch.all(dye[r0 + c: int(s["pad_offsets"][e + 1])] == 0)
+    dw_ref = (dy.float().unsqueeze(1) * ye[sl].float()).sum(-1)
+    assert_close("d_topk_w", dtw, dw_ref.double().cpu().numpy(), 1e-4)
+
+    dg, du = torch.empty_like(g), torch.empty_like(u)
+    dwd = torch.full((shape.E, shape.H, shape.I), 5.0, device=dev())
+    _lib.moe_expert_down_dgrad(p, ws, dye, g, u, w, dg, du)
+    _lib.moe_expert_down_wgrad(p, ws, dye, act, dwd)
+    torch.cuda.synchronize()
+    for e, r0, c in segs:
+        rows = slice(r0, r0 + c)
+        if c == 0:
+            assert torch.all(dwd[e] == 0)
+            continue
+        dA = dye[rows].float() @ wd[e]
+        G, U = g[rows].float(), u[rows].float()
+        sg = torch.sigmoid(G)
+        assert_close(f"dG[{e}]", dg[rows], (dA * U * sg * (1 + G * (1 - sg))).double().cpu().numpy(), 1e-2)
+        assert_close(f"dU[{e}]", du[rows], (dA * G * sg).double().cpu().numpy(), 1e-2)
+        assert_close(f"dWd[{e}]", dwd[e], (dye[rows].float().T @ act[rows].float()).double().cpu().numpy(), 1e-3)
+
+    dxe = torch.empty_like(xe)
+    dwg = torch.full((shape.E, shape.I, shape.H), 5.0, device=dev())
+    dwu = torch.full_like(dwg, 5.0)
+    _lib.moe_expert_gate_up_dgrad(p, ws, dg, du, w, dxe)
+    _lib.moe_expert_gate_up_wgrad(p, ws, dg, du, xe, dwg, dwu)
+    torch.cuda.synchronize()
+    for e, r0, c in segs:
+        rows = slice(r0, r0 + c)
+        if c == 0:
+            assert torch.all(dwg[e] == 0) and torch.all(dwu[e] == 0)
+            continue
+        ref = dg[rows].float() @ wg[e] + du[rows].float() @ wu[e]
+        assert_close(f"dXe[{e}]", dxe[rows], ref.double().cpu().numpy(), 1e-2)
+        assert_close(f"dWg[{e}]", dwg[e], (dg[rows].float().T @ xe[rows].float()).double().cpu().numpy(), 1e-3)
+        assert_close(f"dWu[{e}]", dwu[e], (du[rows].float().T @ xe[rows].float()).double().cpu().numpy(), 1e-3)
+
+    dx = torch.empty_like(x)
+    _lib.moe_reverse_dispatch(p, ws, dxe, dx)
+    torch.cuda.synchronize()
+    assert_close("dx", dx, dxe[sl].float().sum(1).double().cpu().numpy(), 1e-2)
+    assert layer.device_error() == 0
+
+
+def _oracle_compare(shape, inp_cpu, layer, backward=True):
+    logits = inp_cpu["logits"].numpy()
+    bias = None if inp_cpu["bias"] is None else inp_cpu["bias"].numpy()
+    ids, w = oracle.route_topk(logits, bias, shape.k)
+    np.testing.assert_array_equal(layer.topk_ids.cpu().numpy(), ids)
+    y = oracle.forward_bf16(inp_cpu["x"], inp_cpu["wg"], inp_cpu["wu"], inp_cpu["wd"], ids, w)
+    errs = {"y": assert_close("y", layer.y, y)}
+    if backward:
+        r = oracle.backward_bf16(inp_cpu["x"], inp_cpu["wg"], inp_cpu["wu"], inp_cpu["wd"], ids,
+                                 w, inp_cpu["dy"])
+        g = layer.grads
+        for name, got, key in (("dx", g.dx, "dx"), ("dw_gate", g.dw_gate, "dwg"),
+                               ("dw_up", g.dw_up, "dwu"), ("dw_down", g.dw_down, "dwd"),
+                               ("d_topk_w", g.d_topk_w, "dw")):
+            errs[name] = assert_close(name, got, r[key])
+    return errs
+
+
+LAYER_SHAPES = [
+    inputs.TINY,
+    RAGGED,
+    custom_shape(129, 256, 256, 4, 2, name="one_over_tile"),
+    custom_shape(64, 1024, 512, 32, 8, name="many_empty_experts"),
+]
+
+
+@pytest.mark.parametrize("shape", LAYER_SHAPES, ids=lambda s: s.name)
+def test_layer_matches_oracle(shape):
+    inp = inputs.make_inputs(shape, seed=1, device="cpu")
+    layer = run_layer(shape, to_dev(inp))
+    assert layer.device_error() == 0
+    _oracle_compare(shape, inp, layer)
+
+
+def test_expert_without_tokens_gets_zero_weight_gradient():
+    shape = custom_shape(200, 256, 512, 8, 2, name="forced_empty")
+    inp = inputs.make_inputs(shape, seed=2, device="cpu")
+    inp["bias"] = torch.zeros(8)
+    inp["bias"][[3, 6]] = -1e4  # never selected
+    layer = run_layer(shape, to_dev(inp))
+    g = layer.grads
+    for e in (3, 6):
+        assert torch.all(g.dw_gate[e] == 0) and torch.all(g.dw_up[e] == 0)
+        assert torch.all(g.dw_down[e] == 0)
+    _oracle_compare(shape, inp, layer)
+
+
+def test_identity_experts():
+    """Expert output := expert input. With weights summing to 1 the combine
+    returns x up to one bf16 rounding; the reverse rounds return dy and
+    d_topk_w = <dy, x>."""
+    shape = RAGGED
+    inp, layer = _phase_setup(shape, seed=3)
+    p, ws = layer.p, layer.ws
+    sv = layer.saved_tensors()
+    _lib.moe_dispatch(p, ws, inp["x"], sv["xe"])
+    _lib.moe_combine(p, ws, sv["xe"], layer.topk_w, layer.y)
+    torch.cuda.synchronize()
+    x = inp["x"].float()
+    assert torch.max(torch.abs(layer.y.float() - x)) <= 2.0 ** -7 * torch.max(torch.abs(x))
+    dy = inp["dy"]
+    dye = torch.empty_like(sv["xe"])
+    dtw = torch.empty_like(layer.topk_w)
+    _lib.moe_reverse_combine(p, ws, dy, sv["xe"], layer.topk_w, dye, dtw)
+    dx = torch.empty_like(inp["x"])
+    _lib.moe_reverse_dispatch(p, ws, dye, dx)
+    torch.cuda.synchronize()
+    assert torch.max(torch.abs(dx.float() - dy.float())) <= 2.0 ** -6 * torch.max(torch.abs(dy.float()))
+    ref = (dy.double() * inp["x"].double()).sum(1, keepdim=True).expand(-1, shape.k)
+    assert max_rel(dtw, ref.cpu().numpy()) <= 1e-5
+
+
+def test_reruns_are_bitwise_identical():
+    shape = RAGGED
+    inp = to_dev(inputs.make_inputs(shape, seed=4, device="cpu"))
+    a = run_layer(shape, inp)
+    b = run_layer(shape, inp)
+    assert torch.equal(a.y, b.y)
+    rows = int(a.schedule_tensors()["pad_offsets"][shape.E])
+    for key, t in a.saved_tensors().items():
+        assert torch.equal(t[:rows], b.saved_tensors()[key][:rows]), key
+    for f in ("dx", "dw_gate", "dw_up", "dw_down", "d_topk_w"):
+        assert torch.equal(getattr(a.grads, f), getattr(b.grads, f)), f
