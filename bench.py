@@ -38,7 +38,7 @@ UNIT = "tokens/s"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=None, help="workload name (default: skewed fwd+bwd)")
@@ -85,7 +85,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -135,17 +135,32 @@ def phase_flops(shape):
 def phase_bytes(shape, R):
     """Algorithmic HBM bytes of the data-movement phases."""
     N, A, H, E, k = shape.N, shape.N * shape.k, shape.H, shape.E, shape.k
-    return {"route": 4 * N * E + 8 * N * k, "dispatch": 2 * N * H + 2 * A * H + 4 * A,
+    return {"route": 4 * N * E + 8 * N * k, "schedule": 4 * A + 12 * A + 8 * E,
+            "dispatch": 2 * N * H + 2 * A * H + 4 * A,
             "combine": 2 * A * H + 8 * A + 2 * N * H,
             "reverse_combine": 2 * N * H + 2 * A * H + 8 * A + 2 * A * H + 4 * A,
             "reverse_dispatch": 2 * A * H + 4 * A + 2 * N * H}
+
+
+def workload(name):
+    """A named workload, or "N,H,I,E,k[,zipf_s]" for a profiling case."""
+    from mixture_experts_layer_schedule_gb300 import inputs
+    if not name:
+        return inputs.SKEWED
+    if name in inputs.ALL:
+        return inputs.ALL[name]
+    f = name.split(",")
+    N, H, I, E, k = (int(v) for v in f[:5])
+    z = float(f[5]) if len(f) > 5 else None
+    return inputs.LayerShape(f"custom_N{N}_H{H}_I{I}_E{E}_k{k}" + (f"_zipf{z}" if z else ""),
+                             N, H, I, E, k, zipf_s=z)
 
 
 def run_ours(args, ws_, rank, local):
     import torch
     from mixture_experts_layer_schedule_gb300 import MoELayer, _lib, inputs
 
-    shape = inputs.ALL[args.config] if args.config else inputs.SKEWED
+    shape = workload(args.config)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     inp = inputs.make_inputs(shape, seed=rank, device=dev)
@@ -256,7 +271,7 @@ def run_ours(args, ws_, rank, local):
     peaks = load_peaks()
     fl = phase_flops(shape)
     by = phase_bytes(shape, layer.R)
-    dominant = max(ph_ms, key=ph_ms.get)
+    dominant = max((ph for ph in ph_ms if ph in fl or ph in by), key=ph_ms.get)
     if dominant in fl:
         achieved = fl[dominant] / (ph_ms[dominant] * 1e-3) / 1e12
         roof = {"kernel": dominant, "bound": "tensor", "achieved": round(achieved, 1),
@@ -337,10 +352,9 @@ def run_reference(args, ws_, rank):
     import torch
 
     from mixture_experts_layer_schedule_gb300 import inputs
-    shape = inputs.ALL[args.config] if args.config else inputs.SKEWED
+    shape = workload(args.config)
     threads = os.cpu_count() or 1
-    n_tok = args.cpu_tokens or 32
-    small = shape.with_(N=max(n_tok, 1))
+    n_tok = args.cpu_tokens or 16
     inp = inputs.make_inputs(shape.with_(N=n_tok), seed=0, device="cpu")
     for _ in range(args.warmup):
         cpu_sample(shape, inp, n_tok, threads)
