@@ -129,6 +129,26 @@ moe_status moe_route_topk(const moe_problem* p, const float* logits, const float
 moe_status moe_build_schedule(const moe_problem* p, const int32_t* topk_ids, void* ws,
                               void* stream);
 
+/* Allocation-free variant of moe_build_schedule (the pages have no
+ * counterpart; it exists for callers of this library). For callers that
+ * cannot allocate device memory -- e.g. a plugin whose host application owns
+ * the whole device memory pool, or a loop that must never call the
+ * allocator -- and so cannot provide the scan scratch moe_build_schedule
+ * takes from the workspace. The tables are the same as moe_build_schedule's,
+ * written to the caller's arrays in *out (device pointers, 4-byte aligned):
+ * counts[E], offsets[E+1], pad_offsets[E+1], slot_of[N*k],
+ * src_of_row[moe_grouped_rows(p)], tiles[3 * moe_grouped_rows(p) / 128],
+ * n_tiles[1]; device-detected errors go to *err_word (device int32).
+ * The scratch is a static device array owned by the library: 524288 int32
+ * (2 MiB), held on every device that loads the library until the process
+ * exits. Problems needing more than E * ceil(N*k / 256) = 524288 entries
+ * return MOE_ERR_UNSUPPORTED. Allocates and frees nothing. The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress); make
+ * that first call before any stream capture. Every call shares the array, so
+ * calls whose kernels overlap on the GPU (e.g. on two streams) race. */
+moe_status moe_build_schedule_noalloc(const moe_problem* p, const int32_t* topk_ids,
+                                      const moe_schedule* out, int32_t* err_word, void* stream);
+
 /* ---- forward phases (the ws must hold the schedule of this call) ---- */
 
 /* Dispatch ([Clip] key point 2, pull dispatch; on one GPU an HBM copy):

@@ -59,6 +59,7 @@ _SIGS = {
     "moe_schedule_view": ([c_vp, c_vp, c_vp], c_i32),
     "moe_route_topk": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp], c_i32),
     "moe_build_schedule": ([c_vp, c_vp, c_vp, c_vp], c_i32),
+    "moe_build_schedule_noalloc": ([c_vp, c_vp, c_vp, c_vp, c_vp], c_i32),
     "moe_dispatch": ([c_vp, c_vp, c_vp, c_vp, c_vp], c_i32),
     "moe_expert_gate_up": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp], c_i32),
     "moe_expert_down": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_vp], c_i32),
@@ -174,6 +175,13 @@ def moe_route_topk(p, logits, bias, topk_ids, topk_w, ws, stream=None):
 
 def moe_build_schedule(p, topk_ids, ws, stream=None):
     _call("moe_build_schedule", ctypes.byref(p), _ptr(topk_ids), _ptr(ws), _stream(stream))
+
+
+def moe_build_schedule_noalloc(p, topk_ids, out: Schedule, err_word, stream=None):
+    """Schedule tables into the caller's arrays; scan scratch is a static device
+    array inside the library (no allocation)."""
+    _call("moe_build_schedule_noalloc", ctypes.byref(p), _ptr(topk_ids), ctypes.byref(out),
+          _ptr(err_word), _stream(stream))
 
 
 def moe_dispatch(p, ws, x, xe, stream=None):

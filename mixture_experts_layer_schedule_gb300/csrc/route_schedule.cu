@@ -20,6 +20,7 @@
 #include <float.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "moe_common.cuh"
 #include "moe_internal.h"
@@ -322,3 +323,91 @@ cudaError_t launch_build_schedule(const Layout& L, const int32_t* ids, void* ws,
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Allocation-free schedule build.
+//
+// Some callers cannot allocate device memory at all (for example a plugin
+// whose host application owns the whole device memory pool, or a loop that
+// must never call into the allocator), so they cannot provide the scan
+// scratch that moe_build_schedule takes from the workspace. This entry point
+// keeps that scratch in a library-owned static device array instead; the
+// caller only passes the ids and the output tables.
+//
+// The array is shared by every call on a device and is held until the
+// process exits. Nothing in it needs to start at zero: the count kernel writes
+// every entry that the scan and place kernels read. Calls whose kernels
+// overlap on the GPU (e.g. on two streams) race on the array.
+namespace {
+
+constexpr int64_t kNoAllocScratchInts = int64_t(1) << 19;  // 2 MiB of int32
+__device__ __align__(256) int32_t g_sched_scratch[kNoAllocScratchInts];
+
+constexpr int kMaxDevices = 256;
+std::mutex g_scratch_mu;
+int32_t* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_sched_scratch on the current device. In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (the first call on a device does this) and cached.
+cudaError_t scratch_for_current_device(int32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_sched_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+inline bool ok4(const void* p) {
+  return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3) == 0;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_build_schedule_noalloc(const moe_problem* p, const int32_t* topk_ids,
+                                                 const moe_schedule* out, int32_t* err_word,
+                                                 void* stream) {
+  using namespace moe;
+  Layout L;
+  const moe_status st = make_layout(p, &L);
+  if (st != MOE_OK) return st;
+  if (L.E * std::max<int64_t>(L.n_warps, 1) > kNoAllocScratchInts) return MOE_ERR_UNSUPPORTED;
+  if (!out || !ok4(err_word) || (L.N > 0 && !ok4(topk_ids)) || !ok4(out->counts) ||
+      !ok4(out->offsets) || !ok4(out->pad_offsets) || (L.A > 0 && !ok4(out->slot_of)) ||
+      !ok4(out->src_of_row) || !ok4(out->tiles) || !ok4(out->n_tiles))
+    return MOE_ERR_INVALID_ARG;
+  int32_t* scratch = nullptr;
+  if (scratch_for_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int blocks_w = static_cast<int>((L.n_warps + 7) / 8);
+  const size_t smem_w = sizeof(int32_t) * 8 * L.E;
+  if (L.n_warps > 0) {
+    sched_count_kernel<<<blocks_w, 256, smem_w, s>>>(topk_ids, L.A, L.E, L.n_warps, scratch,
+                                                     err_word);
+    note_launch();
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    sched_scan_kernel<<<L.E, 1024, 0, s>>>(scratch, L.n_warps, out->counts);
+    note_launch();
+  } else if (cudaMemsetAsync(out->counts, 0, sizeof(int32_t) * L.E, s) != cudaSuccess) {
+    return MOE_ERR_CUDA;
+  }
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  sched_final_kernel<<<1, 1024, 0, s>>>(out->counts, L.E, out->offsets, out->pad_offsets,
+                                        out->src_of_row, out->tiles, out->n_tiles);
+  note_launch();
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  if (L.n_warps == 0) return MOE_OK;
+  sched_place_kernel<<<blocks_w, 256, smem_w, s>>>(topk_ids, L.A, L.E, L.n_warps, scratch,
+                                                   out->pad_offsets, out->slot_of,
+                                                   out->src_of_row);
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
