@@ -43,7 +43,10 @@ constexpr int BM = 128, BN = 256, BK = 64, kStages = 4;
 constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kBBytes = BN * BK * 2;  // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+// Epilogue staging for TMA stores: per epilogue warp two 32x32 fp32 blocks.
+constexpr int kStageOutBytes = 32 * 32 * 4;
+constexpr int kOutBytes = 4 * 2 * kStageOutBytes;
+constexpr int kSmemBytes = kStages * kStageBytes + kOutBytes + 1024;  // + alignment slack
 constexpr int kGemmThreads = 192;
 constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
 
@@ -51,6 +54,7 @@ enum Mode { GATE_UP = 0, DOWN = 1, DACT = 2, DXE = 3, WGRAD = 4 };
 
 struct Maps {
   CUtensorMap a0, a1, b0, b1;
+  CUtensorMap o0, o1;  // WGRAD outputs: fp32 [E * M, N], 32x32 boxes, 128-byte swizzle
 };
 
 struct Args {
@@ -259,23 +263,46 @@ __device__ __forceinline__ void epilogue(const Args& a, const TileInfo& ti, uint
         pdu[v] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
       }
     }
-  } else {  // WGRAD: fp32 rows of dW[e]
-    const int64_t M_total = static_cast<int64_t>(a.w_mt) * BM;
-    float* out = static_cast<float*>(ti.prob ? a.out1 : a.out0);
-    const int64_t o = (static_cast<int64_t>(ti.e) * M_total + ti.mt * BM + rit) * a.ld_out + ti.nt * BN;
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t d[32];
-      if (ti.nkb > 0) {
-        tmem_ld32(taddr + c, d);
-        tmem_ld_wait();
-      } else {
+  }
+}
+
+// WGRAD epilogue: fp32 dW[e] rows. Each warp moves its 32 rows x 256 columns
+// in eight 32x32 blocks: TMEM -> registers -> shared staging buffer (the
+// 128-byte swizzle spreads one warp store over all banks) -> one TMA store.
+// Two staging buffers per warp let the store of block i overlap block i+1.
+__device__ __forceinline__ void epilogue_wgrad(const Maps& m, const Args& a, const TileInfo& ti,
+                                               uint32_t tmem_acc, int quad, int lane,
+                                               uint8_t* stage_out, uint32_t& nstore) {
+  const uint32_t taddr = tmem_acc + (static_cast<uint32_t>(quad * 32) << 16);
+  const CUtensorMap* om = ti.prob ? &m.o1 : &m.o0;
+  const int32_t y = ti.e * (a.w_mt * BM) + ti.mt * BM + quad * 32;
+  for (int c = 0; c < BN; c += 32) {
+    uint32_t d[32];
+    if (ti.nkb > 0) {
+      tmem_ld32(taddr + c, d);
+      tmem_ld_wait();
+    } else {
 #pragma unroll
-        for (int q = 0; q < 32; ++q) d[q] = 0u;
-      }
-      uint4* p = reinterpret_cast<uint4*>(out + o + c);
-#pragma unroll
-      for (int v = 0; v < 8; ++v) p[v] = make_uint4(d[4 * v], d[4 * v + 1], d[4 * v + 2], d[4 * v + 3]);
+      for (int q = 0; q < 32; ++q) d[q] = 0u;
     }
+    uint8_t* buf = stage_out + (nstore & 1u) * kStageOutBytes;
+    if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
+    __syncwarp();
+    const uint32_t row = smem_u32(buf) + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t addr = row + ((j ^ (lane & 7)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(d[4 * j]),
+                   "r"(d[4 * j + 1]), "r"(d[4 * j + 2]), "r"(d[4 * j + 3])
+                   : "memory");
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(om, buf, ti.nt * BN + c, y);
+      bulk_commit();
+    }
+    ++nstore;
   }
 }
 
@@ -382,18 +409,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ---------------- epilogue warps 2..5 ----------------
     const int quad = warp & 3;  // TMEM lanes this warp may access
+    uint8_t* stage_out = smem + kStages * kStageBytes + (warp - 2) * 2 * kStageOutBytes;
+    uint32_t nstore = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
       const TileInfo ti = decode_tile<MODE>(args, t);
       if (!mbar_wait(&tfull_bar[acc], acc_phase, abortp, args.err)) break;
       tc_fence_after();
-      if (!ti.skip) epilogue<MODE>(args, ti, tmem_base + acc * BN, quad, lane);
-      else if (lane == 0) set_dev_error(args.err, MOE_DEVERR_BAD_EXPERT);
+      if (ti.skip) {
+        if (lane == 0) set_dev_error(args.err, MOE_DEVERR_BAD_EXPERT);
+      } else if constexpr (MODE == WGRAD) {
+        epilogue_wgrad(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
+      } else {
+        epilogue<MODE>(args, ti, tmem_base + acc * BN, quad, lane);
+      }
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
+    if (lane == 0) bulk_wait_all();  // stores done before the CTA exits
   }
 
   tc_fence_before();
@@ -427,19 +462,28 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 view [outer][inner] (inner contiguous), box 64 x box_outer,
-// 128-byte swizzle. Returns false on failure.
-bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int box_outer) {
+// 2-D view [outer][inner] (inner contiguous) of `elem` bytes per element,
+// box box_inner x box_outer, 128-byte swizzle. Returns false on failure.
+bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int box_outer,
+              int box_inner = 64, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+              int elem = 2) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || outer <= 0 || inner <= 0) return false;
-  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (inner * 2) % 16 != 0) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (inner * elem) % 16 != 0) return false;
+  if (box_inner * elem > 128) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner * 2)};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_outer)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner * elem)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner),
+                             static_cast<cuuint32_t>(box_outer)};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(m, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp32 weight-gradient output [rows][cols] for the WGRAD TMA-store epilogue.
+bool make_out_map(CUtensorMap* m, const float* base, int64_t cols, int64_t rows) {
+  return make_map(m, base, cols, rows, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4);
 }
 
 int sm_count() {
@@ -545,6 +589,8 @@ moe_status gemm_down_wgrad(const Layout& L, const void* ws, const void* dye, con
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
   m.b1 = m.b0;
+  if (!make_out_map(&m.o0, dw_down, L.I, static_cast<int64_t>(L.E) * L.H)) return MOE_ERR_CUDA;
+  m.o1 = m.o0;
   Args a = base_args(L, ws);
   a.w_mt = L.H / BM;
   a.w_nt = L.I / BN;
@@ -579,6 +625,9 @@ moe_status gemm_gate_up_wgrad(const Layout& L, const void* ws, const void* dg, c
       !make_map(&m.b0, xe, L.H, L.R, 64))
     return MOE_ERR_CUDA;
   m.b1 = m.b0;
+  if (!make_out_map(&m.o0, dw_gate, L.H, static_cast<int64_t>(L.E) * L.I) ||
+      !make_out_map(&m.o1, dw_up, L.H, static_cast<int64_t>(L.E) * L.I))
+    return MOE_ERR_CUDA;
   Args a = base_args(L, ws);
   a.w_mt = L.I / BM;
   a.w_nt = L.H / BN;
