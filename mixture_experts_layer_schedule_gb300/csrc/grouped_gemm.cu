@@ -61,6 +61,7 @@ struct Args {
   const int32_t* tiles;        // [n][3] (expert, row0, valid) of the 128-row tiles
   const int32_t* n_tiles;      // device count of those tiles
   const int32_t* pad_offsets;  // [E+1] padded segment starts (WGRAD K ranges)
+  const int32_t* order;        // [E] experts by descending padded row count (WGRAD)
   int32_t* err;
   int max_mtiles;              // host bound on *n_tiles (R / 128)
   int64_t rows;                // rows of the expert-grouped buffers (R)
@@ -93,13 +94,19 @@ template <int MODE>
 __device__ __forceinline__ TileInfo decode_tile(const Args& a, int64_t t) {
   TileInfo ti;
   if constexpr (MODE == WGRAD) {
-    const int64_t per_prob = static_cast<int64_t>(a.E) * a.w_mt * a.w_nt;
-    ti.prob = static_cast<int>(t / per_prob);
-    int64_t r = t % per_prob;
-    ti.e = static_cast<int>(r / (a.w_mt * a.w_nt));
-    r %= (a.w_mt * a.w_nt);
-    ti.mt = static_cast<int>(r / a.w_nt);
-    ti.nt = static_cast<int>(r % a.w_nt);
+    // Largest experts first, so the CTAs that stream one expert's long K
+    // panels start together and share them through L2; within an expert,
+    // (mt, nt, problem) with the problem fastest, so dWg and dWu tiles that
+    // read the same Xe panel run side by side.
+    const int64_t per_e = static_cast<int64_t>(a.w_mt) * a.w_nt * a.n_probs;
+    const int rank = static_cast<int>(t / per_e);
+    int64_t r = t % per_e;
+    ti.mt = static_cast<int>(r / (a.w_nt * a.n_probs));
+    r %= (a.w_nt * a.n_probs);
+    ti.nt = static_cast<int>(r / a.n_probs);
+    ti.prob = static_cast<int>(r % a.n_probs);
+    ti.e = a.order[rank];
+    if (ti.e < 0 || ti.e >= a.E) ti.e = 0;
     ti.kstart = a.pad_offsets[ti.e];
     ti.nkb = (a.pad_offsets[ti.e + 1] - ti.kstart) / BK;
     ti.row0 = 0;
@@ -440,6 +447,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+// Experts ranked by padded row count, descending; equal counts keep ascending
+// expert index. One CTA; each thread ranks its experts against all others.
+__global__ void __launch_bounds__(1024) expert_order_kernel(const int32_t* __restrict__ pad_offsets,
+                                                            int E, int32_t* __restrict__ order) {
+  __shared__ int32_t cnt[kMaxE];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = pad_offsets[e + 1] - pad_offsets[e];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int32_t c = cnt[e];
+    int rank = 0;
+    for (int f = 0; f < E; ++f) rank += (cnt[f] > c) || (cnt[f] == c && f < e);
+    order[rank] = e;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Host side: tensor maps and launches.
 
@@ -509,11 +531,19 @@ moe_status launch(const Maps& maps, const Args& args, int64_t tiles_upper, cudaS
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+moe_status launch_expert_order(const Layout& L, const void* ws, cudaStream_t s) {
+  expert_order_kernel<<<1, 1024, 0, s>>>(at<int32_t>(ws, L.pad_offsets), L.E,
+                                         const_cast<int32_t*>(at<int32_t>(ws, L.expert_order)));
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 Args base_args(const Layout& L, const void* ws) {
   Args a{};
   a.tiles = at<int32_t>(ws, L.tiles);
   a.n_tiles = at<int32_t>(ws, L.n_tiles);
   a.pad_offsets = at<int32_t>(ws, L.pad_offsets);
+  a.order = at<int32_t>(ws, L.expert_order);
   a.err = const_cast<int32_t*>(at<int32_t>(ws, L.err));
   a.max_mtiles = static_cast<int>(L.R / BM);
   a.rows = L.R;
@@ -592,6 +622,7 @@ moe_status gemm_down_wgrad(const Layout& L, const void* ws, const void* dye, con
   if (!make_out_map(&m.o0, dw_down, L.I, static_cast<int64_t>(L.E) * L.H)) return MOE_ERR_CUDA;
   m.o1 = m.o0;
   Args a = base_args(L, ws);
+  if (launch_expert_order(L, ws, s) != MOE_OK) return MOE_ERR_CUDA;
   a.w_mt = L.H / BM;
   a.w_nt = L.I / BN;
   a.n_probs = 1;
@@ -629,6 +660,7 @@ moe_status gemm_gate_up_wgrad(const Layout& L, const void* ws, const void* dg, c
       !make_out_map(&m.o1, dw_up, L.H, static_cast<int64_t>(L.E) * L.I))
     return MOE_ERR_CUDA;
   Args a = base_args(L, ws);
+  if (launch_expert_order(L, ws, s) != MOE_OK) return MOE_ERR_CUDA;
   a.w_mt = L.I / BM;
   a.w_nt = L.H / BN;
   a.n_probs = 2;

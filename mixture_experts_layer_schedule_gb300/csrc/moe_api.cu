@@ -51,6 +51,7 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   L->tiles = take(sizeof(int32_t) * 3 * (R / kTileM));
   L->n_tiles = take(sizeof(int32_t));
   L->warp_counts = take(sizeof(int32_t) * p->E * std::max<int64_t>(L->n_warps, 1));
+  L->expert_order = take(sizeof(int32_t) * p->E);
   L->dyxe = take(static_cast<size_t>(R) * p->H * 2);
   L->dg = take(static_cast<size_t>(R) * p->I * 2);
   L->du = take(static_cast<size_t>(R) * p->I * 2);

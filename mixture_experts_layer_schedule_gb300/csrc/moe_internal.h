@@ -23,6 +23,7 @@ struct Layout {
   int64_t n_warps;        // schedule warps = ceil(A / kSchedSub)
   // workspace byte offsets
   size_t err, counts, offsets, pad_offsets, slot_of, src_of_row, tiles, n_tiles, warp_counts,
+      expert_order,
       dyxe, dg, du, ws_bytes;
   // forward-context byte offsets
   size_t xe, g, u, act, ye, saved_bytes;
