@@ -90,18 +90,24 @@ struct TileInfo {
   bool skip;
 };
 
-template <int MODE>
-__device__ __forceinline__ TileInfo decode_tile(const Args& a, int64_t t) {
+// Tile t of this CTA. With CL = 2 (a cluster of two CTAs), t numbers pair
+// tiles and `crank` (the CTA's rank in the cluster) picks the member: the
+// two members share the A tile (token-row modes: neighbouring N tiles) or the
+// B tile (WGRAD: neighbouring M tiles), which they load once, half each,
+// multicast to both.
+template <int MODE, int CL>
+__device__ __forceinline__ TileInfo decode_tile(const Args& a, int64_t t, int crank) {
   TileInfo ti;
   if constexpr (MODE == WGRAD) {
     // Largest experts first, so the CTAs that stream one expert's long K
     // panels start together and share them through L2; within an expert,
     // (mt, nt, problem) with the problem fastest, so dWg and dWu tiles that
     // read the same Xe panel run side by side.
-    const int64_t per_e = static_cast<int64_t>(a.w_mt) * a.w_nt * a.n_probs;
+    const int w_mtp = a.w_mt / CL;
+    const int64_t per_e = static_cast<int64_t>(w_mtp) * a.w_nt * a.n_probs;
     const int rank = static_cast<int>(t / per_e);
     int64_t r = t % per_e;
-    ti.mt = static_cast<int>(r / (a.w_nt * a.n_probs));
+    ti.mt = static_cast<int>(r / (a.w_nt * a.n_probs)) * CL + crank;
     r %= (a.w_nt * a.n_probs);
     ti.nt = static_cast<int>(r / a.n_probs);
     ti.prob = static_cast<int>(r % a.n_probs);
@@ -116,8 +122,9 @@ __device__ __forceinline__ TileInfo decode_tile(const Args& a, int64_t t) {
       ti.skip = true;
     }
   } else {
-    const int mtile = static_cast<int>(t / a.n_nt);
-    ti.nt = static_cast<int>(t % a.n_nt);
+    const int n_ntp = a.n_nt / CL;
+    const int mtile = static_cast<int>(t / n_ntp);
+    ti.nt = static_cast<int>(t % n_ntp) * CL + crank;
     ti.mt = mtile;
     ti.e = a.tiles[3 * mtile + 0];
     ti.row0 = a.tiles[3 * mtile + 1];
@@ -135,32 +142,45 @@ __device__ __forceinline__ TileInfo decode_tile(const Args& a, int64_t t) {
   return ti;
 }
 
-template <int MODE>
+template <int MODE, int CL>
 __device__ __forceinline__ int64_t total_tiles(const Args& a) {
   if constexpr (MODE == WGRAD) {
-    return static_cast<int64_t>(a.n_probs) * a.E * a.w_mt * a.w_nt;
+    return static_cast<int64_t>(a.n_probs) * a.E * (a.w_mt / CL) * a.w_nt;
   } else {
     int n = *a.n_tiles;
     n = n < 0 ? 0 : (n > a.max_mtiles ? a.max_mtiles : n);
-    return static_cast<int64_t>(n) * a.n_nt;
+    return static_cast<int64_t>(n) * (a.n_nt / CL);
   }
 }
 
-template <int MODE>
+// The A tile of the token-row modes: whole (CL = 1) or this CTA's 64-row half,
+// multicast to both CTAs of the pair (CL = 2; the map's box is then 64 rows).
+template <int CL>
+__device__ __forceinline__ void load_a_rows(uint8_t* sA, const CUtensorMap* ma, uint64_t* bar,
+                                            int k0, int row0, int crank) {
+  if constexpr (CL == 1) {
+    tma_load_2d(sA, ma, bar, k0, row0);
+  } else {
+    tma_load_2d_mc(sA + crank * (kABytes / 2), ma, bar, k0, row0 + crank * (BM / 2), 0x3);
+  }
+}
+
+template <int MODE, int CL>
 __device__ __forceinline__ void issue_loads(const Maps& m, const Args& a, const TileInfo& ti,
-                                            int kb, uint8_t* sA, uint8_t* sB, uint64_t* bar) {
+                                            int kb, uint8_t* sA, uint8_t* sB, uint64_t* bar,
+                                            int crank) {
   if constexpr (MODE == GATE_UP) {
-    tma_load_2d(sA, &m.a0, bar, kb * BK, ti.row0);
+    load_a_rows<CL>(sA, &m.a0, bar, kb * BK, ti.row0, crank);
     const int brow = ti.e * a.b_rows + ti.nt * (BN / 2);
     tma_load_2d(sB, &m.b0, bar, kb * BK, brow);
     tma_load_2d(sB + kBBytes / 2, &m.b1, bar, kb * BK, brow);
   } else if constexpr (MODE == DOWN) {
-    tma_load_2d(sA, &m.a0, bar, kb * BK, ti.row0);
+    load_a_rows<CL>(sA, &m.a0, bar, kb * BK, ti.row0, crank);
     tma_load_2d(sB, &m.b0, bar, kb * BK, ti.e * a.b_rows + ti.nt * BN);
   } else if constexpr (MODE == DACT || MODE == DXE) {
     const bool second = (MODE == DXE) && kb >= a.kb1;
     const int kk = second ? kb - a.kb1 : kb;
-    tma_load_2d(sA, second ? &m.a1 : &m.a0, bar, kk * BK, ti.row0);
+    load_a_rows<CL>(sA, second ? &m.a1 : &m.a0, bar, kk * BK, ti.row0, crank);
     const CUtensorMap* mb = second ? &m.b1 : &m.b0;
 #pragma unroll
     for (int c = 0; c < BN / 64; ++c)
@@ -172,9 +192,17 @@ __device__ __forceinline__ void issue_loads(const Maps& m, const Args& a, const 
 #pragma unroll
     for (int c = 0; c < BM / 64; ++c)
       tma_load_2d(sA + c * (64 * BK * 2), ma, bar, ti.mt * BM + c * 64, krow);
+    if constexpr (CL == 1) {
 #pragma unroll
-    for (int c = 0; c < BN / 64; ++c)
-      tma_load_2d(sB + c * (64 * BK * 2), mb, bar, ti.nt * BN + c * 64, krow);
+      for (int c = 0; c < BN / 64; ++c)
+        tma_load_2d(sB + c * (64 * BK * 2), mb, bar, ti.nt * BN + c * 64, krow);
+    } else {  // the pair shares this B tile: two of its four 64-column chunks each
+#pragma unroll
+      for (int h = 0; h < BN / 128; ++h) {
+        const int c = crank * (BN / 128) + h;
+        tma_load_2d_mc(sB + c * (64 * BK * 2), mb, bar, ti.nt * BN + c * 64, krow, 0x3);
+      }
+    }
   }
 }
 
@@ -313,7 +341,7 @@ __device__ __forceinline__ void epilogue_wgrad(const Maps& m, const Args& a, con
   }
 }
 
-template <int MODE>
+template <int MODE, int CL>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ Maps maps, const Args args) {
   extern __shared__ uint8_t smem_raw[];
@@ -327,7 +355,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], CL);  // both CTAs of a pair must have read the stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
@@ -347,10 +375,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CL > 1) cluster_sync();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_slot;
   volatile int* abortp = &abort_flag;
-  const int64_t total = total_tiles<MODE>(args);
+  const int64_t total = total_tiles<MODE, CL>(args);
+  const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int64_t first = blockIdx.x / CL, stride = gridDim.x / CL;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -359,13 +390,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile<MODE>(args, t);
+      for (int64_t t = first; t < total && ok; t += stride) {
+        const TileInfo ti = decode_tile<MODE, CL>(args, t, crank);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, args.err)) { ok = false; break; }
           uint8_t* sA = smem + stage * kStageBytes;
           mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
-          issue_loads<MODE>(maps, args, ti, kb, sA, sA + kABytes, &full_bar[stage]);
+          issue_loads<MODE, CL>(maps, args, ti, kb, sA, sA + kABytes, &full_bar[stage], crank);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -384,8 +415,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile<MODE>(args, t);
+      for (int64_t t = first; t < total && ok; t += stride) {
+        const TileInfo ti = decode_tile<MODE, CL>(args, t, crank);
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abortp, args.err)) break;
         tc_fence_after();
         const uint32_t dtmem = tmem_base + acc * BN;
@@ -403,7 +434,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             else bd = sdesc_sw128(b_addr + ks * 32, 16, 1024);
             umma_bf16(dtmem, ad, bd, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
           }
-          umma_commit(&empty_bar[stage]);  // stage free once these MMAs retire
+          if constexpr (CL == 1) umma_commit(&empty_bar[stage]);  // stage free once read
+          else umma_commit_mc(&empty_bar[stage], 0x3);          // ... in both CTAs' view
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -420,8 +452,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t nstore = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
-      const TileInfo ti = decode_tile<MODE>(args, t);
+    for (int64_t t = first; t < total; t += stride) {
+      const TileInfo ti = decode_tile<MODE, CL>(args, t, crank);
       if (!mbar_wait(&tfull_bar[acc], acc_phase, abortp, args.err)) break;
       tc_fence_after();
       if (ti.skip) {
@@ -445,6 +477,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  if constexpr (CL > 1) cluster_sync();  // no CTA leaves while its peer may still write to it
 }
 
 // Experts ranked by padded row count, descending; equal counts keep ascending
@@ -515,20 +548,65 @@ int sm_count() {
   return n > 0 ? n : 148;
 }
 
-template <int MODE>
-moe_status launch(const Maps& maps, const Args& args, int64_t tiles_upper, cudaStream_t s) {
+// Launch a persistent grid: one CTA per SM (CL = 1), or as many co-resident
+// CTA pairs as the GPU holds (CL = 2, clusters of two), capped by the work
+// units (tiles, or pair tiles) available.
+template <int MODE, int CL>
+moe_status launch(const Maps& maps, const Args& args, int64_t units, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+    attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, CL>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (attr_err == cudaSuccess && CL > 1) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = CL;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(CL * 64);
+      cfg.blockDim = dim3(kGemmThreads);
+      cfg.dynamicSmemBytes = kSmemBytes;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_kernel<MODE, CL>, &cfg);
+      if (attr_err == cudaSuccess && max_clusters <= 0) attr_err = cudaErrorInvalidConfiguration;
+    }
   });
   if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
-  if (tiles_upper <= 0) return MOE_OK;
-  const int grid = static_cast<int>(std::min<int64_t>(sm_count(), tiles_upper));
-  grouped_gemm_kernel<MODE><<<grid, kGemmThreads, kSmemBytes, s>>>(maps, args);
+  if (units <= 0) return MOE_OK;
+  if constexpr (CL == 1) {
+    const int grid = static_cast<int>(std::min<int64_t>(sm_count(), units));
+    grouped_gemm_kernel<MODE, 1><<<grid, kGemmThreads, kSmemBytes, s>>>(maps, args);
+  } else {
+    const int clusters = static_cast<int>(std::min<int64_t>(max_clusters, units));
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = CL;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(CL * clusters);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, CL>, maps, args) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Token-row modes pair neighbouring N tiles when their count is even.
+template <int MODE>
+moe_status launch_rows(const Maps& maps, const Args& args, cudaStream_t s) {
+  if (args.n_nt % 2 == 0)
+    return launch<MODE, 2>(maps, args, static_cast<int64_t>(args.max_mtiles) * (args.n_nt / 2), s);
+  return launch<MODE, 1>(maps, args, static_cast<int64_t>(args.max_mtiles) * args.n_nt, s);
 }
 
 moe_status launch_expert_order(const Layout& L, const void* ws, cudaStream_t s) {
@@ -537,6 +615,10 @@ moe_status launch_expert_order(const Layout& L, const void* ws, cudaStream_t s) 
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
+
+// Rows of the A box of the token-row modes: the whole 128-row tile, or the
+// 64-row half each CTA of a pair loads when the N-tile count allows pairing.
+int a_box_rows(int n_nt) { return n_nt % 2 == 0 ? BM / 2 : BM; }
 
 Args base_args(const Layout& L, const void* ws) {
   Args a{};
@@ -556,7 +638,7 @@ Args base_args(const Layout& L, const void* ws) {
 moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const void* wg,
                         const void* wu, void* g, void* u, void* act, cudaStream_t s) {
   Maps m{};
-  if (!make_map(&m.a0, xe, L.H, L.R, BM) ||
+  if (!make_map(&m.a0, xe, L.H, L.R, a_box_rows(L.I / (BN / 2))) ||
       !make_map(&m.b0, wg, L.H, static_cast<int64_t>(L.E) * L.I, BN / 2) ||
       !make_map(&m.b1, wu, L.H, static_cast<int64_t>(L.E) * L.I, BN / 2))
     return MOE_ERR_CUDA;
@@ -570,13 +652,13 @@ moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const v
   a.out0 = g;
   a.out1 = u;
   a.out2 = act;
-  return launch<GATE_UP>(m, a, static_cast<int64_t>(a.max_mtiles) * a.n_nt, s);
+  return launch_rows<GATE_UP>(m, a, s);
 }
 
 moe_status gemm_down(const Layout& L, const void* ws, const void* act, const void* wd, void* ye,
                      cudaStream_t s) {
   Maps m{};
-  if (!make_map(&m.a0, act, L.I, L.R, BM) ||
+  if (!make_map(&m.a0, act, L.I, L.R, a_box_rows(L.H / BN)) ||
       !make_map(&m.b0, wd, L.I, static_cast<int64_t>(L.E) * L.H, BN))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
@@ -588,13 +670,13 @@ moe_status gemm_down(const Layout& L, const void* ws, const void* act, const voi
   a.b_rows = L.H;
   a.ld_out = L.H;
   a.out0 = ye;
-  return launch<DOWN>(m, a, static_cast<int64_t>(a.max_mtiles) * a.n_nt, s);
+  return launch_rows<DOWN>(m, a, s);
 }
 
 moe_status gemm_down_dgrad(const Layout& L, const void* ws, const void* dye, const void* g,
                            const void* u, const void* wd, void* dg, void* du, cudaStream_t s) {
   Maps m{};
-  if (!make_map(&m.a0, dye, L.H, L.R, BM) ||
+  if (!make_map(&m.a0, dye, L.H, L.R, a_box_rows(L.I / BN)) ||
       !make_map(&m.b0, wd, L.I, static_cast<int64_t>(L.E) * L.H, 64))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
@@ -609,7 +691,7 @@ moe_status gemm_down_dgrad(const Layout& L, const void* ws, const void* dye, con
   a.out1 = du;
   a.in0 = g;
   a.in1 = u;
-  return launch<DACT>(m, a, static_cast<int64_t>(a.max_mtiles) * a.n_nt, s);
+  return launch_rows<DACT>(m, a, s);
 }
 
 moe_status gemm_down_wgrad(const Layout& L, const void* ws, const void* dye, const void* act,
@@ -629,13 +711,14 @@ moe_status gemm_down_wgrad(const Layout& L, const void* ws, const void* dye, con
   a.ld_out = L.I;
   a.out0 = dw_down;
   a.out1 = dw_down;
-  return launch<WGRAD>(m, a, static_cast<int64_t>(L.E) * a.w_mt * a.w_nt, s);
+  return launch<WGRAD, 2>(m, a, static_cast<int64_t>(L.E) * (a.w_mt / 2) * a.w_nt, s);
 }
 
 moe_status gemm_gate_up_dgrad(const Layout& L, const void* ws, const void* dg, const void* du,
                               const void* wg, const void* wu, void* dxe, cudaStream_t s) {
   Maps m{};
-  if (!make_map(&m.a0, dg, L.I, L.R, BM) || !make_map(&m.a1, du, L.I, L.R, BM) ||
+  if (!make_map(&m.a0, dg, L.I, L.R, a_box_rows(L.H / BN)) ||
+      !make_map(&m.a1, du, L.I, L.R, a_box_rows(L.H / BN)) ||
       !make_map(&m.b0, wg, L.H, static_cast<int64_t>(L.E) * L.I, 64) ||
       !make_map(&m.b1, wu, L.H, static_cast<int64_t>(L.E) * L.I, 64))
     return MOE_ERR_CUDA;
@@ -646,7 +729,7 @@ moe_status gemm_gate_up_dgrad(const Layout& L, const void* ws, const void* dg, c
   a.b_rows = L.I;
   a.ld_out = L.H;
   a.out0 = dxe;
-  return launch<DXE>(m, a, static_cast<int64_t>(a.max_mtiles) * a.n_nt, s);
+  return launch_rows<DXE>(m, a, s);
 }
 
 moe_status gemm_gate_up_wgrad(const Layout& L, const void* ws, const void* dg, const void* du,
@@ -667,7 +750,7 @@ moe_status gemm_gate_up_wgrad(const Layout& L, const void* ws, const void* dg, c
   a.ld_out = L.H;
   a.out0 = dw_gate;
   a.out1 = dw_up;
-  return launch<WGRAD>(m, a, 2LL * L.E * a.w_mt * a.w_nt, s);
+  return launch<WGRAD, 2>(m, a, 2LL * L.E * (a.w_mt / 2) * a.w_nt, s);
 }
 
 }  // namespace moe
