@@ -480,6 +480,182 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if constexpr (CL > 1) cluster_sync();  // no CTA leaves while its peer may still write to it
 }
 
+// ---------------------------------------------------------------------------
+// SM-pair variant (tcgen05 cta_group::2), used for the weight gradients.
+//
+// Two CTAs of a cluster compute one 256 x 256 tile of dW[e] with a single MMA
+// stream issued by the even CTA: each CTA stages its own 128 A rows and its
+// half (128 columns) of the shared B tile, so a k-block costs each SM 32 KB
+// of shared-memory fill instead of 48 KB for the same tensor-core work, and
+// six stages fit. D rows land in each CTA's own TMEM and each CTA runs its
+// own epilogue. Barriers: the even CTA's full[s] counts both CTAs' bytes (the
+// odd CTA's copies signal it across the pair); the MMA commits arrive on both
+// CTAs' empty[s] and tfull[a]; the odd CTA's epilogue releases the
+// accumulator with a remote arrive on the even CTA's tempty[a].
+constexpr int kPairStages = 6;
+constexpr int kPairABytes = BM * BK * 2;        // 16 KB: this CTA's 128 A rows
+constexpr int kPairBBytes = (BN / 2) * BK * 2;  // 16 KB: this CTA's 128 B columns
+constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
+constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + kOutBytes + 1024;
+
+template <int MODE>
+__device__ __forceinline__ void issue_loads_pair(const Maps& m, const TileInfo& ti, int kb,
+                                                 uint8_t* sA, uint8_t* sB, uint32_t bar,
+                                                 int crank) {
+  static_assert(MODE == WGRAD, "SM-pair loads are defined for the weight gradients");
+  const CUtensorMap* ma = ti.prob ? &m.a1 : &m.a0;
+  const CUtensorMap* mb = ti.prob ? &m.b1 : &m.b0;
+  const int krow = ti.kstart + kb * BK;
+#pragma unroll
+  for (int c = 0; c < BM / 64; ++c)
+    tma_load_2d_pair(sA + c * (64 * BK * 2), ma, bar, ti.mt * BM + c * 64, krow);
+#pragma unroll
+  for (int c = 0; c < BN / 128; ++c)
+    tma_load_2d_pair(sB + c * (64 * BK * 2), mb, bar, ti.nt * BN + crank * (BN / 2) + c * 64,
+                     krow);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ Maps maps, const Args args) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[kPairStages], empty_bar[kPairStages], tfull_bar[2], tempty_bar[2],
+      drain_bar;
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ int abort_flag;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int crank = static_cast<int>(cluster_ctarank());
+  const bool leader = crank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 8);  // one arrive per epilogue warp of both CTAs
+    }
+    mbar_init(&drain_bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.a0);
+    tma_prefetch_desc(&maps.b0);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&tmem_base_slot, kTmemCols);  // one warp of each CTA, collectively
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_slot;
+  volatile int* abortp = &abort_flag;
+  const int64_t total = total_tiles<MODE, 2>(args);
+  const int64_t first = blockIdx.x / 2, stride = gridDim.x / 2;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs) ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      for (int64_t t = first; t < total && ok; t += stride) {
+        const TileInfo ti = decode_tile<MODE, 2>(args, t, crank);
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, args.err)) { ok = false; break; }
+          uint8_t* sA = smem + stage * kPairStageBytes;
+          if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
+          issue_loads_pair<MODE>(maps, ti, kb, sA, sA + kPairABytes,
+                                 cluster_addr(&full_bar[stage], 0), crank);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (leader)  // the even CTA's full barriers count both CTAs' copies
+        for (int s = 0; s < kPairStages; ++s)
+          if ((issued_mask >> s) & 1u) wait_drain(&full_bar[s], (issued_parity >> s) & 1u, args.err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (even CTA only) ----------------
+      constexpr uint32_t idesc = idesc_bf16(2 * BM, BN, Traits<MODE>::a_mn, Traits<MODE>::b_mn);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int64_t t = first; t < total && ok; t += stride) {
+        const TileInfo ti = decode_tile<MODE, 2>(args, t, crank);
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abortp, args.err)) break;
+        tc_fence_after();
+        const uint32_t dtmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abortp, args.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * kPairStageBytes);
+          const uint32_t b_addr = a_addr + kPairABytes;
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks) {
+            const uint64_t ad = sdesc_sw128(a_addr + ks * 2048, 64 * BK * 2, 1024);
+            const uint64_t bd = sdesc_sw128(b_addr + ks * 2048, 64 * BK * 2, 1024);
+            umma_bf16_pair(dtmem, ad, bd, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit_pair_mc(&empty_bar[stage], 0x3);  // both CTAs may refill the stage
+          if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(&tfull_bar[acc], 0x3);  // both halves of the tile are ready
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      umma_commit_pair(&drain_bar);
+      wait_drain(&drain_bar, 0, args.err);
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 (both CTAs) ----------------
+    const int quad = warp & 3;
+    uint8_t* stage_out = smem + kPairStages * kPairStageBytes + (warp - 2) * 2 * kStageOutBytes;
+    uint32_t nstore = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int64_t t = first; t < total; t += stride) {
+      const TileInfo ti = decode_tile<MODE, 2>(args, t, crank);
+      if (!mbar_wait(&tfull_bar[acc], acc_phase, abortp, args.err)) break;
+      tc_fence_after();
+      if (ti.skip) {
+        if (lane == 0) set_dev_error(args.err, MOE_DEVERR_BAD_EXPERT);
+      } else {
+        epilogue_wgrad(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&tempty_bar[acc]);
+        else mbar_arrive_cluster(cluster_addr(&tempty_bar[acc], 0));
+      }
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the even CTA's MMAs into this CTA's TMEM have retired
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+  cluster_sync();  // no CTA leaves while its peer may still signal it
+}
+
 // Experts ranked by padded row count, descending; equal counts keep ascending
 // expert index. One CTA; each thread ranks its experts against all others.
 __global__ void __launch_bounds__(1024) expert_order_kernel(const int32_t* __restrict__ pad_offsets,
@@ -601,6 +777,44 @@ moe_status launch(const Maps& maps, const Args& args, int64_t units, cudaStream_
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+template <int MODE>
+moe_status launch_pair(const Maps& maps, const Args& args, int64_t units, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;
+  auto config = [](cudaLaunchConfig_t& cfg, cudaLaunchAttribute* at, int clusters) {
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = kPairSmemBytes;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+  };
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<MODE>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+    if (attr_err != cudaSuccess) return;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    config(cfg, at, 64);
+    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_pair_kernel<MODE>, &cfg);
+    if (attr_err == cudaSuccess && max_clusters <= 0) attr_err = cudaErrorInvalidConfiguration;
+  });
+  if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
+  if (units <= 0) return MOE_OK;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  config(cfg, at, static_cast<int>(std::min<int64_t>(max_clusters, units)));
+  cfg.stream = s;
+  if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, maps, args) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 // Token-row modes pair neighbouring N tiles when their count is even.
 template <int MODE>
 moe_status launch_rows(const Maps& maps, const Args& args, cudaStream_t s) {
@@ -711,7 +925,7 @@ moe_status gemm_down_wgrad(const Layout& L, const void* ws, const void* dye, con
   a.ld_out = L.I;
   a.out0 = dw_down;
   a.out1 = dw_down;
-  return launch<WGRAD, 2>(m, a, static_cast<int64_t>(L.E) * (a.w_mt / 2) * a.w_nt, s);
+  return launch_pair<WGRAD>(m, a, static_cast<int64_t>(L.E) * (a.w_mt / 2) * a.w_nt, s);
 }
 
 moe_status gemm_gate_up_dgrad(const Layout& L, const void* ws, const void* dg, const void* du,
@@ -750,7 +964,7 @@ moe_status gemm_gate_up_wgrad(const Layout& L, const void* ws, const void* dg, c
   a.ld_out = L.H;
   a.out0 = dw_gate;
   a.out1 = dw_up;
-  return launch<WGRAD, 2>(m, a, 2LL * L.E * (a.w_mt / 2) * a.w_nt, s);
+  return launch_pair<WGRAD>(m, a, 2LL * L.E * (a.w_mt / 2) * a.w_nt, s);
 }
 
 }  // namespace moe
