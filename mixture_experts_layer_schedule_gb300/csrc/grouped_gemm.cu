@@ -498,6 +498,32 @@ constexpr int kPairBBytes = (BN / 2) * BK * 2;  // 16 KB: this CTA's 128 B colum
 constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
 constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + kOutBytes + 1024;
 
+// Order in which one CTA (pair) visits the size-ordered WGRAD tiles: it
+// alternates between the front of the list (largest experts, long K: tensor
+// work) and the back (smallest experts, short K: mostly fp32 output stores), so
+// the two kinds of tile overlap instead of the store-bound tail running alone.
+// Front tiles are still visited in list order by all CTAs together, which
+// keeps the CTAs on one large expert in step for L2 reuse.
+struct TileSeq {
+  int64_t fi, bi, half, total, stride;
+  int turn;
+  __device__ __forceinline__ TileSeq(int64_t first, int64_t stride_, int64_t total_)
+      : fi(first), bi(first), half((total_ + 1) / 2), total(total_), stride(stride_), turn(0) {}
+  __device__ __forceinline__ bool next(int64_t& t) {
+    const bool f_ok = fi < half, b_ok = bi < total - half;
+    if (!f_ok && !b_ok) return false;
+    if ((turn == 0 && f_ok) || !b_ok) {
+      t = fi;
+      fi += stride;
+    } else {
+      t = total - 1 - bi;
+      bi += stride;
+    }
+    turn ^= 1;
+    return true;
+  }
+};
+
 template <int MODE>
 __device__ __forceinline__ void issue_loads_pair(const Maps& m, const TileInfo& ti, int kb,
                                                  uint8_t* sA, uint8_t* sB, uint32_t bar,
@@ -566,7 +592,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;
       bool ok = true;
-      for (int64_t t = first; t < total && ok; t += stride) {
+      int64_t t;
+      for (TileSeq q(first, stride, total); ok && q.next(t);) {
         const TileInfo ti = decode_tile<MODE, 2>(args, t, crank);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, args.err)) { ok = false; break; }
@@ -592,7 +619,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int64_t t = first; t < total && ok; t += stride) {
+      int64_t t;
+      for (TileSeq q(first, stride, total); ok && q.next(t);) {
         const TileInfo ti = decode_tile<MODE, 2>(args, t, crank);
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abortp, args.err)) break;
         tc_fence_after();
@@ -625,7 +653,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t nstore = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t t = first; t < total; t += stride) {
+    int64_t t;
+    for (TileSeq q(first, stride, total); q.next(t);) {
       const TileInfo ti = decode_tile<MODE, 2>(args, t, crank);
       if (!mbar_wait(&tfull_bar[acc], acc_phase, abortp, args.err)) break;
       tc_fence_after();
