@@ -178,10 +178,13 @@ def workload(name):
     if name in inputs.ALL:
         return inputs.ALL[name]
     f = name.split(",")
+    T = 128
+    if f[-1].startswith("T="):
+        T = int(f.pop()[2:])
     N, H, I, E, k = (int(v) for v in f[:5])
-    z = float(f[5]) if len(f) > 5 else None
-    return inputs.LayerShape(f"custom_N{N}_H{H}_I{I}_E{E}_k{k}" + (f"_zipf{z}" if z else ""),
-                             N, H, I, E, k, zipf_s=z)
+    z = float(f[5]) if len(f) > 5 and float(f[5]) > 0 else None
+    return inputs.LayerShape(f"custom_N{N}_H{H}_I{I}_E{E}_k{k}" + (f"_zipf{z}" if z else "")
+                             + f"_T{T}", N, H, I, E, k, zipf_s=z, minibatch_rows=T)
 
 
 def run_ours(args, ws_, rank, local):
@@ -192,7 +195,8 @@ def run_ours(args, ws_, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     inp = inputs.make_inputs(shape, seed=rank, device=dev)
-    layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev)
+    layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev,
+                     minibatch_rows=shape.minibatch_rows)
     p, wsb = layer.p, layer.ws
     w = _lib.weights(inp["wg"], inp["wu"], inp["wd"])
     sv = layer.saved_tensors()
@@ -335,6 +339,7 @@ def run_ours(args, ws_, rank, local):
         "data": "synthetic (seeded Gaussian inputs and random-init expert weights)",
         "config": {"workload": shape.name, "N": shape.N, "H": shape.H, "I": shape.I,
                    "E": shape.E, "k": shape.k, "zipf_bias": shape.zipf_s,
+                   "minibatch_rows": shape.minibatch_rows,
                    "passes": "fwd+bwd" if backward else "fwd",
                    "l2": "inputs larger than L2 (expert weights alone "
                          f"{3 * shape.E * shape.H * shape.I * 2 / 1e9:.2f} GB)",

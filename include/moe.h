@@ -63,11 +63,17 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_dtype;
 /* Problem size. N tokens, H hidden, I expert intermediate, E experts,
  * k experts per token. Supported: N >= 0, 1 <= k <= min(E, 32), E <= 1024,
  * H and I multiples of 256. dtype: MOE_BF16 (MOE_MXFP8 weights are produced
- * by mxfp8_quantize; the layer entry points take MOE_BF16). */
+ * by mxfp8_quantize; the layer entry points take MOE_BF16).
+ * minibatch_rows T ([Clip] key point 3, minibatch granularity; the "tokens
+ * per expert slot" of the large-batch sweep): each expert's rows are grouped
+ * and padded to a multiple of T. T = 128 (also for 0), 256, 512 or 1024.
+ * Larger T wastes more padding rows but lets two SMs share one 256-row MMA
+ * of an expert (T >= 256 selects the SM-pair kernels). */
 typedef struct {
   int64_t N;
   int32_t H, I, E, k;
   int32_t dtype;
+  int32_t minibatch_rows;
 } moe_problem;
 
 /* Expert weights, bf16, K dimension contiguous:
@@ -79,8 +85,8 @@ typedef struct {
 } moe_weights;
 
 /* Rows of every expert-grouped buffer: each expert's segment of the buffer is
- * rounded up to a multiple of 128 rows (the tile height), so the buffer needs
- * at most N*k + E*127 rows, rounded up to 128. Padding rows hold zeros. */
+ * rounded up to a multiple of T = minibatch_rows, so the buffer needs at most
+ * N*k + E*(T-1) rows, rounded up to T. Padding rows hold zeros. */
 int64_t moe_grouped_rows(const moe_problem* p);
 
 /* Bytes of the workspace (schedule tables, scratch, backward buffers, device
@@ -101,12 +107,13 @@ moe_status moe_saved_layout(const moe_problem* p, void* saved, moe_saved_view* o
  * address arithmetic only; nothing is launched):
  *  counts[E]        assignments per expert
  *  offsets[E+1]     exclusive prefix sum of counts (offsets[E] = N*k)
- *  pad_offsets[E+1] exclusive prefix sum of counts rounded up to 128
+ *  pad_offsets[E+1] exclusive prefix sum of counts rounded up to T
  *  slot_of[N*k]     row of the expert-grouped buffer holding assignment
  *                   (t, j) = pad_offsets[e] + #{t' < t routed to e}
  *  src_of_row[R]    t*k + j of the assignment in row r, -1 on padding rows
  *                   (valid for r < pad_offsets[E])
- *  tiles[R/128][3]  (expert, first row, valid rows) of each 128-row tile
+ *  tiles[R/128][3]  (expert, first row, valid rows >= 0) of each 128-row tile
+ *                   (the tensor-core tile height), in row order
  *  n_tiles[1]       number of tiles = pad_offsets[E] / 128 */
 typedef struct {
   int32_t *counts, *offsets, *pad_offsets, *slot_of, *src_of_row, *tiles, *n_tiles;

@@ -61,7 +61,8 @@ struct Args {
   const int32_t* tiles;        // [n][3] (expert, row0, valid) of the 128-row tiles
   const int32_t* n_tiles;      // device count of those tiles
   const int32_t* pad_offsets;  // [E+1] padded segment starts (WGRAD K ranges)
-  const int32_t* order;        // [E] experts by descending padded row count (WGRAD)
+  const int32_t* order;        // [E] experts by descending row count (WGRAD)
+  const int32_t* counts;       // [E] rows per expert (WGRAD K = count rounded up to 64)
   int32_t* err;
   int max_mtiles;              // host bound on *n_tiles (R / 128)
   int64_t rows;                // rows of the expert-grouped buffers (R)
@@ -114,7 +115,10 @@ __device__ __forceinline__ TileInfo decode_tile(const Args& a, int64_t t, int cr
     ti.e = a.order[rank];
     if (ti.e < 0 || ti.e >= a.E) ti.e = 0;
     ti.kstart = a.pad_offsets[ti.e];
-    ti.nkb = (a.pad_offsets[ti.e + 1] - ti.kstart) / BK;
+    // Rows past the count are zero padding up to the segment end, so K stops
+    // at the count rounded up to the k-block.
+    ti.nkb = (a.counts[ti.e] + BK - 1) / BK;
+    if (ti.kstart + ti.nkb * BK > a.pad_offsets[ti.e + 1]) ti.nkb = -1;
     ti.row0 = 0;
     ti.skip = false;
     if (ti.kstart < 0 || ti.nkb < 0 || ti.kstart + static_cast<int64_t>(ti.nkb) * BK > a.rows) {
@@ -507,8 +511,10 @@ constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + kOutBytes + 1024;
 struct TileSeq {
   int64_t fi, bi, half, total, stride;
   int turn;
-  __device__ __forceinline__ TileSeq(int64_t first, int64_t stride_, int64_t total_)
-      : fi(first), bi(first), half((total_ + 1) / 2), total(total_), stride(stride_), turn(0) {}
+  __device__ __forceinline__ TileSeq(int64_t first, int64_t stride_, int64_t total_,
+                                     bool interleave)
+      : fi(first), bi(first), half(interleave ? (total_ + 1) / 2 : total_), total(total_),
+        stride(stride_), turn(0) {}
   __device__ __forceinline__ bool next(int64_t& t) {
     const bool f_ok = fi < half, b_ok = bi < total - half;
     if (!f_ok && !b_ok) return false;
@@ -524,21 +530,66 @@ struct TileSeq {
   }
 };
 
+// Pair tiles: WGRAD pairs neighbouring M tiles of one expert (shared B); the
+// token-row modes pair the two 128-row tiles of one 256-row block of an expert
+// (T >= 256 guarantees both belong to the same expert) and split the N tile's
+// B rows/columns between the CTAs.
 template <int MODE>
-__device__ __forceinline__ void issue_loads_pair(const Maps& m, const TileInfo& ti, int kb,
-                                                 uint8_t* sA, uint8_t* sB, uint32_t bar,
+__device__ __forceinline__ TileInfo decode_pair_tile(const Args& a, int64_t t, int crank) {
+  if constexpr (MODE == WGRAD) {
+    return decode_tile<MODE, 2>(a, t, crank);
+  } else {
+    const int pm = static_cast<int>(t / a.n_nt);
+    TileInfo ti = decode_tile<MODE, 1>(a, static_cast<int64_t>(2 * pm + crank) * a.n_nt, 0);
+    ti.nt = static_cast<int>(t % a.n_nt);
+    return ti;
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ int64_t total_pair_tiles(const Args& a) {
+  if constexpr (MODE == WGRAD) {
+    return total_tiles<MODE, 2>(a);
+  } else {
+    int n = *a.n_tiles;
+    n = n < 0 ? 0 : (n > a.max_mtiles ? a.max_mtiles : n);
+    return static_cast<int64_t>(n / 2) * a.n_nt;
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ void issue_loads_pair(const Maps& m, const Args& a, const TileInfo& ti,
+                                                 int kb, uint8_t* sA, uint8_t* sB, uint32_t bar,
                                                  int crank) {
-  static_assert(MODE == WGRAD, "SM-pair loads are defined for the weight gradients");
-  const CUtensorMap* ma = ti.prob ? &m.a1 : &m.a0;
-  const CUtensorMap* mb = ti.prob ? &m.b1 : &m.b0;
-  const int krow = ti.kstart + kb * BK;
+  if constexpr (MODE == WGRAD) {
+    const CUtensorMap* ma = ti.prob ? &m.a1 : &m.a0;
+    const CUtensorMap* mb = ti.prob ? &m.b1 : &m.b0;
+    const int krow = ti.kstart + kb * BK;
 #pragma unroll
-  for (int c = 0; c < BM / 64; ++c)
-    tma_load_2d_pair(sA + c * (64 * BK * 2), ma, bar, ti.mt * BM + c * 64, krow);
+    for (int c = 0; c < BM / 64; ++c)
+      tma_load_2d_pair(sA + c * (64 * BK * 2), ma, bar, ti.mt * BM + c * 64, krow);
 #pragma unroll
-  for (int c = 0; c < BN / 128; ++c)
-    tma_load_2d_pair(sB + c * (64 * BK * 2), mb, bar, ti.nt * BN + crank * (BN / 2) + c * 64,
-                     krow);
+    for (int c = 0; c < BN / 128; ++c)
+      tma_load_2d_pair(sB + c * (64 * BK * 2), mb, bar, ti.nt * BN + crank * (BN / 2) + c * 64,
+                       krow);
+  } else if constexpr (MODE == GATE_UP) {
+    // the N tile is 128 gate rows then 128 up rows: the even CTA stages the
+    // gate rows, the odd CTA the up rows
+    tma_load_2d_pair(sA, &m.a0, bar, kb * BK, ti.row0);
+    tma_load_2d_pair(sB, crank ? &m.b1 : &m.b0, bar, kb * BK, ti.e * a.b_rows + ti.nt * (BN / 2));
+  } else if constexpr (MODE == DOWN) {
+    tma_load_2d_pair(sA, &m.a0, bar, kb * BK, ti.row0);
+    tma_load_2d_pair(sB, &m.b0, bar, kb * BK, ti.e * a.b_rows + ti.nt * BN + crank * (BN / 2));
+  } else {  // DACT, DXE: B is MN-major, two 64-column chunks per CTA
+    const bool second = (MODE == DXE) && kb >= a.kb1;
+    const int kk = second ? kb - a.kb1 : kb;
+    tma_load_2d_pair(sA, second ? &m.a1 : &m.a0, bar, kk * BK, ti.row0);
+    const CUtensorMap* mb = second ? &m.b1 : &m.b0;
+#pragma unroll
+    for (int c = 0; c < BN / 128; ++c)
+      tma_load_2d_pair(sB + c * (64 * BK * 2), mb, bar, ti.nt * BN + crank * (BN / 2) + c * 64,
+                       ti.e * a.b_rows + kk * BK);
+  }
 }
 
 template <int MODE>
@@ -582,7 +633,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_slot;
   volatile int* abortp = &abort_flag;
-  const int64_t total = total_tiles<MODE, 2>(args);
+  const int64_t total = total_pair_tiles<MODE>(args);
+  constexpr bool kInterleave = (MODE == WGRAD);
   const int64_t first = blockIdx.x / 2, stride = gridDim.x / 2;
 
   if (warp == 0) {
@@ -593,13 +645,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t issued_mask = 0, issued_parity = 0;
       bool ok = true;
       int64_t t;
-      for (TileSeq q(first, stride, total); ok && q.next(t);) {
-        const TileInfo ti = decode_tile<MODE, 2>(args, t, crank);
+      for (TileSeq q(first, stride, total, kInterleave); ok && q.next(t);) {
+        const TileInfo ti = decode_pair_tile<MODE>(args, t, crank);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, args.err)) { ok = false; break; }
           uint8_t* sA = smem + stage * kPairStageBytes;
           if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
-          issue_loads_pair<MODE>(maps, ti, kb, sA, sA + kPairABytes,
+          issue_loads_pair<MODE>(maps, args, ti, kb, sA, sA + kPairABytes,
                                  cluster_addr(&full_bar[stage], 0), crank);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -620,8 +672,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       int64_t t;
-      for (TileSeq q(first, stride, total); ok && q.next(t);) {
-        const TileInfo ti = decode_tile<MODE, 2>(args, t, crank);
+      for (TileSeq q(first, stride, total, kInterleave); ok && q.next(t);) {
+        const TileInfo ti = decode_pair_tile<MODE>(args, t, crank);
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abortp, args.err)) break;
         tc_fence_after();
         const uint32_t dtmem = tmem_base + acc * BN;
@@ -632,8 +684,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t b_addr = a_addr + kPairABytes;
 #pragma unroll
           for (int ks = 0; ks < BK / 16; ++ks) {
-            const uint64_t ad = sdesc_sw128(a_addr + ks * 2048, 64 * BK * 2, 1024);
-            const uint64_t bd = sdesc_sw128(b_addr + ks * 2048, 64 * BK * 2, 1024);
+            uint64_t ad, bd;
+            if constexpr (Traits<MODE>::a_mn) ad = sdesc_sw128(a_addr + ks * 2048, 64 * BK * 2, 1024);
+            else ad = sdesc_sw128(a_addr + ks * 32, 16, 1024);
+            if constexpr (Traits<MODE>::b_mn) bd = sdesc_sw128(b_addr + ks * 2048, 64 * BK * 2, 1024);
+            else bd = sdesc_sw128(b_addr + ks * 32, 16, 1024);
             umma_bf16_pair(dtmem, ad, bd, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
           }
           umma_commit_pair_mc(&empty_bar[stage], 0x3);  // both CTAs may refill the stage
@@ -654,14 +709,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int64_t t;
-    for (TileSeq q(first, stride, total); q.next(t);) {
-      const TileInfo ti = decode_tile<MODE, 2>(args, t, crank);
+    for (TileSeq q(first, stride, total, kInterleave); q.next(t);) {
+      const TileInfo ti = decode_pair_tile<MODE>(args, t, crank);
       if (!mbar_wait(&tfull_bar[acc], acc_phase, abortp, args.err)) break;
       tc_fence_after();
       if (ti.skip) {
         if (lane == 0) set_dev_error(args.err, MOE_DEVERR_BAD_EXPERT);
-      } else {
+      } else if constexpr (MODE == WGRAD) {
         epilogue_wgrad(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
+      } else {
+        epilogue<MODE>(args, ti, tmem_base + acc * BN, quad, lane);
       }
       tc_fence_before();
       __syncwarp();
@@ -685,12 +742,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   cluster_sync();  // no CTA leaves while its peer may still signal it
 }
 
-// Experts ranked by padded row count, descending; equal counts keep ascending
+// Experts ranked by row count, descending; equal counts keep ascending
 // expert index. One CTA; each thread ranks its experts against all others.
-__global__ void __launch_bounds__(1024) expert_order_kernel(const int32_t* __restrict__ pad_offsets,
+__global__ void __launch_bounds__(1024) expert_order_kernel(const int32_t* __restrict__ counts,
                                                             int E, int32_t* __restrict__ order) {
   __shared__ int32_t cnt[kMaxE];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = pad_offsets[e + 1] - pad_offsets[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = counts[e];
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int32_t c = cnt[e];
@@ -853,15 +910,26 @@ moe_status launch_rows(const Maps& maps, const Args& args, cudaStream_t s) {
 }
 
 moe_status launch_expert_order(const Layout& L, const void* ws, cudaStream_t s) {
-  expert_order_kernel<<<1, 1024, 0, s>>>(at<int32_t>(ws, L.pad_offsets), L.E,
+  expert_order_kernel<<<1, 1024, 0, s>>>(at<int32_t>(ws, L.counts), L.E,
                                          const_cast<int32_t*>(at<int32_t>(ws, L.expert_order)));
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-// Rows of the A box of the token-row modes: the whole 128-row tile, or the
-// 64-row half each CTA of a pair loads when the N-tile count allows pairing.
-int a_box_rows(int n_nt) { return n_nt % 2 == 0 ? BM / 2 : BM; }
+// Rows of the A box of the token-row modes: the CTA's whole 128-row tile (SM
+// pairs, or no pairing), or the 64-row half each CTA of a multicast pair loads.
+int a_box_rows(const Layout& L, int n_nt) {
+  return (L.T < 256 && n_nt % 2 == 0) ? BM / 2 : BM;
+}
+
+// Token-row modes: SM-pair kernels when every expert segment is a multiple of
+// 256 rows (T >= 256), otherwise CTA pairs sharing A by multicast, or single CTAs.
+template <int MODE>
+moe_status launch_tokens(const Layout& L, const Maps& maps, const Args& args, cudaStream_t s) {
+  if (L.T >= 256)
+    return launch_pair<MODE>(maps, args, static_cast<int64_t>(args.max_mtiles / 2) * args.n_nt, s);
+  return launch_rows<MODE>(maps, args, s);
+}
 
 Args base_args(const Layout& L, const void* ws) {
   Args a{};
@@ -869,6 +937,7 @@ Args base_args(const Layout& L, const void* ws) {
   a.n_tiles = at<int32_t>(ws, L.n_tiles);
   a.pad_offsets = at<int32_t>(ws, L.pad_offsets);
   a.order = at<int32_t>(ws, L.expert_order);
+  a.counts = at<int32_t>(ws, L.counts);
   a.err = const_cast<int32_t*>(at<int32_t>(ws, L.err));
   a.max_mtiles = static_cast<int>(L.R / BM);
   a.rows = L.R;
@@ -881,7 +950,7 @@ Args base_args(const Layout& L, const void* ws) {
 moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const void* wg,
                         const void* wu, void* g, void* u, void* act, cudaStream_t s) {
   Maps m{};
-  if (!make_map(&m.a0, xe, L.H, L.R, a_box_rows(L.I / (BN / 2))) ||
+  if (!make_map(&m.a0, xe, L.H, L.R, a_box_rows(L, L.I / (BN / 2))) ||
       !make_map(&m.b0, wg, L.H, static_cast<int64_t>(L.E) * L.I, BN / 2) ||
       !make_map(&m.b1, wu, L.H, static_cast<int64_t>(L.E) * L.I, BN / 2))
     return MOE_ERR_CUDA;
@@ -895,14 +964,14 @@ moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const v
   a.out0 = g;
   a.out1 = u;
   a.out2 = act;
-  return launch_rows<GATE_UP>(m, a, s);
+  return launch_tokens<GATE_UP>(L, m, a, s);
 }
 
 moe_status gemm_down(const Layout& L, const void* ws, const void* act, const void* wd, void* ye,
                      cudaStream_t s) {
   Maps m{};
-  if (!make_map(&m.a0, act, L.I, L.R, a_box_rows(L.H / BN)) ||
-      !make_map(&m.b0, wd, L.I, static_cast<int64_t>(L.E) * L.H, BN))
+  if (!make_map(&m.a0, act, L.I, L.R, a_box_rows(L, L.H / BN)) ||
+      !make_map(&m.b0, wd, L.I, static_cast<int64_t>(L.E) * L.H, L.T >= 256 ? BN / 2 : BN))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
   m.b1 = m.b0;
@@ -913,13 +982,13 @@ moe_status gemm_down(const Layout& L, const void* ws, const void* act, const voi
   a.b_rows = L.H;
   a.ld_out = L.H;
   a.out0 = ye;
-  return launch_rows<DOWN>(m, a, s);
+  return launch_tokens<DOWN>(L, m, a, s);
 }
 
 moe_status gemm_down_dgrad(const Layout& L, const void* ws, const void* dye, const void* g,
                            const void* u, const void* wd, void* dg, void* du, cudaStream_t s) {
   Maps m{};
-  if (!make_map(&m.a0, dye, L.H, L.R, a_box_rows(L.I / BN)) ||
+  if (!make_map(&m.a0, dye, L.H, L.R, a_box_rows(L, L.I / BN)) ||
       !make_map(&m.b0, wd, L.I, static_cast<int64_t>(L.E) * L.H, 64))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
@@ -934,7 +1003,7 @@ moe_status gemm_down_dgrad(const Layout& L, const void* ws, const void* dye, con
   a.out1 = du;
   a.in0 = g;
   a.in1 = u;
-  return launch_rows<DACT>(m, a, s);
+  return launch_tokens<DACT>(L, m, a, s);
 }
 
 moe_status gemm_down_wgrad(const Layout& L, const void* ws, const void* dye, const void* act,
@@ -960,8 +1029,8 @@ moe_status gemm_down_wgrad(const Layout& L, const void* ws, const void* dye, con
 moe_status gemm_gate_up_dgrad(const Layout& L, const void* ws, const void* dg, const void* du,
                               const void* wg, const void* wu, void* dxe, cudaStream_t s) {
   Maps m{};
-  if (!make_map(&m.a0, dg, L.I, L.R, a_box_rows(L.H / BN)) ||
-      !make_map(&m.a1, du, L.I, L.R, a_box_rows(L.H / BN)) ||
+  if (!make_map(&m.a0, dg, L.I, L.R, a_box_rows(L, L.H / BN)) ||
+      !make_map(&m.a1, du, L.I, L.R, a_box_rows(L, L.H / BN)) ||
       !make_map(&m.b0, wg, L.H, static_cast<int64_t>(L.E) * L.I, 64) ||
       !make_map(&m.b1, wu, L.H, static_cast<int64_t>(L.E) * L.I, 64))
     return MOE_ERR_CUDA;
@@ -972,7 +1041,7 @@ moe_status gemm_gate_up_dgrad(const Layout& L, const void* ws, const void* dg, c
   a.b_rows = L.I;
   a.ld_out = L.H;
   a.out0 = dxe;
-  return launch_rows<DXE>(m, a, s);
+  return launch_tokens<DXE>(L, m, a, s);
 }
 
 moe_status gemm_gate_up_wgrad(const Layout& L, const void* ws, const void* dg, const void* du,

@@ -25,8 +25,10 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   if (p->E > kMaxE || p->k > kMaxK) return MOE_ERR_UNSUPPORTED;
   if (p->H % 256 != 0 || p->I % 256 != 0) return MOE_ERR_UNSUPPORTED;
   if (p->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const int32_t T = p->minibatch_rows == 0 ? kTileM : p->minibatch_rows;
+  if (T != 128 && T != 256 && T != 512 && T != 1024) return MOE_ERR_UNSUPPORTED;
   const int64_t A = p->N * p->k;
-  const int64_t R = (A + static_cast<int64_t>(p->E) * (kTileM - 1) + kTileM - 1) / kTileM * kTileM;
+  const int64_t R = (A + static_cast<int64_t>(p->E) * (T - 1) + T - 1) / T * T;
   if (R >= (1LL << 31) - 1 || p->N > (1LL << 31) / p->k) return MOE_ERR_UNSUPPORTED;
   L->N = p->N;
   L->A = A;
@@ -35,6 +37,7 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   L->I = p->I;
   L->E = p->E;
   L->k = p->k;
+  L->T = T;
   L->n_warps = (A + kSchedSub - 1) / kSchedSub;
   size_t o = 0;
   auto take = [&o](size_t bytes) {

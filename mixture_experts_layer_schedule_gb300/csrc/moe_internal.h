@@ -20,6 +20,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 struct Layout {
   int64_t N, A, R;        // tokens, assignments, expert-grouped rows
   int32_t H, I, E, k;
+  int32_t T;              // per-expert row granularity (minibatch rows)
   int64_t n_warps;        // schedule warps = ceil(A / kSchedSub)
   // workspace byte offsets
   size_t err, counts, offsets, pad_offsets, slot_of, src_of_row, tiles, n_tiles, warp_counts,

@@ -176,7 +176,8 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int32_t* __restrict__ 
 
 // Kernel 3: offsets, padded offsets, tile list, padding rows.
 __global__ void __launch_bounds__(1024) sched_final_kernel(const int32_t* __restrict__ counts,
-                                                           int E, int32_t* __restrict__ offsets,
+                                                           int E, int T,
+                                                           int32_t* __restrict__ offsets,
                                                            int32_t* __restrict__ pad_offsets,
                                                            int32_t* __restrict__ src_of_row,
                                                            int32_t* __restrict__ tiles,
@@ -186,7 +187,7 @@ __global__ void __launch_bounds__(1024) sched_final_kernel(const int32_t* __rest
   __shared__ int32_t s_cnt[kMaxE];
   const int e = threadIdx.x;
   const int32_t c = e < E ? counts[e] : 0;
-  const int32_t cp = (c + kTileM - 1) / kTileM * kTileM;
+  const int32_t cp = (c + T - 1) / T * T;
   int32_t tot_c, tot_p;
   const int32_t off = block_exclusive_scan(c, sm, &tot_c);
   const int32_t poff = block_exclusive_scan(cp, sm, &tot_p);
@@ -213,11 +214,11 @@ __global__ void __launch_bounds__(1024) sched_final_kernel(const int32_t* __rest
     }
     tiles[3 * i + 0] = lo;
     tiles[3 * i + 1] = r0;
-    tiles[3 * i + 2] = min(kTileM, s_pad[lo] + s_cnt[lo] - r0);
+    tiles[3 * i + 2] = max(0, min(kTileM, s_pad[lo] + s_cnt[lo] - r0));
   }
-  // padding rows of every segment
-  for (int32_t q = threadIdx.x; q < E * kTileM; q += blockDim.x) {
-    const int ex = q / kTileM, r = q % kTileM;
+  // padding rows of every segment (fewer than T each)
+  for (int32_t q = threadIdx.x; q < E * T; q += blockDim.x) {
+    const int ex = q / T, r = q % T;
     const int32_t row = s_pad[ex] + s_cnt[ex] + r;
     if (row < s_pad[ex + 1]) src_of_row[row] = -1;
   }
@@ -308,7 +309,7 @@ cudaError_t launch_build_schedule_with_scratch(const Layout& L, const int32_t* i
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  sched_final_kernel<<<1, 1024, 0, s>>>(counts, L.E, offsets, pad, src, tiles, n_tiles);
+  sched_final_kernel<<<1, 1024, 0, s>>>(counts, L.E, L.T, offsets, pad, src, tiles, n_tiles);
   note_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess || L.n_warps == 0) return e;
@@ -400,7 +401,7 @@ extern "C" moe_status moe_build_schedule_noalloc(const moe_problem* p, const int
     return MOE_ERR_CUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  sched_final_kernel<<<1, 1024, 0, s>>>(out->counts, L.E, out->offsets, out->pad_offsets,
+  sched_final_kernel<<<1, 1024, 0, s>>>(out->counts, L.E, L.T, out->offsets, out->pad_offsets,
                                         out->src_of_row, out->tiles, out->n_tiles);
   note_launch();
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;

@@ -26,10 +26,11 @@ class Grads:
 class MoELayer:
     """Buffers of one problem size on one device, reused across calls."""
 
-    def __init__(self, N, H, I, E, k, device="cuda", allocate_grads=True):
+    def __init__(self, N, H, I, E, k, device="cuda", allocate_grads=True, minibatch_rows=128):
         self.N, self.H, self.I, self.E, self.k = int(N), int(H), int(I), int(E), int(k)
+        self.T = int(minibatch_rows)
         self.device = torch.device(device)
-        self.p = _lib.problem(N, H, I, E, k)
+        self.p = _lib.problem(N, H, I, E, k, minibatch_rows=self.T)
         self.R = _lib.moe_grouped_rows(self.p)
         dev = self.device
         self.ws = torch.empty(_lib.moe_workspace_bytes(self.p), dtype=torch.uint8, device=dev)

@@ -55,6 +55,8 @@ def lib():
             L.orc_route_topk.argtypes = [i64, i32, i32, vp, vp, vp, vp]
             L.orc_build_schedule.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, vp,
                                              vp, i64, vp, i64, vp]
+            L.orc_build_schedule_padded.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp,
+                                                    vp, vp, i64, vp, i64, vp]
             fw = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int]
             L.orc_forward_f64.argtypes = fw
             L.orc_forward_bf16.argtypes = fw
@@ -113,11 +115,13 @@ def route_topk(logits, bias, k):
     return ids, w
 
 
-def build_schedule(ids, E, tile_m=128):
+def build_schedule(ids, E, tile_m=128, pad_m=None):
+    """Schedule tables; expert segments padded to pad_m (default tile_m) rows."""
+    pad_m = tile_m if pad_m is None else pad_m
     ids = _c(ids, np.int32)
     N, k = ids.shape
     A = N * k
-    rows_cap = A + E * (tile_m - 1)
+    rows_cap = A + E * (pad_m - 1)
     tiles_cap = rows_cap // tile_m + 1
     counts = np.empty(E, np.int32)
     offsets = np.empty(E + 1, np.int32)
@@ -126,9 +130,10 @@ def build_schedule(ids, E, tile_m=128):
     src_of_row = np.empty(rows_cap, np.int32)
     tiles = np.empty((tiles_cap, 3), np.int32)
     n_tiles = np.zeros(1, np.int32)
-    _check(lib().orc_build_schedule(N, k, E, tile_m, _p(ids), _p(counts), _p(offsets),
-                                    _p(pad_offsets), _p(slot_of), _p(src_of_row), rows_cap,
-                                    _p(tiles), tiles_cap, _p(n_tiles)))
+    _check(lib().orc_build_schedule_padded(N, k, E, tile_m, pad_m, _p(ids), _p(counts),
+                                           _p(offsets), _p(pad_offsets), _p(slot_of),
+                                           _p(src_of_row), rows_cap, _p(tiles), tiles_cap,
+                                           _p(n_tiles)))
     rows = int(pad_offsets[E])
     nt = int(n_tiles[0])
     return dict(counts=counts, offsets=offsets, pad_offsets=pad_offsets,

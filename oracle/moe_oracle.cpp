@@ -290,7 +290,17 @@ int orc_build_schedule(int64_t N, int32_t k, int32_t E, int32_t tile_m,
                        int32_t* pad_offsets, int32_t* slot_of,
                        int32_t* src_of_row, int64_t rows_cap, int32_t* tiles,
                        int64_t tiles_cap, int32_t* n_tiles) {
-  if (N < 0 || k <= 0 || E <= 0 || tile_m <= 0) return ORC_ERR_ARG;
+  return orc_build_schedule_padded(N, k, E, tile_m, tile_m, ids, counts, offsets, pad_offsets,
+                                   slot_of, src_of_row, rows_cap, tiles, tiles_cap, n_tiles);
+}
+
+int orc_build_schedule_padded(int64_t N, int32_t k, int32_t E, int32_t tile_m, int32_t pad_m,
+                              const int32_t* ids, int32_t* counts, int32_t* offsets,
+                              int32_t* pad_offsets, int32_t* slot_of,
+                              int32_t* src_of_row, int64_t rows_cap, int32_t* tiles,
+                              int64_t tiles_cap, int32_t* n_tiles) {
+  if (N < 0 || k <= 0 || E <= 0 || tile_m <= 0 || pad_m <= 0 || pad_m % tile_m != 0)
+    return ORC_ERR_ARG;
   const int64_t A = N * k;
   for (int32_t e = 0; e < E; ++e) counts[e] = 0;
   for (int64_t a = 0; a < A; ++a) {
@@ -301,7 +311,7 @@ int orc_build_schedule(int64_t N, int32_t k, int32_t E, int32_t tile_m,
   pad_offsets[0] = 0;
   for (int32_t e = 0; e < E; ++e) {
     offsets[e + 1] = offsets[e] + counts[e];
-    const int32_t padded = (counts[e] + tile_m - 1) / tile_m * tile_m;
+    const int32_t padded = (counts[e] + pad_m - 1) / pad_m * pad_m;
     pad_offsets[e + 1] = pad_offsets[e] + padded;
   }
   const int64_t rows = pad_offsets[E];
@@ -323,7 +333,7 @@ int orc_build_schedule(int64_t N, int32_t k, int32_t E, int32_t tile_m,
     for (int32_t r0 = pad_offsets[e]; r0 < pad_offsets[e + 1]; r0 += tile_m) {
       tiles[3 * i + 0] = e;
       tiles[3 * i + 1] = r0;
-      tiles[3 * i + 2] = std::min(tile_m, pad_offsets[e] + counts[e] - r0);
+      tiles[3 * i + 2] = std::max(0, std::min(tile_m, pad_offsets[e] + counts[e] - r0));
       ++i;
     }
   *n_tiles = static_cast<int32_t>(i);

@@ -64,6 +64,14 @@ int orc_build_schedule(int64_t N, int32_t k, int32_t E, int32_t tile_m,
                        int32_t* pad_offsets, int32_t* slot_of,
                        int32_t* src_of_row, int64_t rows_cap, int32_t* tiles,
                        int64_t tiles_cap, int32_t* n_tiles);
+/* Same tables with each expert's segment padded to a multiple of pad_m (a
+ * multiple of tile_m; the minibatch granularity) while tiles stay tile_m rows
+ * high; a tile lying wholly in padding has 0 valid rows. */
+int orc_build_schedule_padded(int64_t N, int32_t k, int32_t E, int32_t tile_m, int32_t pad_m,
+                              const int32_t* ids, int32_t* counts, int32_t* offsets,
+                              int32_t* pad_offsets, int32_t* slot_of,
+                              int32_t* src_of_row, int64_t rows_cap, int32_t* tiles,
+                              int64_t tiles_cap, int32_t* n_tiles);
 
 /* Layer forward. Inputs either all fp64 (the *_f64 entry points, used for
  * finite differences) or bf16 bit patterns (x, wg, wu, wd).

@@ -32,12 +32,13 @@ def to_dev(d):
     return {k: (v.to(dev()) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
 
 
-def custom_shape(N, H, I, E, k, zipf_s=None, name="custom"):
-    return inputs.LayerShape(name, N, H, I, E, k, zipf_s=zipf_s)
+def custom_shape(N, H, I, E, k, zipf_s=None, name="custom", T=128):
+    return inputs.LayerShape(name, N, H, I, E, k, zipf_s=zipf_s, minibatch_rows=T)
 
 
 def run_layer(shape, inp_dev, backward=True):
-    layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev())
+    layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev(),
+                     minibatch_rows=shape.minibatch_rows)
     layer.step(inp_dev["x"], inp_dev["logits"], inp_dev["bias"], inp_dev["wg"], inp_dev["wu"],
                inp_dev["wd"], inp_dev.get("dy"), backward=backward)
     torch.cuda.synchronize()

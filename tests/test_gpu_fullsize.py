@@ -24,8 +24,8 @@ from gpu_helpers import BF16_TOL, W_RTOL, assert_close, dev
 
 pytestmark = pytest.mark.gpu
 
-FULL = [inputs.FINE_GRAINED_FWD, inputs.SKEWED, inputs.large_batch(8192),
-        inputs.large_batch(65536)]
+FULL = [inputs.FINE_GRAINED_FWD, inputs.SKEWED, inputs.SKEWED.with_(name=inputs.SKEWED.name + "_T256", minibatch_rows=256),
+        inputs.large_batch(8192, 256), inputs.large_batch(65536, 1024)]
 
 
 def _host(t):
@@ -38,7 +38,7 @@ def test_full_size_sampled_parity(shape):
     d = dev()
     inp = inputs.make_inputs(shape, seed=0, device=d)
     layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=d,
-                     allocate_grads=shape.backward)
+                     allocate_grads=shape.backward, minibatch_rows=shape.minibatch_rows)
     layer.step(inp["x"], inp["logits"], inp["bias"], inp["wg"], inp["wu"], inp["wd"],
                inp.get("dy"), backward=shape.backward)
     torch.cuda.synchronize()
@@ -51,7 +51,7 @@ def test_full_size_sampled_parity(shape):
     np.testing.assert_array_equal(layer.topk_ids.cpu().numpy(), ids)
     wg_gpu = layer.topk_w.cpu().numpy().astype(np.float64)
     assert np.max(np.abs(wg_gpu - w) / w) <= W_RTOL
-    ref = oracle.build_schedule(ids, shape.E, 128)
+    ref = oracle.build_schedule(ids, shape.E, 128, shape.minibatch_rows)
     got = {k: v.cpu().numpy() for k, v in layer.schedule_tensors().items()}
     for key in ("counts", "offsets", "pad_offsets"):
         np.testing.assert_array_equal(got[key], ref[key])

@@ -25,7 +25,8 @@ RAGGED = custom_shape(300, 512, 768, 16, 4, zipf_s=1.2, name="ragged_skewed")
 
 def _phase_setup(shape, seed=0):
     inp = to_dev(inputs.make_inputs(shape, seed=seed, device="cpu"))
-    layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev())
+    layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev(),
+                     minibatch_rows=shape.minibatch_rows)
     layer.route(inp["logits"], inp["bias"])
     layer.build_schedule()
     return inp, layer
@@ -36,7 +37,11 @@ def _segments(layer):
     return [(e, int(s["pad_offsets"][e]), int(s["counts"][e])) for e in range(layer.E)], s
 
 
-@pytest.mark.parametrize("shape", [inputs.TINY, RAGGED], ids=lambda s: s.name)
+PHASE_SHAPES = [inputs.TINY, RAGGED, inputs.TINY.with_(name="tiny_T256", minibatch_rows=256),
+                RAGGED.with_(name="ragged_skewed_T256", minibatch_rows=256)]
+
+
+@pytest.mark.parametrize("shape", PHASE_SHAPES, ids=lambda s: s.name)
 def test_phases_match_torch_fp32(shape):
     inp, layer = _phase_setup(shape)
     p, ws = layer.p, layer.ws
@@ -158,6 +163,9 @@ LAYER_SHAPES = [
     RAGGED,
     custom_shape(129, 256, 256, 4, 2, name="one_over_tile"),
     custom_shape(64, 1024, 512, 32, 8, name="many_empty_experts"),
+    custom_shape(300, 512, 768, 16, 4, zipf_s=1.2, name="ragged_skewed_T256", T=256),
+    custom_shape(129, 256, 512, 4, 2, name="one_over_tile_T1024", T=1024),
+    custom_shape(64, 1024, 512, 32, 8, name="many_empty_experts_T512", T=512),
 ]
 
 

@@ -18,8 +18,8 @@ from gpu_helpers import W_RTOL, dev
 pytestmark = pytest.mark.gpu
 
 
-def _route_and_schedule(N, E, k, logits, bias, H=256, I=256):
-    layer = MoELayer(N, H, I, E, k, device=dev(), allocate_grads=False)
+def _route_and_schedule(N, E, k, logits, bias, H=256, I=256, T=128):
+    layer = MoELayer(N, H, I, E, k, device=dev(), allocate_grads=False, minibatch_rows=T)
     lg = torch.as_tensor(logits).to(dev())
     bs = None if bias is None else torch.as_tensor(bias).to(dev())
     layer.route(lg, bs)
@@ -29,7 +29,7 @@ def _route_and_schedule(N, E, k, logits, bias, H=256, I=256):
 
 
 def _check_schedule(layer, ids_np, E):
-    ref = oracle.build_schedule(ids_np, E, 128)
+    ref = oracle.build_schedule(ids_np, E, 128, layer.T)
     got = {k: v.cpu().numpy() for k, v in layer.schedule_tensors().items()}
     np.testing.assert_array_equal(got["counts"], ref["counts"])
     np.testing.assert_array_equal(got["offsets"], ref["offsets"])
@@ -52,15 +52,16 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("T", [128, 256, 1024])
 @pytest.mark.parametrize("name,N,E,k,zipf", CASES, ids=[c[0] for c in CASES])
-def test_route_and_schedule_match_oracle(name, N, E, k, zipf):
+def test_route_and_schedule_match_oracle(name, N, E, k, zipf, T):
     g = torch.Generator().manual_seed(N * 31 + E)
     logits = torch.randn((N, E), generator=g).float().numpy()
     bias = None
     if zipf is not None:
         r = torch.randperm(E, generator=g).double() + 1.0
         bias = (-zipf * torch.log(r)).float().numpy()
-    layer = _route_and_schedule(N, E, k, logits, bias)
+    layer = _route_and_schedule(N, E, k, logits, bias, T=T)
     ids_ref, w_ref = oracle.route_topk(logits, bias, k)
     np.testing.assert_array_equal(layer.topk_ids.cpu().numpy(), ids_ref)
     w = layer.topk_w.cpu().numpy().astype(np.float64)

@@ -30,18 +30,18 @@ def _zipf(E, s=1.2):
 
 
 @pytest.mark.parametrize("name,ids,E", list(_cases()), ids=[c[0] for c in _cases()])
-@pytest.mark.parametrize("tile_m", [128, 32])
-def test_schedule_invariants(name, ids, E, tile_m):
+@pytest.mark.parametrize("tile_m,pad_m", [(128, 128), (32, 32), (128, 512), (32, 64)])
+def test_schedule_invariants(name, ids, E, tile_m, pad_m):
     N, k = ids.shape
     A = N * k
-    s = oracle.build_schedule(ids, E, tile_m)
+    s = oracle.build_schedule(ids, E, tile_m, pad_m)
     counts, offsets, pad = s["counts"], s["offsets"], s["pad_offsets"]
     np.testing.assert_array_equal(counts, np.bincount(ids.ravel(), minlength=E))
     assert counts.sum() == A and offsets[E] == A
     np.testing.assert_array_equal(offsets, np.concatenate([[0], np.cumsum(counts)]))
-    padded = (counts + tile_m - 1) // tile_m * tile_m
+    padded = (counts + pad_m - 1) // pad_m * pad_m
     np.testing.assert_array_equal(pad, np.concatenate([[0], np.cumsum(padded)]))
-    assert np.all(pad % tile_m == 0)
+    assert np.all(pad % pad_m == 0)
 
     # Permutation: the stable sort of assignments by expert, placed at each
     # expert's padded segment start.
@@ -68,7 +68,7 @@ def test_schedule_invariants(name, ids, E, tile_m):
         np.testing.assert_array_equal(tiles[:, 1], np.arange(s["n_tiles"]) * tile_m)
         for e, r0, valid in tiles:
             assert pad[e] <= r0 < pad[e + 1]
-            assert valid == min(tile_m, pad[e] + counts[e] - r0) and valid > 0
+            assert valid == max(0, min(tile_m, pad[e] + counts[e] - r0))
             rows = src[r0:r0 + tile_m]
             assert np.all(rows[:valid] >= 0) and np.all(rows[valid:] == -1)
             assert np.all(ids.ravel()[rows[:valid]] == e)
