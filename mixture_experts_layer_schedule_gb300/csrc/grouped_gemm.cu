@@ -54,7 +54,7 @@ enum Mode { GATE_UP = 0, DOWN = 1, DACT = 2, DXE = 3, WGRAD = 4 };
 
 struct Maps {
   CUtensorMap a0, a1, b0, b1;
-  CUtensorMap o0, o1;  // WGRAD outputs: fp32 [E * M, N], 32x32 boxes, 128-byte swizzle
+  CUtensorMap o0, o1, o2;  // outputs (TMA stores): fp32 32x32 or bf16 64x32 boxes, 128-B swizzle
 };
 
 struct Args {
@@ -212,57 +212,80 @@ __device__ __forceinline__ void issue_loads(const Maps& m, const Args& a, const 
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
+// One 32-row x 64-column bf16 block of a warp's output: 64 fp32 values per
+// thread (its row) -> bf16 -> shared staging buffer (128-byte swizzle: one
+// warp store covers all banks) -> one TMA store. Two staging buffers per warp
+// let a store overlap the next block.
+__device__ __forceinline__ void store_block_bf16(const CUtensorMap* om, const float (&v)[64],
+                                                 int32_t x, int32_t y, int lane,
+                                                 uint8_t* stage_out, uint32_t& nstore) {
+  uint8_t* buf = stage_out + (nstore & 1u) * kStageOutBytes;
+  if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
+  __syncwarp();
+  const uint32_t row = smem_u32(buf) + lane * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t addr = row + ((j ^ (lane & 7)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                 "r"(pack_bf16x2(v[8 * j + 0], v[8 * j + 1])),
+                 "r"(pack_bf16x2(v[8 * j + 2], v[8 * j + 3])),
+                 "r"(pack_bf16x2(v[8 * j + 4], v[8 * j + 5])),
+                 "r"(pack_bf16x2(v[8 * j + 6], v[8 * j + 7]))
+                 : "memory");
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(om, buf, x, y);
+    bulk_commit();
+  }
+  ++nstore;
+}
+
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r0[32], r1[32];
+  tmem_ld32(taddr, r0);
+  tmem_ld32(taddr + 32, r1);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = __uint_as_float(r0[i]);
+    v[32 + i] = __uint_as_float(r1[i]);
+  }
+}
+
+// Epilogues of the token-row modes (bf16 outputs), one warp = 32 tile rows:
+//   GATE_UP  G, U and Act = silu(G) * U  (accumulator columns: 128 G, 128 U)
+//   DOWN/DXE the accumulator rounded to bf16
+//   DACT     dG, dU from dAct and the saved G, U of the same rows (stored
+//            directly: this epilogue also reads G and U, and interleaving those
+//            reads with the stores in 32-column steps measured faster)
 template <int MODE>
-__device__ __forceinline__ void epilogue(const Args& a, const TileInfo& ti, uint32_t tmem_acc,
-                                         int quad, int lane) {
-  const int rit = quad * 32 + lane;  // row within the tile
+__device__ __forceinline__ void epilogue(const Maps& m, const Args& a, const TileInfo& ti,
+                                         uint32_t tmem_acc, int quad, int lane,
+                                         uint8_t* stage_out, uint32_t& nstore) {
   const uint32_t taddr = tmem_acc + (static_cast<uint32_t>(quad * 32) << 16);
+  const int32_t y = ti.row0 + quad * 32;
   if constexpr (MODE == GATE_UP) {
-    const int64_t row = ti.row0 + rit;
-    const int64_t o = row * a.ld_out + ti.nt * (BN / 2);
-    for (int c = 0; c < BN / 2; c += 32) {
-      uint32_t g[32], u[32];
-      tmem_ld32(taddr + c, g);
-      tmem_ld32(taddr + BN / 2 + c, u);
-      tmem_ld_wait();
-      uint4* pg = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out0) + o + c);
-      uint4* pu = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out1) + o + c);
-      uint4* pa = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out2) + o + c);
+    const int32_t x0 = ti.nt * (BN / 2);
+    for (int c = 0; c < BN / 2; c += 64) {
+      float g[64], u[64];
+      tmem_ld64(taddr + c, g);
+      tmem_ld64(taddr + BN / 2 + c, u);
+      store_block_bf16(&m.o0, g, x0 + c, y, lane, stage_out, nstore);
+      store_block_bf16(&m.o1, u, x0 + c, y, lane, stage_out, nstore);
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        uint32_t wg[4], wu[4], wa[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float g0 = __uint_as_float(g[8 * v + 2 * q]), g1 = __uint_as_float(g[8 * v + 2 * q + 1]);
-          const float u0 = __uint_as_float(u[8 * v + 2 * q]), u1 = __uint_as_float(u[8 * v + 2 * q + 1]);
-          wg[q] = pack_bf16x2(g0, g1);
-          wu[q] = pack_bf16x2(u0, u1);
-          wa[q] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
-        }
-        pg[v] = make_uint4(wg[0], wg[1], wg[2], wg[3]);
-        pu[v] = make_uint4(wu[0], wu[1], wu[2], wu[3]);
-        pa[v] = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-      }
+      for (int i = 0; i < 64; ++i) g[i] = silu(g[i]) * u[i];
+      store_block_bf16(&m.o2, g, x0 + c, y, lane, stage_out, nstore);
     }
   } else if constexpr (MODE == DOWN || MODE == DXE) {
-    const int64_t row = ti.row0 + rit;
-    const int64_t o = row * a.ld_out + ti.nt * BN;
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t d[32];
-      tmem_ld32(taddr + c, d);
-      tmem_ld_wait();
-      uint4* p = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out0) + o + c);
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        uint32_t w4[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          w4[q] = pack_bf16x2(__uint_as_float(d[8 * v + 2 * q]), __uint_as_float(d[8 * v + 2 * q + 1]));
-        p[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      }
+    for (int c = 0; c < BN; c += 64) {
+      float d[64];
+      tmem_ld64(taddr + c, d);
+      store_block_bf16(&m.o0, d, ti.nt * BN + c, y, lane, stage_out, nstore);
     }
-  } else if constexpr (MODE == DACT) {
-    const int64_t row = ti.row0 + rit;
+  } else {  // DACT: direct 16-byte stores, G and U read alongside in 32-column steps
+    const int64_t row = static_cast<int64_t>(y) + lane;
     const int64_t o = row * a.ld_out + ti.nt * BN;
     for (int c = 0; c < BN; c += 32) {
       uint32_t d[32];
@@ -291,9 +314,9 @@ __device__ __forceinline__ void epilogue(const Args& a, const TileInfo& ti, uint
             const float da = __uint_as_float(d[8 * v + 2 * q + h]);
             const float g = h ? bf16hi(gw[q]) : bf16lo(gw[q]);
             const float u = h ? bf16hi(uw[q]) : bf16lo(uw[q]);
-            const float s = 1.0f / (1.0f + expf(-g));
-            dg2[h] = da * u * s * (1.0f + g * (1.0f - s));
-            du2[h] = da * g * s;
+            const float sg = 1.0f / (1.0f + expf(-g));
+            dg2[h] = da * u * sg * (1.0f + g * (1.0f - sg));
+            du2[h] = da * g * sg;
           }
           og[q] = pack_bf16x2(dg2[0], dg2[1]);
           ou[q] = pack_bf16x2(du2[0], du2[1]);
@@ -465,7 +488,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else if constexpr (MODE == WGRAD) {
         epilogue_wgrad(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
       } else {
-        epilogue<MODE>(args, ti, tmem_base + acc * BN, quad, lane);
+        epilogue<MODE>(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
@@ -718,7 +741,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else if constexpr (MODE == WGRAD) {
         epilogue_wgrad(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
       } else {
-        epilogue<MODE>(args, ti, tmem_base + acc * BN, quad, lane);
+        epilogue<MODE>(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
       }
       tc_fence_before();
       __syncwarp();
@@ -796,6 +819,11 @@ bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, in
   return fn(m, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 output [rows][cols] for the token-row TMA-store epilogues.
+bool make_bf16_out_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows) {
+  return make_map(m, base, cols, rows, 32, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2);
 }
 
 // fp32 weight-gradient output [rows][cols] for the WGRAD TMA-store epilogue.
@@ -955,6 +983,9 @@ moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const v
       !make_map(&m.b1, wu, L.H, static_cast<int64_t>(L.E) * L.I, BN / 2))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
+  if (!make_bf16_out_map(&m.o0, g, L.I, L.R) || !make_bf16_out_map(&m.o1, u, L.I, L.R) ||
+      !make_bf16_out_map(&m.o2, act, L.I, L.R))
+    return MOE_ERR_CUDA;
   Args a = base_args(L, ws);
   a.n_nt = L.I / (BN / 2);
   a.kb1 = L.H / BK;
@@ -975,6 +1006,7 @@ moe_status gemm_down(const Layout& L, const void* ws, const void* act, const voi
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
   m.b1 = m.b0;
+  if (!make_bf16_out_map(&m.o0, ye, L.H, L.R)) return MOE_ERR_CUDA;
   Args a = base_args(L, ws);
   a.n_nt = L.H / BN;
   a.kb1 = L.I / BK;
@@ -1034,6 +1066,7 @@ moe_status gemm_gate_up_dgrad(const Layout& L, const void* ws, const void* dg, c
       !make_map(&m.b0, wg, L.H, static_cast<int64_t>(L.E) * L.I, 64) ||
       !make_map(&m.b1, wu, L.H, static_cast<int64_t>(L.E) * L.I, 64))
     return MOE_ERR_CUDA;
+  if (!make_bf16_out_map(&m.o0, dxe, L.H, L.R)) return MOE_ERR_CUDA;
   Args a = base_args(L, ws);
   a.n_nt = L.H / BN;
   a.kb1 = L.I / BK;
