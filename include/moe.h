@@ -180,6 +180,23 @@ moe_status moe_expert_down(const moe_problem* p, const void* ws, const void* act
 moe_status moe_combine(const moe_problem* p, const void* ws, const void* ye, const float* topk_w,
                        void* y, void* stream);
 
+/* Gate/up GEMM with the dispatch fused into its producer ([Clip] flowchart:
+ * dispatch feeding the expert FFN through a token buffer): the rows of each
+ * expert tile are gathered from the token-ordered x (bf16 [N,H]) by TMA
+ * straight into the shared-memory stage ring, so Xe is never written. Same
+ * G, U, Act as moe_dispatch + moe_expert_gate_up on every real row; padding
+ * rows hold finite values of another row instead of zeros (they are never
+ * read by the combine). g and u may both be NULL: then only Act is stored. */
+moe_status moe_expert_gate_up_gather(const moe_problem* p, const void* ws, const void* x,
+                                     const moe_weights* w, void* g, void* u, void* act,
+                                     void* stream);
+
+/* Forward without a context (inference): gathered gate/up (Act only), down,
+ * combine. Uses the workspace's backward buffers as scratch for Act and Ye,
+ * so it must not run between a moe_forward and its moe_backward. */
+moe_status moe_forward_inference(const moe_problem* p, const void* x, const moe_weights* w,
+                                 const float* topk_w, void* y, void* ws, void* stream);
+
 /* Whole forward: dispatch, gate/up, down, combine; saved = forward context. */
 moe_status moe_forward(const moe_problem* p, const void* x, const moe_weights* w,
                        const float* topk_w, void* y, void* saved, void* ws, void* stream);

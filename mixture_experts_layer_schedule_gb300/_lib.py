@@ -65,6 +65,8 @@ _SIGS = {
     "moe_expert_down": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_vp], c_i32),
     "moe_combine": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_vp], c_i32),
     "moe_forward": ([c_vp] * 8, c_i32),
+    "moe_expert_gate_up_gather": ([c_vp] * 8, c_i32),
+    "moe_forward_inference": ([c_vp] * 7, c_i32),
     "moe_reverse_combine": ([c_vp] * 8, c_i32),
     "moe_expert_down_dgrad": ([c_vp] * 9, c_i32),
     "moe_expert_down_wgrad": ([c_vp] * 6, c_i32),
@@ -206,6 +208,16 @@ def moe_combine(p, ws, ye, topk_w, y, stream=None):
 def moe_forward(p, x, w: Weights, topk_w, y, saved, ws, stream=None):
     _call("moe_forward", ctypes.byref(p), _ptr(x), ctypes.byref(w), _ptr(topk_w), _ptr(y),
           _ptr(saved), _ptr(ws), _stream(stream))
+
+
+def moe_expert_gate_up_gather(p, ws, x, w: Weights, g, u, act, stream=None):
+    _call("moe_expert_gate_up_gather", ctypes.byref(p), _ptr(ws), _ptr(x), ctypes.byref(w),
+          _ptr(g), _ptr(u), _ptr(act), _stream(stream))
+
+
+def moe_forward_inference(p, x, w: Weights, topk_w, y, ws, stream=None):
+    _call("moe_forward_inference", ctypes.byref(p), _ptr(x), ctypes.byref(w), _ptr(topk_w),
+          _ptr(y), _ptr(ws), _stream(stream))
 
 
 def moe_reverse_combine(p, ws, dy, ye, topk_w, dye, d_topk_w, stream=None):

@@ -50,7 +50,10 @@ constexpr int kSmemBytes = kStages * kStageBytes + kOutBytes + 1024;  // + align
 constexpr int kGemmThreads = 192;
 constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
 
-enum Mode { GATE_UP = 0, DOWN = 1, DACT = 2, DXE = 3, WGRAD = 4 };
+// GATE_UP_GATHER: GATE_UP with the dispatch fused into the producer -- the A
+// rows are gathered from the token-ordered x by TMA (tile::gather4), so the
+// expert-grouped Xe never exists in HBM; G and U may be skipped (inference).
+enum Mode { GATE_UP = 0, DOWN = 1, DACT = 2, DXE = 3, WGRAD = 4, GATE_UP_GATHER = 5 };
 
 struct Maps {
   CUtensorMap a0, a1, b0, b1;
@@ -71,6 +74,9 @@ struct Args {
   int b_rows;                  // rows per expert in B's 2-D view
   int E, w_mt, w_nt, n_probs;  // WGRAD tiling
   int ld_out;                  // output row length (elements)
+  const int32_t* src_of_row;   // GATE_UP_GATHER: assignment index of each row (-1: padding)
+  int k;                       // GATE_UP_GATHER: experts per token
+  int store_gu;                // GATE_UP(_GATHER): also store G and U
   void *out0, *out1, *out2;
   const void *in0, *in1;
 };
@@ -173,7 +179,9 @@ template <int MODE, int CL>
 __device__ __forceinline__ void issue_loads(const Maps& m, const Args& a, const TileInfo& ti,
                                             int kb, uint8_t* sA, uint8_t* sB, uint64_t* bar,
                                             int crank) {
-  if constexpr (MODE == GATE_UP) {
+  if constexpr (MODE == GATE_UP_GATHER) {
+    // loaded by the whole producer warp (see the kernel)
+  } else if constexpr (MODE == GATE_UP) {
     load_a_rows<CL>(sA, &m.a0, bar, kb * BK, ti.row0, crank);
     const int brow = ti.e * a.b_rows + ti.nt * (BN / 2);
     tma_load_2d(sB, &m.b0, bar, kb * BK, brow);
@@ -266,14 +274,16 @@ __device__ __forceinline__ void epilogue(const Maps& m, const Args& a, const Til
                                          uint8_t* stage_out, uint32_t& nstore) {
   const uint32_t taddr = tmem_acc + (static_cast<uint32_t>(quad * 32) << 16);
   const int32_t y = ti.row0 + quad * 32;
-  if constexpr (MODE == GATE_UP) {
+  if constexpr (MODE == GATE_UP || MODE == GATE_UP_GATHER) {
     const int32_t x0 = ti.nt * (BN / 2);
     for (int c = 0; c < BN / 2; c += 64) {
       float g[64], u[64];
       tmem_ld64(taddr + c, g);
       tmem_ld64(taddr + BN / 2 + c, u);
-      store_block_bf16(&m.o0, g, x0 + c, y, lane, stage_out, nstore);
-      store_block_bf16(&m.o1, u, x0 + c, y, lane, stage_out, nstore);
+      if (a.store_gu) {
+        store_block_bf16(&m.o0, g, x0 + c, y, lane, stage_out, nstore);
+        store_block_bf16(&m.o1, u, x0 + c, y, lane, stage_out, nstore);
+      }
 #pragma unroll
       for (int i = 0; i < 64; ++i) g[i] = silu(g[i]) * u[i];
       store_block_bf16(&m.o2, g, x0 + c, y, lane, stage_out, nstore);
@@ -410,8 +420,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const int64_t first = blockIdx.x / CL, stride = gridDim.x / CL;
 
-  if (warp == 0) {
-    if (lane == 0) {
+  if (warp == 0 && MODE == GATE_UP_GATHER) {
+   if constexpr (MODE == GATE_UP_GATHER) {
+    // ---------------- TMA producer, gathering A rows (whole warp) ----------------
+    // Lane l owns rows 4l..4l+3 of the 128-row tile: it looks up their tokens
+    // once per tile and issues one gather4 per k-block; lane 0 arms the stage
+    // barrier and loads the gate/up weight rows.
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_mask = 0, issued_parity = 0;
+    bool ok = true;
+    for (int64_t t = first; t < total && ok; t += stride) {
+      const TileInfo ti = decode_tile<MODE, CL>(args, t, crank);
+      int32_t tok[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int32_t src = ti.nkb > 0 ? args.src_of_row[ti.row0 + 4 * lane + r] : -1;
+        tok[r] = src >= 0 ? src / args.k : 0;  // padding rows read token 0 (finite, unused)
+      }
+      for (int kb = 0; kb < ti.nkb; ++kb) {
+        int ready = 1;
+        if (lane == 0) ready = mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, args.err) ? 1 : 0;
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        if (!ready) { ok = false; break; }
+        uint8_t* sA = smem + stage * kStageBytes;
+        if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
+        __syncwarp();
+        tma_gather4(sA + lane * 4 * (BK * 2), &maps.a0, &full_bar[stage], kb * BK, tok[0], tok[1],
+                    tok[2], tok[3]);
+        if (lane == 0) {
+          const int brow = ti.e * args.b_rows + ti.nt * (BN / 2);
+          tma_load_2d(sA + kABytes, &maps.b0, &full_bar[stage], kb * BK, brow);
+          tma_load_2d(sA + kABytes + kBBytes / 2, &maps.b1, &full_bar[stage], kb * BK, brow);
+        }
+        issued_mask |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (lane == 0)
+      for (int s = 0; s < kStages; ++s)
+        if ((issued_mask >> s) & 1u) wait_drain(&full_bar[s], (issued_parity >> s) & 1u, args.err);
+   }
+  } else if (warp == 0) {
+    if (lane == 0 && MODE != GATE_UP_GATHER) {
       // ---------------- TMA producer ----------------
       int stage = 0;
       uint32_t phase = 0;
@@ -995,7 +1047,33 @@ moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const v
   a.out0 = g;
   a.out1 = u;
   a.out2 = act;
+  a.store_gu = 1;
   return launch_tokens<GATE_UP>(L, m, a, s);
+}
+
+moe_status gemm_gate_up_gather(const Layout& L, const void* ws, const void* x, const void* wg,
+                               const void* wu, void* g, void* u, void* act, cudaStream_t s) {
+  if (L.N == 0) return MOE_OK;
+  Maps m{};
+  if (!make_map(&m.a0, x, L.H, L.N, 1) ||
+      !make_map(&m.b0, wg, L.H, static_cast<int64_t>(L.E) * L.I, BN / 2) ||
+      !make_map(&m.b1, wu, L.H, static_cast<int64_t>(L.E) * L.I, BN / 2) ||
+      !make_bf16_out_map(&m.o2, act, L.I, L.R))
+    return MOE_ERR_CUDA;
+  const bool store_gu = g != nullptr && u != nullptr;
+  if (store_gu && (!make_bf16_out_map(&m.o0, g, L.I, L.R) || !make_bf16_out_map(&m.o1, u, L.I, L.R)))
+    return MOE_ERR_CUDA;
+  m.a1 = m.a0;
+  Args a = base_args(L, ws);
+  a.n_nt = L.I / (BN / 2);
+  a.kb1 = L.H / BK;
+  a.kb2 = 0;
+  a.b_rows = L.I;
+  a.ld_out = L.I;
+  a.src_of_row = at<int32_t>(ws, L.src_of_row);
+  a.k = L.k;
+  a.store_gu = store_gu ? 1 : 0;
+  return launch<GATE_UP_GATHER, 1>(m, a, static_cast<int64_t>(a.max_mtiles) * a.n_nt, s);
 }
 
 moe_status gemm_down(const Layout& L, const void* ws, const void* act, const void* wd, void* ye,

@@ -201,6 +201,29 @@ moe_status moe_combine(const moe_problem* p, const void* ws, const void* ye, con
   return cu(launch_combine(L, ws, ye, topk_w, y, S(stream)));
 }
 
+moe_status moe_expert_gate_up_gather(const moe_problem* p, const void* ws, const void* x,
+                                     const moe_weights* w, void* g, void* u, void* act,
+                                     void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if ((L.N > 0 && !aligned(x, 16)) || !weights_ok(w) || !aligned(act, 16))
+    return MOE_ERR_INVALID_ARG;
+  if ((g == nullptr) != (u == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (g && (!aligned(g, 16) || !aligned(u, 16))) return MOE_ERR_INVALID_ARG;
+  return gemm_gate_up_gather(L, ws, x, w->w_gate, w->w_up, g, u, act, S(stream));
+}
+
+moe_status moe_forward_inference(const moe_problem* p, const void* x, const moe_weights* w,
+                                 const float* topk_w, void* y, void* ws, void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  void* act = at<char>(ws, L.dg);    // [R, I] scratch
+  void* ye = at<char>(ws, L.dyxe);   // [R, H] scratch
+  MOE_TRY(moe_expert_gate_up_gather(p, ws, x, w, nullptr, nullptr, act, stream));
+  MOE_TRY(moe_expert_down(p, ws, act, w, ye, stream));
+  return moe_combine(p, ws, ye, topk_w, y, stream);
+}
+
 moe_status moe_forward(const moe_problem* p, const void* x, const moe_weights* w,
                        const float* topk_w, void* y, void* saved, void* ws, void* stream) {
   moe_saved_view v;

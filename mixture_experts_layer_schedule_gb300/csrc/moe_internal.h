@@ -63,6 +63,8 @@ cudaError_t launch_mxfp8_quantize(const void* src, int64_t rows, int64_t cols, u
 // Grouped GEMMs (tcgen05). Return MOE_ERR_CUDA on a driver/launch failure.
 moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const void* wg,
                         const void* wu, void* g, void* u, void* act, cudaStream_t s);
+moe_status gemm_gate_up_gather(const Layout& L, const void* ws, const void* x, const void* wg,
+                               const void* wu, void* g, void* u, void* act, cudaStream_t s);
 moe_status gemm_down(const Layout& L, const void* ws, const void* act, const void* wd, void* ye,
                      cudaStream_t s);
 moe_status gemm_down_dgrad(const Layout& L, const void* ws, const void* dye, const void* g,

@@ -87,6 +87,13 @@ class MoELayer:
                          self.saved, self.ws, stream)
         return self.y
 
+    def forward_inference(self, x, wg, wu, wd, topk_w=None, stream=None):
+        """Forward without a saved context; the dispatch is fused into gate/up."""
+        w = _lib.weights(wg, wu, wd)
+        _lib.moe_forward_inference(self.p, x, w, self.topk_w if topk_w is None else topk_w,
+                                   self.y, self.ws, stream)
+        return self.y
+
     def backward(self, dy, wg, wu, wd, topk_w=None, stream=None) -> Grads:
         g = self.grads
         w = _lib.weights(wg, wu, wd)
