@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--cpu-tokens", type=int, default=0,
                     help="oracle sample size in tokens (0 = sized for ~15 s)")
     ap.add_argument("--phase-report", action="store_true", help="print per-phase timings")
+    ap.add_argument("--inference", action="store_true",
+                    help="forward-only workloads: time the context-free forward (dispatch "
+                         "fused into gate/up) instead of the training forward")
     return ap.parse_args()
 
 
@@ -155,7 +158,8 @@ class ClockSampler:
 def phase_flops(shape):
     """Algorithmic flops of each GEMM phase (padding rows excluded)."""
     A, H, I = shape.N * shape.k, shape.H, shape.I
-    return {"gate_up": 4 * A * H * I, "down": 2 * A * H * I, "down_dgrad": 2 * A * H * I,
+    return {"gate_up": 4 * A * H * I, "gate_up_gather": 4 * A * H * I,
+            "down": 2 * A * H * I, "down_dgrad": 2 * A * H * I,
             "down_wgrad": 2 * A * H * I, "gate_up_dgrad": 4 * A * H * I,
             "gate_up_wgrad": 4 * A * H * I}
 
@@ -207,7 +211,10 @@ def run_ours(args, ws_, rank, local):
     stream = torch.cuda.current_stream()
     backward = shape.backward
 
+    inference = args.inference and not backward
     phases = ["route", "schedule", "dispatch", "gate_up", "down", "combine"]
+    if inference:
+        phases = ["route", "schedule", "gate_up_gather", "down", "combine"]
     if backward:
         phases += ["reverse_combine", "down_dgrad", "down_wgrad", "gate_up_dgrad",
                    "gate_up_wgrad", "reverse_dispatch"]
@@ -218,6 +225,8 @@ def run_ours(args, ws_, rank, local):
         "dispatch": lambda: _lib.moe_dispatch(p, wsb, inp["x"], sv["xe"]),
         "gate_up": lambda: _lib.moe_expert_gate_up(p, wsb, sv["xe"], w, sv["g"], sv["u"],
                                                    sv["act"]),
+        "gate_up_gather": lambda: _lib.moe_expert_gate_up_gather(p, wsb, inp["x"], w, None, None,
+                                                                 sv["act"]),
         "down": lambda: _lib.moe_expert_down(p, wsb, sv["act"], w, sv["ye"]),
         "combine": lambda: _lib.moe_combine(p, wsb, sv["ye"], layer.topk_w, layer.y),
         "reverse_combine": lambda: _lib.moe_reverse_combine(p, wsb, inp["dy"], sv["ye"],
@@ -286,8 +295,13 @@ def run_ours(args, ws_, rank, local):
     for _ in range(args.e2e_steps):
         for k, v in pin.items():
             dx_in[k].copy_(v, non_blocking=True)
-        layer.step(dx_in["x"], dx_in["logits"], inp["bias"], inp["wg"], inp["wu"], inp["wd"],
-                   dx_in.get("dy"), backward=backward)
+        if inference:
+            layer.route(dx_in["logits"], inp["bias"])
+            layer.build_schedule()
+            layer.forward_inference(dx_in["x"], inp["wg"], inp["wu"], inp["wd"])
+        else:
+            layer.step(dx_in["x"], dx_in["logits"], inp["bias"], inp["wg"], inp["wu"], inp["wd"],
+                       dx_in.get("dy"), backward=backward)
         out_y.copy_(layer.y, non_blocking=True)
         if backward:
             out_dx.copy_(g.dx, non_blocking=True)
@@ -340,7 +354,8 @@ def run_ours(args, ws_, rank, local):
         "config": {"workload": shape.name, "N": shape.N, "H": shape.H, "I": shape.I,
                    "E": shape.E, "k": shape.k, "zipf_bias": shape.zipf_s,
                    "minibatch_rows": shape.minibatch_rows,
-                   "passes": "fwd+bwd" if backward else "fwd",
+                   "passes": "fwd+bwd" if backward else ("fwd (inference)" if inference
+                                                           else "fwd"),
                    "l2": "inputs larger than L2 (expert weights alone "
                          f"{3 * shape.E * shape.H * shape.I * 2 / 1e9:.2f} GB)",
                    "parallelism": f"replicas x{ws_}"},

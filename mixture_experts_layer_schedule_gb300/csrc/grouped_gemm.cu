@@ -423,9 +423,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && MODE == GATE_UP_GATHER) {
    if constexpr (MODE == GATE_UP_GATHER) {
     // ---------------- TMA producer, gathering A rows (whole warp) ----------------
-    // Lane l owns rows 4l..4l+3 of the 128-row tile: it looks up their tokens
-    // once per tile and issues one gather4 per k-block; lane 0 arms the stage
-    // barrier and loads the gate/up weight rows.
+    // Lane l owns rows 4l..4l+3 of the CTA's share of the 128-row tile (all of
+    // it, or with CL = 2 one 64-row half, multicast to both CTAs of the pair,
+    // which compute neighbouring N tiles of the same rows): it looks up their
+    // tokens once per tile and issues one gather4 per k-block; lane 0 arms the
+    // stage barrier and loads the gate/up weight rows.
+    constexpr int kRowsPerCta = BM / CL;
+    const bool gathers = lane < kRowsPerCta / 4;
+    const int rbase = crank * kRowsPerCta + 4 * lane;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
@@ -435,7 +440,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int32_t tok[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int32_t src = ti.nkb > 0 ? args.src_of_row[ti.row0 + 4 * lane + r] : -1;
+        const int32_t src = (ti.nkb > 0 && gathers) ? args.src_of_row[ti.row0 + rbase + r] : -1;
         tok[r] = src >= 0 ? src / args.k : 0;  // padding rows read token 0 (finite, unused)
       }
       for (int kb = 0; kb < ti.nkb; ++kb) {
@@ -446,8 +451,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint8_t* sA = smem + stage * kStageBytes;
         if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
         __syncwarp();
-        tma_gather4(sA + lane * 4 * (BK * 2), &maps.a0, &full_bar[stage], kb * BK, tok[0], tok[1],
-                    tok[2], tok[3]);
+        if (gathers) {
+          if constexpr (CL == 1)
+            tma_gather4(sA + rbase * (BK * 2), &maps.a0, &full_bar[stage], kb * BK, tok[0],
+                        tok[1], tok[2], tok[3]);
+          else
+            tma_gather4_mc(sA + rbase * (BK * 2), &maps.a0, &full_bar[stage], kb * BK, tok[0],
+                           tok[1], tok[2], tok[3], (1u << CL) - 1);
+        }
         if (lane == 0) {
           const int brow = ti.e * args.b_rows + ti.nt * (BN / 2);
           tma_load_2d(sA + kABytes, &maps.b0, &full_bar[stage], kb * BK, brow);
@@ -514,7 +525,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             umma_bf16(dtmem, ad, bd, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
           }
           if constexpr (CL == 1) umma_commit(&empty_bar[stage]);  // stage free once read
-          else umma_commit_mc(&empty_bar[stage], 0x3);          // ... in both CTAs' view
+          else umma_commit_mc(&empty_bar[stage], (1u << CL) - 1);  // ... in every CTA's view
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -1073,6 +1084,13 @@ moe_status gemm_gate_up_gather(const Layout& L, const void* ws, const void* x, c
   a.src_of_row = at<int32_t>(ws, L.src_of_row);
   a.k = L.k;
   a.store_gu = store_gu ? 1 : 0;
+  // clusters of four CTAs (neighbouring N tiles of the same rows) gather a
+  // quarter of the rows each and multicast them: the gather instruction count
+  // per CTA, not bandwidth, limits a gathering producer
+  if (a.n_nt % 4 == 0)
+    return launch<GATE_UP_GATHER, 4>(m, a, static_cast<int64_t>(a.max_mtiles) * (a.n_nt / 4), s);
+  if (a.n_nt % 2 == 0)
+    return launch<GATE_UP_GATHER, 2>(m, a, static_cast<int64_t>(a.max_mtiles) * (a.n_nt / 2), s);
   return launch<GATE_UP_GATHER, 1>(m, a, static_cast<int64_t>(a.max_mtiles) * a.n_nt, s);
 }
 

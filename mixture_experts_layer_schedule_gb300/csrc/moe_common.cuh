@@ -119,6 +119,18 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tm, ui
       : "memory");
 }
 
+// gather4 delivered to the same offset of every CTA in cta_mask.
+__device__ __forceinline__ void tma_gather4_mc(void* dst, const CUtensorMap* tm, uint64_t* bar,
+                                               int32_t c0, int32_t r0, int32_t r1, int32_t r2,
+                                               int32_t r3, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2),
+      "r"(r3), "h"(cta_mask)
+      : "memory");
+}
+
 // ---- thread-block clusters ----------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
