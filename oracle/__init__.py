@@ -70,6 +70,8 @@ def lib():
                                                 vp, vp, vp, i32, i64, vp, i64, vp, vp, vp,
                                                 vp, ctypes.c_int]
             L.orc_mxfp8_quantize.argtypes = [i64, i64, vp, vp, vp]
+            L.orc_layer_mxfp8.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp,
+                                          ctypes.c_int, vp, vp, vp, vp, vp, vp, ctypes.c_int]
             L.orc_e4m3_encode.argtypes = [ctypes.c_double]
             L.orc_e4m3_encode.restype = ctypes.c_uint8
             L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
@@ -226,6 +228,21 @@ def expert_wgrad_bf16(x, wg, wu, wd, ids, w, dy, e, i_list, h_list, threads=0):
                                        _p(w), _p(dy), int(e), len(il), _p(il), len(hl), _p(hl),
                                        _p(dwg), _p(dwu), _p(dwd), threads))
     return dict(dwg=dwg, dwu=dwu, dwd=dwd)
+
+
+def layer_mxfp8(x, wg, wu, wd, ids, w, dy, quantize=True, threads=0):
+    """MXFP8 layer forward + backward (quantised GEMM operands, fp64 sums)."""
+    x, wg, wu, wd, dy = (as_bf16_bits(a) for a in (x, wg, wu, wd, dy))
+    ids, w = _c(ids, np.int32), _c(w, np.float64)
+    N, H = x.shape
+    E, I, _ = wg.shape
+    k = ids.shape[1]
+    y = np.empty((N, H))
+    dx, dwg, dwu, dwd, dw = _bw_out(N, H, I, E, k)
+    _check(lib().orc_layer_mxfp8(N, H, I, E, k, _p(x), _p(wg), _p(wu), _p(wd), _p(ids), _p(w),
+                                 _p(dy), 1 if quantize else 0, _p(y), _p(dx), _p(dwg), _p(dwu),
+                                 _p(dwd), _p(dw), threads))
+    return dict(y=y, dx=dx, dwg=dwg, dwu=dwu, dwd=dwd, dw=dw)
 
 
 def mxfp8_quantize(src_bits):

@@ -514,4 +514,204 @@ int orc_mxfp8_quantize(int64_t rows, int64_t cols, const uint16_t* src,
   return ORC_OK;
 }
 
+// ---------------------------------------------------------------------------
+// MXFP8 layer: every operand of every GEMM is quantised to MXFP8 along that
+// GEMM's K (1x32 blocks, E8M0 scale, E4M3 elements; the rule of
+// orc_mxfp8_quantize) and dequantised exactly; products are summed in fp64.
+// An intermediate is first rounded to bf16 (where the layer stores it) and
+// then quantised. Token-axis blocks (weight gradients) hold 32 consecutive
+// assignments of one expert in slot order (ascending token) and restart at
+// each expert; a short last block is padded with zeros.
+
+int orc_mxfp8_quantize(int64_t rows, int64_t cols, const uint16_t* src, uint8_t* q,
+                       uint8_t* scale);
+
+namespace {
+
+double round_bf16(double v) {
+  float f = static_cast<float>(v);  // correctly rounded fp64 -> fp32
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  // fp32 -> bf16 round to nearest even (finite values)
+  u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
+  std::memcpy(&f, &u, 4);
+  return static_cast<double>(f);
+}
+
+// Quantise-dequantise one block of n <= 32 values (each exactly a bf16 value).
+void qdq_block(double* v, int n) {
+  double amax = 0.0;
+  for (int i = 0; i < n; ++i) amax = std::max(amax, std::fabs(v[i]));
+  int code = 0;
+  if (amax > 0.0) {
+    int ex;
+    std::frexp(amax, &ex);
+    code = std::min(254, std::max(0, (ex - 1) - 8 + 127));
+  }
+  for (int i = 0; i < n; ++i)
+    v[i] = orc_e4m3_decode(orc_e4m3_encode(std::ldexp(v[i], 127 - code))) *
+           std::ldexp(1.0, code - 127);
+}
+
+// Quantise-dequantise a vector along its length in blocks of 32.
+void qdq_vec(double* v, int64_t n) {
+  for (int64_t b = 0; b < n; b += 32) qdq_block(v + b, static_cast<int>(std::min<int64_t>(32, n - b)));
+}
+
+}  // namespace
+
+extern "C" int orc_layer_mxfp8(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k,
+                               const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
+                               const uint16_t* wd, const int32_t* ids, const double* w,
+                               const uint16_t* dy, int quantize, double* y, double* dx,
+                               double* dwg, double* dwu, double* dwd, double* dw,
+                               int threads) {
+  if (N < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || k > E) return ORC_ERR_ARG;
+  const int64_t A = N * k;
+  for (int64_t a = 0; a < A; ++a)
+    if (ids[a] < 0 || ids[a] >= E) return ORC_ERR_ARG;
+  auto q = [quantize](double* v, int64_t n) { if (quantize) qdq_vec(v, n); };
+  auto rb = [quantize](double v) { return quantize ? round_bf16(v) : v; };
+  const int64_t HI = static_cast<int64_t>(H) * I;
+  // Weights as each GEMM reads them:
+  //   gate/up forward: rows of Wg[e], Wu[e] along H;  down forward: rows of Wd[e] along I;
+  //   down backward (dA = Wd^T dye): columns of Wd[e] along H;
+  //   gate/up backward (dxe = Wg^T dg + Wu^T du): columns of Wg[e], Wu[e] along I.
+  std::vector<double> wg_h(E * HI), wu_h(E * HI), wd_i(E * HI), wd_h(E * HI), wg_i(E * HI),
+      wu_i(E * HI);
+  for (int64_t i = 0; i < E * HI; ++i) {
+    wg_h[i] = wg_i[i] = bf16_to_double(wg[i]);
+    wu_h[i] = wu_i[i] = bf16_to_double(wu[i]);
+    wd_i[i] = wd_h[i] = bf16_to_double(wd[i]);
+  }
+  std::vector<double> col(std::max(H, I));
+  for (int32_t e = 0; e < E; ++e) {
+    const int64_t o = e * HI;
+    for (int32_t i = 0; i < I; ++i) {           // Wg/Wu [e][i][:] along H
+      q(&wg_h[o + static_cast<int64_t>(i) * H], H);
+      q(&wu_h[o + static_cast<int64_t>(i) * H], H);
+    }
+    for (int32_t h = 0; h < H; ++h) q(&wd_i[o + static_cast<int64_t>(h) * I], I);  // Wd [e][h][:]
+    for (int32_t i = 0; i < I; ++i) {           // Wd [e][:][i] along H
+      for (int32_t h = 0; h < H; ++h) col[h] = wd_h[o + static_cast<int64_t>(h) * I + i];
+      q(col.data(), H);
+      for (int32_t h = 0; h < H; ++h) wd_h[o + static_cast<int64_t>(h) * I + i] = col[h];
+    }
+    for (int32_t h = 0; h < H; ++h) {           // Wg/Wu [e][:][h] along I
+      for (int32_t i = 0; i < I; ++i) col[i] = wg_i[o + static_cast<int64_t>(i) * H + h];
+      q(col.data(), I);
+      for (int32_t i = 0; i < I; ++i) wg_i[o + static_cast<int64_t>(i) * H + h] = col[i];
+      for (int32_t i = 0; i < I; ++i) col[i] = wu_i[o + static_cast<int64_t>(i) * H + h];
+      q(col.data(), I);
+      for (int32_t i = 0; i < I; ++i) wu_i[o + static_cast<int64_t>(i) * H + h] = col[i];
+    }
+  }
+  // Per-assignment forward and backward.
+  std::vector<double> G(A * I), U(A * I), Ab(A * I), DYe(A * H), DG(A * I), DU(A * I), YE(A * H);
+  parallel_for(N, threads, [&](int64_t t) {
+    std::vector<double> xq(H), aq(I), dq(H), da(I), gq(I), uq(I);
+    for (int32_t h = 0; h < H; ++h) xq[h] = bf16_to_double(x[t * H + h]);
+    q(xq.data(), H);                                                   // Xe rows along H
+    for (int32_t h = 0; h < H; ++h) { y[t * H + h] = 0.0; dx[t * H + h] = 0.0; }
+    for (int32_t j = 0; j < k; ++j) {
+      const int64_t a = t * k + j;
+      const int32_t e = ids[a];
+      const int64_t o = e * HI;
+      for (int32_t i = 0; i < I; ++i) {
+        double gs = 0.0, us = 0.0;
+        for (int32_t h = 0; h < H; ++h) {
+          gs += wg_h[o + static_cast<int64_t>(i) * H + h] * xq[h];
+          us += wu_h[o + static_cast<int64_t>(i) * H + h] * xq[h];
+        }
+        G[a * I + i] = gs;
+        U[a * I + i] = us;
+        Ab[a * I + i] = rb(gs * sigmoid(gs) * us);                     // Act, stored bf16
+        aq[i] = Ab[a * I + i];
+      }
+      q(aq.data(), I);                                                 // Act rows along I
+      double dwa = 0.0;
+      for (int32_t h = 0; h < H; ++h) {
+        double acc = 0.0;
+        for (int32_t i = 0; i < I; ++i) acc += wd_i[o + static_cast<int64_t>(h) * I + i] * aq[i];
+        YE[a * H + h] = acc;
+        y[t * H + h] += w[a] * acc;                                    // combine
+        const double dyv = bf16_to_double(dy[t * H + h]);
+        dwa += dyv * acc;
+        DYe[a * H + h] = rb(w[a] * dyv);                               // dYe, stored bf16
+        dq[h] = DYe[a * H + h];
+      }
+      dw[a] = dwa;
+      q(dq.data(), H);                                                 // dYe rows along H
+      for (int32_t i = 0; i < I; ++i) {
+        double acc = 0.0;
+        for (int32_t h = 0; h < H; ++h) acc += wd_h[o + static_cast<int64_t>(h) * I + i] * dq[h];
+        da[i] = acc;
+      }
+      for (int32_t i = 0; i < I; ++i) {
+        const double g = G[a * I + i], u = U[a * I + i], sg = sigmoid(g);
+        DG[a * I + i] = rb(da[i] * u * sg * (1.0 + g * (1.0 - sg)));  // dG, dU stored bf16
+        DU[a * I + i] = rb(da[i] * g * sg);
+        gq[i] = DG[a * I + i];
+        uq[i] = DU[a * I + i];
+      }
+      q(gq.data(), I);                                                 // dG, dU rows along I
+      q(uq.data(), I);
+      for (int32_t h = 0; h < H; ++h) {
+        double acc = 0.0;
+        for (int32_t i = 0; i < I; ++i)
+          acc += wg_i[o + static_cast<int64_t>(i) * H + h] * gq[i] +
+                 wu_i[o + static_cast<int64_t>(i) * H + h] * uq[i];
+        dx[t * H + h] += acc;                                          // reverse-dispatch
+      }
+    }
+  });
+  // Weight gradients: contraction over each expert's assignments (slot order),
+  // each operand column quantised along that axis in blocks of 32.
+  std::vector<std::vector<int64_t>> of_e(E);
+  for (int64_t a = 0; a < A; ++a) of_e[ids[a]].push_back(a);
+  parallel_for(E, threads, [&](int64_t e) {
+    const std::vector<int64_t>& as = of_e[e];
+    const int64_t M = static_cast<int64_t>(as.size());
+    const int64_t o = e * HI;
+    std::vector<double> c1(M), c2(M);
+    // token-axis quantised operands, column by column
+    std::vector<double> dyeT(H * M), actT(I * M), dgT(I * M), duT(I * M), xeT(H * M);
+    for (int32_t h = 0; h < H; ++h) {
+      for (int64_t m = 0; m < M; ++m) c1[m] = DYe[as[m] * H + h];
+      q(c1.data(), M);
+      for (int64_t m = 0; m < M; ++m) c2[m] = bf16_to_double(x[(as[m] / k) * H + h]);
+      q(c2.data(), M);
+      for (int64_t m = 0; m < M; ++m) { dyeT[h * M + m] = c1[m]; xeT[h * M + m] = c2[m]; }
+    }
+    for (int32_t i = 0; i < I; ++i) {
+      for (int64_t m = 0; m < M; ++m) c1[m] = Ab[as[m] * I + i];
+      q(c1.data(), M);
+      for (int64_t m = 0; m < M; ++m) actT[i * M + m] = c1[m];
+      for (int64_t m = 0; m < M; ++m) c1[m] = DG[as[m] * I + i];
+      q(c1.data(), M);
+      for (int64_t m = 0; m < M; ++m) dgT[i * M + m] = c1[m];
+      for (int64_t m = 0; m < M; ++m) c1[m] = DU[as[m] * I + i];
+      q(c1.data(), M);
+      for (int64_t m = 0; m < M; ++m) duT[i * M + m] = c1[m];
+    }
+    for (int32_t h = 0; h < H; ++h)
+      for (int32_t i = 0; i < I; ++i) {
+        double acc = 0.0;
+        for (int64_t m = 0; m < M; ++m) acc += dyeT[h * M + m] * actT[i * M + m];
+        dwd[o + static_cast<int64_t>(h) * I + i] = acc;
+      }
+    for (int32_t i = 0; i < I; ++i)
+      for (int32_t h = 0; h < H; ++h) {
+        double ag = 0.0, au = 0.0;
+        for (int64_t m = 0; m < M; ++m) {
+          ag += dgT[i * M + m] * xeT[h * M + m];
+          au += duT[i * M + m] * xeT[h * M + m];
+        }
+        dwg[o + static_cast<int64_t>(i) * H + h] = ag;
+        dwu[o + static_cast<int64_t>(i) * H + h] = au;
+      }
+  });
+  return ORC_OK;
+}
+
 }  // extern "C"

@@ -125,6 +125,24 @@ int orc_expert_wgrad_bf16(int64_t N, int32_t H, int32_t I, int32_t E,
                           const int32_t* h_list, double* dwg_rows,
                           double* dwu_rows, double* dwd_rows, int threads);
 
+/* MXFP8 layer (the MXFP8 workload): the layer forward + backward with every
+ * operand of every GEMM quantised to MXFP8 along that GEMM's K and
+ * dequantised exactly (rule of orc_mxfp8_quantize):
+ *   gate/up fwd: Xe rows and Wg/Wu rows along H; down fwd: Act rows and Wd
+ *   rows along I; down bwd: dYe rows and Wd columns along H; gate/up bwd:
+ *   dG/dU rows and Wg/Wu columns along I; weight gradients: both operands
+ *   along the token axis in blocks of 32 consecutive assignments of one
+ *   expert (slot order), restarting per expert, zero-padded.
+ * Intermediates that are quantised (Act, dYe, dG, dU) are first rounded to
+ * bf16. quantize = 0 skips every quantisation and rounding (then the result
+ * equals orc_backward_bf16 / orc_forward_bf16 exactly). Outputs as in
+ * orc_forward_bf16 / orc_backward_bf16 (y, dx, dwg, dwu, dwd, dw). */
+int orc_layer_mxfp8(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k, const uint16_t* x,
+                    const uint16_t* wg, const uint16_t* wu, const uint16_t* wd,
+                    const int32_t* ids, const double* w, const uint16_t* dy, int quantize,
+                    double* y, double* dx, double* dwg, double* dwu, double* dwd, double* dw,
+                    int threads);
+
 /* MXFP8 quantiser (OCP MX v1.0, MXFP8 E4M3): for each block of 32
  * consecutive values along a row, X = 2^(floor(log2(amax)) - 8) (8 = the
  * largest E4M3 exponent), scale code = that exponent + 127 clamped to

@@ -1,0 +1,81 @@
+"""Pins for the oracle's MXFP8 layer (every GEMM operand quantised to MXFP8
+along that GEMM's K; the MXFP8 workload of the pages' benchmark set).
+
+* quantisation off: identical to the fp64 layer oracle (pins the plumbing:
+  which products are summed, in which order);
+* quantisation on: within the MXFP8 error scale of the unquantised layer and
+  different from it;
+* quantisation axis of one GEMM operand: a huge outlier in one column of the
+  down weights flushes the small values sharing its 1x32 blocks to zero only
+  when the blocks run along H (the K of the down backward), which changes the
+  data gradient by a predictable, large amount.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+def _bits(a):
+    u = np.ascontiguousarray(a, np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def _layer(N, H, I, E, k, seed):
+    rng = np.random.default_rng(seed)
+    x = _bits(rng.standard_normal((N, H)))
+    wg = _bits(rng.standard_normal((E, I, H)) / math.sqrt(H))
+    wu = _bits(rng.standard_normal((E, I, H)) / math.sqrt(H))
+    wd = _bits(rng.standard_normal((E, H, I)) / math.sqrt(H))
+    dy = _bits(rng.standard_normal((N, H)))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(N)]).astype(np.int32)
+    w = rng.random((N, k)) + 0.1
+    w /= w.sum(1, keepdims=True)
+    return x, wg, wu, wd, ids, w, dy
+
+
+def test_without_quantisation_equals_the_layer_oracle():
+    x, wg, wu, wd, ids, w, dy = _layer(40, 64, 96, 5, 2, 1)
+    r = oracle.layer_mxfp8(x, wg, wu, wd, ids, w, dy, quantize=False)
+    yb = oracle.forward_bf16(x, wg, wu, wd, ids, w)
+    rb = oracle.backward_bf16(x, wg, wu, wd, ids, w, dy)
+    np.testing.assert_array_equal(r["y"], yb)
+    for key in ("dx", "dwg", "dwu", "dwd", "dw"):
+        np.testing.assert_array_equal(r[key], rb[key])
+
+
+def test_quantised_layer_stays_within_the_mxfp8_error_scale():
+    x, wg, wu, wd, ids, w, dy = _layer(64, 64, 96, 4, 2, 2)
+    r = oracle.layer_mxfp8(x, wg, wu, wd, ids, w, dy, quantize=True)
+    ref = oracle.layer_mxfp8(x, wg, wu, wd, ids, w, dy, quantize=False)
+    for key in ("y", "dx", "dwg", "dwu", "dwd", "dw"):
+        err = np.max(np.abs(r[key] - ref[key])) / np.max(np.abs(ref[key]))
+        # E4M3 keeps 3 mantissa bits (relative rounding <= 2^-4 per operand);
+        # a few quantised factors per output stay well inside 0.25
+        assert 1e-4 < err < 0.25, (key, err)
+
+
+def test_down_backward_quantises_wd_along_h():
+    """dx depends on Wd only through dA = Wd^T dYe, whose K is H. An outlier
+    2^20 times larger than the rest in Wd[0][0][i] shares its H-blocks
+    (h = 0..31, fixed i) with 31 small values that then flush to zero, so
+    dA[i] loses their contribution for every i of the outlier row. Putting the
+    outliers in a whole row h = 0 makes the flush cover every i."""
+    N, H, I, E, k = 3, 64, 64, 1, 1
+    x, wg, wu, wd, ids, w, dy = _layer(N, H, I, E, k, 3)
+    wd_f = oracle.bf16_bits_to_f64(wd)
+    wd_f[0, 0, :] = 2.0 ** 20
+    wd_out = _bits(wd_f)
+    base = oracle.layer_mxfp8(x, wg, wu, wd_out, ids, w, dy, quantize=True)
+    # Same weights but rows h = 1..31 of Wd zeroed: if Wd is quantised along
+    # H those rows are flushed anyway, so dx must not change at all.
+    wd_z = wd_f.copy()
+    wd_z[0, 1:32, :] = 0.0
+    flushed = oracle.layer_mxfp8(x, wg, wu, _bits(wd_z), ids, w, dy, quantize=True)
+    np.testing.assert_array_equal(base["dx"], flushed["dx"])
+    # ... while without quantisation zeroing those rows does change dx
+    a = oracle.layer_mxfp8(x, wg, wu, wd_out, ids, w, dy, quantize=False)
+    b = oracle.layer_mxfp8(x, wg, wu, _bits(wd_z), ids, w, dy, quantize=False)
+    assert np.max(np.abs(a["dx"] - b["dx"])) > 0
