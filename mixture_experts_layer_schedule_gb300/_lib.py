@@ -29,7 +29,8 @@ class Problem(ctypes.Structure):
 
 
 class Weights(ctypes.Structure):
-    _fields_ = [("w_gate", c_vp), ("w_up", c_vp), ("w_down", c_vp)]
+    _fields_ = [("w_gate", c_vp), ("w_up", c_vp), ("w_down", c_vp),
+                ("w_gate_bwd", c_vp), ("w_up_bwd", c_vp), ("w_down_bwd", c_vp)]
 
 
 class Schedule(ctypes.Structure):
@@ -75,6 +76,7 @@ _SIGS = {
     "moe_reverse_dispatch": ([c_vp] * 5, c_i32),
     "moe_backward": ([c_vp] * 12, c_i32),
     "mxfp8_quantize": ([c_vp, c_i64, c_i64, c_vp, c_vp, c_vp], c_i32),
+    "mxfp8_qdq": ([c_vp, c_vp, c_i64, c_i64, c_i32, c_vp], c_i32),
     "moe_get_device_error": ([c_vp, c_vp, c_vp, c_vp], c_i32),
     "moe_clear_device_error": ([c_vp, c_vp, c_vp], c_i32),
     "moe_status_string": ([c_i32], ctypes.c_char_p),
@@ -127,8 +129,8 @@ def problem(N, H, I, E, k, dtype=MOE_BF16, minibatch_rows=128) -> Problem:
     return Problem(int(N), int(H), int(I), int(E), int(k), int(dtype), int(minibatch_rows))
 
 
-def weights(wg, wu, wd) -> Weights:
-    return Weights(_ptr(wg), _ptr(wu), _ptr(wd))
+def weights(wg, wu, wd, wg_bwd=None, wu_bwd=None, wd_bwd=None) -> Weights:
+    return Weights(_ptr(wg), _ptr(wu), _ptr(wd), _ptr(wg_bwd), _ptr(wu_bwd), _ptr(wd_bwd))
 
 
 def _call(name, *args):
@@ -260,6 +262,10 @@ def moe_backward(p, saved, w: Weights, topk_w, dy, dx, dw_gate, dw_up, dw_down, 
 def mxfp8_quantize(src, rows, cols, q, scale, stream=None):
     _call("mxfp8_quantize", _ptr(src), int(rows), int(cols), _ptr(q), _ptr(scale),
           _stream(stream))
+
+
+def mxfp8_qdq(src, dst, rows, cols, axis, stream=None):
+    _call("mxfp8_qdq", _ptr(src), _ptr(dst), int(rows), int(cols), int(axis), _stream(stream))
 
 
 def moe_get_device_error(p, ws, stream=None) -> int:

@@ -24,7 +24,7 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   if (p->k > p->E) return MOE_ERR_INVALID_ARG;
   if (p->E > kMaxE || p->k > kMaxK) return MOE_ERR_UNSUPPORTED;
   if (p->H % 256 != 0 || p->I % 256 != 0) return MOE_ERR_UNSUPPORTED;
-  if (p->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (p->dtype != MOE_BF16 && p->dtype != MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
   const int32_t T = p->minibatch_rows == 0 ? kTileM : p->minibatch_rows;
   if (T != 128 && T != 256 && T != 512 && T != 1024) return MOE_ERR_UNSUPPORTED;
   const int64_t A = p->N * p->k;
@@ -38,6 +38,7 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   L->E = p->E;
   L->k = p->k;
   L->T = T;
+  L->dtype = p->dtype;
   L->n_warps = (A + kSchedSub - 1) / kSchedSub;
   size_t o = 0;
   auto take = [&o](size_t bytes) {
@@ -58,6 +59,13 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   L->dyxe = take(static_cast<size_t>(R) * p->H * 2);
   L->dg = take(static_cast<size_t>(R) * p->I * 2);
   L->du = take(static_cast<size_t>(R) * p->I * 2);
+  const bool mx = p->dtype == MOE_MXFP8;
+  L->mx_rh = mx ? take(static_cast<size_t>(R) * p->H * 2) : 0;
+  L->mx_ri1 = mx ? take(static_cast<size_t>(R) * p->I * 2) : 0;
+  L->mx_ri2 = mx ? take(static_cast<size_t>(R) * p->I * 2) : 0;
+  L->mx_ch = mx ? take(static_cast<size_t>(R) * p->H * 2) : 0;
+  L->mx_ci1 = mx ? take(static_cast<size_t>(R) * p->I * 2) : 0;
+  L->mx_ci2 = mx ? take(static_cast<size_t>(R) * p->I * 2) : 0;
   L->ws_bytes = o;
   o = 0;
   L->xe = take(static_cast<size_t>(R) * p->H * 2);
@@ -229,6 +237,18 @@ moe_status moe_forward(const moe_problem* p, const void* x, const moe_weights* w
   moe_saved_view v;
   MOE_TRY(moe_saved_layout(p, saved, &v));
   MOE_TRY(moe_dispatch(p, ws, x, v.xe, stream));
+  if (p->dtype == MOE_MXFP8) {
+    // MXFP8: gate/up reads Xe quantised along H, down reads Act quantised along I
+    Layout L;
+    MOE_TRY(prep(p, ws, &L));
+    void* xq = at<char>(ws, L.mx_rh);
+    void* aq = at<char>(ws, L.mx_ri1);
+    MOE_TRY(mxfp8_qdq(v.xe, xq, L.R, L.H, 0, stream));
+    MOE_TRY(moe_expert_gate_up(p, ws, xq, w, v.g, v.u, v.act, stream));
+    MOE_TRY(mxfp8_qdq(v.act, aq, L.R, L.I, 0, stream));
+    MOE_TRY(moe_expert_down(p, ws, aq, w, v.ye, stream));
+    return moe_combine(p, ws, v.ye, topk_w, y, stream);
+  }
   MOE_TRY(moe_expert_gate_up(p, ws, v.xe, w, v.g, v.u, v.act, stream));
   MOE_TRY(moe_expert_down(p, ws, v.act, w, v.ye, stream));
   return moe_combine(p, ws, v.ye, topk_w, y, stream);
@@ -304,6 +324,37 @@ moe_status moe_backward(const moe_problem* p, const void* saved, const moe_weigh
   void* dyxe = at<char>(ws, L.dyxe);
   void* dg = at<char>(ws, L.dg);
   void* du = at<char>(ws, L.du);
+  if (p->dtype == MOE_MXFP8) {
+    // Each GEMM operand quantised along that GEMM's K: rows of dYe along H,
+    // rows of dG/dU along I; for the weight gradients both operands along the
+    // token axis (blocks of 32 rows; expert segments start at multiples of T).
+    // The backward weight pointers hold Wd quantised along H, Wg/Wu along I.
+    if (!w || !w->w_gate_bwd || !w->w_up_bwd || !w->w_down_bwd) return MOE_ERR_INVALID_ARG;
+    moe_weights wb = *w;
+    wb.w_gate = w->w_gate_bwd;
+    wb.w_up = w->w_up_bwd;
+    wb.w_down = w->w_down_bwd;
+    void* rh = at<char>(ws, L.mx_rh);
+    void* ri1 = at<char>(ws, L.mx_ri1);
+    void* ri2 = at<char>(ws, L.mx_ri2);
+    void* ch = at<char>(ws, L.mx_ch);
+    void* ci1 = at<char>(ws, L.mx_ci1);
+    void* ci2 = at<char>(ws, L.mx_ci2);
+    MOE_TRY(moe_reverse_combine(p, ws, dy, v.ye, topk_w, dyxe, d_topk_w, stream));
+    MOE_TRY(mxfp8_qdq(dyxe, rh, L.R, L.H, 0, stream));
+    MOE_TRY(moe_expert_down_dgrad(p, ws, rh, v.g, v.u, &wb, dg, du, stream));
+    MOE_TRY(mxfp8_qdq(dyxe, ch, L.R, L.H, 1, stream));
+    MOE_TRY(mxfp8_qdq(v.act, ci1, L.R, L.I, 1, stream));
+    MOE_TRY(moe_expert_down_wgrad(p, ws, ch, ci1, dw_down, stream));
+    MOE_TRY(mxfp8_qdq(dg, ri1, L.R, L.I, 0, stream));
+    MOE_TRY(mxfp8_qdq(du, ri2, L.R, L.I, 0, stream));
+    MOE_TRY(moe_expert_gate_up_dgrad(p, ws, ri1, ri2, &wb, dyxe, stream));
+    MOE_TRY(mxfp8_qdq(dg, ci1, L.R, L.I, 1, stream));
+    MOE_TRY(mxfp8_qdq(du, ci2, L.R, L.I, 1, stream));
+    MOE_TRY(mxfp8_qdq(v.xe, ch, L.R, L.H, 1, stream));
+    MOE_TRY(moe_expert_gate_up_wgrad(p, ws, ci1, ci2, ch, dw_gate, dw_up, stream));
+    return moe_reverse_dispatch(p, ws, dyxe, dx, stream);
+  }
   MOE_TRY(moe_reverse_combine(p, ws, dy, v.ye, topk_w, dyxe, d_topk_w, stream));
   MOE_TRY(moe_expert_down_dgrad(p, ws, dyxe, v.g, v.u, w, dg, du, stream));
   MOE_TRY(moe_expert_down_wgrad(p, ws, dyxe, v.act, dw_down, stream));
@@ -311,6 +362,16 @@ moe_status moe_backward(const moe_problem* p, const void* saved, const moe_weigh
   MOE_TRY(moe_expert_gate_up_dgrad(p, ws, dg, du, w, dyxe, stream));
   MOE_TRY(moe_expert_gate_up_wgrad(p, ws, dg, du, v.xe, dw_gate, dw_up, stream));
   return moe_reverse_dispatch(p, ws, dyxe, dx, stream);
+}
+
+moe_status mxfp8_qdq(const void* src_bf16, void* dst_bf16, int64_t rows, int64_t cols, int axis,
+                     void* stream) {
+  if (rows < 0 || cols < 0 || (axis != 0 && axis != 1)) return MOE_ERR_INVALID_ARG;
+  if (axis == 0 && cols % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (axis == 1 && (rows % 32 != 0 || cols % 2 != 0)) return MOE_ERR_INVALID_ARG;
+  if (rows * cols == 0) return MOE_OK;
+  if (!aligned(src_bf16, 16) || !aligned(dst_bf16, 16)) return MOE_ERR_INVALID_ARG;
+  return cu(launch_mxfp8_qdq(src_bf16, dst_bf16, rows, cols, axis, S(stream)));
 }
 
 moe_status mxfp8_quantize(const void* src_bf16, int64_t rows, int64_t cols, uint8_t* q_e4m3,

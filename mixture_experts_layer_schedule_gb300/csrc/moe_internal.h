@@ -21,10 +21,12 @@ struct Layout {
   int64_t N, A, R;        // tokens, assignments, expert-grouped rows
   int32_t H, I, E, k;
   int32_t T;              // per-expert row granularity (minibatch rows)
+  int32_t dtype;          // MOE_BF16 or MOE_MXFP8
   int64_t n_warps;        // schedule warps = ceil(A / kSchedSub)
   // workspace byte offsets
   size_t err, counts, offsets, pad_offsets, slot_of, src_of_row, tiles, n_tiles, warp_counts,
       expert_order,
+      mx_rh, mx_ri1, mx_ri2, mx_ch, mx_ci1, mx_ci2,  // MXFP8 quantised operands
       dyxe, dg, du, ws_bytes;
   // forward-context byte offsets
   size_t xe, g, u, act, ye, saved_bytes;
@@ -57,6 +59,8 @@ cudaError_t launch_reverse_combine(const Layout& L, const void* ws, const void* 
                                    cudaStream_t s);
 cudaError_t launch_reverse_dispatch(const Layout& L, const void* ws, const void* dxe, void* dx,
                                     cudaStream_t s);
+cudaError_t launch_mxfp8_qdq(const void* src, void* dst, int64_t rows, int64_t cols, int axis,
+                             cudaStream_t s);
 cudaError_t launch_mxfp8_quantize(const void* src, int64_t rows, int64_t cols, uint8_t* q,
                                   uint8_t* scale, cudaStream_t s);
 

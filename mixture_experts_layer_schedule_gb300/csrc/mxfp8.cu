@@ -12,6 +12,8 @@
 // memory. The scale exponent comes straight from the fp32 exponent field of
 // amax (bf16 values are exact in fp32); v / scale is a power-of-two product,
 // exact in fp32 for every value that does not round to zero in E4M3.
+#include <cuda_fp16.h>
+
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -62,7 +64,90 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const uint4* __rest
   q[b * 2 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
 }
 
+// Quantise-dequantise: the MXFP8 value of each element, written back as bf16
+// (exact: an E4M3 value times a power of two fits bf16 for every scale the
+// quantiser produces from bf16 data of normal magnitude).
+__device__ __forceinline__ void qdq32(float (&f)[32]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  const int biased = (__float_as_uint(amax) >> 23) & 0xFF;
+  const int code = biased == 0 ? 0 : max(0, biased - 8);
+  const float inv = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);  // 2^(127-code)
+  // 2^(code-127) as a product of two normal floats (code may be < 1)
+  const float sc_hi = __uint_as_float(static_cast<uint32_t>(max(code, 1)) << 23);
+  const float sc_lo = code >= 1 ? 1.0f : 0.5f;
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const uint32_t q = e4m3x2(f[i] * inv, f[i + 1] * inv);
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(q)));
+    const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+    f[i] = __low2float(hv) * sc_hi * sc_lo;
+    f[i + 1] = __high2float(hv) * sc_hi * sc_lo;
+  }
+}
+
+// Blocks of 32 consecutive columns of a row; one thread per block.
+__global__ void __launch_bounds__(256) qdq_rows_kernel(const uint4* __restrict__ src,
+                                                       int64_t n_blocks, uint4* __restrict__ dst) {
+  const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (b >= n_blocks) return;
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 r = src[b * 4 + i];
+    f[8 * i + 0] = bf16lo(r.x); f[8 * i + 1] = bf16hi(r.x);
+    f[8 * i + 2] = bf16lo(r.y); f[8 * i + 3] = bf16hi(r.y);
+    f[8 * i + 4] = bf16lo(r.z); f[8 * i + 5] = bf16hi(r.z);
+    f[8 * i + 6] = bf16lo(r.w); f[8 * i + 7] = bf16hi(r.w);
+  }
+  qdq32(f);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    dst[b * 4 + i] = make_uint4(pack_bf16x2(f[8 * i], f[8 * i + 1]), pack_bf16x2(f[8 * i + 2], f[8 * i + 3]),
+                                pack_bf16x2(f[8 * i + 4], f[8 * i + 5]), pack_bf16x2(f[8 * i + 6], f[8 * i + 7]));
+}
+
+// Blocks of 32 consecutive rows of a column; one thread per (row block, column
+// pair), so a warp reads 128 contiguous bytes of each row.
+__global__ void __launch_bounds__(256) qdq_cols_kernel(const uint32_t* __restrict__ src,
+                                                       int64_t rows, int64_t cols2,
+                                                       uint32_t* __restrict__ dst) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t n = (rows / 32) * cols2;
+  if (idx >= n) return;
+  const int64_t rb = idx / cols2, c = idx % cols2;
+  float lo[32], hi[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    const uint32_t v = src[(rb * 32 + r) * cols2 + c];
+    lo[r] = bf16lo(v);
+    hi[r] = bf16hi(v);
+  }
+  qdq32(lo);
+  qdq32(hi);
+#pragma unroll
+  for (int r = 0; r < 32; ++r) dst[(rb * 32 + r) * cols2 + c] = pack_bf16x2(lo[r], hi[r]);
+}
+
 }  // namespace
+
+cudaError_t launch_mxfp8_qdq(const void* src, void* dst, int64_t rows, int64_t cols, int axis,
+                             cudaStream_t s) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  if (axis == 0) {
+    const int64_t n_blocks = rows * (cols / 32);
+    qdq_rows_kernel<<<static_cast<unsigned>((n_blocks + 255) / 256), 256, 0, s>>>(
+        static_cast<const uint4*>(src), n_blocks, static_cast<uint4*>(dst));
+  } else {
+    const int64_t n = (rows / 32) * (cols / 2);
+    qdq_cols_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
+        static_cast<const uint32_t*>(src), rows, cols / 2, static_cast<uint32_t*>(dst));
+  }
+  note_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_mxfp8_quantize(const void* src, int64_t rows, int64_t cols, uint8_t* q,
                                   uint8_t* scale, cudaStream_t s) {

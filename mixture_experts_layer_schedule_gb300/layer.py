@@ -26,11 +26,15 @@ class Grads:
 class MoELayer:
     """Buffers of one problem size on one device, reused across calls."""
 
-    def __init__(self, N, H, I, E, k, device="cuda", allocate_grads=True, minibatch_rows=128):
+    def __init__(self, N, H, I, E, k, device="cuda", allocate_grads=True, minibatch_rows=128,
+                 dtype="bf16"):
         self.N, self.H, self.I, self.E, self.k = int(N), int(H), int(I), int(E), int(k)
         self.T = int(minibatch_rows)
+        self.dtype = dtype
         self.device = torch.device(device)
-        self.p = _lib.problem(N, H, I, E, k, minibatch_rows=self.T)
+        self.p = _lib.problem(N, H, I, E, k,
+                              dtype=_lib.MOE_MXFP8 if dtype == "mxfp8" else _lib.MOE_BF16,
+                              minibatch_rows=self.T)
         self.R = _lib.moe_grouped_rows(self.p)
         dev = self.device
         self.ws = torch.empty(_lib.moe_workspace_bytes(self.p), dtype=torch.uint8, device=dev)
@@ -81,6 +85,22 @@ class MoELayer:
         _lib.moe_build_schedule(self.p, self.topk_ids if topk_ids is None else topk_ids, self.ws,
                                 stream)
 
+    @staticmethod
+    def prepare_mxfp8_weights(wg, wu, wd, stream=None):
+        """MXFP8 weights as the GEMMs read them (exact bf16 values of the MXFP8
+        numbers): forward -- gate/up along H, down along I; backward -- gate/up
+        along I, down along H. Returns ((wg, wu, wd), (wg_bwd, wu_bwd, wd_bwd))."""
+        E, I, H = wg.shape
+        fwd, bwd = [], []
+        for t, rows, cols in ((wg, E * I, H), (wu, E * I, H), (wd, E * H, I)):
+            f = torch.empty_like(t)
+            b = torch.empty_like(t)
+            _lib.mxfp8_qdq(t, f, rows, cols, 0, stream)
+            _lib.mxfp8_qdq(t, b, rows, cols, 1, stream)
+            fwd.append(f)
+            bwd.append(b)
+        return tuple(fwd), tuple(bwd)
+
     def forward(self, x, wg, wu, wd, topk_w=None, stream=None):
         w = _lib.weights(wg, wu, wd)
         _lib.moe_forward(self.p, x, w, self.topk_w if topk_w is None else topk_w, self.y,
@@ -94,20 +114,21 @@ class MoELayer:
                                    self.y, self.ws, stream)
         return self.y
 
-    def backward(self, dy, wg, wu, wd, topk_w=None, stream=None) -> Grads:
+    def backward(self, dy, wg, wu, wd, topk_w=None, stream=None, bwd=None) -> Grads:
+        """bwd: the backward-direction weights (required for MXFP8)."""
         g = self.grads
-        w = _lib.weights(wg, wu, wd)
+        w = _lib.weights(wg, wu, wd, *(bwd if bwd is not None else (None, None, None)))
         _lib.moe_backward(self.p, self.saved, w, self.topk_w if topk_w is None else topk_w, dy,
                           g.dx, g.dw_gate, g.dw_up, g.dw_down, g.d_topk_w, self.ws, stream)
         return g
 
-    def step(self, x, logits, bias, wg, wu, wd, dy, stream=None, backward=True):
+    def step(self, x, logits, bias, wg, wu, wd, dy, stream=None, backward=True, bwd=None):
         """Route, schedule, forward and (optionally) backward: one layer pass."""
         self.route(logits, bias, stream)
         self.build_schedule(None, stream)
         y = self.forward(x, wg, wu, wd, None, stream)
         if backward:
-            self.backward(dy, wg, wu, wd, None, stream)
+            self.backward(dy, wg, wu, wd, None, stream, bwd=bwd)
         return y
 
     def device_error(self, stream=None) -> int:

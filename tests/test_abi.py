@@ -51,9 +51,15 @@ def test_sizes_and_validation(lib):
         with pytest.raises(_lib.MoEError) as ei:
             _lib.moe_workspace_bytes(_lib.problem(*bad))
         assert ei.value.status == status
-    with pytest.raises(_lib.MoEError) as ei:
-        _lib.moe_workspace_bytes(_lib.problem(256, 256, 512, 8, 2, dtype=_lib.MOE_MXFP8))
-    assert ei.value.status == _lib.MOE_ERR_UNSUPPORTED
+    for bad_kw in (dict(dtype=7), dict(minibatch_rows=192), dict(minibatch_rows=2048)):
+        with pytest.raises(_lib.MoEError) as ei:
+            _lib.moe_workspace_bytes(_lib.problem(256, 256, 512, 8, 2, **bad_kw))
+        assert ei.value.status == _lib.MOE_ERR_UNSUPPORTED
+    # MXFP8 adds the quantised-operand buffers; T = 256 grows the padded rows
+    mx = _lib.moe_workspace_bytes(_lib.problem(256, 256, 512, 8, 2, dtype=_lib.MOE_MXFP8))
+    assert mx > ws + R * (2 * 256 + 4 * 512) * 2 - 4096
+    assert _lib.moe_grouped_rows(_lib.problem(256, 256, 512, 8, 2, minibatch_rows=256)) == \
+        ((512 + 8 * 255 + 255) // 256) * 256
 
 
 def test_null_and_misaligned_pointers_are_rejected_before_any_launch(lib):
