@@ -206,6 +206,7 @@ def run_ours(args, ws_, rank, local):
     wbwd = None
     if mx:  # weights pre-quantised once, outside the timed steps
         fwd_w, wbwd = MoELayer.prepare_mxfp8_weights(inp["wg"], inp["wu"], inp["wd"])
+        inp["w_src"] = (inp["wg"], inp["wu"], inp["wd"])  # the bf16 weights, for the oracle
         inp["wg"], inp["wu"], inp["wd"] = fwd_w
     w = _lib.weights(inp["wg"], inp["wu"], inp["wd"])
     wfull = _lib.weights(inp["wg"], inp["wu"], inp["wd"], *(wbwd or (None, None, None)))
@@ -426,6 +427,9 @@ def run_ours(args, ws_, rank, local):
     return rec, shape, inp
 
 
+MX_NOTE = "; MXFP8 weight copies quantised once before the sample, as on the GPU"
+
+
 def cpu_sample(shape, inp, n_tok, threads):
     """Run the oracle on the first n_tok tokens of the workload (fwd+bwd with
     weight gradients). Returns (seconds, tokens)."""
@@ -436,11 +440,19 @@ def cpu_sample(shape, inp, n_tok, threads):
     bias = None if inp["bias"] is None else inp["bias"].cpu().numpy()
     x = oracle.as_bf16_bits(inp["x"][:n_tok])
     dy = oracle.as_bf16_bits(inp["dy"][:n_tok]) if inp.get("dy") is not None else None
-    wg, wu, wd = (oracle.as_bf16_bits(inp[k]) for k in ("wg", "wu", "wd"))
+    wg, wu, wd = (oracle.as_bf16_bits(t) for t in inp.get("w_src", (inp["wg"], inp["wu"], inp["wd"])))
+    if shape.dtype == "mxfp8":
+        if "oracle_w" not in inp:
+            inp["oracle_w"] = oracle.mxfp8_weights(wg, wu, wd, threads=threads)
+        prepared = inp["oracle_w"]
     t0 = time.perf_counter()
     ids, w = oracle.route_topk(logits, bias, shape.k)
     oracle.build_schedule(ids, shape.E)
-    if shape.backward:
+    if shape.dtype == "mxfp8":
+        # the weights' quantisation is not part of a step (the GPU run also
+        # prepares them once, before its timed steps)
+        oracle.layer_mxfp8_prepared(x, prepared, ids, w, dy, threads=threads)
+    elif shape.backward:
         oracle.forward_bf16(x, wg, wu, wd, ids, w, threads=threads)
         oracle.backward_bf16(x, wg, wu, wd, ids, w, dy, threads=threads)
     else:
@@ -476,7 +488,8 @@ def run_reference(args, ws_, rank):
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads,
                          "kind": "oracle",
                          "sample": f"first {n_tok} tokens of the workload per step "
-                                   f"(full expert weights, fwd+bwd with weight gradients)"},
+                                   f"(full expert weights, fwd+bwd with weight gradients"
+                                   f"{MX_NOTE if shape.dtype == 'mxfp8' else ''})"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -507,7 +520,8 @@ def main():
         rec["cpu_baseline"] = {"value": round(n / secs, 3), "unit": UNIT, "cores": threads,
                                "kind": "oracle",
                                "sample": f"first {n} tokens of the workload (full expert "
-                                         f"weights, fwd+bwd with weight gradients), "
+                                         f"weights, fwd+bwd with weight gradients"
+                                         f"{MX_NOTE if shape.dtype == 'mxfp8' else ''}), "
                                          f"{secs:.1f} s"}
     if rank == 0:
         if not args.phase_report:

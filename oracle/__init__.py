@@ -72,6 +72,11 @@ def lib():
             L.orc_mxfp8_quantize.argtypes = [i64, i64, vp, vp, vp]
             L.orc_layer_mxfp8.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp,
                                           ctypes.c_int, vp, vp, vp, vp, vp, vp, ctypes.c_int]
+            L.orc_mxfp8_weights.argtypes = [i32, i32, i32, vp, vp, vp, ctypes.c_int, vp, vp, vp,
+                                            vp, vp, vp, ctypes.c_int]
+            L.orc_layer_mxfp8_prepared.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+                                                   vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp,
+                                                   vp, vp, vp, ctypes.c_int]
             L.orc_e4m3_encode.argtypes = [ctypes.c_double]
             L.orc_e4m3_encode.restype = ctypes.c_uint8
             L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
@@ -242,6 +247,35 @@ def layer_mxfp8(x, wg, wu, wd, ids, w, dy, quantize=True, threads=0):
     _check(lib().orc_layer_mxfp8(N, H, I, E, k, _p(x), _p(wg), _p(wu), _p(wd), _p(ids), _p(w),
                                  _p(dy), 1 if quantize else 0, _p(y), _p(dx), _p(dwg), _p(dwu),
                                  _p(dwd), _p(dw), threads))
+    return dict(y=y, dx=dx, dwg=dwg, dwu=dwu, dwd=dwd, dw=dw)
+
+
+MXFP8_WEIGHT_COPIES = ("wg_h", "wu_h", "wd_i", "wd_h", "wg_i", "wu_i")
+
+
+def mxfp8_weights(wg, wu, wd, quantize=True, threads=0):
+    """The six quantised weight copies the MXFP8 layer reads (see
+    orc_mxfp8_weights), as a dict of fp64 arrays."""
+    wg, wu, wd = (as_bf16_bits(a) for a in (wg, wu, wd))
+    E, I, H = wg.shape
+    out = {n: np.empty(wg.shape if n[1] != "d" else wd.shape) for n in MXFP8_WEIGHT_COPIES}
+    _check(lib().orc_mxfp8_weights(H, I, E, _p(wg), _p(wu), _p(wd), 1 if quantize else 0,
+                                   *(_p(out[n]) for n in MXFP8_WEIGHT_COPIES), threads))
+    return out
+
+
+def layer_mxfp8_prepared(x, prepared, ids, w, dy, quantize=True, threads=0):
+    """layer_mxfp8 on weights from mxfp8_weights (same quantize flag)."""
+    x, dy = as_bf16_bits(x), as_bf16_bits(dy)
+    ids, w = _c(ids, np.int32), _c(w, np.float64)
+    N, H = x.shape
+    E, I, _ = prepared["wg_h"].shape
+    k = ids.shape[1]
+    y = np.empty((N, H))
+    dx, dwg, dwu, dwd, dw = _bw_out(N, H, I, E, k)
+    _check(lib().orc_layer_mxfp8_prepared(
+        N, H, I, E, k, _p(x), *(_p(prepared[n]) for n in MXFP8_WEIGHT_COPIES), _p(ids), _p(w),
+        _p(dy), 1 if quantize else 0, _p(y), _p(dx), _p(dwg), _p(dwu), _p(dwd), _p(dw), threads))
     return dict(y=y, dx=dx, dwg=dwg, dwu=dwu, dwd=dwd, dw=dw)
 
 

@@ -560,33 +560,25 @@ void qdq_vec(double* v, int64_t n) {
 
 }  // namespace
 
-extern "C" int orc_layer_mxfp8(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k,
-                               const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
-                               const uint16_t* wd, const int32_t* ids, const double* w,
-                               const uint16_t* dy, int quantize, double* y, double* dx,
-                               double* dwg, double* dwu, double* dwd, double* dw,
-                               int threads) {
-  if (N < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || k > E) return ORC_ERR_ARG;
-  const int64_t A = N * k;
-  for (int64_t a = 0; a < A; ++a)
-    if (ids[a] < 0 || ids[a] >= E) return ORC_ERR_ARG;
-  auto q = [quantize](double* v, int64_t n) { if (quantize) qdq_vec(v, n); };
-  auto rb = [quantize](double v) { return quantize ? round_bf16(v) : v; };
+extern "C" int orc_mxfp8_weights(int32_t H, int32_t I, int32_t E, const uint16_t* wg,
+                                 const uint16_t* wu, const uint16_t* wd, int quantize,
+                                 double* wg_h, double* wu_h, double* wd_i, double* wd_h,
+                                 double* wg_i, double* wu_i, int threads) {
+  if (H <= 0 || I <= 0 || E <= 0) return ORC_ERR_ARG;
   const int64_t HI = static_cast<int64_t>(H) * I;
   // Weights as each GEMM reads them:
   //   gate/up forward: rows of Wg[e], Wu[e] along H;  down forward: rows of Wd[e] along I;
   //   down backward (dA = Wd^T dye): columns of Wd[e] along H;
   //   gate/up backward (dxe = Wg^T dg + Wu^T du): columns of Wg[e], Wu[e] along I.
-  std::vector<double> wg_h(E * HI), wu_h(E * HI), wd_i(E * HI), wd_h(E * HI), wg_i(E * HI),
-      wu_i(E * HI);
-  for (int64_t i = 0; i < E * HI; ++i) {
-    wg_h[i] = wg_i[i] = bf16_to_double(wg[i]);
-    wu_h[i] = wu_i[i] = bf16_to_double(wu[i]);
-    wd_i[i] = wd_h[i] = bf16_to_double(wd[i]);
-  }
-  std::vector<double> col(std::max(H, I));
-  for (int32_t e = 0; e < E; ++e) {
+  parallel_for(E, threads, [&](int64_t e) {
+    auto q = [quantize](double* v, int64_t n) { if (quantize) qdq_vec(v, n); };
     const int64_t o = e * HI;
+    for (int64_t i = o; i < o + HI; ++i) {
+      wg_h[i] = wg_i[i] = bf16_to_double(wg[i]);
+      wu_h[i] = wu_i[i] = bf16_to_double(wu[i]);
+      wd_i[i] = wd_h[i] = bf16_to_double(wd[i]);
+    }
+    std::vector<double> col(std::max(H, I));
     for (int32_t i = 0; i < I; ++i) {           // Wg/Wu [e][i][:] along H
       q(&wg_h[o + static_cast<int64_t>(i) * H], H);
       q(&wu_h[o + static_cast<int64_t>(i) * H], H);
@@ -605,7 +597,42 @@ extern "C" int orc_layer_mxfp8(int64_t N, int32_t H, int32_t I, int32_t E, int32
       q(col.data(), I);
       for (int32_t i = 0; i < I; ++i) wu_i[o + static_cast<int64_t>(i) * H + h] = col[i];
     }
-  }
+  });
+  return ORC_OK;
+}
+
+extern "C" int orc_layer_mxfp8(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k,
+                               const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
+                               const uint16_t* wd, const int32_t* ids, const double* w,
+                               const uint16_t* dy, int quantize, double* y, double* dx,
+                               double* dwg, double* dwu, double* dwd, double* dw,
+                               int threads) {
+  if (H <= 0 || I <= 0 || E <= 0) return ORC_ERR_ARG;
+  const int64_t n = static_cast<int64_t>(E) * H * I;
+  std::vector<double> wg_h(n), wu_h(n), wd_i(n), wd_h(n), wg_i(n), wu_i(n);
+  const int st = orc_mxfp8_weights(H, I, E, wg, wu, wd, quantize, wg_h.data(), wu_h.data(),
+                                   wd_i.data(), wd_h.data(), wg_i.data(), wu_i.data(), threads);
+  if (st != ORC_OK) return st;
+  return orc_layer_mxfp8_prepared(N, H, I, E, k, x, wg_h.data(), wu_h.data(), wd_i.data(),
+                                  wd_h.data(), wg_i.data(), wu_i.data(), ids, w, dy, quantize,
+                                  y, dx, dwg, dwu, dwd, dw, threads);
+}
+
+extern "C" int orc_layer_mxfp8_prepared(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k,
+                                        const uint16_t* x, const double* wg_h,
+                                        const double* wu_h, const double* wd_i,
+                                        const double* wd_h, const double* wg_i,
+                                        const double* wu_i, const int32_t* ids, const double* w,
+                                        const uint16_t* dy, int quantize, double* y, double* dx,
+                                        double* dwg, double* dwu, double* dwd, double* dw,
+                                        int threads) {
+  if (N < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || k > E) return ORC_ERR_ARG;
+  const int64_t A = N * k;
+  for (int64_t a = 0; a < A; ++a)
+    if (ids[a] < 0 || ids[a] >= E) return ORC_ERR_ARG;
+  auto q = [quantize](double* v, int64_t n) { if (quantize) qdq_vec(v, n); };
+  auto rb = [quantize](double v) { return quantize ? round_bf16(v) : v; };
+  const int64_t HI = static_cast<int64_t>(H) * I;
   // Per-assignment forward and backward.
   std::vector<double> G(A * I), U(A * I), Ab(A * I), DYe(A * H), DG(A * I), DU(A * I), YE(A * H);
   parallel_for(N, threads, [&](int64_t t) {

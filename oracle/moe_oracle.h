@@ -143,6 +143,23 @@ int orc_layer_mxfp8(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k, const
                     double* y, double* dx, double* dwg, double* dwu, double* dwd, double* dw,
                     int threads);
 
+/* The weight half of orc_layer_mxfp8, done once per set of weights: the six
+ * copies the GEMMs read, each [E, I, H] (wg_h, wu_h, wg_i, wu_i) or [E, H, I]
+ * (wd_i, wd_h) in fp64, the suffix naming the quantisation axis (h: blocks
+ * along H, i: blocks along I). quantize = 0 gives the plain bf16 values. */
+int orc_mxfp8_weights(int32_t H, int32_t I, int32_t E, const uint16_t* wg, const uint16_t* wu,
+                      const uint16_t* wd, int quantize, double* wg_h, double* wu_h, double* wd_i,
+                      double* wd_h, double* wg_i, double* wu_i, int threads);
+
+/* The per-batch half of orc_layer_mxfp8 on weights from orc_mxfp8_weights
+ * (orc_layer_mxfp8 = orc_mxfp8_weights followed by this). */
+int orc_layer_mxfp8_prepared(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k,
+                             const uint16_t* x, const double* wg_h, const double* wu_h,
+                             const double* wd_i, const double* wd_h, const double* wg_i,
+                             const double* wu_i, const int32_t* ids, const double* w,
+                             const uint16_t* dy, int quantize, double* y, double* dx, double* dwg,
+                             double* dwu, double* dwd, double* dw, int threads);
+
 /* MXFP8 quantiser (OCP MX v1.0, MXFP8 E4M3): for each block of 32
  * consecutive values along a row, X = 2^(floor(log2(amax)) - 8) (8 = the
  * largest E4M3 exponent), scale code = that exponent + 127 clamped to

@@ -79,3 +79,27 @@ def test_down_backward_quantises_wd_along_h():
     a = oracle.layer_mxfp8(x, wg, wu, wd_out, ids, w, dy, quantize=False)
     b = oracle.layer_mxfp8(x, wg, wu, _bits(wd_z), ids, w, dy, quantize=False)
     assert np.max(np.abs(a["dx"] - b["dx"])) > 0
+
+
+def test_weight_copies_are_the_quantiser_s_values_and_the_two_halves_compose():
+    """The prepared weight copies hold the decoded MXFP8 values of each row
+    (blocks along the stored axis) or of each column (blocks across it), and
+    weights-then-layer gives exactly the one-call layer."""
+    x, wg, wu, wd, ids, w, dy = _layer(24, 64, 96, 3, 2, 3)
+    pw = oracle.mxfp8_weights(wg, wu, wd)
+
+    def dequant(bits2d):
+        q, s = oracle.mxfp8_quantize(bits2d)
+        vals = np.array([oracle.e4m3_decode(c) for c in range(256)])
+        scale = np.exp2(s.astype(np.float64) - 127.0)
+        return vals[q] * np.repeat(scale, 32, axis=1)
+
+    e = 1
+    np.testing.assert_array_equal(pw["wg_h"][e], dequant(wg[e]))
+    np.testing.assert_array_equal(pw["wd_i"][e], dequant(wd[e]))
+    np.testing.assert_array_equal(pw["wu_i"][e], dequant(np.ascontiguousarray(wu[e].T)).T)
+    np.testing.assert_array_equal(pw["wd_h"][e], dequant(np.ascontiguousarray(wd[e].T)).T)
+    r1 = oracle.layer_mxfp8(x, wg, wu, wd, ids, w, dy)
+    r2 = oracle.layer_mxfp8_prepared(x, pw, ids, w, dy)
+    for key in r1:
+        np.testing.assert_array_equal(r1[key], r2[key])
