@@ -67,11 +67,11 @@ def dist_env():
 GEMM_SRC = ("mixture_experts_layer_schedule_gb300/csrc/grouped_gemm.cu",
             "mixture_experts_layer_schedule_gb300/csrc/moe_common.cuh")
 MEASURED_TRAFFIC = {
-    "src_sha256": "2541143f7dbfb08e3e1db922b4e8cc022ebe28ae5ba4b68d443e95ae667c4aae",
+    "src_sha256": "057c0b38001dd382d292792ad8713fe03d76c0d36f7a2bb0e285afc110ddb986",
     "workload": "skewed_fwd_bwd_N16384_H4096_I1536_E128_k8_zipf1.2",
-    "bytes": {"gate_up": 5.04e9 + 1.32e9, "down": 2.05e9 + 1.15e9,
-              "down_dgrad": 3.96e9 + 0.853e9, "down_wgrad": 2.51e9 + 3.16e9,
-              "gate_up_dgrad": 4.39e9 + 1.16e9, "gate_up_wgrad": 4.66e9 + 6.38e9},
+    "bytes": {"gate_up": 5.1015e9 + 1.3024e9, "down": 2.0517e9 + 1.1503e9,
+              "down_dgrad": 3.9778e9 + 0.8521e9, "down_wgrad": 2.3732e9 + 3.1563e9,
+              "gate_up_dgrad": 4.5052e9 + 1.1557e9, "gate_up_wgrad": 5.2863e9 + 6.3780e9},
 }
 
 
