@@ -87,6 +87,27 @@ typedef struct {
  * gate/up, I for down) and the *_bwd pointers the weights quantised along the
  * backward GEMMs' K (I for gate/up, H for down), both as exact bf16 values of
  * the MXFP8 numbers (see mxfp8_qdq). */
+/* One MXFP8 operand as the block-scaled tensor-core GEMMs read it (see
+ * mxfp8_quantize_mma): q = E4M3 codes of a K-major [rows, K] matrix, s = its
+ * E8M0 scales (rows * K / 32 bytes) in the tensor-memory chunk layout. */
+typedef struct {
+  const uint8_t* q;
+  const uint8_t* s;
+} moe_mxfp8_operand;
+
+/* MXFP8 expert weights for the tensor-core path, each made by
+ * mxfp8_quantize_mma from the bf16 weights viewed as 2-D matrices:
+ *   gate, up   [E*I, H] (transpose 0: K = H)  -- gate/up forward
+ *   down       [E*H, I] (transpose 0: K = I)  -- down forward
+ *   gate_t, up_t [H, E*I] (transpose 1 of [E*I, H]: K = I) -- gate/up data gradient
+ *   down_t     [I, E*H] (transpose 1 of [E*H, I]: K = H)   -- down data gradient
+ * A NULL q in gate_t / up_t / down_t makes moe_backward run those GEMMs on the
+ * bf16 values in w_*_bwd instead. */
+typedef struct {
+  moe_mxfp8_operand gate, up, down;
+  moe_mxfp8_operand gate_t, up_t, down_t;
+} moe_mxfp8_weights;
+
 typedef struct {
   const void* w_gate;
   const void* w_up;
@@ -94,6 +115,13 @@ typedef struct {
   const void* w_gate_bwd;
   const void* w_up_bwd;
   const void* w_down_bwd;
+  /* MOE_MXFP8 only: the weights as E4M3 codes + E8M0 scales. Non-NULL makes
+   * moe_forward / moe_forward_inference run the expert GEMMs as block-scaled
+   * FP8 MMAs (tcgen05 kind::mxf8f6f4, fp32 accumulation) on the codes, with
+   * the activations quantised to E4M3 + E8M0 by the library; NULL runs them
+   * on the bf16 values of the MXFP8 numbers in w_gate / w_up / w_down. Both
+   * compute the same products of the same MXFP8 numbers. */
+  const moe_mxfp8_weights* mx;
 } moe_weights;
 
 /* Rows of every expert-grouped buffer: each expert's segment of the buffer is
@@ -266,6 +294,22 @@ moe_status moe_backward(const moe_problem* p, const void* saved, const moe_weigh
  * [rows, cols/32]. */
 moe_status mxfp8_quantize(const void* src_bf16, int64_t rows, int64_t cols, uint8_t* q_e4m3,
                           uint8_t* scale_e8m0, void* stream);
+
+/* MXFP8 quantiser for the block-scaled tensor-core GEMMs (same rounding rule
+ * as mxfp8_quantize), rows % 128 == 0 and cols % 128 == 0, q 16-byte aligned.
+ *   transpose 0: q [rows, cols], blocks of 32 consecutive columns of a row
+ *                (the operand's K = cols);
+ *   transpose 1: q [cols, rows] = src^T, blocks of 32 consecutive source rows
+ *                of a column (the operand's K = rows).
+ * s (rows * cols / 32 bytes) holds the scales of the K-major operand
+ * [R', K'] (R' = rows or cols) in 512-byte chunks, one per (128 K, 128 rows):
+ * chunk (K'/128 index kc, row block rb) at byte ((kc * R'/128) + rb) * 512; in
+ * it the scale of (operand row r, 32-wide K block j) at byte
+ * (r % 32) * 16 + ((r / 32) % 4) * 4 + j % 4 -- the order in which the
+ * tensor-memory copy (tcgen05.cp 32x128b, warpx4) places scales for the MMA.
+ * Not in the pages: the layout is fixed by the tensor-core instruction. */
+moe_status mxfp8_quantize_mma(const void* src_bf16, int64_t rows, int64_t cols, int transpose,
+                              uint8_t* q_e4m3, uint8_t* s_e8m0, void* stream);
 
 /* MXFP8 quantise-dequantise of bf16 [rows, cols]: each value replaced by the
  * bf16 form of its MXFP8 number (the rule of mxfp8_quantize). axis 0: blocks

@@ -28,9 +28,21 @@ class Problem(ctypes.Structure):
                 ("dtype", c_i32), ("minibatch_rows", c_i32)]
 
 
+class MXFP8Operand(ctypes.Structure):
+    _fields_ = [("q", c_vp), ("s", c_vp)]
+
+
+MXFP8_WEIGHT_OPERANDS = ("gate", "up", "down", "gate_t", "up_t", "down_t")
+
+
+class MXFP8Weights(ctypes.Structure):
+    _fields_ = [(n, MXFP8Operand) for n in MXFP8_WEIGHT_OPERANDS]
+
+
 class Weights(ctypes.Structure):
     _fields_ = [("w_gate", c_vp), ("w_up", c_vp), ("w_down", c_vp),
-                ("w_gate_bwd", c_vp), ("w_up_bwd", c_vp), ("w_down_bwd", c_vp)]
+                ("w_gate_bwd", c_vp), ("w_up_bwd", c_vp), ("w_down_bwd", c_vp),
+                ("mx", ctypes.POINTER(MXFP8Weights))]
 
 
 class Schedule(ctypes.Structure):
@@ -77,6 +89,7 @@ _SIGS = {
     "moe_backward": ([c_vp] * 12, c_i32),
     "mxfp8_quantize": ([c_vp, c_i64, c_i64, c_vp, c_vp, c_vp], c_i32),
     "mxfp8_qdq": ([c_vp, c_vp, c_i64, c_i64, c_i32, c_vp], c_i32),
+    "mxfp8_quantize_mma": ([c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp], c_i32),
     "moe_get_device_error": ([c_vp, c_vp, c_vp, c_vp], c_i32),
     "moe_clear_device_error": ([c_vp, c_vp, c_vp], c_i32),
     "moe_status_string": ([c_i32], ctypes.c_char_p),
@@ -129,8 +142,20 @@ def problem(N, H, I, E, k, dtype=MOE_BF16, minibatch_rows=128) -> Problem:
     return Problem(int(N), int(H), int(I), int(E), int(k), int(dtype), int(minibatch_rows))
 
 
-def weights(wg, wu, wd, wg_bwd=None, wu_bwd=None, wd_bwd=None) -> Weights:
-    return Weights(_ptr(wg), _ptr(wu), _ptr(wd), _ptr(wg_bwd), _ptr(wu_bwd), _ptr(wd_bwd))
+def mxfp8_weights(operands: dict) -> MXFP8Weights:
+    """operands: name -> (q, s) tensors (names of MXFP8_WEIGHT_OPERANDS; missing ones NULL)."""
+    st = MXFP8Weights()
+    for n in MXFP8_WEIGHT_OPERANDS:
+        q, sc = operands.get(n, (None, None))
+        setattr(st, n, MXFP8Operand(_ptr(q), _ptr(sc)))
+    return st
+
+
+def weights(wg, wu, wd, wg_bwd=None, wu_bwd=None, wd_bwd=None, mx: MXFP8Weights = None) -> Weights:
+    w = Weights(_ptr(wg), _ptr(wu), _ptr(wd), _ptr(wg_bwd), _ptr(wu_bwd), _ptr(wd_bwd),
+                ctypes.pointer(mx) if mx is not None else None)
+    w._keep = mx  # the pointed-to struct lives as long as this one
+    return w
 
 
 def _call(name, *args):
@@ -261,6 +286,11 @@ def moe_backward(p, saved, w: Weights, topk_w, dy, dx, dw_gate, dw_up, dw_down, 
 
 def mxfp8_quantize(src, rows, cols, q, scale, stream=None):
     _call("mxfp8_quantize", _ptr(src), int(rows), int(cols), _ptr(q), _ptr(scale),
+          _stream(stream))
+
+
+def mxfp8_quantize_mma(src, rows, cols, transpose, q, s, stream=None):
+    _call("mxfp8_quantize_mma", _ptr(src), int(rows), int(cols), int(transpose), _ptr(q), _ptr(s),
           _stream(stream))
 
 

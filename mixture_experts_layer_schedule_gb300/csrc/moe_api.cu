@@ -66,6 +66,10 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   L->mx_ch = mx ? take(static_cast<size_t>(R) * p->H * 2) : 0;
   L->mx_ci1 = mx ? take(static_cast<size_t>(R) * p->I * 2) : 0;
   L->mx_ci2 = mx ? take(static_cast<size_t>(R) * p->I * 2) : 0;
+  L->mq_rh = mx ? take(static_cast<size_t>(R) * p->H) : 0;
+  L->ms_rh = mx ? take(static_cast<size_t>(R) * p->H / 32) : 0;
+  L->mq_ri = mx ? take(static_cast<size_t>(R) * p->I) : 0;
+  L->ms_ri = mx ? take(static_cast<size_t>(R) * p->I / 32) : 0;
   L->ws_bytes = o;
   o = 0;
   L->xe = take(static_cast<size_t>(R) * p->H * 2);
@@ -103,6 +107,29 @@ moe_status prep(const moe_problem* p, const void* ws, Layout* L) {
 
 bool weights_ok(const moe_weights* w) {
   return w && aligned(w->w_gate, 16) && aligned(w->w_up, 16) && aligned(w->w_down, 16);
+}
+
+bool operand_ok(const moe_mxfp8_operand& o) { return aligned(o.q, 16) && aligned(o.s, 16); }
+
+// The forward MXFP8 tensor-core operands are present and aligned.
+bool mx_forward_ok(const moe_weights* w) {
+  return w && w->mx && operand_ok(w->mx->gate) && operand_ok(w->mx->up) &&
+         operand_ok(w->mx->down);
+}
+
+// MXFP8 forward on the block-scaled tensor cores: Xe quantised along H feeds
+// gate/up, Act quantised along I feeds down. g/u may be NULL (inference).
+moe_status mx_forward_gemms(const Layout& L, void* ws, const moe_mxfp8_weights& mx,
+                            const void* xe, void* g, void* u, void* act, void* ye,
+                            cudaStream_t s) {
+  uint8_t* xq = at<uint8_t>(ws, L.mq_rh);
+  uint8_t* xs = at<uint8_t>(ws, L.ms_rh);
+  uint8_t* aq = at<uint8_t>(ws, L.mq_ri);
+  uint8_t* as = at<uint8_t>(ws, L.ms_ri);
+  MOE_TRY(cu(launch_mxfp8_quantize_mma(xe, L.R, L.H, 0, xq, xs, s)));
+  MOE_TRY(gemm_mx_gate_up(L, ws, xq, xs, mx.gate, mx.up, g, u, act, s));
+  MOE_TRY(cu(launch_mxfp8_quantize_mma(act, L.R, L.I, 0, aq, as, s)));
+  return gemm_mx_down(L, ws, aq, as, mx.down, ye, s);
 }
 
 }  // namespace
@@ -227,6 +254,23 @@ moe_status moe_forward_inference(const moe_problem* p, const void* x, const moe_
   MOE_TRY(prep(p, ws, &L));
   void* act = at<char>(ws, L.dg);    // [R, I] scratch
   void* ye = at<char>(ws, L.dyxe);   // [R, H] scratch
+  if (p->dtype == MOE_MXFP8) {
+    // Xe must exist to be quantised along H: dispatch into scratch first.
+    void* xe = at<char>(ws, L.mx_ch);
+    MOE_TRY(moe_dispatch(p, ws, x, xe, stream));
+    if (mx_forward_ok(w)) {
+      MOE_TRY(mx_forward_gemms(L, ws, *w->mx, xe, nullptr, nullptr, act, ye, S(stream)));
+    } else {
+      void* xq = at<char>(ws, L.mx_rh);
+      void* aq = at<char>(ws, L.mx_ri1);
+      MOE_TRY(mxfp8_qdq(xe, xq, L.R, L.H, 0, stream));
+      MOE_TRY(moe_expert_gate_up(p, ws, xq, w, at<char>(ws, L.mx_ci1), at<char>(ws, L.mx_ci2),
+                                 act, stream));
+      MOE_TRY(mxfp8_qdq(act, aq, L.R, L.I, 0, stream));
+      MOE_TRY(moe_expert_down(p, ws, aq, w, ye, stream));
+    }
+    return moe_combine(p, ws, ye, topk_w, y, stream);
+  }
   MOE_TRY(moe_expert_gate_up_gather(p, ws, x, w, nullptr, nullptr, act, stream));
   MOE_TRY(moe_expert_down(p, ws, act, w, ye, stream));
   return moe_combine(p, ws, ye, topk_w, y, stream);
@@ -237,8 +281,16 @@ moe_status moe_forward(const moe_problem* p, const void* x, const moe_weights* w
   moe_saved_view v;
   MOE_TRY(moe_saved_layout(p, saved, &v));
   MOE_TRY(moe_dispatch(p, ws, x, v.xe, stream));
+  if (p->dtype == MOE_MXFP8 && w && w->mx) {
+    Layout L;
+    MOE_TRY(prep(p, ws, &L));
+    if (!mx_forward_ok(w)) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(mx_forward_gemms(L, ws, *w->mx, v.xe, v.g, v.u, v.act, v.ye, S(stream)));
+    return moe_combine(p, ws, v.ye, topk_w, y, stream);
+  }
   if (p->dtype == MOE_MXFP8) {
-    // MXFP8: gate/up reads Xe quantised along H, down reads Act quantised along I
+    // MXFP8 on bf16 MMAs: gate/up reads Xe quantised along H, down reads Act
+    // quantised along I, as exact bf16 values
     Layout L;
     MOE_TRY(prep(p, ws, &L));
     void* xq = at<char>(ws, L.mx_rh);
@@ -372,6 +424,16 @@ moe_status mxfp8_qdq(const void* src_bf16, void* dst_bf16, int64_t rows, int64_t
   if (rows * cols == 0) return MOE_OK;
   if (!aligned(src_bf16, 16) || !aligned(dst_bf16, 16)) return MOE_ERR_INVALID_ARG;
   return cu(launch_mxfp8_qdq(src_bf16, dst_bf16, rows, cols, axis, S(stream)));
+}
+
+moe_status mxfp8_quantize_mma(const void* src_bf16, int64_t rows, int64_t cols, int transpose,
+                              uint8_t* q_e4m3, uint8_t* s_e8m0, void* stream) {
+  if (rows < 0 || cols < 0 || rows % 128 != 0 || cols % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (transpose != 0 && transpose != 1) return MOE_ERR_INVALID_ARG;
+  if (rows * cols == 0) return MOE_OK;
+  if (!aligned(src_bf16, 16) || !aligned(q_e4m3, 16) || !s_e8m0) return MOE_ERR_INVALID_ARG;
+  return cu(launch_mxfp8_quantize_mma(src_bf16, rows, cols, transpose, q_e4m3, s_e8m0,
+                                      S(stream)));
 }
 
 moe_status mxfp8_quantize(const void* src_bf16, int64_t rows, int64_t cols, uint8_t* q_e4m3,

@@ -26,7 +26,8 @@ struct Layout {
   // workspace byte offsets
   size_t err, counts, offsets, pad_offsets, slot_of, src_of_row, tiles, n_tiles, warp_counts,
       expert_order,
-      mx_rh, mx_ri1, mx_ri2, mx_ch, mx_ci1, mx_ci2,  // MXFP8 quantised operands
+      mx_rh, mx_ri1, mx_ri2, mx_ch, mx_ci1, mx_ci2,  // MXFP8 quantised operands (bf16 values)
+      mq_rh, ms_rh, mq_ri, ms_ri,  // MXFP8 E4M3 codes + scale chunks of Xe and Act (tensor cores)
       dyxe, dg, du, ws_bytes;
   // forward-context byte offsets
   size_t xe, g, u, act, ye, saved_bytes;
@@ -61,6 +62,8 @@ cudaError_t launch_reverse_dispatch(const Layout& L, const void* ws, const void*
                                     cudaStream_t s);
 cudaError_t launch_mxfp8_qdq(const void* src, void* dst, int64_t rows, int64_t cols, int axis,
                              cudaStream_t s);
+cudaError_t launch_mxfp8_quantize_mma(const void* src, int64_t rows, int64_t cols, int transpose,
+                                      uint8_t* q, uint8_t* sf, cudaStream_t s);
 cudaError_t launch_mxfp8_quantize(const void* src, int64_t rows, int64_t cols, uint8_t* q,
                                   uint8_t* scale, cudaStream_t s);
 
@@ -79,6 +82,14 @@ moe_status gemm_gate_up_dgrad(const Layout& L, const void* ws, const void* dg, c
                               const void* wg, const void* wu, void* dxe, cudaStream_t s);
 moe_status gemm_gate_up_wgrad(const Layout& L, const void* ws, const void* dg, const void* du,
                               const void* xe, float* dw_gate, float* dw_up, cudaStream_t s);
+
+// Block-scaled FP8 grouped GEMMs (tcgen05 kind::mxf8f6f4) of the MXFP8 layer.
+// xq/aq: E4M3 codes [R, H] / [R, I]; xs/as: their scale chunks.
+moe_status gemm_mx_gate_up(const Layout& L, const void* ws, const uint8_t* xq, const uint8_t* xs,
+                           const moe_mxfp8_operand& wg, const moe_mxfp8_operand& wu, void* g,
+                           void* u, void* act, cudaStream_t s);
+moe_status gemm_mx_down(const Layout& L, const void* ws, const uint8_t* aq, const uint8_t* as,
+                        const moe_mxfp8_operand& wd, void* ye, cudaStream_t s);
 
 // Launch accounting (every kernel launch of the library calls note_launch).
 void note_launch();

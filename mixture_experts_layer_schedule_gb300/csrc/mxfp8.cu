@@ -131,7 +131,105 @@ __global__ void __launch_bounds__(256) qdq_cols_kernel(const uint32_t* __restric
   for (int r = 0; r < 32; ++r) dst[(rb * 32 + r) * cols2 + c] = pack_bf16x2(lo[r], hi[r]);
 }
 
+// Quantiser for the block-scaled tensor-core GEMMs: E4M3 codes of a K-major
+// operand [rows, K] and its E8M0 scales in the layout tcgen05.cp (32x128b,
+// warpx4) moves into tensor memory: 512-byte chunks, one per (128 K, 128 rows),
+// chunk (kc, rb) at ((kc * rows/128) + rb) * 512, and inside a chunk the scale
+// of (row r, 32-wide K block j) at byte (r % 32) * 16 + ((r / 32) % 4) * 4 + j % 4.
+__device__ __forceinline__ size_t sf_mma_index(int64_t r, int64_t kb32, int64_t rows) {
+  return static_cast<size_t>(((kb32 >> 2) * (rows >> 7) + (r >> 7)) * 512 + (r & 31) * 16 +
+                             ((r >> 5) & 3) * 4 + (kb32 & 3));
+}
+
+// Codes of one block of 32 values (rule of mxfp8_quantize_kernel); returns the
+// scale code.
+__device__ __forceinline__ uint8_t quant32(const float (&f)[32], uint32_t (&packed)[8]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  const int biased = (__float_as_uint(amax) >> 23) & 0xFF;
+  const int code = biased == 0 ? 0 : max(0, biased - 8);
+  const float inv = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t lo = e4m3x2(f[4 * i + 0] * inv, f[4 * i + 1] * inv);
+    const uint32_t hi = e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
+    packed[i] = lo | (hi << 16);
+  }
+  return static_cast<uint8_t>(code);
+}
+
+// Row form: blocks of 32 consecutive values of a row; q [rows, cols].
+__global__ void __launch_bounds__(256) quant_mma_rows_kernel(const uint4* __restrict__ src,
+                                                             int64_t rows, int64_t cols,
+                                                             uint4* __restrict__ q,
+                                                             uint8_t* __restrict__ sf) {
+  const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t per_row = cols / 32;
+  if (b >= rows * per_row) return;
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 r = src[b * 4 + i];
+    f[8 * i + 0] = bf16lo(r.x); f[8 * i + 1] = bf16hi(r.x);
+    f[8 * i + 2] = bf16lo(r.y); f[8 * i + 3] = bf16hi(r.y);
+    f[8 * i + 4] = bf16lo(r.z); f[8 * i + 5] = bf16hi(r.z);
+    f[8 * i + 6] = bf16lo(r.w); f[8 * i + 7] = bf16hi(r.w);
+  }
+  uint32_t packed[8];
+  const uint8_t code = quant32(f, packed);
+  q[b * 2 + 0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  q[b * 2 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  sf[sf_mma_index(b / per_row, b % per_row, rows)] = code;
+}
+
+// Transposed form: q [cols, rows] = src^T, blocks of 32 consecutive source
+// rows of a column (the K of the transposed operand). One thread per (32-row
+// block, column pair): a warp reads 128 contiguous bytes of each source row.
+__global__ void __launch_bounds__(256) quant_mma_cols_kernel(const uint32_t* __restrict__ src,
+                                                             int64_t rows, int64_t cols2,
+                                                             uint8_t* __restrict__ q,
+                                                             uint8_t* __restrict__ sf) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= (rows / 32) * cols2) return;
+  const int64_t rb = idx / cols2, c2 = idx % cols2;
+  float lo[32], hi[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    const uint32_t v = src[(rb * 32 + r) * cols2 + c2];
+    lo[r] = bf16lo(v);
+    hi[r] = bf16hi(v);
+  }
+  const int64_t cols = cols2 * 2;
+  uint32_t packed[8];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint8_t code = quant32(h ? hi : lo, packed);
+    const int64_t orow = 2 * c2 + h;  // row of the transposed operand
+    uint4* dst = reinterpret_cast<uint4*>(q + orow * rows + rb * 32);
+    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    sf[sf_mma_index(orow, rb, cols)] = code;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_mxfp8_quantize_mma(const void* src, int64_t rows, int64_t cols, int transpose,
+                                      uint8_t* q, uint8_t* sf, cudaStream_t s) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  if (!transpose) {
+    const int64_t n = rows * (cols / 32);
+    quant_mma_rows_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
+        static_cast<const uint4*>(src), rows, cols, reinterpret_cast<uint4*>(q), sf);
+  } else {
+    const int64_t n = (rows / 32) * (cols / 2);
+    quant_mma_cols_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
+        static_cast<const uint32_t*>(src), rows, cols / 2, q, sf);
+  }
+  note_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_mxfp8_qdq(const void* src, void* dst, int64_t rows, int64_t cols, int axis,
                              cudaStream_t s) {

@@ -14,6 +14,15 @@ import torch
 from . import _lib
 
 
+class MXFP8MMAWeights:
+    """E4M3 codes + E8M0 scale chunks of the expert weights (tensors kept
+    alive here) and the C struct that points at them."""
+
+    def __init__(self, operands: dict):
+        self.operands = operands
+        self.struct = _lib.mxfp8_weights(operands)
+
+
 @dataclass
 class Grads:
     dx: torch.Tensor
@@ -101,15 +110,31 @@ class MoELayer:
             bwd.append(b)
         return tuple(fwd), tuple(bwd)
 
-    def forward(self, x, wg, wu, wd, topk_w=None, stream=None):
-        w = _lib.weights(wg, wu, wd)
+    @staticmethod
+    def prepare_mxfp8_mma_weights(wg, wu, wd, stream=None) -> "MXFP8MMAWeights":
+        """MXFP8 weights for the block-scaled tensor-core GEMMs: E4M3 codes and
+        E8M0 scale chunks of gate/up [E*I, H] and down [E*H, I] (forward)."""
+        E, I, H = wg.shape
+        dev = wg.device
+        ops = {}
+        for name, t, rows, cols in (("gate", wg, E * I, H), ("up", wu, E * I, H),
+                                    ("down", wd, E * H, I)):
+            q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+            sc = torch.empty((rows * cols // 32,), dtype=torch.uint8, device=dev)
+            _lib.mxfp8_quantize_mma(t, rows, cols, 0, q, sc, stream)
+            ops[name] = (q, sc)
+        return MXFP8MMAWeights(ops)
+
+    def forward(self, x, wg, wu, wd, topk_w=None, stream=None, mx=None):
+        """mx: MXFP8MMAWeights (MXFP8 layers): run the GEMMs on the FP8 tensor cores."""
+        w = _lib.weights(wg, wu, wd, mx=mx.struct if mx is not None else None)
         _lib.moe_forward(self.p, x, w, self.topk_w if topk_w is None else topk_w, self.y,
                          self.saved, self.ws, stream)
         return self.y
 
-    def forward_inference(self, x, wg, wu, wd, topk_w=None, stream=None):
-        """Forward without a saved context; the dispatch is fused into gate/up."""
-        w = _lib.weights(wg, wu, wd)
+    def forward_inference(self, x, wg, wu, wd, topk_w=None, stream=None, mx=None):
+        """Forward without a saved context; the dispatch is fused into gate/up (bf16)."""
+        w = _lib.weights(wg, wu, wd, mx=mx.struct if mx is not None else None)
         _lib.moe_forward_inference(self.p, x, w, self.topk_w if topk_w is None else topk_w,
                                    self.y, self.ws, stream)
         return self.y
@@ -122,11 +147,12 @@ class MoELayer:
                           g.dx, g.dw_gate, g.dw_up, g.dw_down, g.d_topk_w, self.ws, stream)
         return g
 
-    def step(self, x, logits, bias, wg, wu, wd, dy, stream=None, backward=True, bwd=None):
+    def step(self, x, logits, bias, wg, wu, wd, dy, stream=None, backward=True, bwd=None,
+             mx=None):
         """Route, schedule, forward and (optionally) backward: one layer pass."""
         self.route(logits, bias, stream)
         self.build_schedule(None, stream)
-        y = self.forward(x, wg, wu, wd, None, stream)
+        y = self.forward(x, wg, wu, wd, None, stream, mx=mx)
         if backward:
             self.backward(dy, wg, wu, wd, None, stream, bwd=bwd)
         return y

@@ -1,0 +1,135 @@
+"""MXFP8 on the block-scaled tensor cores (tcgen05 kind::mxf8f6f4).
+
+* The MMA-layout quantiser, row and transposed forms, gives the oracle
+  quantiser's E4M3 codes bit-exactly and its E8M0 scales at the chunk
+  positions include/moe.h documents.
+* The MXFP8 forward on FP8 MMAs matches the same forward on bf16 MMAs of the
+  exact MXFP8 values (the same products, fp32 sums in another order) to
+  1e-2 * max|ref| per tensor, is bitwise identical across reruns, and the
+  whole layer (FP8 forward, backward on the quantised bf16 values) matches the
+  oracle's MXFP8 layer within 6e-2 * max|ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_layer_schedule_gb300 import MoELayer, _lib, inputs
+
+from gpu_helpers import assert_close, custom_shape, dev, max_rel, to_dev
+
+pytestmark = pytest.mark.gpu
+
+MX_TOL = 6e-2
+SAME_PRODUCTS_TOL = 1e-2
+
+
+def untile_scales(s, rows, k):
+    """Scales [rows, k/32] from the 512-byte chunk layout of a K-major operand."""
+    r = np.arange(rows)[:, None]
+    j = np.arange(k // 32)[None, :]
+    idx = ((j // 4) * (rows // 128) + r // 128) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (j % 4)
+    return s[idx]
+
+
+@pytest.mark.parametrize("transpose", [0, 1])
+@pytest.mark.parametrize("rows,cols", [(128, 128), (256, 384), (384, 1024)])
+def test_quantize_mma_matches_oracle(transpose, rows, cols):
+    g = torch.Generator().manual_seed(rows + cols + transpose)
+    spread = torch.exp(torch.empty((rows, 1)).uniform_(-8, 8, generator=g))
+    x = (torch.randn((rows, cols), generator=g) * spread).bfloat16()
+    x[0, :64] = 0.0  # all-zero blocks take scale code 0
+    q = torch.empty(rows * cols, dtype=torch.uint8, device=dev())
+    s = torch.empty(rows * cols // 32, dtype=torch.uint8, device=dev())
+    _lib.mxfp8_quantize_mma(x.to(dev()), rows, cols, transpose, q, s)
+    torch.cuda.synchronize()
+    src = oracle.as_bf16_bits(x)
+    if transpose:
+        src = np.ascontiguousarray(src.T)
+    ref_q, ref_s = oracle.mxfp8_quantize(src)
+    R, K = ref_q.shape
+    np.testing.assert_array_equal(q.cpu().numpy().reshape(R, K), ref_q)
+    np.testing.assert_array_equal(untile_scales(s.cpu().numpy(), R, K), ref_s)
+
+
+def test_quantize_mma_rejects_unaligned_sizes():
+    x = torch.zeros((128, 96), dtype=torch.bfloat16, device=dev())
+    q = torch.empty(128 * 96, dtype=torch.uint8, device=dev())
+    s = torch.empty(128 * 3, dtype=torch.uint8, device=dev())
+    with pytest.raises(_lib.MoEError):
+        _lib.mxfp8_quantize_mma(x, 128, 96, 0, q, s)
+
+
+SHAPES = [inputs.TINY.with_(name="tiny_mxfp8", dtype="mxfp8"),
+          custom_shape(300, 512, 768, 16, 4, zipf_s=1.2, name="ragged_skewed_mxfp8").with_(dtype="mxfp8"),
+          custom_shape(300, 768, 512, 16, 4, name="odd_h_tiles_mxfp8").with_(dtype="mxfp8"),
+          custom_shape(300, 512, 768, 16, 4, zipf_s=1.2, name="ragged_T256_mxfp8", T=256).with_(dtype="mxfp8")]
+
+
+def _layer(shape):
+    return MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev(),
+                    minibatch_rows=shape.minibatch_rows, dtype="mxfp8")
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: s.name)
+def test_fp8_forward_matches_bf16_mma_forward(shape):
+    inp = to_dev(inputs.make_inputs(shape, seed=5, device="cpu"))
+    fwd, _ = MoELayer.prepare_mxfp8_weights(inp["wg"], inp["wu"], inp["wd"])
+    mx = MoELayer.prepare_mxfp8_mma_weights(inp["wg"], inp["wu"], inp["wd"])
+    a, b = _layer(shape), _layer(shape)
+    for lay in (a, b):
+        lay.route(inp["logits"], inp["bias"])
+        lay.build_schedule()
+    a.forward(inp["x"], *fwd, mx=mx)
+    b.forward(inp["x"], *fwd)
+    torch.cuda.synchronize()
+    assert a.device_error() == 0 and b.device_error() == 0
+    rows = int(a.schedule_tensors()["pad_offsets"][shape.E].item())
+    sa, sb = a.saved_tensors(), b.saved_tensors()
+    for name in ("g", "u", "act", "ye"):
+        e = max_rel(sa[name][:rows], sb[name][:rows].float().cpu().numpy())
+        assert e <= SAME_PRODUCTS_TOL, (name, e)
+    e = max_rel(a.y, b.y.float().cpu().numpy())
+    assert e <= SAME_PRODUCTS_TOL, ("y", e)
+    y1 = a.y.clone()
+    a.forward(inp["x"], *fwd, mx=mx)
+    torch.cuda.synchronize()
+    assert torch.equal(a.y, y1), "FP8 forward is not bitwise reproducible"
+
+
+@pytest.mark.parametrize("shape", SHAPES[:2], ids=lambda s: s.name)
+def test_fp8_layer_matches_oracle(shape):
+    inp_cpu = inputs.make_inputs(shape, seed=3, device="cpu")
+    inp = to_dev(inp_cpu)
+    fwd, bwd = MoELayer.prepare_mxfp8_weights(inp["wg"], inp["wu"], inp["wd"])
+    mx = MoELayer.prepare_mxfp8_mma_weights(inp["wg"], inp["wu"], inp["wd"])
+    layer = _layer(shape)
+    layer.step(inp["x"], inp["logits"], inp["bias"], *fwd, inp["dy"], bwd=bwd, mx=mx)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    logits = inp_cpu["logits"].numpy()
+    bias = None if inp_cpu["bias"] is None else inp_cpu["bias"].numpy()
+    ids, w = oracle.route_topk(logits, bias, shape.k)
+    r = oracle.layer_mxfp8(inp_cpu["x"], inp_cpu["wg"], inp_cpu["wu"], inp_cpu["wd"], ids, w,
+                           inp_cpu["dy"], quantize=True)
+    g = layer.grads
+    assert_close("y", layer.y, r["y"], MX_TOL)
+    for name, got, key in (("dx", g.dx, "dx"), ("dw_gate", g.dw_gate, "dwg"),
+                           ("dw_up", g.dw_up, "dwu"), ("dw_down", g.dw_down, "dwd"),
+                           ("d_topk_w", g.d_topk_w, "dw")):
+        assert_close(name, got, r[key], MX_TOL)
+
+
+def test_fp8_inference_forward_matches_training_forward():
+    shape = SHAPES[1]
+    inp = to_dev(inputs.make_inputs(shape, seed=9, device="cpu"))
+    fwd, _ = MoELayer.prepare_mxfp8_weights(inp["wg"], inp["wu"], inp["wd"])
+    mx = MoELayer.prepare_mxfp8_mma_weights(inp["wg"], inp["wu"], inp["wd"])
+    a, b = _layer(shape), _layer(shape)
+    for lay in (a, b):
+        lay.route(inp["logits"], inp["bias"])
+        lay.build_schedule()
+    a.forward(inp["x"], *fwd, mx=mx)
+    b.forward_inference(inp["x"], *fwd, mx=mx)
+    torch.cuda.synchronize()
+    assert torch.equal(a.y, b.y)
