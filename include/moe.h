@@ -120,7 +120,9 @@ typedef struct {
    * FP8 MMAs (tcgen05 kind::mxf8f6f4, fp32 accumulation) on the codes, with
    * the activations quantised to E4M3 + E8M0 by the library; NULL runs them
    * on the bf16 values of the MXFP8 numbers in w_gate / w_up / w_down. Both
-   * compute the same products of the same MXFP8 numbers. */
+   * compute the same products of the same MXFP8 numbers. moe_backward uses
+   * the tensor-core path when mx->gate_t.q is non-NULL (then gate_t, up_t,
+   * down_t must all be set), else the bf16 values in w_*_bwd. */
   const moe_mxfp8_weights* mx;
 } moe_weights;
 

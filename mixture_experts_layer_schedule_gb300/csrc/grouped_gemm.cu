@@ -1000,13 +1000,6 @@ moe_status launch_rows(const Maps& maps, const Args& args, cudaStream_t s) {
   return launch<MODE, 1>(maps, args, static_cast<int64_t>(args.max_mtiles) * args.n_nt, s);
 }
 
-moe_status launch_expert_order(const Layout& L, const void* ws, cudaStream_t s) {
-  expert_order_kernel<<<1, 1024, 0, s>>>(at<int32_t>(ws, L.counts), L.E,
-                                         const_cast<int32_t*>(at<int32_t>(ws, L.expert_order)));
-  note_launch();
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-}
-
 // Rows of the A box of the token-row modes: the CTA's whole 128-row tile (SM
 // pairs, or no pairing), or the 64-row half each CTA of a multicast pair loads.
 int a_box_rows(const Layout& L, int n_nt) {
@@ -1037,6 +1030,13 @@ Args base_args(const Layout& L, const void* ws) {
 }
 
 }  // namespace
+
+moe_status launch_expert_order(const Layout& L, const void* ws, cudaStream_t s) {
+  expert_order_kernel<<<1, 1024, 0, s>>>(at<int32_t>(ws, L.counts), L.E,
+                                         const_cast<int32_t*>(at<int32_t>(ws, L.expert_order)));
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const void* wg,
                         const void* wu, void* g, void* u, void* act, cudaStream_t s) {

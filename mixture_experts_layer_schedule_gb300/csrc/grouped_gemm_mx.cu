@@ -23,6 +23,16 @@
 // Scale chunks of stage s live in TMEM columns 256 + 16 s, so the copy of a
 // stage never overwrites scales an MMA of an earlier stage may still read.
 // Every wait is bounded (timeout -> MOE_DEVERR_TIMEOUT, drain, free TMEM).
+//
+// Every GEMM is TN (both operands K-major): the backward ones read the
+// weights through transposed quantised copies and the weight gradients read
+// token-axis quantised, transposed activations, so one operand path serves
+//   GATE_UP  G|U = Xe . [Wg[e]; Wu[e]]^T  -> G, U, Act = silu(G) * U (bf16)
+//   DOWN     Ye  = Act . Wd[e]^T           -> bf16
+//   DACT     dAct = dYe . (Wd[e]^T)^T      -> dG, dU via the SwiGLU backward
+//   DXE      dXe = dG . (Wg[e]^T)^T + dU . (Wu[e]^T)^T  (two K phases) -> bf16
+//   WGRAD    dW[e] = P_e^T . Q_e (K = the expert's rows) -> fp32, one or two
+//            problems per launch (dWg and dWu share Q = Xe).
 #include <algorithm>
 #include <mutex>
 
@@ -38,38 +48,47 @@ constexpr int kQStages = 4;
 constexpr int kQA = QM * QK;  // 16 KB
 constexpr int kQB = QN * QK;  // 32 KB
 constexpr int kQSfa = 512, kQSfb = 1024;
-constexpr int kQStageUsed = kQA + kQB + kQSfa + kQSfb;
-constexpr int kQStageBytes = 51200;  // stages start on 1024-byte boundaries
-static_assert(kQStageUsed <= kQStageBytes && kQStageBytes % 1024 == 0, "stage layout");
-constexpr int kQSmem = kQStages * kQStageBytes + 1024;
+constexpr int kQStageBytes = kQA + kQB;   // operand tiles of a stage (1024-byte multiple)
+constexpr int kQSfBytes = kQSfa + kQSfb;   // scale chunks of a stage, in a ring of their own
+constexpr int kQStageTx = kQStageBytes + kQSfBytes;  // bytes that complete a stage
+// Epilogue staging for TMA stores: per epilogue warp two 32-row x 32-byte buffers.
+constexpr int kQOutBuf = 1024;
+constexpr int kQOutBytes = 8 * 2 * kQOutBuf;
+constexpr int kQSmem = kQStages * (kQStageBytes + kQSfBytes) + kQOutBytes + 1024;
 constexpr int kQThreads = 320;
 constexpr uint32_t kQTmemCols = 512;
 constexpr uint32_t kQSfCol = 256;
 
-enum QMode { Q_GATE_UP = 0, Q_DOWN = 1 };
+enum QMode { Q_GATE_UP = 0, Q_DOWN = 1, Q_DACT = 2, Q_DXE = 3, Q_WGRAD = 4 };
 
 struct QMaps {
-  CUtensorMap a, b0, b1;
+  CUtensorMap a0, a1, b0, b1;
+  CUtensorMap o0, o1, o2;  // outputs (TMA stores): 32 rows x 32 bytes, no swizzle
 };
 
 struct QArgs {
-  const int32_t* tiles;    // [n][3] (expert, row0, valid) of the 128-row tiles
-  const int32_t* n_tiles;  // device count of those tiles
+  const int32_t* tiles;        // [n][3] (expert, row0, valid) of the 128-row tiles
+  const int32_t* n_tiles;      // device count of those tiles
+  const int32_t* pad_offsets;  // [E+1] padded segment starts (WGRAD K ranges)
+  const int32_t* order;        // [E] experts by descending row count (WGRAD)
+  const int32_t* counts;       // [E] rows per expert (WGRAD K = count rounded up to 128)
   int32_t* err;
-  int max_mtiles;          // host bound on *n_tiles
-  int64_t rows;            // rows of the expert-grouped buffers
-  int n_nt;                // N tiles per M tile
-  int nkb;                 // K blocks of 128
-  int b_rows;              // rows per expert in B's 2-D view
-  int E;
-  const uint8_t* sfa;      // scale chunks of A [rows, K]
-  const uint8_t* sfb0;     // scale chunks of B (gate rows for GATE_UP)
-  const uint8_t* sfb1;     // up rows (GATE_UP)
-  int64_t a_rblocks;       // rows of A / 128
-  int64_t b_rblocks;       // rows of B / 128
-  int ld_out;              // output row length (elements)
-  int store_gu;            // GATE_UP: also store G and U
-  void *out0, *out1, *out2;
+  int max_mtiles;              // host bound on *n_tiles
+  int64_t rows;                // rows of the expert-grouped buffers
+  int n_nt;                    // N tiles per M tile (token-row modes)
+  int kb1, kb2;                // K blocks of 128 of phase 1 and 2
+  int b_rows;                  // GATE_UP / DOWN: rows per expert in B's 2-D view
+  int k_exp;                   // DACT / DXE: K per expert in the transposed weights
+  int E, w_mt, w_nt, n_probs;  // WGRAD tiling (M, N tiles of dW[e]; problems)
+  const uint8_t* sfa0;         // scale chunks of A (phase / problem 0)
+  const uint8_t* sfa1;         // ... of the second A (DXE phase 2, WGRAD problem 1)
+  const uint8_t* sfb0;         // scale chunks of B (gate rows for GATE_UP)
+  const uint8_t* sfb1;         // up rows (GATE_UP), second B (DXE)
+  int64_t a_rblocks;           // rows of A / 128
+  int64_t b_rblocks;           // rows of B / 128
+  int ld_out;                  // output row length (elements)
+  int store_gu;                // GATE_UP: also store G and U
+  const void *in0, *in1;       // DACT: the saved G, U
 };
 
 // ---- PTX used only here --------------------------------------------------
@@ -128,41 +147,159 @@ __device__ __forceinline__ bool q_wait_drain(uint64_t* bar, uint32_t parity, int
 }
 
 struct QTile {
-  int e, row0, nt;
+  int e, row0, mt, nt, prob, kstart, nkb;
   bool skip;
 };
 
-template <int CL>
+// Tile t of this CTA. With CL = 2 the two CTAs of a cluster take neighbouring
+// N tiles of the same A rows (token rows, or dW rows of one expert and
+// problem) and load that A tile once, half each, multicast to both.
+template <int MODE, int CL>
 __device__ __forceinline__ QTile q_decode(const QArgs& a, int64_t t, int crank) {
   QTile ti;
-  const int n_ntp = a.n_nt / CL;
-  const int mtile = static_cast<int>(t / n_ntp);
-  ti.nt = static_cast<int>(t % n_ntp) * CL + crank;
-  ti.e = a.tiles[3 * mtile + 0];
-  ti.row0 = a.tiles[3 * mtile + 1];
   ti.skip = false;
-  if (ti.e < 0 || ti.e >= a.E || ti.row0 < 0 || ti.row0 > a.rows - QM) {
-    ti.e = 0;  // corrupt schedule: compute nothing, store nothing
+  if constexpr (MODE == Q_WGRAD) {
+    // Largest experts first; within an expert (mt, N tile pair, problem), the
+    // problem fastest, so dWg and dWu tiles reading one Xe panel run together.
+    const int w_ntp = a.w_nt / CL;
+    const int64_t per_e = static_cast<int64_t>(a.w_mt) * w_ntp * a.n_probs;
+    const int rank = static_cast<int>(t / per_e);
+    int64_t r = t % per_e;
+    ti.mt = static_cast<int>(r / (w_ntp * a.n_probs));
+    r %= (w_ntp * a.n_probs);
+    ti.nt = static_cast<int>(r / a.n_probs) * CL + crank;
+    ti.prob = static_cast<int>(r % a.n_probs);
+    ti.e = a.order[rank];
+    if (ti.e < 0 || ti.e >= a.E) ti.e = 0;
+    ti.kstart = a.pad_offsets[ti.e];
+    ti.nkb = (a.counts[ti.e] + QK - 1) / QK;  // rows past the count are zero padding
     ti.row0 = 0;
-    ti.skip = true;
+    if (ti.kstart < 0 || ti.kstart % QK != 0 || ti.nkb < 0 ||
+        ti.kstart + static_cast<int64_t>(ti.nkb) * QK > a.pad_offsets[ti.e + 1] ||
+        ti.kstart + static_cast<int64_t>(ti.nkb) * QK > a.rows) {
+      ti.kstart = 0;  // corrupt schedule: compute nothing, store nothing
+      ti.nkb = 0;
+      ti.skip = true;
+    }
+  } else {
+    const int n_ntp = a.n_nt / CL;
+    const int mtile = static_cast<int>(t / n_ntp);
+    ti.nt = static_cast<int>(t % n_ntp) * CL + crank;
+    ti.mt = mtile;
+    ti.prob = 0;
+    ti.kstart = 0;
+    ti.e = a.tiles[3 * mtile + 0];
+    ti.row0 = a.tiles[3 * mtile + 1];
+    ti.nkb = a.kb1 + a.kb2;
+    if (ti.e < 0 || ti.e >= a.E || ti.row0 < 0 || ti.row0 > a.rows - QM) {
+      ti.e = 0;
+      ti.row0 = 0;
+      ti.nkb = 0;
+      ti.skip = true;
+    }
   }
   return ti;
 }
 
-template <int CL>
+template <int MODE, int CL>
 __device__ __forceinline__ int64_t q_total(const QArgs& a) {
-  int n = *a.n_tiles;
-  n = n < 0 ? 0 : (n > a.max_mtiles ? a.max_mtiles : n);
-  return static_cast<int64_t>(n) * (a.n_nt / CL);
+  if constexpr (MODE == Q_WGRAD) {
+    return static_cast<int64_t>(a.n_probs) * a.E * a.w_mt * (a.w_nt / CL);
+  } else {
+    int n = *a.n_tiles;
+    n = n < 0 ? 0 : (n > a.max_mtiles ? a.max_mtiles : n);
+    return static_cast<int64_t>(n) * (a.n_nt / CL);
+  }
+}
+
+// The copies of one stage: A (whole, or this CTA's multicast half), B, and
+// the scale chunks of both. Coordinates are (K element, row).
+template <int MODE, int CL>
+__device__ __forceinline__ void q_issue_loads(const QMaps& m, const QArgs& a, const QTile& ti,
+                                              int kb, uint8_t* sA, uint8_t* sSa, uint64_t* bar,
+                                              int crank) {
+  uint8_t* sB = sA + kQA;
+  uint8_t* sSb = sSa + kQSfa;
+  const CUtensorMap* ma = &m.a0;
+  const uint8_t* sfa = a.sfa0;
+  int ax, ay;            // A tile origin
+  int64_t a_chunk;       // A scale chunk index
+  const CUtensorMap* mb = &m.b0;
+  const uint8_t* sfb = a.sfb0;
+  int bx, by;            // B tile origin
+  int64_t b_chunk;
+  if constexpr (MODE == Q_WGRAD) {
+    if (ti.prob) { ma = &m.a1; sfa = a.sfa1; }
+    const int k0 = ti.kstart + kb * QK;
+    ax = k0;
+    ay = ti.mt * QM;
+    a_chunk = static_cast<int64_t>(k0 / QK) * a.a_rblocks + ti.mt;
+    bx = k0;
+    by = ti.nt * QN;
+    b_chunk = static_cast<int64_t>(k0 / QK) * a.b_rblocks + ti.nt * (QN / 128);
+  } else if constexpr (MODE == Q_DACT || MODE == Q_DXE) {
+    const bool second = (MODE == Q_DXE) && kb >= a.kb1;
+    const int kk = second ? kb - a.kb1 : kb;
+    if (second) { ma = &m.a1; sfa = a.sfa1; mb = &m.b1; sfb = a.sfb1; }
+    ax = kk * QK;
+    ay = ti.row0;
+    a_chunk = static_cast<int64_t>(kk) * a.a_rblocks + ti.row0 / 128;
+    bx = ti.e * a.k_exp + kk * QK;
+    by = ti.nt * QN;
+    b_chunk = static_cast<int64_t>(bx / QK) * a.b_rblocks + ti.nt * (QN / 128);
+  } else {  // GATE_UP, DOWN
+    ax = kb * QK;
+    ay = ti.row0;
+    a_chunk = static_cast<int64_t>(kb) * a.a_rblocks + ti.row0 / 128;
+    bx = kb * QK;
+    by = MODE == Q_GATE_UP ? ti.e * a.b_rows + ti.nt * (QN / 2) : ti.e * a.b_rows + ti.nt * QN;
+    b_chunk = static_cast<int64_t>(kb) * a.b_rblocks + by / 128;
+  }
+  if constexpr (CL == 1) tma_load_2d(sA, ma, bar, ax, ay);
+  else tma_load_2d_mc(sA + crank * (kQA / 2), ma, bar, ax, ay + crank * (QM / 2), 0x3);
+  bulk_load(sSa, sfa + a_chunk * 512, kQSfa, bar);
+  if constexpr (MODE == Q_GATE_UP) {
+    // the N tile is 128 gate rows then 128 up rows of the same expert
+    tma_load_2d(sB, &m.b0, bar, bx, by);
+    tma_load_2d(sB + kQB / 2, &m.b1, bar, bx, by);
+    bulk_load(sSb, a.sfb0 + b_chunk * 512, 512, bar);
+    bulk_load(sSb + 512, a.sfb1 + b_chunk * 512, 512, bar);
+  } else {
+    tma_load_2d(sB, mb, bar, bx, by);
+    bulk_load(sSb, sfb + b_chunk * 512, kQSfb, bar);
+  }
 }
 
 __device__ __forceinline__ float q_silu(float g) { return g / (1.0f + expf(-g)); }
 
-// 8 consecutive fp32 values -> one 16-byte bf16 store.
-__device__ __forceinline__ void st_bf16x8(void* dst, const float* v) {
-  *reinterpret_cast<uint4*>(dst) =
-      make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                 pack_bf16x2(v[6], v[7]));
+// 16 consecutive fp32 values -> 16 bf16 (8 words).
+__device__ __forceinline__ void pack16(const float* v, uint32_t (&w)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+}
+
+// One 32-row x 32-byte block of a warp's output (32 bytes of each lane's row)
+// through a shared staging buffer to one TMA store at (x, y); two buffers per
+// warp let a store overlap the next block.
+__device__ __forceinline__ void q_store(const CUtensorMap* om, const uint32_t (&w)[8], int32_t x,
+                                        int32_t y, int lane, uint8_t* bufs, uint32_t& n) {
+  uint8_t* buf = bufs + (n & 1u) * kQOutBuf;
+  if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
+  __syncwarp();
+  const uint32_t a = smem_u32(buf) + lane * 32;
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3])
+               : "memory");
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a + 16), "r"(w[4]), "r"(w[5]),
+               "r"(w[6]), "r"(w[7])
+               : "memory");
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(om, buf, x, y);
+    bulk_commit();
+  }
+  ++n;
 }
 
 template <int MODE, int CL>
@@ -188,7 +325,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&maps.a);
+    tma_prefetch_desc(&maps.a0);
     tma_prefetch_desc(&maps.b0);
   }
   if (warp == 1) {
@@ -201,9 +338,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_slot;
   volatile int* abortp = &abort_flag;
-  const int64_t total = q_total<CL>(args);
+  const int64_t total = q_total<MODE, CL>(args);
   const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const int64_t first = blockIdx.x / CL, stride = gridDim.x / CL;
+  uint8_t* sf_ring = smem + kQStages * kQStageBytes;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -213,37 +351,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
       uint32_t issued_mask = 0, issued_parity = 0;
       bool ok = true;
       for (int64_t t = first; t < total && ok; t += stride) {
-        const QTile ti = q_decode<CL>(args, t, crank);
-        const int nkb = ti.skip ? 0 : args.nkb;
-        for (int kb = 0; kb < nkb; ++kb) {
+        const QTile ti = q_decode<MODE, CL>(args, t, crank);
+        for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, args.err)) { ok = false; break; }
-          uint8_t* sA = smem + stage * kQStageBytes;
-          uint8_t* sB = sA + kQA;
-          uint8_t* sSa = sB + kQB;
-          uint8_t* sSb = sSa + kQSfa;
           uint64_t* bar = &full_bar[stage];
-          mbar_arrive_expect_tx(bar, kQStageUsed);
-          if constexpr (CL == 1) {
-            tma_load_2d(sA, &maps.a, bar, kb * QK, ti.row0);
-          } else {
-            tma_load_2d_mc(sA + crank * (kQA / 2), &maps.a, bar, kb * QK,
-                           ti.row0 + crank * (QM / 2), 0x3);
-          }
-          bulk_load(sSa, args.sfa + (static_cast<int64_t>(kb) * args.a_rblocks + ti.row0 / 128) * 512,
-                    kQSfa, bar);
-          if constexpr (MODE == Q_GATE_UP) {
-            const int brow = ti.e * args.b_rows + ti.nt * (QN / 2);
-            tma_load_2d(sB, &maps.b0, bar, kb * QK, brow);
-            tma_load_2d(sB + kQB / 2, &maps.b1, bar, kb * QK, brow);
-            const int64_t so = (static_cast<int64_t>(kb) * args.b_rblocks + brow / 128) * 512;
-            bulk_load(sSb, args.sfb0 + so, 512, bar);
-            bulk_load(sSb + 512, args.sfb1 + so, 512, bar);
-          } else {
-            const int brow = ti.e * args.b_rows + ti.nt * QN;
-            tma_load_2d(sB, &maps.b0, bar, kb * QK, brow);
-            bulk_load(sSb, args.sfb0 + (static_cast<int64_t>(kb) * args.b_rblocks + brow / 128) * 512,
-                      kQSfb, bar);
-          }
+          mbar_arrive_expect_tx(bar, kQStageTx);
+          q_issue_loads<MODE, CL>(maps, args, ti, kb, smem + stage * kQStageBytes,
+                                  sf_ring + stage * kQSfBytes, bar, crank);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kQStages) { stage = 0; phase ^= 1u; }
@@ -261,16 +375,15 @@ __global__ void __launch_bounds__(kQThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int64_t t = first; t < total && ok; t += stride) {
-        const QTile ti = q_decode<CL>(args, t, crank);
-        const int nkb = ti.skip ? 0 : args.nkb;
+        const QTile ti = q_decode<MODE, CL>(args, t, crank);
         if (!mbar_wait(&tempty_bar, acc_phase ^ 1u, abortp, args.err)) break;
         tc_fence_after();
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abortp, args.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + stage * kQStageBytes);
           const uint32_t b_addr = a_addr + kQA;
-          const uint32_t sfa_s = b_addr + kQB;
+          const uint32_t sfa_s = smem_u32(sf_ring + stage * kQSfBytes);
           const uint32_t sfb_s = sfa_s + kQSfa;
           const uint32_t sf_t = tmem_base + kQSfCol + stage * 16;
           tmem_cp_sf(sf_t, sdesc_sf(sfa_s));
@@ -298,9 +411,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
     // ---------------- epilogue warps 2..9 ----------------
     const int quad = warp & 3;        // TMEM lanes this warp may access
     const int half = (warp - 2) >> 2;  // which half of the accumulator columns
+    uint8_t* out_bufs = sf_ring + kQStages * kQSfBytes + (warp - 2) * 2 * kQOutBuf;
+    uint32_t nstore = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = first; t < total; t += stride) {
-      const QTile ti = q_decode<CL>(args, t, crank);
+      const QTile ti = q_decode<MODE, CL>(args, t, crank);
       if (!mbar_wait(&tfull_bar, acc_phase, abortp, args.err)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
@@ -326,30 +441,84 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (lane == 0) set_dev_error(args.err, MOE_DEVERR_BAD_EXPERT);
         continue;
       }
-      const int64_t row = static_cast<int64_t>(ti.row0) + quad * 32 + lane;
-      if constexpr (MODE == Q_GATE_UP) {
-        const int64_t o = row * args.ld_out + ti.nt * (QN / 2) + 64 * half;
-        __nv_bfloat16* pg = static_cast<__nv_bfloat16*>(args.out0) + o;
-        __nv_bfloat16* pu = static_cast<__nv_bfloat16*>(args.out1) + o;
-        __nv_bfloat16* pa = static_cast<__nv_bfloat16*>(args.out2) + o;
+      const int32_t y = ti.row0 + quad * 32;  // first output row of this warp (token modes)
+      if constexpr (MODE == Q_WGRAD) {
+        // fp32 dW[e] rows; an expert without rows has an all-zero gradient
+        if (ti.nkb == 0) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) v[i] = 0.0f;
+        }
+        const CUtensorMap* om = ti.prob ? &maps.o1 : &maps.o0;
+        const int32_t wy = ti.e * (args.w_mt * QM) + ti.mt * QM + quad * 32;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          uint32_t w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(v[8 * j + i]);
+          q_store(om, w, ti.nt * QN + 128 * half + 8 * j, wy, lane, out_bufs, nstore);
+        }
+      } else if constexpr (MODE == Q_DACT) {
+        // dG, dU from dAct and the saved G, U of the same rows and columns
+        const int64_t row = static_cast<int64_t>(y) + lane;
+        const int32_t x0 = ti.nt * QN + 128 * half;
+        const int64_t o = row * args.ld_out + x0;
+        const uint4* pg = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.in0) + o);
+        const uint4* pu = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.in1) + o);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {  // fully unrolled: v stays in registers
+          uint32_t og[8], ou[8];
+#pragma unroll
+          for (int hv = 0; hv < 2; ++hv) {
+            const uint4 gv = pg[2 * j + hv], uv = pu[2 * j + hv];
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+            const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float dg2[2], du2[2];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const float da = v[16 * j + 8 * hv + 2 * q + h];
+                const float g = h ? bf16hi(gw[q]) : bf16lo(gw[q]);
+                const float u = h ? bf16hi(uw[q]) : bf16lo(uw[q]);
+                const float sg = 1.0f / (1.0f + expf(-g));
+                dg2[h] = da * u * sg * (1.0f + g * (1.0f - sg));
+                du2[h] = da * g * sg;
+              }
+              og[4 * hv + q] = pack_bf16x2(dg2[0], dg2[1]);
+              ou[4 * hv + q] = pack_bf16x2(du2[0], du2[1]);
+            }
+          }
+          q_store(&maps.o0, og, x0 + 16 * j, y, lane, out_bufs, nstore);
+          q_store(&maps.o1, ou, x0 + 16 * j, y, lane, out_bufs, nstore);
+        }
+      } else if constexpr (MODE == Q_GATE_UP) {
+        const int32_t x0 = ti.nt * (QN / 2) + 64 * half;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t w[8];
+          if (args.store_gu) {
+            pack16(v + 16 * j, w);
+            q_store(&maps.o0, w, x0 + 16 * j, y, lane, out_bufs, nstore);
+            pack16(v + 64 + 16 * j, w);
+            q_store(&maps.o1, w, x0 + 16 * j, y, lane, out_bufs, nstore);
+          }
+          float act[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) act[i] = q_silu(v[16 * j + i]) * v[64 + 16 * j + i];
+          pack16(act, w);
+          q_store(&maps.o2, w, x0 + 16 * j, y, lane, out_bufs, nstore);
+        }
+      } else {  // DOWN, DXE
+        const int32_t x0 = ti.nt * QN + 128 * half;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          if (args.store_gu) {
-            st_bf16x8(pg + 8 * j, v + 8 * j);
-            st_bf16x8(pu + 8 * j, v + 64 + 8 * j);
-          }
-          float act[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) act[i] = q_silu(v[8 * j + i]) * v[64 + 8 * j + i];
-          st_bf16x8(pa + 8 * j, act);
+          uint32_t w[8];
+          pack16(v + 16 * j, w);
+          q_store(&maps.o0, w, x0 + 16 * j, y, lane, out_bufs, nstore);
         }
-      } else {
-        __nv_bfloat16* py = static_cast<__nv_bfloat16*>(args.out0) + row * args.ld_out +
-                            ti.nt * QN + 128 * half;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) st_bf16x8(py + 8 * j, v + 8 * j);
       }
     }
+    if (lane == 0) bulk_wait_all();  // stores done before the CTA exits
   }
 
   tc_fence_before();
@@ -423,10 +592,23 @@ bool fp8_map(CUtensorMap* m, const void* base, int64_t k, int64_t rows, int box_
   return tma_map_2d(m, base, k, rows, box_rows, QK, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1);
 }
 
+// Output [rows, cols] for the epilogue's TMA stores: 32 rows x 32 bytes.
+bool out_map_bf16(CUtensorMap* m, const void* base, int64_t cols, int64_t rows) {
+  return tma_map_2d(m, base, cols, rows, 32, 16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+bool out_map_f32(CUtensorMap* m, const void* base, int64_t cols, int64_t rows) {
+  return tma_map_2d(m, base, cols, rows, 32, 8, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 QArgs q_base(const Layout& L, const void* ws) {
   QArgs a{};
   a.tiles = at<int32_t>(ws, L.tiles);
   a.n_tiles = at<int32_t>(ws, L.n_tiles);
+  a.pad_offsets = at<int32_t>(ws, L.pad_offsets);
+  a.order = at<int32_t>(ws, L.expert_order);
+  a.counts = at<int32_t>(ws, L.counts);
   a.err = const_cast<int32_t*>(at<int32_t>(ws, L.err));
   a.max_mtiles = static_cast<int>(L.R / QM);
   a.rows = L.R;
@@ -435,52 +617,164 @@ QArgs q_base(const Layout& L, const void* ws) {
   return a;
 }
 
+// A box of the token-row modes: the CTA's half (CTA pairs) or the whole tile.
+int a_box(int n_nt) { return n_nt % 2 == 0 ? QM / 2 : QM; }
+
+template <int MODE>
+moe_status q_launch_wgrad(const QMaps& maps, const QArgs& args, cudaStream_t s) {
+  const int64_t per = static_cast<int64_t>(args.n_probs) * args.E * args.w_mt;
+  if (args.w_nt % 2 == 0) return q_launch<MODE, 2>(maps, args, per * (args.w_nt / 2), s);
+  return q_launch<MODE, 1>(maps, args, per * args.w_nt, s);
+}
+
 }  // namespace
 
-moe_status gemm_mx_gate_up(const Layout& L, const void* ws, const uint8_t* xq, const uint8_t* xs,
+moe_status gemm_mx_gate_up(const Layout& L, const void* ws, moe_mxfp8_operand xe,
                            const moe_mxfp8_operand& wg, const moe_mxfp8_operand& wu, void* g,
                            void* u, void* act, cudaStream_t s) {
   const int n_nt = L.I / (QN / 2);
   QMaps m{};
-  if (!fp8_map(&m.a, xq, L.H, L.R, n_nt % 2 == 0 ? QM / 2 : QM) ||
+  if (!fp8_map(&m.a0, xe.q, L.H, L.R, a_box(n_nt)) ||
       !fp8_map(&m.b0, wg.q, L.H, static_cast<int64_t>(L.E) * L.I, QN / 2) ||
       !fp8_map(&m.b1, wu.q, L.H, static_cast<int64_t>(L.E) * L.I, QN / 2))
     return MOE_ERR_CUDA;
+  m.a1 = m.a0;
   QArgs a = q_base(L, ws);
   a.n_nt = n_nt;
-  a.nkb = L.H / QK;
+  a.kb1 = L.H / QK;
   a.b_rows = L.I;
-  a.sfa = xs;
+  a.sfa0 = a.sfa1 = xe.s;
   a.sfb0 = wg.s;
   a.sfb1 = wu.s;
   a.b_rblocks = static_cast<int64_t>(L.E) * L.I / 128;
   a.ld_out = L.I;
   a.store_gu = (g != nullptr && u != nullptr) ? 1 : 0;
-  a.out0 = g;
-  a.out1 = u;
-  a.out2 = act;
+  if (!out_map_bf16(&m.o2, act, L.I, L.R)) return MOE_ERR_CUDA;
+  if (a.store_gu && (!out_map_bf16(&m.o0, g, L.I, L.R) || !out_map_bf16(&m.o1, u, L.I, L.R)))
+    return MOE_ERR_CUDA;
   return q_launch_rows<Q_GATE_UP>(m, a, s);
 }
 
-moe_status gemm_mx_down(const Layout& L, const void* ws, const uint8_t* aq, const uint8_t* as,
+moe_status gemm_mx_down(const Layout& L, const void* ws, moe_mxfp8_operand act,
                         const moe_mxfp8_operand& wd, void* ye, cudaStream_t s) {
   const int n_nt = L.H / QN;
   QMaps m{};
-  if (!fp8_map(&m.a, aq, L.I, L.R, n_nt % 2 == 0 ? QM / 2 : QM) ||
+  if (!fp8_map(&m.a0, act.q, L.I, L.R, a_box(n_nt)) ||
       !fp8_map(&m.b0, wd.q, L.I, static_cast<int64_t>(L.E) * L.H, QN))
     return MOE_ERR_CUDA;
+  m.a1 = m.a0;
   m.b1 = m.b0;
   QArgs a = q_base(L, ws);
   a.n_nt = n_nt;
-  a.nkb = L.I / QK;
+  a.kb1 = L.I / QK;
   a.b_rows = L.H;
-  a.sfa = as;
-  a.sfb0 = wd.s;
-  a.sfb1 = wd.s;
+  a.sfa0 = a.sfa1 = act.s;
+  a.sfb0 = a.sfb1 = wd.s;
   a.b_rblocks = static_cast<int64_t>(L.E) * L.H / 128;
   a.ld_out = L.H;
-  a.out0 = ye;
+  if (!out_map_bf16(&m.o0, ye, L.H, L.R)) return MOE_ERR_CUDA;
   return q_launch_rows<Q_DOWN>(m, a, s);
+}
+
+moe_status gemm_mx_down_dgrad(const Layout& L, const void* ws, moe_mxfp8_operand dye,
+                              const moe_mxfp8_operand& wd_t, const void* g, const void* u,
+                              void* dg, void* du, cudaStream_t s) {
+  const int n_nt = L.I / QN;
+  QMaps m{};
+  if (!fp8_map(&m.a0, dye.q, L.H, L.R, a_box(n_nt)) ||
+      !fp8_map(&m.b0, wd_t.q, static_cast<int64_t>(L.E) * L.H, L.I, QN))
+    return MOE_ERR_CUDA;
+  m.a1 = m.a0;
+  m.b1 = m.b0;
+  QArgs a = q_base(L, ws);
+  a.n_nt = n_nt;
+  a.kb1 = L.H / QK;
+  a.k_exp = L.H;
+  a.sfa0 = a.sfa1 = dye.s;
+  a.sfb0 = a.sfb1 = wd_t.s;
+  a.b_rblocks = L.I / 128;
+  a.ld_out = L.I;
+  a.in0 = g;
+  a.in1 = u;
+  if (!out_map_bf16(&m.o0, dg, L.I, L.R) || !out_map_bf16(&m.o1, du, L.I, L.R))
+    return MOE_ERR_CUDA;
+  return q_launch_rows<Q_DACT>(m, a, s);
+}
+
+moe_status gemm_mx_gate_up_dgrad(const Layout& L, const void* ws, moe_mxfp8_operand dg,
+                                 moe_mxfp8_operand du, const moe_mxfp8_operand& wg_t,
+                                 const moe_mxfp8_operand& wu_t, void* dxe, cudaStream_t s) {
+  const int n_nt = L.H / QN;
+  QMaps m{};
+  if (!fp8_map(&m.a0, dg.q, L.I, L.R, a_box(n_nt)) ||
+      !fp8_map(&m.a1, du.q, L.I, L.R, a_box(n_nt)) ||
+      !fp8_map(&m.b0, wg_t.q, static_cast<int64_t>(L.E) * L.I, L.H, QN) ||
+      !fp8_map(&m.b1, wu_t.q, static_cast<int64_t>(L.E) * L.I, L.H, QN))
+    return MOE_ERR_CUDA;
+  QArgs a = q_base(L, ws);
+  a.n_nt = n_nt;
+  a.kb1 = L.I / QK;
+  a.kb2 = L.I / QK;
+  a.k_exp = L.I;
+  a.sfa0 = dg.s;
+  a.sfa1 = du.s;
+  a.sfb0 = wg_t.s;
+  a.sfb1 = wu_t.s;
+  a.b_rblocks = L.H / 128;
+  a.ld_out = L.H;
+  if (!out_map_bf16(&m.o0, dxe, L.H, L.R)) return MOE_ERR_CUDA;
+  return q_launch_rows<Q_DXE>(m, a, s);
+}
+
+moe_status gemm_mx_down_wgrad(const Layout& L, const void* ws, moe_mxfp8_operand dye_t,
+                              moe_mxfp8_operand act_t, float* dw_down, cudaStream_t s) {
+  const int w_nt = L.I / QN;
+  QMaps m{};
+  if (!fp8_map(&m.a0, dye_t.q, L.R, L.H, w_nt % 2 == 0 ? QM / 2 : QM) ||
+      !fp8_map(&m.b0, act_t.q, L.R, L.I, QN))
+    return MOE_ERR_CUDA;
+  m.a1 = m.a0;
+  m.b1 = m.b0;
+  QArgs a = q_base(L, ws);
+  if (launch_expert_order(L, ws, s) != MOE_OK) return MOE_ERR_CUDA;
+  a.w_mt = L.H / QM;
+  a.w_nt = w_nt;
+  a.n_probs = 1;
+  a.sfa0 = a.sfa1 = dye_t.s;
+  a.sfb0 = a.sfb1 = act_t.s;
+  a.a_rblocks = L.H / 128;
+  a.b_rblocks = L.I / 128;
+  a.ld_out = L.I;
+  if (!out_map_f32(&m.o0, dw_down, L.I, static_cast<int64_t>(L.E) * L.H)) return MOE_ERR_CUDA;
+  m.o1 = m.o0;
+  return q_launch_wgrad<Q_WGRAD>(m, a, s);
+}
+
+moe_status gemm_mx_gate_up_wgrad(const Layout& L, const void* ws, moe_mxfp8_operand dg_t,
+                                 moe_mxfp8_operand du_t, moe_mxfp8_operand xe_t, float* dw_gate,
+                                 float* dw_up, cudaStream_t s) {
+  const int w_nt = L.H / QN;
+  QMaps m{};
+  if (!fp8_map(&m.a0, dg_t.q, L.R, L.I, w_nt % 2 == 0 ? QM / 2 : QM) ||
+      !fp8_map(&m.a1, du_t.q, L.R, L.I, w_nt % 2 == 0 ? QM / 2 : QM) ||
+      !fp8_map(&m.b0, xe_t.q, L.R, L.H, QN))
+    return MOE_ERR_CUDA;
+  m.b1 = m.b0;
+  QArgs a = q_base(L, ws);
+  if (launch_expert_order(L, ws, s) != MOE_OK) return MOE_ERR_CUDA;
+  a.w_mt = L.I / QM;
+  a.w_nt = w_nt;
+  a.n_probs = 2;
+  a.sfa0 = dg_t.s;
+  a.sfa1 = du_t.s;
+  a.sfb0 = a.sfb1 = xe_t.s;
+  a.a_rblocks = L.I / 128;
+  a.b_rblocks = L.H / 128;
+  a.ld_out = L.H;
+  if (!out_map_f32(&m.o0, dw_gate, L.H, static_cast<int64_t>(L.E) * L.I) ||
+      !out_map_f32(&m.o1, dw_up, L.H, static_cast<int64_t>(L.E) * L.I))
+    return MOE_ERR_CUDA;
+  return q_launch_wgrad<Q_WGRAD>(m, a, s);
 }
 
 }  // namespace moe

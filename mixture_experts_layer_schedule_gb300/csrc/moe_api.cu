@@ -70,6 +70,14 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   L->ms_rh = mx ? take(static_cast<size_t>(R) * p->H / 32) : 0;
   L->mq_ri = mx ? take(static_cast<size_t>(R) * p->I) : 0;
   L->ms_ri = mx ? take(static_cast<size_t>(R) * p->I / 32) : 0;
+  L->mq_ri2 = mx ? take(static_cast<size_t>(R) * p->I) : 0;
+  L->ms_ri2 = mx ? take(static_cast<size_t>(R) * p->I / 32) : 0;
+  L->mq_th = mx ? take(static_cast<size_t>(R) * p->H) : 0;
+  L->ms_th = mx ? take(static_cast<size_t>(R) * p->H / 32) : 0;
+  L->mq_ti = mx ? take(static_cast<size_t>(R) * p->I) : 0;
+  L->ms_ti = mx ? take(static_cast<size_t>(R) * p->I / 32) : 0;
+  L->mq_ti2 = mx ? take(static_cast<size_t>(R) * p->I) : 0;
+  L->ms_ti2 = mx ? take(static_cast<size_t>(R) * p->I / 32) : 0;
   L->ws_bytes = o;
   o = 0;
   L->xe = take(static_cast<size_t>(R) * p->H * 2);
@@ -117,19 +125,64 @@ bool mx_forward_ok(const moe_weights* w) {
          operand_ok(w->mx->down);
 }
 
+// The backward MXFP8 tensor-core operands (transposed weights) are present.
+bool mx_backward_ok(const moe_weights* w) {
+  return mx_forward_ok(w) && operand_ok(w->mx->gate_t) && operand_ok(w->mx->up_t) &&
+         operand_ok(w->mx->down_t);
+}
+
+// A workspace MXFP8 operand buffer: codes at `q`, scale chunks at `s`.
+moe_mxfp8_operand ws_operand(void* ws, size_t q, size_t s) {
+  return moe_mxfp8_operand{at<uint8_t>(ws, q), at<uint8_t>(ws, s)};
+}
+
+// Quantise bf16 [rows, cols] into a workspace operand (transpose: along rows).
+moe_status quantize_into(const void* src, int64_t rows, int64_t cols, int transpose,
+                         moe_mxfp8_operand o, cudaStream_t s) {
+  return cu(launch_mxfp8_quantize_mma(src, rows, cols, transpose, const_cast<uint8_t*>(o.q),
+                                      const_cast<uint8_t*>(o.s), s));
+}
+
 // MXFP8 forward on the block-scaled tensor cores: Xe quantised along H feeds
 // gate/up, Act quantised along I feeds down. g/u may be NULL (inference).
 moe_status mx_forward_gemms(const Layout& L, void* ws, const moe_mxfp8_weights& mx,
                             const void* xe, void* g, void* u, void* act, void* ye,
                             cudaStream_t s) {
-  uint8_t* xq = at<uint8_t>(ws, L.mq_rh);
-  uint8_t* xs = at<uint8_t>(ws, L.ms_rh);
-  uint8_t* aq = at<uint8_t>(ws, L.mq_ri);
-  uint8_t* as = at<uint8_t>(ws, L.ms_ri);
-  MOE_TRY(cu(launch_mxfp8_quantize_mma(xe, L.R, L.H, 0, xq, xs, s)));
-  MOE_TRY(gemm_mx_gate_up(L, ws, xq, xs, mx.gate, mx.up, g, u, act, s));
-  MOE_TRY(cu(launch_mxfp8_quantize_mma(act, L.R, L.I, 0, aq, as, s)));
-  return gemm_mx_down(L, ws, aq, as, mx.down, ye, s);
+  const moe_mxfp8_operand xq = ws_operand(ws, L.mq_rh, L.ms_rh);
+  const moe_mxfp8_operand aq = ws_operand(ws, L.mq_ri, L.ms_ri);
+  MOE_TRY(quantize_into(xe, L.R, L.H, 0, xq, s));
+  MOE_TRY(gemm_mx_gate_up(L, ws, xq, mx.gate, mx.up, g, u, act, s));
+  MOE_TRY(quantize_into(act, L.R, L.I, 0, aq, s));
+  return gemm_mx_down(L, ws, aq, mx.down, ye, s);
+}
+
+// MXFP8 backward on the block-scaled tensor cores. Each GEMM operand is
+// quantised along that GEMM's K: dYe rows along H (data gradient of down),
+// dG/dU rows along I (data gradient of gate/up), and for the weight
+// gradients dYe, Act, dG, dU, Xe along the token axis (transposed, blocks of
+// 32 rows of one expert segment; segments start at multiples of T >= 128).
+moe_status mx_backward_gemms(const Layout& L, void* ws, const moe_mxfp8_weights& mx,
+                             const moe_saved_view& v, void* dyxe, void* dg, void* du,
+                             float* dw_gate, float* dw_up, float* dw_down, cudaStream_t s) {
+  const moe_mxfp8_operand rh = ws_operand(ws, L.mq_rh, L.ms_rh);
+  const moe_mxfp8_operand ri = ws_operand(ws, L.mq_ri, L.ms_ri);
+  const moe_mxfp8_operand ri2 = ws_operand(ws, L.mq_ri2, L.ms_ri2);
+  const moe_mxfp8_operand th = ws_operand(ws, L.mq_th, L.ms_th);
+  const moe_mxfp8_operand ti = ws_operand(ws, L.mq_ti, L.ms_ti);
+  const moe_mxfp8_operand ti2 = ws_operand(ws, L.mq_ti2, L.ms_ti2);
+  MOE_TRY(quantize_into(dyxe, L.R, L.H, 0, rh, s));
+  MOE_TRY(quantize_into(dyxe, L.R, L.H, 1, th, s));
+  MOE_TRY(quantize_into(v.act, L.R, L.I, 1, ti, s));
+  MOE_TRY(gemm_mx_down_dgrad(L, ws, rh, mx.down_t, v.g, v.u, dg, du, s));
+  MOE_TRY(gemm_mx_down_wgrad(L, ws, th, ti, dw_down, s));
+  MOE_TRY(quantize_into(dg, L.R, L.I, 0, ri, s));
+  MOE_TRY(quantize_into(du, L.R, L.I, 0, ri2, s));
+  // dXe overwrites dYe in the shared buffer: dYe's last readers ran above.
+  MOE_TRY(gemm_mx_gate_up_dgrad(L, ws, ri, ri2, mx.gate_t, mx.up_t, dyxe, s));
+  MOE_TRY(quantize_into(dg, L.R, L.I, 1, ti, s));
+  MOE_TRY(quantize_into(du, L.R, L.I, 1, ti2, s));
+  MOE_TRY(quantize_into(v.xe, L.R, L.H, 1, th, s));
+  return gemm_mx_gate_up_wgrad(L, ws, ti, ti2, th, dw_gate, dw_up, s);
 }
 
 }  // namespace
@@ -376,6 +429,15 @@ moe_status moe_backward(const moe_problem* p, const void* saved, const moe_weigh
   void* dyxe = at<char>(ws, L.dyxe);
   void* dg = at<char>(ws, L.dg);
   void* du = at<char>(ws, L.du);
+  if (p->dtype == MOE_MXFP8 && w && w->mx && w->mx->gate_t.q) {
+    if (!mx_backward_ok(w) || !aligned(dw_gate, 16) || !aligned(dw_up, 16) ||
+        !aligned(dw_down, 16))
+      return MOE_ERR_INVALID_ARG;
+    MOE_TRY(moe_reverse_combine(p, ws, dy, v.ye, topk_w, dyxe, d_topk_w, stream));
+    MOE_TRY(mx_backward_gemms(L, ws, *w->mx, v, dyxe, dg, du, dw_gate, dw_up, dw_down,
+                              S(stream)));
+    return moe_reverse_dispatch(p, ws, dyxe, dx, stream);
+  }
   if (p->dtype == MOE_MXFP8) {
     // Each GEMM operand quantised along that GEMM's K: rows of dYe along H,
     // rows of dG/dU along I; for the weight gradients both operands along the

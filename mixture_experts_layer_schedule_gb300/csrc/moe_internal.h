@@ -27,7 +27,9 @@ struct Layout {
   size_t err, counts, offsets, pad_offsets, slot_of, src_of_row, tiles, n_tiles, warp_counts,
       expert_order,
       mx_rh, mx_ri1, mx_ri2, mx_ch, mx_ci1, mx_ci2,  // MXFP8 quantised operands (bf16 values)
-      mq_rh, ms_rh, mq_ri, ms_ri,  // MXFP8 E4M3 codes + scale chunks of Xe and Act (tensor cores)
+      // MXFP8 E4M3 codes + scale chunks (tensor-core path): token rows [R, H] and
+      // [R, I] x2 quantised along K; transposed [H, R] and [I, R] x2 along tokens
+      mq_rh, ms_rh, mq_ri, ms_ri, mq_ri2, ms_ri2, mq_th, ms_th, mq_ti, ms_ti, mq_ti2, ms_ti2,
       dyxe, dg, du, ws_bytes;
   // forward-context byte offsets
   size_t xe, g, u, act, ye, saved_bytes;
@@ -83,13 +85,34 @@ moe_status gemm_gate_up_dgrad(const Layout& L, const void* ws, const void* dg, c
 moe_status gemm_gate_up_wgrad(const Layout& L, const void* ws, const void* dg, const void* du,
                               const void* xe, float* dw_gate, float* dw_up, cudaStream_t s);
 
+// Experts ranked by row count, descending (ties: ascending index), into the
+// workspace's expert_order (the weight-gradient tile order).
+moe_status launch_expert_order(const Layout& L, const void* ws, cudaStream_t s);
+
 // Block-scaled FP8 grouped GEMMs (tcgen05 kind::mxf8f6f4) of the MXFP8 layer.
-// xq/aq: E4M3 codes [R, H] / [R, I]; xs/as: their scale chunks.
-moe_status gemm_mx_gate_up(const Layout& L, const void* ws, const uint8_t* xq, const uint8_t* xs,
+// Every operand is an E4M3 K-major matrix with its scale chunks
+// (moe_mxfp8_operand): token rows [R, K] quantised along K, transposed
+// weights, or transposed activations [C, R] quantised along the token axis.
+moe_status gemm_mx_gate_up(const Layout& L, const void* ws, moe_mxfp8_operand xe,
                            const moe_mxfp8_operand& wg, const moe_mxfp8_operand& wu, void* g,
                            void* u, void* act, cudaStream_t s);
-moe_status gemm_mx_down(const Layout& L, const void* ws, const uint8_t* aq, const uint8_t* as,
+moe_status gemm_mx_down(const Layout& L, const void* ws, moe_mxfp8_operand act,
                         const moe_mxfp8_operand& wd, void* ye, cudaStream_t s);
+// dG, dU = SwiGLU backward of dYe . Wd[e] (B = Wd transposed, [I, E*H]).
+moe_status gemm_mx_down_dgrad(const Layout& L, const void* ws, moe_mxfp8_operand dye,
+                              const moe_mxfp8_operand& wd_t, const void* g, const void* u,
+                              void* dg, void* du, cudaStream_t s);
+// dXe = dG . Wg[e] + dU . Wu[e] (B = Wg, Wu transposed, [H, E*I]).
+moe_status gemm_mx_gate_up_dgrad(const Layout& L, const void* ws, moe_mxfp8_operand dg,
+                                 moe_mxfp8_operand du, const moe_mxfp8_operand& wg_t,
+                                 const moe_mxfp8_operand& wu_t, void* dxe, cudaStream_t s);
+// dWd[e] = dYe_e^T . Act_e from dYe^T [H, R] and Act^T [I, R] (token-axis blocks).
+moe_status gemm_mx_down_wgrad(const Layout& L, const void* ws, moe_mxfp8_operand dye_t,
+                              moe_mxfp8_operand act_t, float* dw_down, cudaStream_t s);
+// dWg[e] = dG_e^T . Xe_e, dWu[e] = dU_e^T . Xe_e from dG^T, dU^T [I, R], Xe^T [H, R].
+moe_status gemm_mx_gate_up_wgrad(const Layout& L, const void* ws, moe_mxfp8_operand dg_t,
+                                 moe_mxfp8_operand du_t, moe_mxfp8_operand xe_t, float* dw_gate,
+                                 float* dw_up, cudaStream_t s);
 
 // Launch accounting (every kernel launch of the library calls note_launch).
 void note_launch();

@@ -29,11 +29,12 @@ inline EncodeTiledFnT tma_encode_fn() {
 }
 
 // 2-D view [outer][inner] (inner contiguous) of `elem`-byte elements, box
-// box_inner x box_outer, 128-byte swizzle. false if the view or box is not
-// encodable (base 16-byte aligned, row pitch a multiple of 16 bytes, box row
-// at most 128 bytes).
+// box_inner x box_outer, 128-byte swizzle unless told otherwise. false if the
+// view or box is not encodable (base 16-byte aligned, row pitch a multiple of
+// 16 bytes, box row at most 128 bytes).
 inline bool tma_map_2d(CUtensorMap* m, const void* base, int64_t inner, int64_t outer,
-                       int box_outer, int box_inner, CUtensorMapDataType dtype, int elem) {
+                       int box_outer, int box_inner, CUtensorMapDataType dtype, int elem,
+                       CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFnT fn = tma_encode_fn();
   if (!fn || outer <= 0 || inner <= 0 || box_outer <= 0 || box_outer > 256) return false;
   if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (inner * elem) % 16 != 0) return false;
@@ -44,7 +45,7 @@ inline bool tma_map_2d(CUtensorMap* m, const void* base, int64_t inner, int64_t 
                              static_cast<cuuint32_t>(box_outer)};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

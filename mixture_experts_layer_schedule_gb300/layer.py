@@ -111,17 +111,23 @@ class MoELayer:
         return tuple(fwd), tuple(bwd)
 
     @staticmethod
-    def prepare_mxfp8_mma_weights(wg, wu, wd, stream=None) -> "MXFP8MMAWeights":
+    def prepare_mxfp8_mma_weights(wg, wu, wd, stream=None, backward=True) -> "MXFP8MMAWeights":
         """MXFP8 weights for the block-scaled tensor-core GEMMs: E4M3 codes and
-        E8M0 scale chunks of gate/up [E*I, H] and down [E*H, I] (forward)."""
+        E8M0 scale chunks of gate/up [E*I, H] and down [E*H, I] (forward) and,
+        with backward, of their transposes [H, E*I] and [I, E*H] quantised
+        along I and H (the K of the data-gradient GEMMs)."""
         E, I, H = wg.shape
         dev = wg.device
         ops = {}
-        for name, t, rows, cols in (("gate", wg, E * I, H), ("up", wu, E * I, H),
-                                    ("down", wd, E * H, I)):
-            q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+        todo = [("gate", wg, E * I, H, 0), ("up", wu, E * I, H, 0), ("down", wd, E * H, I, 0)]
+        if backward:
+            todo += [("gate_t", wg, E * I, H, 1), ("up_t", wu, E * I, H, 1),
+                     ("down_t", wd, E * H, I, 1)]
+        for name, t, rows, cols, tr in todo:
+            shape = (cols, rows) if tr else (rows, cols)
+            q = torch.empty(shape, dtype=torch.uint8, device=dev)
             sc = torch.empty((rows * cols // 32,), dtype=torch.uint8, device=dev)
-            _lib.mxfp8_quantize_mma(t, rows, cols, 0, q, sc, stream)
+            _lib.mxfp8_quantize_mma(t, rows, cols, tr, q, sc, stream)
             ops[name] = (q, sc)
         return MXFP8MMAWeights(ops)
 
@@ -139,10 +145,13 @@ class MoELayer:
                                    self.y, self.ws, stream)
         return self.y
 
-    def backward(self, dy, wg, wu, wd, topk_w=None, stream=None, bwd=None) -> Grads:
-        """bwd: the backward-direction weights (required for MXFP8)."""
+    def backward(self, dy, wg, wu, wd, topk_w=None, stream=None, bwd=None, mx=None) -> Grads:
+        """MXFP8: mx (MXFP8MMAWeights with the transposed copies) runs the GEMMs on
+        the FP8 tensor cores; otherwise bwd (the backward-direction bf16 MXFP8
+        values) feeds bf16 MMAs."""
         g = self.grads
-        w = _lib.weights(wg, wu, wd, *(bwd if bwd is not None else (None, None, None)))
+        w = _lib.weights(wg, wu, wd, *(bwd if bwd is not None else (None, None, None)),
+                         mx=mx.struct if mx is not None else None)
         _lib.moe_backward(self.p, self.saved, w, self.topk_w if topk_w is None else topk_w, dy,
                           g.dx, g.dw_gate, g.dw_up, g.dw_down, g.d_topk_w, self.ws, stream)
         return g
@@ -154,7 +163,7 @@ class MoELayer:
         self.build_schedule(None, stream)
         y = self.forward(x, wg, wu, wd, None, stream, mx=mx)
         if backward:
-            self.backward(dy, wg, wu, wd, None, stream, bwd=bwd)
+            self.backward(dy, wg, wu, wd, None, stream, bwd=bwd, mx=mx)
         return y
 
     def device_error(self, stream=None) -> int:
