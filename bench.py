@@ -41,7 +41,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default=None, help="workload name (default: skewed fwd+bwd)")
+    ap.add_argument("--config", default=None,
+                    help="workload name (default: skewed fwd+bwd) or N,H,I,E,k[,zipf][,T=..][,mxfp8]")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=0,
@@ -182,13 +183,17 @@ def workload(name):
     if name in inputs.ALL:
         return inputs.ALL[name]
     f = name.split(",")
+    dtype = "bf16"
+    if f[-1] == "mxfp8":
+        dtype = f.pop()
     T = 128
     if f[-1].startswith("T="):
         T = int(f.pop()[2:])
     N, H, I, E, k = (int(v) for v in f[:5])
     z = float(f[5]) if len(f) > 5 and float(f[5]) > 0 else None
     return inputs.LayerShape(f"custom_N{N}_H{H}_I{I}_E{E}_k{k}" + (f"_zipf{z}" if z else "")
-                             + f"_T{T}", N, H, I, E, k, zipf_s=z, minibatch_rows=T)
+                             + f"_T{T}" + ("_mxfp8" if dtype == "mxfp8" else ""), N, H, I, E, k,
+                             zipf_s=z, minibatch_rows=T, dtype=dtype)
 
 
 def run_ours(args, ws_, rank, local):

@@ -184,33 +184,36 @@ __global__ void __launch_bounds__(256) quant_mma_rows_kernel(const uint4* __rest
 }
 
 // Transposed form: q [cols, rows] = src^T, blocks of 32 consecutive source
-// rows of a column (the K of the transposed operand). One thread per (32-row
-// block, column pair): a warp reads 128 contiguous bytes of each source row.
-__global__ void __launch_bounds__(256) quant_mma_cols_kernel(const uint32_t* __restrict__ src,
-                                                             int64_t rows, int64_t cols2,
-                                                             uint8_t* __restrict__ q,
-                                                             uint8_t* __restrict__ sf) {
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= (rows / 32) * cols2) return;
-  const int64_t rb = idx / cols2, c2 = idx % cols2;
-  float lo[32], hi[32];
-#pragma unroll
-  for (int r = 0; r < 32; ++r) {
-    const uint32_t v = src[(rb * 32 + r) * cols2 + c2];
-    lo[r] = bf16lo(v);
-    hi[r] = bf16hi(v);
+// rows of a column (the K of the transposed operand). A CTA stages a
+// 128-row x 64-column tile in shared memory (coalesced 128-byte row reads);
+// thread (column c, block b) then quantises rows 32b..32b+31 of column c and
+// writes its 32 codes as one contiguous piece of output row c.
+constexpr int kQtRows = 128, kQtCols = 64;
+
+__global__ void __launch_bounds__(256) quant_mma_t_kernel(const uint16_t* __restrict__ src,
+                                                          int64_t rows, int64_t cols,
+                                                          uint8_t* __restrict__ q,
+                                                          uint8_t* __restrict__ sf) {
+  __shared__ __align__(16) uint16_t tile[kQtRows][kQtCols];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kQtRows;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.y) * kQtCols;
+  for (int i = threadIdx.x; i < kQtRows * kQtCols / 8; i += blockDim.x) {
+    const int r = i / (kQtCols / 8), cv = i % (kQtCols / 8);
+    *reinterpret_cast<uint4*>(&tile[r][cv * 8]) =
+        *reinterpret_cast<const uint4*>(src + (r0 + r) * cols + c0 + cv * 8);
   }
-  const int64_t cols = cols2 * 2;
+  __syncthreads();
+  const int c = threadIdx.x % kQtCols, b = threadIdx.x / kQtCols;
+  float f[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) f[r] = __uint_as_float(static_cast<uint32_t>(tile[32 * b + r][c]) << 16);
   uint32_t packed[8];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint8_t code = quant32(h ? hi : lo, packed);
-    const int64_t orow = 2 * c2 + h;  // row of the transposed operand
-    uint4* dst = reinterpret_cast<uint4*>(q + orow * rows + rb * 32);
-    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-    sf[sf_mma_index(orow, rb, cols)] = code;
-  }
+  const uint8_t code = quant32(f, packed);
+  const int64_t orow = c0 + c;  // row of the transposed operand
+  uint4* dst = reinterpret_cast<uint4*>(q + orow * rows + r0 + 32 * b);
+  dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  sf[sf_mma_index(orow, (r0 >> 5) + b, cols)] = code;
 }
 
 }  // namespace
@@ -223,9 +226,8 @@ cudaError_t launch_mxfp8_quantize_mma(const void* src, int64_t rows, int64_t col
     quant_mma_rows_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
         static_cast<const uint4*>(src), rows, cols, reinterpret_cast<uint4*>(q), sf);
   } else {
-    const int64_t n = (rows / 32) * (cols / 2);
-    quant_mma_cols_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
-        static_cast<const uint32_t*>(src), rows, cols / 2, q, sf);
+    const dim3 grid(static_cast<unsigned>(rows / kQtRows), static_cast<unsigned>(cols / kQtCols));
+    quant_mma_t_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(src), rows, cols, q, sf);
   }
   note_launch();
   return cudaGetLastError();
