@@ -329,6 +329,48 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ---- MXFP8 (OCP MX v1.0, E4M3 elements, E8M0 block scales) ------------------
+
+// Two fp32 values to two E4M3 codes (round to nearest even, saturating to
+// +-448): lo in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  // first source goes to the upper byte, second to the lower byte
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Quantiser for the block-scaled tensor-core GEMMs: E4M3 codes of a K-major
+// operand [rows, K] and its E8M0 scales in the layout tcgen05.cp (32x128b,
+// warpx4) moves into tensor memory: 512-byte chunks, one per (128 K, 128 rows),
+// chunk (kc, rb) at ((kc * rows/128) + rb) * 512, and inside a chunk the scale
+// of (row r, 32-wide K block j) at byte (r % 32) * 16 + ((r / 32) % 4) * 4 + j % 4.
+__device__ __forceinline__ size_t sf_mma_index(int64_t r, int64_t kb32, int64_t rows) {
+  return static_cast<size_t>(((kb32 >> 2) * (rows >> 7) + (r >> 7)) * 512 + (r & 31) * 16 +
+                             ((r >> 5) & 3) * 4 + (kb32 & 3));
+}
+
+// E4M3 codes of one block of 32 values, packed four to a word in order, and
+// the block's E8M0 scale code (returned): code = biased exponent of amax - 8,
+// i.e. scale 2^(floor(log2 amax) - 8), clamped at 0 (0 for an all-zero or
+// subnormal-amax block); each value is divided by the scale (an exact power
+// of two) and rounded to nearest even E4M3, saturating to +-448.
+__device__ __forceinline__ uint8_t quant32(const float (&f)[32], uint32_t (&packed)[8]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  const int biased = (__float_as_uint(amax) >> 23) & 0xFF;
+  const int code = biased == 0 ? 0 : max(0, biased - 8);
+  const float inv = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t lo = e4m3x2(f[4 * i + 0] * inv, f[4 * i + 1] * inv);
+    const uint32_t hi = e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
+    packed[i] = lo | (hi << 16);
+  }
+  return static_cast<uint8_t>(code);
+}
+
 // ---- tile order of the weight-gradient GEMMs --------------------------------
 
 // Order in which one CTA (pair) visits the size-ordered WGRAD tiles: it

@@ -20,13 +20,6 @@
 namespace moe {
 namespace {
 
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  // first source goes to the upper byte, second to the lower byte
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const uint4* __restrict__ src,
                                                              int64_t n_blocks,
                                                              uint4* __restrict__ q,
@@ -44,22 +37,8 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const uint4* __rest
     f[8 * i + 4] = bf16lo(raw[i].z); f[8 * i + 5] = bf16hi(raw[i].z);
     f[8 * i + 6] = bf16lo(raw[i].w); f[8 * i + 7] = bf16hi(raw[i].w);
   }
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
-  // floor(log2(amax)) = biased exponent - 127 for normal amax; zero and
-  // subnormal amax give code 0 after the clamp.
-  const int biased = (__float_as_uint(amax) >> 23) & 0xFF;
-  const int code = biased == 0 ? 0 : max(0, biased - 8);  // (biased-127) - 8 + 127
-  scale[b] = static_cast<uint8_t>(code);
-  const float inv = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);  // 2^(127-code)
   uint32_t packed[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t lo = e4m3x2(f[4 * i + 0] * inv, f[4 * i + 1] * inv);
-    const uint32_t hi = e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
-    packed[i] = lo | (hi << 16);
-  }
+  scale[b] = quant32(f, packed);
   q[b * 2 + 0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
   q[b * 2 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
 }
@@ -129,34 +108,6 @@ __global__ void __launch_bounds__(256) qdq_cols_kernel(const uint32_t* __restric
   qdq32(hi);
 #pragma unroll
   for (int r = 0; r < 32; ++r) dst[(rb * 32 + r) * cols2 + c] = pack_bf16x2(lo[r], hi[r]);
-}
-
-// Quantiser for the block-scaled tensor-core GEMMs: E4M3 codes of a K-major
-// operand [rows, K] and its E8M0 scales in the layout tcgen05.cp (32x128b,
-// warpx4) moves into tensor memory: 512-byte chunks, one per (128 K, 128 rows),
-// chunk (kc, rb) at ((kc * rows/128) + rb) * 512, and inside a chunk the scale
-// of (row r, 32-wide K block j) at byte (r % 32) * 16 + ((r / 32) % 4) * 4 + j % 4.
-__device__ __forceinline__ size_t sf_mma_index(int64_t r, int64_t kb32, int64_t rows) {
-  return static_cast<size_t>(((kb32 >> 2) * (rows >> 7) + (r >> 7)) * 512 + (r & 31) * 16 +
-                             ((r >> 5) & 3) * 4 + (kb32 & 3));
-}
-
-// Codes of one block of 32 values (rule of mxfp8_quantize_kernel); returns the
-// scale code.
-__device__ __forceinline__ uint8_t quant32(const float (&f)[32], uint32_t (&packed)[8]) {
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
-  const int biased = (__float_as_uint(amax) >> 23) & 0xFF;
-  const int code = biased == 0 ? 0 : max(0, biased - 8);
-  const float inv = __uint_as_float(static_cast<uint32_t>(254 - code) << 23);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t lo = e4m3x2(f[4 * i + 0] * inv, f[4 * i + 1] * inv);
-    const uint32_t hi = e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv);
-    packed[i] = lo | (hi << 16);
-  }
-  return static_cast<uint8_t>(code);
 }
 
 // Row form: blocks of 32 consecutive values of a row; q [rows, cols].
