@@ -77,6 +77,9 @@ def lib():
             L.orc_layer_mxfp8_prepared.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp,
                                                    vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp,
                                                    vp, vp, vp, ctypes.c_int]
+            L.orc_router_logits.argtypes = [i64, i32, i32, vp, vp, vp, ctypes.c_int]
+            L.orc_router_backward.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              ctypes.c_int]
             L.orc_e4m3_encode.argtypes = [ctypes.c_double]
             L.orc_e4m3_encode.restype = ctypes.c_uint8
             L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
@@ -120,6 +123,31 @@ def route_topk(logits, bias, k):
     w = np.empty((N, k), np.float64)
     _check(lib().orc_route_topk(N, E, k, _p(logits), _p(b), _p(ids), _p(w)))
     return ids, w
+
+
+def router_logits(x, wr, threads=0):
+    """logits = x . Wr^T in fp64 (x bf16 [N, H], Wr bf16 [E, H])."""
+    x, wr = as_bf16_bits(x), as_bf16_bits(wr)
+    N, H = x.shape
+    E = wr.shape[0]
+    out = np.empty((N, E))
+    _check(lib().orc_router_logits(N, H, E, _p(x), _p(wr), _p(out), threads))
+    return out
+
+
+def router_backward(x, wr, ids, w, dw, threads=0):
+    """dz [N, k], dWr [E, H], router share of dx [N, H] (fp64; routing held fixed)."""
+    x, wr = as_bf16_bits(x), as_bf16_bits(wr)
+    ids, w, dw = _c(ids, np.int32), _c(w, np.float64), _c(dw, np.float64)
+    N, H = x.shape
+    E = wr.shape[0]
+    k = ids.shape[1]
+    dz = np.empty((N, k))
+    dwr = np.empty((E, H))
+    dx = np.empty((N, H))
+    _check(lib().orc_router_backward(N, H, E, k, _p(x), _p(wr), _p(ids), _p(w), _p(dw), _p(dz),
+                                     _p(dwr), _p(dx), threads))
+    return dict(dz=dz, dwr=dwr, dx=dx)
 
 
 def build_schedule(ids, E, tile_m=128, pad_m=None):

@@ -285,6 +285,51 @@ int orc_route_topk(int64_t N, int32_t E, int32_t k, const float* logits,
   return ORC_OK;
 }
 
+int orc_router_logits(int64_t N, int32_t H, int32_t E, const uint16_t* x, const uint16_t* wr,
+                      double* logits, int threads) {
+  if (N < 0 || H <= 0 || E <= 0) return ORC_ERR_ARG;
+  // logits[t][e] = sum_h x[t][h] * Wr[e][h], every product and sum in fp64
+  parallel_for(N, threads, [&](int64_t t) {
+    for (int32_t e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int32_t h = 0; h < H; ++h)
+        acc += bf16_to_double(x[t * H + h]) * bf16_to_double(wr[static_cast<int64_t>(e) * H + h]);
+      logits[t * E + e] = acc;
+    }
+  });
+  return ORC_OK;
+}
+
+int orc_router_backward(int64_t N, int32_t H, int32_t E, int32_t k, const uint16_t* x,
+                        const uint16_t* wr, const int32_t* ids, const double* w,
+                        const double* dw, double* dz, double* dwr, double* dx, int threads) {
+  if (N < 0 || H <= 0 || E <= 0 || k <= 0 || k > E) return ORC_ERR_ARG;
+  for (int64_t a = 0; a < N * k; ++a)
+    if (ids[a] < 0 || ids[a] >= E) return ORC_ERR_ARG;
+  // w = softmax over the k selected logits z_j: dL/dz_j = w_j (dL/dw_j - sum_i w_i dL/dw_i)
+  for (int64_t t = 0; t < N; ++t) {
+    double s = 0.0;
+    for (int32_t j = 0; j < k; ++j) s += w[t * k + j] * dw[t * k + j];
+    for (int32_t j = 0; j < k; ++j) dz[t * k + j] = w[t * k + j] * (dw[t * k + j] - s);
+  }
+  // logits = x Wr^T: dWr[e] = sum over (t, j) routed to e of dz[t,j] x[t]; dx[t] = sum_j dz[t,j] Wr[ids[t,j]]
+  parallel_for(E, threads, [&](int64_t e) {
+    for (int32_t h = 0; h < H; ++h) dwr[e * H + h] = 0.0;
+    for (int64_t a = 0; a < N * k; ++a)
+      if (ids[a] == e)
+        for (int32_t h = 0; h < H; ++h) dwr[e * H + h] += dz[a] * bf16_to_double(x[(a / k) * H + h]);
+  });
+  parallel_for(N, threads, [&](int64_t t) {
+    for (int32_t h = 0; h < H; ++h) {
+      double acc = 0.0;
+      for (int32_t j = 0; j < k; ++j)
+        acc += dz[t * k + j] * bf16_to_double(wr[static_cast<int64_t>(ids[t * k + j]) * H + h]);
+      dx[t * H + h] = acc;
+    }
+  });
+  return ORC_OK;
+}
+
 int orc_build_schedule(int64_t N, int32_t k, int32_t E, int32_t tile_m,
                        const int32_t* ids, int32_t* counts, int32_t* offsets,
                        int32_t* pad_offsets, int32_t* slot_of,

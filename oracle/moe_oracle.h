@@ -125,6 +125,23 @@ int orc_expert_wgrad_bf16(int64_t N, int32_t H, int32_t I, int32_t E,
                           const int32_t* h_list, double* dwg_rows,
                           double* dwu_rows, double* dwd_rows, int threads);
 
+/* Router (the GEMM in front of the routing): logits[t][e] = x[t] . Wr[e]
+ * over H, x bf16 [N][H], Wr bf16 [E][H], in fp64. */
+int orc_router_logits(int64_t N, int32_t H, int32_t E, const uint16_t* x, const uint16_t* wr,
+                      double* logits, int threads);
+
+/* Router backward with the top-k selection held fixed (it is piecewise
+ * constant): the routing weights are the softmax over the k selected logits,
+ * so with dw = dL/d(routing weights) [N][k]:
+ *   dz[t][j] = w[t][j] * (dw[t][j] - sum_i w[t][i] * dw[t][i])   (dL/d logit of
+ *              the j-th selected expert; the other logits get 0),
+ *   dwr[e][h] = sum over (t, j) with ids[t][j] = e of dz[t][j] * x[t][h],
+ *   dx[t][h]  = sum_j dz[t][j] * Wr[ids[t][j]][h]   (the router's share of dL/dx).
+ * All fp64; dz [N][k], dwr [E][H], dx [N][H] are outputs. */
+int orc_router_backward(int64_t N, int32_t H, int32_t E, int32_t k, const uint16_t* x,
+                        const uint16_t* wr, const int32_t* ids, const double* w,
+                        const double* dw, double* dz, double* dwr, double* dx, int threads);
+
 /* MXFP8 layer (the MXFP8 workload): the layer forward + backward with every
  * operand of every GEMM quantised to MXFP8 along that GEMM's K and
  * dequantised exactly (rule of orc_mxfp8_quantize):
