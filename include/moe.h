@@ -288,6 +288,32 @@ moe_status moe_backward(const moe_problem* p, const void* saved, const moe_weigh
                         const float* topk_w, const void* dy, void* dx, float* dw_gate,
                         float* dw_up, float* dw_down, float* d_topk_w, void* ws, void* stream);
 
+/* Router ([Clip] key flowchart, Router node: the router picks the top-k
+ * experts of each token from its logits). logits = x . w_router^T with x bf16
+ * [N, H], w_router bf16 [E][H] (K contiguous), fp32 accumulation on the
+ * tensor cores, then the top-k and weights of moe_route_topk on
+ * fl32(logit + bias). logits (fp32 [N, E], 16-byte aligned) receives the
+ * logits if non-NULL (else the workspace holds them). E <= 256 and
+ * E % 4 == 0, else MOE_ERR_UNSUPPORTED. Not in the layer's timed path: the
+ * layer's routing input is top-k ids ([MoK] use the functional API). */
+moe_status moe_route(const moe_problem* p, const void* x, const void* w_router, const float* bias,
+                     float* logits, int32_t* topk_ids, float* topk_w, void* ws, void* stream);
+
+/* Router backward, the selection held fixed (top-k is piecewise constant).
+ * With w = topk_w (the softmax over the k selected logits) and
+ * dw = d_topk_w (from moe_backward):
+ *   dz[t,j] = w[t,j] * (dw[t,j] - sum_i w[t,i] * dw[t,i])   (dL/d logit),
+ *   dx[t]  += sum_j dz[t,j] * w_router[topk_ids[t,j]]       (bf16 in place: fp32
+ *             sum in j order onto the current value, one rounding),
+ *   dw_router[e] = sum over the tokens routed to e of dz * x (fp32 [E][H],
+ *             written whole; fixed order: 128-row tiles of the expert-grouped
+ *             Xe in `saved`, then the tiles of each expert in order).
+ * Uses the schedule in `ws` and Xe in `saved` from this batch's moe_forward. */
+moe_status moe_router_backward(const moe_problem* p, const void* saved, const void* w_router,
+                               const int32_t* topk_ids, const float* topk_w,
+                               const float* d_topk_w, void* dx, float* dw_router, void* ws,
+                               void* stream);
+
 /* [MoK] core concepts, MXFP8 row: quantise bf16 [rows, cols] (cols % 32 == 0)
  * to MXFP8 along each row: per 1x32 block, E8M0 scale code =
  * clamp(floor(log2(amax)) - 8 + 127, 0, 254) (0 for an all-zero block), and

@@ -72,6 +72,8 @@ _SIGS = {
     "moe_schedule_view": ([c_vp, c_vp, c_vp], c_i32),
     "moe_route_topk": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp], c_i32),
     "moe_build_schedule": ([c_vp, c_vp, c_vp, c_vp], c_i32),
+    "moe_route": ([c_vp] * 9, c_i32),
+    "moe_router_backward": ([c_vp] * 10, c_i32),
     "moe_build_schedule_noalloc": ([c_vp, c_vp, c_vp, c_vp, c_vp], c_i32),
     "moe_dispatch": ([c_vp, c_vp, c_vp, c_vp, c_vp], c_i32),
     "moe_expert_gate_up": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp], c_i32),
@@ -282,6 +284,17 @@ def moe_backward(p, saved, w: Weights, topk_w, dy, dx, dw_gate, dw_up, dw_down, 
     _call("moe_backward", ctypes.byref(p), _ptr(saved), ctypes.byref(w), _ptr(topk_w), _ptr(dy),
           _ptr(dx), _ptr(dw_gate), _ptr(dw_up), _ptr(dw_down), _ptr(d_topk_w), _ptr(ws),
           _stream(stream))
+
+
+def moe_route(p, x, w_router, bias, logits, topk_ids, topk_w, ws, stream=None):
+    _call("moe_route", ctypes.byref(p), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(logits),
+          _ptr(topk_ids), _ptr(topk_w), _ptr(ws), _stream(stream))
+
+
+def moe_router_backward(p, saved, w_router, topk_ids, topk_w, d_topk_w, dx, dw_router, ws,
+                        stream=None):
+    _call("moe_router_backward", ctypes.byref(p), _ptr(saved), _ptr(w_router), _ptr(topk_ids),
+          _ptr(topk_w), _ptr(d_topk_w), _ptr(dx), _ptr(dw_router), _ptr(ws), _stream(stream))
 
 
 def mxfp8_quantize(src, rows, cols, q, scale, stream=None):

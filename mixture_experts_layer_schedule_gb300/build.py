@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
 SOURCES = ["route_schedule.cu", "dispatch_combine.cu", "grouped_gemm.cu", "grouped_gemm_mx.cu",
-           "mxfp8.cu", "moe_api.cu"]
+           "mxfp8.cu", "router.cu", "moe_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -53,7 +53,9 @@ constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
 // GATE_UP_GATHER: GATE_UP with the dispatch fused into the producer -- the A
 // rows are gathered from the token-ordered x by TMA (tile::gather4), so the
 // expert-grouped Xe never exists in HBM; G and U may be skipped (inference).
-enum Mode { GATE_UP = 0, DOWN = 1, DACT = 2, DXE = 3, WGRAD = 4, GATE_UP_GATHER = 5 };
+// ROUTER: the dense router GEMM in front of the routing, logits = x . Wr^T
+// (M tiles over the N tokens, one N tile of up to 256 experts, fp32 out).
+enum Mode { GATE_UP = 0, DOWN = 1, DACT = 2, DXE = 3, WGRAD = 4, GATE_UP_GATHER = 5, ROUTER = 6 };
 
 struct Maps {
   CUtensorMap a0, a1, b0, b1;
@@ -105,7 +107,16 @@ struct TileInfo {
 template <int MODE, int CL>
 __device__ __forceinline__ TileInfo decode_tile(const Args& a, int64_t t, int crank) {
   TileInfo ti;
-  if constexpr (MODE == WGRAD) {
+  if constexpr (MODE == ROUTER) {
+    ti.mt = static_cast<int>(t);
+    ti.nt = 0;
+    ti.row0 = static_cast<int>(t) * BM;  // rows past N are zero-filled loads, clipped stores
+    ti.e = 0;
+    ti.prob = 0;
+    ti.kstart = 0;
+    ti.nkb = a.kb1;
+    ti.skip = false;
+  } else if constexpr (MODE == WGRAD) {
     // Largest experts first, so the CTAs that stream one expert's long K
     // panels start together and share them through L2; within an expert,
     // (mt, nt, problem) with the problem fastest, so dWg and dWu tiles that
@@ -154,7 +165,9 @@ __device__ __forceinline__ TileInfo decode_tile(const Args& a, int64_t t, int cr
 
 template <int MODE, int CL>
 __device__ __forceinline__ int64_t total_tiles(const Args& a) {
-  if constexpr (MODE == WGRAD) {
+  if constexpr (MODE == ROUTER) {
+    return a.max_mtiles;
+  } else if constexpr (MODE == WGRAD) {
     return static_cast<int64_t>(a.n_probs) * a.E * (a.w_mt / CL) * a.w_nt;
   } else {
     int n = *a.n_tiles;
@@ -181,6 +194,9 @@ __device__ __forceinline__ void issue_loads(const Maps& m, const Args& a, const 
                                             int crank) {
   if constexpr (MODE == GATE_UP_GATHER) {
     // loaded by the whole producer warp (see the kernel)
+  } else if constexpr (MODE == ROUTER) {
+    tma_load_2d(sA, &m.a0, bar, kb * BK, ti.row0);
+    tma_load_2d(sB, &m.b0, bar, kb * BK, 0);  // all E router rows; rows past E read as zeros
   } else if constexpr (MODE == GATE_UP) {
     load_a_rows<CL>(sA, &m.a0, bar, kb * BK, ti.row0, crank);
     const int brow = ti.e * a.b_rows + ti.nt * (BN / 2);
@@ -338,17 +354,16 @@ __device__ __forceinline__ void epilogue(const Maps& m, const Args& a, const Til
   }
 }
 
-// WGRAD epilogue: fp32 dW[e] rows. Each warp moves its 32 rows x 256 columns
-// in eight 32x32 blocks: TMEM -> registers -> shared staging buffer (the
-// 128-byte swizzle spreads one warp store over all banks) -> one TMA store.
+// fp32 epilogue (WGRAD: dW[e] rows; ROUTER: logits): each warp moves its 32
+// rows x the first `ncols` (a multiple of 32) of the 256 columns in 32x32
+// blocks: TMEM -> registers -> shared staging buffer (the 128-byte swizzle
+// spreads one warp store over all banks) -> one TMA store at (x0 + c, y).
 // Two staging buffers per warp let the store of block i overlap block i+1.
-__device__ __forceinline__ void epilogue_wgrad(const Maps& m, const Args& a, const TileInfo& ti,
-                                               uint32_t tmem_acc, int quad, int lane,
-                                               uint8_t* stage_out, uint32_t& nstore) {
+__device__ __forceinline__ void epilogue_f32(const CUtensorMap* om, const TileInfo& ti, int32_t x0,
+                                             int32_t y, int ncols, uint32_t tmem_acc, int quad,
+                                             int lane, uint8_t* stage_out, uint32_t& nstore) {
   const uint32_t taddr = tmem_acc + (static_cast<uint32_t>(quad * 32) << 16);
-  const CUtensorMap* om = ti.prob ? &m.o1 : &m.o0;
-  const int32_t y = ti.e * (a.w_mt * BM) + ti.mt * BM + quad * 32;
-  for (int c = 0; c < BN; c += 32) {
+  for (int c = 0; c < ncols; c += 32) {
     uint32_t d[32];
     if (ti.nkb > 0) {
       tmem_ld32(taddr + c, d);
@@ -371,11 +386,27 @@ __device__ __forceinline__ void epilogue_wgrad(const Maps& m, const Args& a, con
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(om, buf, ti.nt * BN + c, y);
+      tma_store_2d(om, buf, x0 + c, y);
       bulk_commit();
     }
     ++nstore;
   }
+}
+
+__device__ __forceinline__ void epilogue_wgrad(const Maps& m, const Args& a, const TileInfo& ti,
+                                               uint32_t tmem_acc, int quad, int lane,
+                                               uint8_t* stage_out, uint32_t& nstore) {
+  epilogue_f32(ti.prob ? &m.o1 : &m.o0, ti, ti.nt * BN, ti.e * (a.w_mt * BM) + ti.mt * BM + quad * 32,
+               BN, tmem_acc, quad, lane, stage_out, nstore);
+}
+
+// Router logits: row block row0 + quad*32, the first E columns (ld_out = E;
+// stores clip the rows past N and the columns past E).
+__device__ __forceinline__ void epilogue_router(const Maps& m, const Args& a, const TileInfo& ti,
+                                                uint32_t tmem_acc, int quad, int lane,
+                                                uint8_t* stage_out, uint32_t& nstore) {
+  epilogue_f32(&m.o0, ti, 0, ti.row0 + quad * 32, (a.ld_out + 31) / 32 * 32, tmem_acc, quad, lane,
+               stage_out, nstore);
 }
 
 template <int MODE, int CL>
@@ -550,6 +581,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) set_dev_error(args.err, MOE_DEVERR_BAD_EXPERT);
       } else if constexpr (MODE == WGRAD) {
         epilogue_wgrad(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
+      } else if constexpr (MODE == ROUTER) {
+        epilogue_router(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
       } else {
         epilogue<MODE>(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
       }
@@ -1008,6 +1041,26 @@ moe_status launch_expert_order(const Layout& L, const void* ws, cudaStream_t s) 
                                          const_cast<int32_t*>(at<int32_t>(ws, L.expert_order)));
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status gemm_router(const Layout& L, const void* ws, const void* x, const void* w_router,
+                       float* logits, cudaStream_t s) {
+  if (L.N == 0) return MOE_OK;
+  Maps m{};
+  if (!make_map(&m.a0, x, L.H, L.N, BM) || !make_map(&m.b0, w_router, L.H, L.E, BN) ||
+      !make_out_map(&m.o0, logits, L.E, L.N))
+    return MOE_ERR_CUDA;
+  m.a1 = m.a0;
+  m.b1 = m.b0;
+  m.o1 = m.o0;
+  Args a = base_args(L, ws);
+  a.max_mtiles = static_cast<int>((L.N + BM - 1) / BM);
+  a.rows = L.N;
+  a.n_nt = 1;
+  a.kb1 = L.H / BK;
+  a.kb2 = 0;
+  a.ld_out = L.E;
+  return launch<ROUTER, 1>(m, a, a.max_mtiles, s);
 }
 
 moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const void* wg,

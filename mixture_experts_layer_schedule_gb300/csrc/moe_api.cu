@@ -56,6 +56,9 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   L->n_tiles = take(sizeof(int32_t));
   L->warp_counts = take(sizeof(int32_t) * p->E * std::max<int64_t>(L->n_warps, 1));
   L->expert_order = take(sizeof(int32_t) * p->E);
+  L->router_logits = take(sizeof(float) * std::max<int64_t>(p->N, 1) * p->E);
+  L->router_dz = take(sizeof(float) * std::max<int64_t>(A, 1));
+  L->router_partial = take(sizeof(float) * static_cast<size_t>(R / kTileM) * p->H);
   L->dyxe = take(static_cast<size_t>(R) * p->H * 2);
   L->dg = take(static_cast<size_t>(R) * p->I * 2);
   L->du = take(static_cast<size_t>(R) * p->I * 2);
@@ -244,6 +247,36 @@ moe_status moe_route_topk(const moe_problem* p, const float* logits, const float
     return MOE_ERR_INVALID_ARG;
   if (bias && !aligned(bias, 4)) return MOE_ERR_INVALID_ARG;
   return cu(launch_route_topk(L, logits, bias, topk_ids, topk_w, at<int32_t>(ws, L.err), S(stream)));
+}
+
+moe_status moe_route(const moe_problem* p, const void* x, const void* w_router, const float* bias,
+                     float* logits, int32_t* topk_ids, float* topk_w, void* ws, void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (L.E > 256 || L.E % 4 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!aligned(w_router, 16) || (logits && !aligned(logits, 16)) || (bias && !aligned(bias, 4)))
+    return MOE_ERR_INVALID_ARG;
+  if (L.N > 0 && (!aligned(x, 16) || !aligned(topk_ids, 4) || !aligned(topk_w, 4)))
+    return MOE_ERR_INVALID_ARG;
+  float* lg = logits ? logits : at<float>(ws, L.router_logits);
+  MOE_TRY(gemm_router(L, ws, x, w_router, lg, S(stream)));
+  return cu(launch_route_topk(L, lg, bias, topk_ids, topk_w, at<int32_t>(ws, L.err), S(stream)));
+}
+
+moe_status moe_router_backward(const moe_problem* p, const void* saved, const void* w_router,
+                               const int32_t* topk_ids, const float* topk_w,
+                               const float* d_topk_w, void* dx, float* dw_router, void* ws,
+                               void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  moe_saved_view v;
+  MOE_TRY(moe_saved_layout(p, const_cast<void*>(saved), &v));
+  if (!aligned(w_router, 16) || !aligned(dw_router, 16)) return MOE_ERR_INVALID_ARG;
+  if (L.N > 0 && (!aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(d_topk_w, 4) ||
+                  !aligned(dx, 16)))
+    return MOE_ERR_INVALID_ARG;
+  return cu(launch_router_backward(L, ws, v.xe, w_router, topk_ids, topk_w, d_topk_w, dx,
+                                   dw_router, S(stream)));
 }
 
 moe_status moe_build_schedule(const moe_problem* p, const int32_t* topk_ids, void* ws,

@@ -30,6 +30,7 @@ struct Layout {
       // MXFP8 E4M3 codes + scale chunks (tensor-core path): token rows [R, H] and
       // [R, I] x2 quantised along K; transposed [H, R] and [I, R] x2 along tokens
       mq_rh, ms_rh, mq_ri, ms_ri, mq_ri2, ms_ri2, mq_th, ms_th, mq_ti, ms_ti, mq_ti2, ms_ti2,
+      router_logits, router_dz, router_partial,  // router: logits scratch [N,E], dz [A], tile partials
       dyxe, dg, du, ws_bytes;
   // forward-context byte offsets
   size_t xe, g, u, act, ye, saved_bytes;
@@ -113,6 +114,14 @@ moe_status gemm_mx_down_wgrad(const Layout& L, const void* ws, moe_mxfp8_operand
 moe_status gemm_mx_gate_up_wgrad(const Layout& L, const void* ws, moe_mxfp8_operand dg_t,
                                  moe_mxfp8_operand du_t, moe_mxfp8_operand xe_t, float* dw_gate,
                                  float* dw_up, cudaStream_t s);
+
+// Router GEMM: logits [N, E] fp32 = x [N, H] . w_router [E, H]^T (E <= 256, E % 4 == 0).
+moe_status gemm_router(const Layout& L, const void* ws, const void* x, const void* w_router,
+                       float* logits, cudaStream_t s);
+// Router backward (see router.cu): dx += router share, dw_router [E, H] fp32.
+cudaError_t launch_router_backward(const Layout& L, const void* ws, const void* xe,
+                                   const void* w_router, const int32_t* ids, const float* w,
+                                   const float* dw, void* dx, float* dw_router, cudaStream_t s);
 
 // Launch accounting (every kernel launch of the library calls note_launch).
 void note_launch();

@@ -110,7 +110,9 @@ def make_inputs(shape: LayerShape, seed: int = 0, device="cpu", with_dy: bool = 
         g = _gen(seed, "bias", torch.device("cpu"))
         r = torch.randperm(E, generator=g).double() + 1.0
         bias = (-shape.zipf_s * torch.log(r)).float().to(dev)
-    out = dict(x=x, wg=wg, wu=wu, wd=wd, logits=logits, bias=bias)
+    # the same router weights as the device router GEMM reads them: bf16 [E, H]
+    w_router = wr.t().contiguous().to(torch.bfloat16)
+    out = dict(x=x, wg=wg, wu=wu, wd=wd, logits=logits, bias=bias, w_router=w_router)
     if with_dy:
         out["dy"] = _normal((N, H), 1.0, _gen(seed, "dy", dev), dev)
     return out

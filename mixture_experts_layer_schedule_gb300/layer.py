@@ -90,6 +90,20 @@ class MoELayer:
         _lib.moe_route_topk(self.p, logits, bias, self.topk_ids, self.topk_w, self.ws, stream)
         return self.topk_ids, self.topk_w
 
+    def route_from_x(self, x, w_router, bias=None, logits=None, stream=None):
+        """Router GEMM (logits = x . w_router^T on the tensor cores) + top-k."""
+        _lib.moe_route(self.p, x, w_router, bias, logits, self.topk_ids, self.topk_w, self.ws,
+                       stream)
+        return self.topk_ids, self.topk_w
+
+    def router_backward(self, w_router, dw_router, stream=None):
+        """Router share of dx (added to grads.dx) and dw_router [E, H] fp32; call
+        after backward() of the same batch."""
+        g = self.grads
+        _lib.moe_router_backward(self.p, self.saved, w_router, self.topk_ids, self.topk_w,
+                                 g.d_topk_w, g.dx, dw_router, self.ws, stream)
+        return dw_router
+
     def build_schedule(self, topk_ids=None, stream=None):
         _lib.moe_build_schedule(self.p, self.topk_ids if topk_ids is None else topk_ids, self.ws,
                                 stream)
