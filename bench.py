@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--cpu-tokens", type=int, default=0,
                     help="oracle sample size in tokens (0 = sized for ~15 s)")
     ap.add_argument("--phase-report", action="store_true", help="print per-phase timings")
+    ap.add_argument("--router", action="store_true",
+                    help="start from x: the router GEMM (x . Wr^T) and its backward run on the "
+                         "GPU inside the step (default: the step starts from router logits)")
     ap.add_argument("--inference", action="store_true",
                     help="forward-only workloads: time the context-free forward (dispatch "
                          "fused into gate/up) instead of the training forward")
@@ -165,10 +168,14 @@ def phase_flops(shape):
             "gate_up_wgrad": 4 * A * H * I, "forward": 6 * A * H * I, "backward": 12 * A * H * I}
 
 
-def phase_bytes(shape, R):
+def phase_bytes(shape, R, router=False):
     """Algorithmic HBM bytes of the data-movement phases."""
     N, A, H, E, k = shape.N, shape.N * shape.k, shape.H, shape.E, shape.k
-    return {"route": 4 * N * E + 8 * N * k, "schedule": 4 * A + 12 * A + 8 * E,
+    # route: logits in, ids and weights out; with the router GEMM, x and Wr in instead
+    route = (2 * N * H + 2 * E * H if router else 4 * N * E) + 8 * N * k
+    return {"route": route, "schedule": 4 * A + 12 * A + 8 * E,
+            # dz, the router share of dx (dx read and written), Xe read once, dWr written
+            "router_backward": 16 * A + 4 * N * H + 2 * A * H + 4 * E * H,
             "dispatch": 2 * N * H + 2 * A * H + 4 * A,
             "combine": 2 * A * H + 8 * A + 2 * N * H,
             "reverse_combine": 2 * N * H + 2 * A * H + 8 * A + 2 * A * H + 4 * A,
@@ -234,9 +241,18 @@ def run_ours(args, ws_, rank, local):
     elif backward:
         phases += ["reverse_combine", "down_dgrad", "down_wgrad", "gate_up_dgrad",
                    "gate_up_wgrad", "reverse_dispatch"]
+    router = args.router
+    if router and backward:
+        phases += ["router_backward"]
+    dwr = torch.empty((shape.E, shape.H), dtype=torch.float32, device=dev) if router else None
     calls = {
-        "route": lambda: _lib.moe_route_topk(p, inp["logits"], inp["bias"], layer.topk_ids,
-                                             layer.topk_w, wsb),
+        "route": (lambda: _lib.moe_route(p, inp["x"], inp["w_router"], inp["bias"], None,
+                                         layer.topk_ids, layer.topk_w, wsb)) if router else
+                 (lambda: _lib.moe_route_topk(p, inp["logits"], inp["bias"], layer.topk_ids,
+                                              layer.topk_w, wsb)),
+        "router_backward": lambda: _lib.moe_router_backward(
+            p, layer.saved, inp["w_router"], layer.topk_ids, layer.topk_w, g.d_topk_w, g.dx, dwr,
+            wsb),
         "schedule": lambda: _lib.moe_build_schedule(p, layer.topk_ids, wsb),
         "dispatch": lambda: _lib.moe_dispatch(p, wsb, inp["x"], sv["xe"]),
         "gate_up": lambda: _lib.moe_expert_gate_up(p, wsb, sv["xe"], w, sv["g"], sv["u"],
@@ -308,6 +324,8 @@ def run_ours(args, ws_, rank, local):
     # let the copies of neighbouring steps run on a copy stream while a step
     # computes; the timed region spans the first upload to the last download.
     pin = {k: inp[k].cpu().pin_memory() for k in ("x", "logits", "dy") if inp.get(k) is not None}
+    if router:
+        pin.pop("logits")
     if inference or not backward:
         pin.pop("dy", None)
     layers = [layer, MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev,
@@ -325,7 +343,17 @@ def run_ours(args, ws_, rank, local):
     ev_out = [torch.cuda.Event() for _ in range(2)]
 
     def run_one(lay, din):
-        if inference:
+        if router:
+            lay.route_from_x(din["x"], inp["w_router"], inp["bias"])
+            lay.build_schedule()
+            if inference:
+                lay.forward_inference(din["x"], inp["wg"], inp["wu"], inp["wd"], mx=mxw)
+                return
+            lay.forward(din["x"], inp["wg"], inp["wu"], inp["wd"], mx=mxw)
+            if backward:
+                lay.backward(din["dy"], inp["wg"], inp["wu"], inp["wd"], bwd=wbwd, mx=mxw)
+                lay.router_backward(inp["w_router"], dwr)
+        elif inference:
             lay.route(din["logits"], inp["bias"])
             lay.build_schedule()
             lay.forward_inference(din["x"], inp["wg"], inp["wu"], inp["wd"], mx=mxw)
@@ -377,7 +405,7 @@ def run_ours(args, ws_, rank, local):
     # ---- roofline of the dominant kernel ----
     peaks = load_peaks()
     fl = phase_flops(shape)
-    by = phase_bytes(shape, layer.R)
+    by = phase_bytes(shape, layer.R, router)
     dominant = max((ph for ph in ph_ms if ph in fl or ph in by), key=ph_ms.get)
     # MXFP8 runs its GEMMs on the FP8 tensor cores: their peak is the measured
     # bf16 one times the nominal FP8 / bf16 ratio (4.5 / 2.25 PFLOP/s dense)
@@ -422,7 +450,9 @@ def run_ours(args, ws_, rank, local):
                                                            else "fwd"),
                    "l2": "inputs larger than L2 (expert weights alone "
                          f"{3 * shape.E * shape.H * shape.I * 2 / 1e9:.2f} GB)",
-                   "parallelism": f"replicas x{ws_}"},
+                   "parallelism": f"replicas x{ws_}",
+                   "router": ("GPU router GEMM x.Wr^T and its backward inside the step" if router
+                              else "router logits are an input (x.Wr^T formed on the host)")},
         "gemm_tflops": round(gemm_flops / (gemm_ms * 1e-3) / 1e12, 1),
         "gemm_frac_of_peak": round(gemm_flops / (gemm_ms * 1e-3) / 1e12 / t_peak, 4),
         "roofline": roof,
@@ -436,15 +466,21 @@ def run_ours(args, ws_, rank, local):
 
 
 MX_NOTE = "; MXFP8 weight copies quantised once before the sample, as on the GPU"
+ROUTER_NOTE = "; router GEMM and router backward included"
 
 
-def cpu_sample(shape, inp, n_tok, threads):
+def cpu_sample(shape, inp, n_tok, threads, router=False):
     """Run the oracle on the first n_tok tokens of the workload (fwd+bwd with
-    weight gradients). Returns (seconds, tokens)."""
+    weight gradients; with router, the router GEMM and its backward too).
+    Returns (seconds, tokens)."""
     import numpy as np
 
     import oracle
     logits = inp["logits"][:n_tok].cpu().numpy()
+    if router:
+        t0 = time.perf_counter()
+        logits = oracle.router_logits(inp["x"][:n_tok], inp["w_router"], threads).astype(np.float32)
+        t_router = time.perf_counter() - t0
     bias = None if inp["bias"] is None else inp["bias"].cpu().numpy()
     x = oracle.as_bf16_bits(inp["x"][:n_tok])
     dy = oracle.as_bf16_bits(inp["dy"][:n_tok]) if inp.get("dy") is not None else None
@@ -459,13 +495,15 @@ def cpu_sample(shape, inp, n_tok, threads):
     if shape.dtype == "mxfp8":
         # the weights' quantisation is not part of a step (the GPU run also
         # prepares them once, before its timed steps)
-        oracle.layer_mxfp8_prepared(x, prepared, ids, w, dy, threads=threads)
+        r = oracle.layer_mxfp8_prepared(x, prepared, ids, w, dy, threads=threads)
     elif shape.backward:
         oracle.forward_bf16(x, wg, wu, wd, ids, w, threads=threads)
-        oracle.backward_bf16(x, wg, wu, wd, ids, w, dy, threads=threads)
+        r = oracle.backward_bf16(x, wg, wu, wd, ids, w, dy, threads=threads)
     else:
         oracle.forward_bf16(x, wg, wu, wd, ids, w, threads=threads)
-    return time.perf_counter() - t0, n_tok
+    if router and shape.backward:
+        oracle.router_backward(x, inp["w_router"], ids, w, r["dw"], threads)
+    return time.perf_counter() - t0 + (t_router if router else 0.0), n_tok
 
 
 def run_reference(args, ws_, rank):
@@ -480,8 +518,8 @@ def run_reference(args, ws_, rank):
     n_tok = args.cpu_tokens or 16
     inp = inputs.make_inputs(shape.with_(N=n_tok), seed=0, device="cpu")
     for _ in range(args.warmup):
-        cpu_sample(shape, inp, n_tok, threads)
-    times = [cpu_sample(shape, inp, n_tok, threads)[0] for _ in range(args.steps)]
+        cpu_sample(shape, inp, n_tok, threads, args.router)
+    times = [cpu_sample(shape, inp, n_tok, threads, args.router)[0] for _ in range(args.steps)]
     tot = sum(times)
     value = n_tok * args.steps / tot
     return {
@@ -497,7 +535,8 @@ def run_reference(args, ws_, rank):
                          "kind": "oracle",
                          "sample": f"first {n_tok} tokens of the workload per step "
                                    f"(full expert weights, fwd+bwd with weight gradients"
-                                   f"{MX_NOTE if shape.dtype == 'mxfp8' else ''})"},
+                                   f"{MX_NOTE if shape.dtype == 'mxfp8' else ''}"
+                                   f"{ROUTER_NOTE if args.router else ''})"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -524,12 +563,13 @@ def main():
     if rank == 0 and ws_ == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
         n_tok = args.cpu_tokens or 256
-        secs, n = cpu_sample(shape, inp, n_tok, threads)
+        secs, n = cpu_sample(shape, inp, n_tok, threads, args.router)
         rec["cpu_baseline"] = {"value": round(n / secs, 3), "unit": UNIT, "cores": threads,
                                "kind": "oracle",
                                "sample": f"first {n} tokens of the workload (full expert "
                                          f"weights, fwd+bwd with weight gradients"
-                                         f"{MX_NOTE if shape.dtype == 'mxfp8' else ''}), "
+                                         f"{MX_NOTE if shape.dtype == 'mxfp8' else ''}"
+                                         f"{ROUTER_NOTE if args.router else ''}), "
                                          f"{secs:.1f} s"}
     if rank == 0:
         if not args.phase_report:

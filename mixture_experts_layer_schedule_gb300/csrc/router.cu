@@ -63,20 +63,26 @@ __global__ void __launch_bounds__(kThreads) router_dx_kernel(
 }
 
 // Partial of one 128-row tile of the expert-grouped buffer over 1024 columns:
-// thread i owns 8 columns; rows in order; padding rows (no assignment) skip.
+// thread i owns 8 columns; rows in order (padding rows: dz 0 and Xe 0).
 __global__ void __launch_bounds__(128) router_wgrad_partial_kernel(
     const uint4* __restrict__ xe, const int32_t* __restrict__ src_of_row,
     const int32_t* __restrict__ pad_offsets, const float* __restrict__ dz, int E, int64_t A,
     int hv, float* __restrict__ partial) {
+  __shared__ float dz_row[128];  // dz of each row of the tile (0 for padding rows)
   const int64_t tile = blockIdx.x;
   const int v = blockIdx.y * blockDim.x + threadIdx.x;  // 8-column vector index
   const int64_t row0 = tile * 128;
-  if (row0 >= pad_offsets[E] || v >= hv) return;  // past the last segment: never read
+  if (row0 >= pad_offsets[E]) return;  // past the last segment: never read (whole CTA)
+  {
+    const int32_t a = src_of_row[row0 + threadIdx.x];  // blockDim.x == 128 rows
+    dz_row[threadIdx.x] = (a >= 0 && a < A) ? dz[a] : 0.0f;
+  }
+  __syncthreads();
+  if (v >= hv) return;
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll 8
   for (int r = 0; r < 128; ++r) {
-    const int32_t a = src_of_row[row0 + r];
-    if (a < 0 || a >= A) continue;
-    const float d = dz[a];
+    const float d = dz_row[r];  // padding rows hold zeros in Xe as well
     const uint4 x = xe[(row0 + r) * hv + v];
     const float f[8] = {bf16lo(x.x), bf16hi(x.x), bf16lo(x.y), bf16hi(x.y),
                         bf16lo(x.z), bf16hi(x.z), bf16lo(x.w), bf16hi(x.w)};
