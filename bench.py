@@ -71,11 +71,11 @@ def dist_env():
 GEMM_SRC = ("mixture_experts_layer_schedule_gb300/csrc/grouped_gemm.cu",
             "mixture_experts_layer_schedule_gb300/csrc/moe_common.cuh")
 MEASURED_TRAFFIC = {
-    "src_sha256": "87d6cc8743897b1fa8f4d46fbaa85da7af6287f8bca4eef6ae8383e85f4872aa",
+    "src_sha256": "358267911035ed314553f1572f090d46dae56cb26c26550ef34319c6bc4a3d3f",
     "workload": "skewed_fwd_bwd_N16384_H4096_I1536_E128_k8_zipf1.2",
-    "bytes": {"gate_up": 5.0883e9 + 1.3023e9, "down": 2.0505e9 + 1.1500e9,
-              "down_dgrad": 3.9582e9 + 0.8519e9, "down_wgrad": 2.6589e9 + 3.1563e9,
-              "gate_up_dgrad": 4.4505e9 + 1.1557e9, "gate_up_wgrad": 6.0422e9 + 6.3783e9},
+    "bytes": {"gate_up": 5.0780e9 + 1.3023e9, "down": 2.0481e9 + 1.1501e9,
+              "down_dgrad": 3.9648e9 + 0.8519e9, "down_wgrad": 2.3490e9 + 3.1561e9,
+              "gate_up_dgrad": 4.4882e9 + 1.1556e9, "gate_up_wgrad": 5.0709e9 + 6.3776e9},
 }
 
 

@@ -35,6 +35,7 @@
 
 #include "moe_common.cuh"
 #include "moe_internal.h"
+#include "tma_map.h"
 
 namespace moe {
 namespace {
@@ -851,42 +852,12 @@ __global__ void __launch_bounds__(1024) expert_order_kernel(const int32_t* __res
 // ---------------------------------------------------------------------------
 // Host side: tensor maps and launches.
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-// 2-D view [outer][inner] (inner contiguous) of `elem` bytes per element,
-// box box_inner x box_outer, 128-byte swizzle. Returns false on failure.
+// 2-D view [outer][inner] (inner contiguous) of `elem`-byte elements, box
+// box_inner x box_outer, 128-byte swizzle. Returns false on failure.
 bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int box_outer,
               int box_inner = 64, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
               int elem = 2) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn || outer <= 0 || inner <= 0) return false;
-  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (inner * elem) % 16 != 0) return false;
-  if (box_inner * elem > 128) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner * elem)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner),
-                             static_cast<cuuint32_t>(box_outer)};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return tma_map_2d(m, base, inner, outer, box_outer, box_inner, dtype, elem);
 }
 
 // bf16 output [rows][cols] for the token-row TMA-store epilogues.

@@ -179,3 +179,29 @@ def test_fp8_path_matches_bf16_mma_path_at_full_size():
         assert e <= SAME_PRODUCTS_TOL, (name, e)
     del a, b
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("T", [512, 1024])
+def test_fp8_layer_large_minibatch_rows(T):
+    """Expert segments padded to 512 / 1024 rows (many all-padding tiles)."""
+    shape = custom_shape(300, 512, 768, 16, 4, zipf_s=1.2, name=f"T{T}_mxfp8", T=T).with_(
+        dtype="mxfp8")
+    a, b, *_ = _step_pair(shape, 13)
+    for name in ("dx", "dw_gate", "dw_up", "dw_down"):
+        ref = getattr(b.grads, name).float().cpu().numpy()
+        assert max_rel(getattr(a.grads, name), ref) <= SAME_PRODUCTS_TOL, name
+
+
+def test_fp8_layer_empty_batch():
+    """N = 0: nothing routed; every weight gradient is zero, nothing faults."""
+    shape = custom_shape(0, 512, 512, 8, 2, name="empty_mxfp8").with_(dtype="mxfp8")
+    inp = to_dev(inputs.make_inputs(custom_shape(8, 512, 512, 8, 2), seed=1, device="cpu"))
+    empty = {k: (v[:0] if k in ("x", "logits", "dy") else v) for k, v in inp.items()}
+    fwd, bwd = MoELayer.prepare_mxfp8_weights(inp["wg"], inp["wu"], inp["wd"])
+    mx = MoELayer.prepare_mxfp8_mma_weights(inp["wg"], inp["wu"], inp["wd"])
+    layer = _layer(shape)
+    layer.grads.dw_gate.fill_(1.0)
+    layer.step(empty["x"], empty["logits"], empty["bias"], *fwd, empty["dy"], bwd=bwd, mx=mx)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert torch.all(layer.grads.dw_gate == 0) and torch.all(layer.grads.dw_down == 0)

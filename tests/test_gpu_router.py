@@ -87,3 +87,25 @@ def test_router_backward(shape):
     layer.router_backward(inp["w_router"], dwr)
     torch.cuda.synchronize()
     assert torch.equal(layer.grads.dx, dx1) and torch.equal(dwr, dwr1)
+
+
+def test_router_empty_batch_and_unsupported_sizes():
+    shape = custom_shape(16, 256, 256, 8, 2, name="small")
+    inp = to_dev(inputs.make_inputs(shape, seed=1, device="cpu"))
+    empty = custom_shape(0, 256, 256, 8, 2, name="empty")
+    layer = _layer(empty)
+    layer.route_from_x(inp["x"][:0], inp["w_router"], None)
+    layer.build_schedule()
+    layer.forward(inp["x"][:0], inp["wg"], inp["wu"], inp["wd"])
+    layer.backward(inp["dy"][:0], inp["wg"], inp["wu"], inp["wd"])
+    dwr = torch.full((8, 256), 1.0, dtype=torch.float32, device=dev())
+    layer.router_backward(inp["w_router"], dwr)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0 and torch.all(dwr == 0)
+    # E = 6 (not a multiple of 4) and E > 256 are rejected before any launch
+    from mixture_experts_layer_schedule_gb300 import _lib
+    for E in (6, 512):
+        bad = MoELayer(16, 256, 256, E, 2, device=dev())
+        wr = torch.zeros((E, 256), dtype=torch.bfloat16, device=dev())
+        with pytest.raises(_lib.MoEError):
+            bad.route_from_x(inp["x"], wr, None)
