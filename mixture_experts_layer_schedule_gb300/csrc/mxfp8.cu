@@ -137,8 +137,9 @@ __global__ void __launch_bounds__(256) quant_mma_rows_kernel(const uint4* __rest
 // Transposed form: q [cols, rows] = src^T, blocks of 32 consecutive source
 // rows of a column (the K of the transposed operand). A CTA stages a
 // 128-row x 64-column tile in shared memory (coalesced 128-byte row reads);
-// thread (column c, block b) then quantises rows 32b..32b+31 of column c and
-// writes its 32 codes as one contiguous piece of output row c.
+// thread (column c, block b) quantises rows 32b..32b+31 of column c into the
+// shared output tile (64 output rows of 128 code bytes), which the warps then
+// write out with coalesced 16-byte stores (8 lanes per 128-byte output row).
 constexpr int kQtRows = 128, kQtCols = 64;
 
 __global__ void __launch_bounds__(256) quant_mma_t_kernel(const uint16_t* __restrict__ src,
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(256) quant_mma_t_kernel(const uint16_t* __rest
                                                           uint8_t* __restrict__ q,
                                                           uint8_t* __restrict__ sf) {
   __shared__ __align__(16) uint16_t tile[kQtRows][kQtCols];
+  __shared__ __align__(16) uint8_t out[kQtCols][kQtRows + 16];  // +16: conflict-free rows
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kQtRows;
   const int64_t c0 = static_cast<int64_t>(blockIdx.y) * kQtCols;
   for (int i = threadIdx.x; i < kQtRows * kQtCols / 8; i += blockDim.x) {
@@ -160,11 +162,16 @@ __global__ void __launch_bounds__(256) quant_mma_t_kernel(const uint16_t* __rest
   for (int r = 0; r < 32; ++r) f[r] = __uint_as_float(static_cast<uint32_t>(tile[32 * b + r][c]) << 16);
   uint32_t packed[8];
   const uint8_t code = quant32(f, packed);
-  const int64_t orow = c0 + c;  // row of the transposed operand
-  uint4* dst = reinterpret_cast<uint4*>(q + orow * rows + r0 + 32 * b);
-  dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-  sf[sf_mma_index(orow, (r0 >> 5) + b, cols)] = code;
+  uint4* o = reinterpret_cast<uint4*>(&out[c][32 * b]);
+  o[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  o[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  sf[sf_mma_index(c0 + c, (r0 >> 5) + b, cols)] = code;
+  __syncthreads();
+  for (int i = threadIdx.x; i < kQtCols * kQtRows / 16; i += blockDim.x) {
+    const int oc = i / (kQtRows / 16), piece = i % (kQtRows / 16);
+    *reinterpret_cast<uint4*>(q + (c0 + oc) * rows + r0 + 16 * piece) =
+        *reinterpret_cast<const uint4*>(&out[oc][16 * piece]);
+  }
 }
 
 }  // namespace
