@@ -355,6 +355,12 @@ moe_status moe_get_device_error(const moe_problem* p, const void* ws, int32_t* c
 /* Enqueue a reset of the device error word to MOE_DEVERR_NONE. */
 moe_status moe_clear_device_error(const moe_problem* p, void* ws, void* stream);
 
+/* Test of the failure detection: launches one CTA whose barrier wait can never
+ * complete; the wait's time limit (about one second) runs out, the kernel
+ * records MOE_DEVERR_TIMEOUT in the workspace error word and returns, and the
+ * context stays usable. No counterpart in the pages. */
+moe_status moe_test_wait_timeout(const moe_problem* p, void* ws, void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* moe_status_string(moe_status s);
 

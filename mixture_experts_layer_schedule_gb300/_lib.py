@@ -95,6 +95,7 @@ _SIGS = {
     "moe_get_device_error": ([c_vp, c_vp, c_vp, c_vp], c_i32),
     "moe_clear_device_error": ([c_vp, c_vp, c_vp], c_i32),
     "moe_status_string": ([c_i32], ctypes.c_char_p),
+    "moe_test_wait_timeout": ([c_vp, c_vp, c_vp], c_i32),
     "moe_launch_count": ([], ctypes.c_uint64),
 }
 
@@ -318,6 +319,10 @@ def moe_get_device_error(p, ws, stream=None) -> int:
     (torch.cuda.current_stream() if stream is None else stream).synchronize() \
         if not isinstance(stream, int) else torch.cuda.synchronize()
     return int(out.item())
+
+
+def moe_test_wait_timeout(p, ws, stream=None):
+    _call("moe_test_wait_timeout", ctypes.byref(p), _ptr(ws), _stream(stream))
 
 
 def moe_launch_count() -> int:

@@ -9,6 +9,7 @@
 #include <algorithm>
 #include <atomic>
 
+#include "moe_common.cuh"
 #include "moe_internal.h"
 
 namespace moe {
@@ -90,6 +91,21 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   L->ye = take(static_cast<size_t>(R) * p->H * 2);
   L->saved_bytes = o;
   return MOE_OK;
+}
+
+// Failure-detection check: one CTA waits, through the bounded wait every
+// kernel uses, on an mbarrier nothing arrives at. The wait runs out (about
+// kWaitBudgetCycles), records MOE_DEVERR_TIMEOUT in the error word and the
+// kernel returns normally, leaving the context usable.
+__global__ void wait_timeout_kernel(int32_t* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    mbar_wait(&bar, 0, &abort_flag, err);  // phase 0 never completes: expected to time out
+  }
 }
 
 }  // namespace moe
@@ -555,6 +571,14 @@ moe_status moe_clear_device_error(const moe_problem* p, void* ws, void* stream) 
 }
 
 uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+moe_status moe_test_wait_timeout(const moe_problem* p, void* ws, void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  wait_timeout_kernel<<<1, 32, 0, S(stream)>>>(at<int32_t>(ws, L.err));
+  note_launch();
+  return cu(cudaGetLastError());
+}
 
 const char* moe_status_string(moe_status s) {
   switch (s) {
