@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--router", action="store_true",
                     help="start from x: the router GEMM (x . Wr^T) and its backward run on the "
                          "GPU inside the step (default: the step starts from router logits)")
+    ap.add_argument("--sweep-T", action="store_true",
+                    help="the minibatch knob sweep: run the workload at minibatch_rows T = 128, "
+                         "256, 512, 1024 and print one line with every T's result and the best")
     ap.add_argument("--inference", action="store_true",
                     help="forward-only workloads: time the context-free forward (dispatch "
                          "fused into gate/up) instead of the training forward")
@@ -203,11 +206,11 @@ def workload(name):
                              zipf_s=z, minibatch_rows=T, dtype=dtype)
 
 
-def run_ours(args, ws_, rank, local):
+def run_ours(args, ws_, rank, local, shape=None):
     import torch
     from mixture_experts_layer_schedule_gb300 import MoELayer, _lib, inputs
 
-    shape = workload(args.config)
+    shape = shape or workload(args.config)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     inp = inputs.make_inputs(shape, seed=rank, device=dev)
@@ -558,6 +561,25 @@ def main():
         rec = run_reference(args, ws_, rank)
         if rec is not None:
             print(json.dumps(rec), flush=True)
+        return
+    if args.sweep_T:
+        import torch
+        base = workload(args.config)
+        res = {}
+        for T in (128, 256, 512, 1024):
+            r, _, _ = run_ours(args, ws_, rank, local,
+                               base.with_(name=f"{base.name}_T{T}", minibatch_rows=T))
+            res[T] = {"value": r["value"], "ms_per_step": r["ms_per_step"],
+                      "gemm_tflops": r["gemm_tflops"], "clocks": r["clocks"]}
+            del r
+            torch.cuda.empty_cache()
+        best = max(res, key=lambda t: res[t]["value"])
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "unit": UNIT, "higher_is_better": True,
+                              "sweep": "minibatch_rows", "workload": base.name, "n_gpus": ws_,
+                              "steps": args.steps, "warmup": args.warmup, "results": res,
+                              "best_minibatch_rows": best, "value": res[best]["value"]}),
+                  flush=True)
         return
     rec, shape, inp = run_ours(args, ws_, rank, local)
     if rank == 0 and ws_ == 1 and not args.no_cpu_baseline:
