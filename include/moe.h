@@ -65,7 +65,8 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_dtype;
  * H and I multiples of 256. dtype MOE_BF16, or MOE_MXFP8: every operand of
  * every expert GEMM is quantised to MXFP8 (1x32 blocks along that GEMM's K,
  * E8M0 scale, E4M3 values; token-axis blocks restart per expert) and the
- * GEMMs run on the exact bf16 values of those numbers (fp32 accumulation);
+ * GEMMs multiply those numbers with fp32 accumulation -- as block-scaled FP8
+ * MMAs when moe_weights.mx is given, else on their exact bf16 values;
  * moe_forward / moe_backward insert the activation quantisations.
  * minibatch_rows T ([Clip] key point 3, minibatch granularity; the "tokens
  * per expert slot" of the large-batch sweep): each expert's rows are grouped
@@ -79,14 +80,6 @@ typedef struct {
   int32_t minibatch_rows;
 } moe_problem;
 
-/* Expert weights, bf16, K dimension contiguous:
- *   w_gate [E][I][H], w_up [E][I][H], w_down [E][H][I].
- * The *_bwd pointers are the same tensors as the backward data-gradient GEMMs
- * read them; NULL means "same as the forward ones" (MOE_BF16). For MOE_MXFP8
- * the forward pointers hold the weights quantised along their K (H for
- * gate/up, I for down) and the *_bwd pointers the weights quantised along the
- * backward GEMMs' K (I for gate/up, H for down), both as exact bf16 values of
- * the MXFP8 numbers (see mxfp8_qdq). */
 /* One MXFP8 operand as the block-scaled tensor-core GEMMs read it (see
  * mxfp8_quantize_mma): q = E4M3 codes of a K-major [rows, K] matrix, s = its
  * E8M0 scales (rows * K / 32 bytes) in the tensor-memory chunk layout. */
@@ -108,6 +101,14 @@ typedef struct {
   moe_mxfp8_operand gate_t, up_t, down_t;
 } moe_mxfp8_weights;
 
+/* Expert weights, bf16, K dimension contiguous:
+ *   w_gate [E][I][H], w_up [E][I][H], w_down [E][H][I].
+ * The *_bwd pointers are the same tensors as the backward data-gradient GEMMs
+ * read them; NULL means "same as the forward ones" (MOE_BF16). For MOE_MXFP8
+ * the forward pointers hold the weights quantised along their K (H for
+ * gate/up, I for down) and the *_bwd pointers the weights quantised along the
+ * backward GEMMs' K (I for gate/up, H for down), both as exact bf16 values of
+ * the MXFP8 numbers (see mxfp8_qdq). */
 typedef struct {
   const void* w_gate;
   const void* w_up;
