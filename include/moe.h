@@ -325,7 +325,8 @@ moe_status mxfp8_quantize(const void* src_bf16, int64_t rows, int64_t cols, uint
                           uint8_t* scale_e8m0, void* stream);
 
 /* MXFP8 quantiser for the block-scaled tensor-core GEMMs (same rounding rule
- * as mxfp8_quantize), rows % 128 == 0 and cols % 128 == 0, q 16-byte aligned.
+ * as mxfp8_quantize), rows % 128 == 0 and cols % 128 == 0; src, q and s
+ * 16-byte aligned (else MOE_ERR_INVALID_ARG).
  *   transpose 0: q [rows, cols], blocks of 32 consecutive columns of a row
  *                (the operand's K = cols);
  *   transpose 1: q [cols, rows] = src^T, blocks of 32 consecutive source rows

@@ -270,7 +270,12 @@ __device__ __forceinline__ void q_issue_loads(const QMaps& m, const QArgs& a, co
   }
 }
 
-__device__ __forceinline__ float q_silu(float g) { return g / (1.0f + expf(-g)); }
+// The SwiGLU epilogues use the fast exponential and division intrinsics
+// (__expf: at most 2 + floor(1.16 |x|) ulp; __fdividef: 2 ulp): their error is
+// far below the bf16 rounding of G, U, Act, dG and dU, and the exact forms
+// made the dAct epilogue, not the MMAs, the bound of that GEMM.
+__device__ __forceinline__ float q_sigmoid(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
+__device__ __forceinline__ float q_silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // 16 consecutive fp32 values -> 16 bf16 (8 words).
 __device__ __forceinline__ void pack16(const float* v, uint32_t (&w)[8]) {
@@ -480,7 +485,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
                 const float da = v[16 * j + 8 * hv + 2 * q + h];
                 const float g = h ? bf16hi(gw[q]) : bf16lo(gw[q]);
                 const float u = h ? bf16hi(uw[q]) : bf16lo(uw[q]);
-                const float sg = 1.0f / (1.0f + expf(-g));
+                const float sg = q_sigmoid(g);
                 dg2[h] = da * u * sg * (1.0f + g * (1.0f - sg));
                 du2[h] = da * g * sg;
               }

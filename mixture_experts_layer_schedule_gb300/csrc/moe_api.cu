@@ -162,6 +162,17 @@ moe_status quantize_into(const void* src, int64_t rows, int64_t cols, int transp
                                       const_cast<uint8_t*>(o.s), s));
 }
 
+// Quantise bf16 [rows, cols] into the row form (K = cols) and/or the
+// transposed form (K = rows) in one pass; a NULL operand is skipped.
+moe_status quantize_forms(const void* src, int64_t rows, int64_t cols,
+                          const moe_mxfp8_operand* row_form, const moe_mxfp8_operand* t_form,
+                          cudaStream_t s) {
+  auto q = [](const moe_mxfp8_operand* o) { return o ? const_cast<uint8_t*>(o->q) : nullptr; };
+  auto sf = [](const moe_mxfp8_operand* o) { return o ? const_cast<uint8_t*>(o->s) : nullptr; };
+  return cu(launch_mxfp8_quantize_mma_forms(src, rows, cols, q(row_form), sf(row_form),
+                                            q(t_form), sf(t_form), s));
+}
+
 // MXFP8 forward on the block-scaled tensor cores: Xe quantised along H feeds
 // gate/up, Act quantised along I feeds down. g/u may be NULL (inference).
 moe_status mx_forward_gemms(const Layout& L, void* ws, const moe_mxfp8_weights& mx,
@@ -189,18 +200,16 @@ moe_status mx_backward_gemms(const Layout& L, void* ws, const moe_mxfp8_weights&
   const moe_mxfp8_operand th = ws_operand(ws, L.mq_th, L.ms_th);
   const moe_mxfp8_operand ti = ws_operand(ws, L.mq_ti, L.ms_ti);
   const moe_mxfp8_operand ti2 = ws_operand(ws, L.mq_ti2, L.ms_ti2);
-  MOE_TRY(quantize_into(dyxe, L.R, L.H, 0, rh, s));
-  MOE_TRY(quantize_into(dyxe, L.R, L.H, 1, th, s));
-  MOE_TRY(quantize_into(v.act, L.R, L.I, 1, ti, s));
+  MOE_TRY(quantize_forms(dyxe, L.R, L.H, &rh, &th, s));
+  MOE_TRY(quantize_forms(v.act, L.R, L.I, nullptr, &ti, s));
   MOE_TRY(gemm_mx_down_dgrad(L, ws, rh, mx.down_t, v.g, v.u, dg, du, s));
   MOE_TRY(gemm_mx_down_wgrad(L, ws, th, ti, dw_down, s));
-  MOE_TRY(quantize_into(dg, L.R, L.I, 0, ri, s));
-  MOE_TRY(quantize_into(du, L.R, L.I, 0, ri2, s));
+  // Act^T's last reader ran above: dG^T and dU^T reuse its buffers.
+  MOE_TRY(quantize_forms(dg, L.R, L.I, &ri, &ti, s));
+  MOE_TRY(quantize_forms(du, L.R, L.I, &ri2, &ti2, s));
   // dXe overwrites dYe in the shared buffer: dYe's last readers ran above.
   MOE_TRY(gemm_mx_gate_up_dgrad(L, ws, ri, ri2, mx.gate_t, mx.up_t, dyxe, s));
-  MOE_TRY(quantize_into(dg, L.R, L.I, 1, ti, s));
-  MOE_TRY(quantize_into(du, L.R, L.I, 1, ti2, s));
-  MOE_TRY(quantize_into(v.xe, L.R, L.H, 1, th, s));
+  MOE_TRY(quantize_forms(v.xe, L.R, L.H, nullptr, &th, s));
   return gemm_mx_gate_up_wgrad(L, ws, ti, ti2, th, dw_gate, dw_up, s);
 }
 
@@ -542,7 +551,8 @@ moe_status mxfp8_quantize_mma(const void* src_bf16, int64_t rows, int64_t cols, 
   if (rows < 0 || cols < 0 || rows % 128 != 0 || cols % 128 != 0) return MOE_ERR_INVALID_ARG;
   if (transpose != 0 && transpose != 1) return MOE_ERR_INVALID_ARG;
   if (rows * cols == 0) return MOE_OK;
-  if (!aligned(src_bf16, 16) || !aligned(q_e4m3, 16) || !s_e8m0) return MOE_ERR_INVALID_ARG;
+  if (!aligned(src_bf16, 16) || !aligned(q_e4m3, 16) || !aligned(s_e8m0, 16))
+    return MOE_ERR_INVALID_ARG;
   return cu(launch_mxfp8_quantize_mma(src_bf16, rows, cols, transpose, q_e4m3, s_e8m0,
                                       S(stream)));
 }

@@ -65,6 +65,12 @@ cudaError_t launch_reverse_dispatch(const Layout& L, const void* ws, const void*
                                     cudaStream_t s);
 cudaError_t launch_mxfp8_qdq(const void* src, void* dst, int64_t rows, int64_t cols, int axis,
                              cudaStream_t s);
+// Both MMA-layout MXFP8 forms of bf16 [rows, cols] from one read: the row
+// form (q_r, sf_r; blocks along cols) and the transposed form (q_t, sf_t;
+// blocks along rows). Either pair may be NULL. rows, cols multiples of 128.
+cudaError_t launch_mxfp8_quantize_mma_forms(const void* src, int64_t rows, int64_t cols,
+                                            uint8_t* q_r, uint8_t* sf_r, uint8_t* q_t,
+                                            uint8_t* sf_t, cudaStream_t s);
 cudaError_t launch_mxfp8_quantize_mma(const void* src, int64_t rows, int64_t cols, int transpose,
                                       uint8_t* q, uint8_t* sf, cudaStream_t s);
 cudaError_t launch_mxfp8_quantize(const void* src, int64_t rows, int64_t cols, uint8_t* q,
