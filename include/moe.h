@@ -71,8 +71,8 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_dtype;
  * minibatch_rows T ([Clip] key point 3, minibatch granularity; the "tokens
  * per expert slot" of the large-batch sweep): each expert's rows are grouped
  * and padded to a multiple of T. T = 128 (also for 0), 256, 512 or 1024.
- * Larger T wastes more padding rows but lets two SMs share one 256-row MMA
- * of an expert (T >= 256 selects the SM-pair kernels). */
+ * Larger T only adds padding rows on one GPU (the expert GEMMs run on SM
+ * pairs at every T); it is kept as the pages' minibatch knob. */
 typedef struct {
   int64_t N;
   int32_t H, I, E, k;

@@ -7,8 +7,11 @@
 // key flowchart node "expert FFN + SwiGLU"). The backward rounds (key point
 // 2) need the matching data-gradient and weight-gradient GEMMs.
 //
-// One persistent kernel template serves every GEMM of the layer. Each CTA
-// (one per SM) runs three roles that hand work over through mbarriers:
+// Two persistent kernel templates serve the GEMMs of the layer: the SM-pair
+// kernel (tcgen05 cta_group::2, further below) runs the four token-row modes
+// and the weight gradients; the single-CTA kernel runs the router GEMM and
+// the gate/up GEMM with the dispatch fused into its producer. In both, each
+// CTA (one per SM) runs three roles that hand work over through mbarriers:
 //   warp 0      TMA producer: streams 64-wide K slices of the A and B tiles
 //               into a ring of shared-memory stages (128-byte swizzle);
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256,
@@ -21,9 +24,9 @@
 // i+1. Every wait is bounded; a timeout records MOE_DEVERR_TIMEOUT, drains
 // the copies and MMAs in flight, frees TMEM and returns.
 //
-// Modes (rows of the expert-grouped buffer are padded per expert to 128, and
-// padding rows hold zeros, so every tile is a full 128-row tile of one
-// expert):
+// Modes (rows of the expert-grouped buffer are padded per expert to a
+// multiple of 128, and padding rows hold zeros, so every tile is a full
+// 128-row tile of one expert):
 //   GATE_UP  G|U = Xe . [Wg[e]; Wu[e]]^T   -> G, U, Act = silu(G) * U (bf16)
 //   DOWN     Ye  = Act . Wd[e]^T            -> bf16
 //   DACT     dAct = dYe . Wd[e]             -> dG, dU via the SwiGLU backward (bf16)
@@ -60,12 +63,15 @@ enum Mode { GATE_UP = 0, DOWN = 1, DACT = 2, DXE = 3, WGRAD = 4, GATE_UP_GATHER 
 
 struct Maps {
   CUtensorMap a0, a1, b0, b1;
+  CUtensorMap a0h, a1h;    // SM-pair kernels: A with a 64-row box (128-row items)
   CUtensorMap o0, o1, o2;  // outputs (TMA stores): fp32 32x32 or bf16 64x32 boxes, 128-B swizzle
 };
 
 struct Args {
   const int32_t* tiles;        // [n][3] (expert, row0, valid) of the 128-row tiles
   const int32_t* n_tiles;      // device count of those tiles
+  const int32_t* ptiles;       // [n][3] (expert, row0, rows 256 or 128) SM-pair items
+  const int32_t* n_ptiles;     // device count of those items
   const int32_t* pad_offsets;  // [E+1] padded segment starts (WGRAD K ranges)
   const int32_t* order;        // [E] experts by descending row count (WGRAD)
   const int32_t* counts;       // [E] rows per expert (WGRAD K = count rounded up to 64)
@@ -98,6 +104,7 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, int32
 struct TileInfo {
   int e, row0, mt, nt, prob, kstart, nkb;
   bool skip;
+  bool fold;  // SM-pair item of 128 rows: M=128 pair MMA, 64 rows per CTA
 };
 
 // Tile t of this CTA. With CL = 2 (a cluster of two CTAs), t numbers pair
@@ -108,6 +115,7 @@ struct TileInfo {
 template <int MODE, int CL>
 __device__ __forceinline__ TileInfo decode_tile(const Args& a, int64_t t, int crank) {
   TileInfo ti;
+  ti.fold = false;
   if constexpr (MODE == ROUTER) {
     ti.mt = static_cast<int>(t);
     ti.nt = 0;
@@ -177,62 +185,17 @@ __device__ __forceinline__ int64_t total_tiles(const Args& a) {
   }
 }
 
-// The A tile of the token-row modes: whole (CL = 1) or this CTA's 64-row half,
-// multicast to both CTAs of the pair (CL = 2; the map's box is then 64 rows).
-template <int CL>
-__device__ __forceinline__ void load_a_rows(uint8_t* sA, const CUtensorMap* ma, uint64_t* bar,
-                                            int k0, int row0, int crank) {
-  if constexpr (CL == 1) {
-    tma_load_2d(sA, ma, bar, k0, row0);
-  } else {
-    tma_load_2d_mc(sA + crank * (kABytes / 2), ma, bar, k0, row0 + crank * (BM / 2), 0x3);
-  }
-}
-
+// Loads of one k-block for the single-CTA kernel's modes.
 template <int MODE, int CL>
 __device__ __forceinline__ void issue_loads(const Maps& m, const Args& a, const TileInfo& ti,
                                             int kb, uint8_t* sA, uint8_t* sB, uint64_t* bar,
                                             int crank) {
-  if constexpr (MODE == GATE_UP_GATHER) {
-    // loaded by the whole producer warp (see the kernel)
-  } else if constexpr (MODE == ROUTER) {
+  static_assert(MODE == GATE_UP_GATHER || MODE == ROUTER, "single-CTA kernel modes");
+  if constexpr (MODE == ROUTER) {
     tma_load_2d(sA, &m.a0, bar, kb * BK, ti.row0);
     tma_load_2d(sB, &m.b0, bar, kb * BK, 0);  // all E router rows; rows past E read as zeros
-  } else if constexpr (MODE == GATE_UP) {
-    load_a_rows<CL>(sA, &m.a0, bar, kb * BK, ti.row0, crank);
-    const int brow = ti.e * a.b_rows + ti.nt * (BN / 2);
-    tma_load_2d(sB, &m.b0, bar, kb * BK, brow);
-    tma_load_2d(sB + kBBytes / 2, &m.b1, bar, kb * BK, brow);
-  } else if constexpr (MODE == DOWN) {
-    load_a_rows<CL>(sA, &m.a0, bar, kb * BK, ti.row0, crank);
-    tma_load_2d(sB, &m.b0, bar, kb * BK, ti.e * a.b_rows + ti.nt * BN);
-  } else if constexpr (MODE == DACT || MODE == DXE) {
-    const bool second = (MODE == DXE) && kb >= a.kb1;
-    const int kk = second ? kb - a.kb1 : kb;
-    load_a_rows<CL>(sA, second ? &m.a1 : &m.a0, bar, kk * BK, ti.row0, crank);
-    const CUtensorMap* mb = second ? &m.b1 : &m.b0;
-#pragma unroll
-    for (int c = 0; c < BN / 64; ++c)
-      tma_load_2d(sB + c * (64 * BK * 2), mb, bar, ti.nt * BN + c * 64, ti.e * a.b_rows + kk * BK);
-  } else {  // WGRAD
-    const CUtensorMap* ma = ti.prob ? &m.a1 : &m.a0;
-    const CUtensorMap* mb = ti.prob ? &m.b1 : &m.b0;
-    const int krow = ti.kstart + kb * BK;
-#pragma unroll
-    for (int c = 0; c < BM / 64; ++c)
-      tma_load_2d(sA + c * (64 * BK * 2), ma, bar, ti.mt * BM + c * 64, krow);
-    if constexpr (CL == 1) {
-#pragma unroll
-      for (int c = 0; c < BN / 64; ++c)
-        tma_load_2d(sB + c * (64 * BK * 2), mb, bar, ti.nt * BN + c * 64, krow);
-    } else {  // the pair shares this B tile: two of its four 64-column chunks each
-#pragma unroll
-      for (int h = 0; h < BN / 128; ++h) {
-        const int c = crank * (BN / 128) + h;
-        tma_load_2d_mc(sB + c * (64 * BK * 2), mb, bar, ti.nt * BN + c * 64, krow, 0x3);
-      }
-    }
   }
+  // GATE_UP_GATHER: loaded by the whole producer warp (see the kernel)
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
@@ -280,41 +243,51 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 }
 
 // Epilogues of the token-row modes (bf16 outputs), one warp = 32 tile rows:
-//   GATE_UP  G, U and Act = silu(G) * U  (accumulator columns: 128 G, 128 U)
+//   GATE_UP  G, U and Act = silu(G) * U
 //   DOWN/DXE the accumulator rounded to bf16
 //   DACT     dG, dU from dAct and the saved G, U of the same rows (stored
 //            directly: this epilogue also reads G and U, and interleaving those
 //            reads with the stores in 32-column steps measured faster)
-template <int MODE>
+// The warp's TMEM lanes hold all BN columns of its 32 rows, except in a
+// folded SM-pair item (M=128 over two CTAs, 64 rows each): there TMEM lanes
+// 0-63 hold D columns [0, BN/2) of the CTA's 64 rows and lanes 64-127 columns
+// [BN/2, BN) of the same rows, both in TMEM columns [0, BN/2).
+// GATE_UP D column order: single CTA, 128 G then 128 U columns of the N tile;
+// SM pair, per half of the N tile (one CTA's B rows) 64 G then 64 U columns.
+template <int MODE, bool PAIR>
 __device__ __forceinline__ void epilogue(const Maps& m, const Args& a, const TileInfo& ti,
                                          uint32_t tmem_acc, int quad, int lane,
                                          uint8_t* stage_out, uint32_t& nstore) {
   const uint32_t taddr = tmem_acc + (static_cast<uint32_t>(quad * 32) << 16);
-  const int32_t y = ti.row0 + quad * 32;
+  const int32_t y = ti.row0 + (ti.fold ? (quad & 1) : quad) * 32;
+  const int dc0 = ti.fold ? (quad >> 1) * (BN / 2) : 0;  // first D column held
+  const int ncol = ti.fold ? BN / 2 : BN;                // D columns held
   if constexpr (MODE == GATE_UP || MODE == GATE_UP_GATHER) {
     const int32_t x0 = ti.nt * (BN / 2);
-    for (int c = 0; c < BN / 2; c += 64) {
+    for (int c = 0; c < ncol / 2; c += 64) {
       float g[64], u[64];
-      tmem_ld64(taddr + c, g);
-      tmem_ld64(taddr + BN / 2 + c, u);
+      const int tg = PAIR ? 2 * c : c, tu = PAIR ? 2 * c + 64 : BN / 2 + c;
+      const int32_t xo = x0 + (PAIR ? (dc0 + 2 * c) / 2 : c);
+      tmem_ld64(taddr + tg, g);
+      tmem_ld64(taddr + tu, u);
       if (a.store_gu) {
-        store_block_bf16(&m.o0, g, x0 + c, y, lane, stage_out, nstore);
-        store_block_bf16(&m.o1, u, x0 + c, y, lane, stage_out, nstore);
+        store_block_bf16(&m.o0, g, xo, y, lane, stage_out, nstore);
+        store_block_bf16(&m.o1, u, xo, y, lane, stage_out, nstore);
       }
 #pragma unroll
       for (int i = 0; i < 64; ++i) g[i] = silu(g[i]) * u[i];
-      store_block_bf16(&m.o2, g, x0 + c, y, lane, stage_out, nstore);
+      store_block_bf16(&m.o2, g, xo, y, lane, stage_out, nstore);
     }
   } else if constexpr (MODE == DOWN || MODE == DXE) {
-    for (int c = 0; c < BN; c += 64) {
+    for (int c = 0; c < ncol; c += 64) {
       float d[64];
       tmem_ld64(taddr + c, d);
-      store_block_bf16(&m.o0, d, ti.nt * BN + c, y, lane, stage_out, nstore);
+      store_block_bf16(&m.o0, d, ti.nt * BN + dc0 + c, y, lane, stage_out, nstore);
     }
   } else {  // DACT: direct 16-byte stores, G and U read alongside in 32-column steps
     const int64_t row = static_cast<int64_t>(y) + lane;
-    const int64_t o = row * a.ld_out + ti.nt * BN;
-    for (int c = 0; c < BN; c += 32) {
+    const int64_t o = row * a.ld_out + ti.nt * BN + dc0;
+    for (int c = 0; c < ncol; c += 32) {
       uint32_t d[32];
       tmem_ld32(taddr + c, d);
       const uint4* pg = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.in0) + o + c);
@@ -413,6 +386,7 @@ __device__ __forceinline__ void epilogue_router(const Maps& m, const Args& a, co
 template <int MODE, int CL>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ Maps maps, const Args args) {
+  static_assert(MODE == GATE_UP_GATHER || MODE == ROUTER, "single-CTA kernel modes");
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], drain_bar;
   __shared__ uint32_t tmem_base_slot;
@@ -580,12 +554,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       if (ti.skip) {
         if (lane == 0) set_dev_error(args.err, MOE_DEVERR_BAD_EXPERT);
-      } else if constexpr (MODE == WGRAD) {
-        epilogue_wgrad(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
       } else if constexpr (MODE == ROUTER) {
         epilogue_router(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
       } else {
-        epilogue<MODE>(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
+        epilogue<MODE, false>(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
@@ -623,17 +595,33 @@ constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
 constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + kOutBytes + 1024;
 
 // Pair tiles: WGRAD pairs neighbouring M tiles of one expert (shared B); the
-// token-row modes pair the two 128-row tiles of one 256-row block of an expert
-// (T >= 256 guarantees both belong to the same expert) and split the N tile's
-// B rows/columns between the CTAs.
+// token-row modes take the schedule's SM-pair items (256 rows of one expert,
+// 128 rows per CTA; or an expert's last 128 rows, 64 per CTA, as an M=128
+// pair MMA) and split the N tile's B rows/columns between the CTAs.
 template <int MODE>
 __device__ __forceinline__ TileInfo decode_pair_tile(const Args& a, int64_t t, int crank) {
   if constexpr (MODE == WGRAD) {
     return decode_tile<MODE, 2>(a, t, crank);
   } else {
     const int pm = static_cast<int>(t / a.n_nt);
-    TileInfo ti = decode_tile<MODE, 1>(a, static_cast<int64_t>(2 * pm + crank) * a.n_nt, 0);
+    TileInfo ti;
+    ti.e = a.ptiles[3 * pm + 0];
+    const int r0 = a.ptiles[3 * pm + 1], nr = a.ptiles[3 * pm + 2];
+    ti.fold = nr == BM;
+    ti.row0 = r0 + crank * (ti.fold ? BM / 2 : BM);
+    ti.mt = pm;
     ti.nt = static_cast<int>(t % a.n_nt);
+    ti.prob = 0;
+    ti.kstart = 0;
+    ti.nkb = a.kb1 + a.kb2;
+    ti.skip = false;
+    if (ti.e < 0 || ti.e >= a.E || r0 < 0 || (nr != BM && nr != 2 * BM) || r0 > a.rows - nr) {
+      ti.e = 0;  // corrupt schedule: compute nothing, store nothing
+      ti.row0 = 0;
+      ti.nkb = 0;
+      ti.skip = true;
+      ti.fold = false;
+    }
     return ti;
   }
 }
@@ -643,9 +631,9 @@ __device__ __forceinline__ int64_t total_pair_tiles(const Args& a) {
   if constexpr (MODE == WGRAD) {
     return total_tiles<MODE, 2>(a);
   } else {
-    int n = *a.n_tiles;
+    int n = *a.n_ptiles;
     n = n < 0 ? 0 : (n > a.max_mtiles ? a.max_mtiles : n);
-    return static_cast<int64_t>(n / 2) * a.n_nt;
+    return static_cast<int64_t>(n) * a.n_nt;
   }
 }
 
@@ -665,17 +653,20 @@ __device__ __forceinline__ void issue_loads_pair(const Maps& m, const Args& a, c
       tma_load_2d_pair(sB + c * (64 * BK * 2), mb, bar, ti.nt * BN + crank * (BN / 2) + c * 64,
                        krow);
   } else if constexpr (MODE == GATE_UP) {
-    // the N tile is 128 gate rows then 128 up rows: the even CTA stages the
-    // gate rows, the odd CTA the up rows
-    tma_load_2d_pair(sA, &m.a0, bar, kb * BK, ti.row0);
-    tma_load_2d_pair(sB, crank ? &m.b1 : &m.b0, bar, kb * BK, ti.e * a.b_rows + ti.nt * (BN / 2));
+    // the N tile covers 128 gate and 128 up rows of the weights; each CTA
+    // stages 64 gate rows then the 64 up rows of the same I columns
+    tma_load_2d_pair(sA, ti.fold ? &m.a0h : &m.a0, bar, kb * BK, ti.row0);
+    const int brow = ti.e * a.b_rows + ti.nt * (BN / 2) + crank * (BN / 4);
+    tma_load_2d_pair(sB, &m.b0, bar, kb * BK, brow);
+    tma_load_2d_pair(sB + (BN / 4) * BK * 2, &m.b1, bar, kb * BK, brow);
   } else if constexpr (MODE == DOWN) {
-    tma_load_2d_pair(sA, &m.a0, bar, kb * BK, ti.row0);
+    tma_load_2d_pair(sA, ti.fold ? &m.a0h : &m.a0, bar, kb * BK, ti.row0);
     tma_load_2d_pair(sB, &m.b0, bar, kb * BK, ti.e * a.b_rows + ti.nt * BN + crank * (BN / 2));
   } else {  // DACT, DXE: B is MN-major, two 64-column chunks per CTA
     const bool second = (MODE == DXE) && kb >= a.kb1;
     const int kk = second ? kb - a.kb1 : kb;
-    tma_load_2d_pair(sA, second ? &m.a1 : &m.a0, bar, kk * BK, ti.row0);
+    const CUtensorMap* ma = second ? (ti.fold ? &m.a1h : &m.a1) : (ti.fold ? &m.a0h : &m.a0);
+    tma_load_2d_pair(sA, ma, bar, kk * BK, ti.row0);
     const CUtensorMap* mb = second ? &m.b1 : &m.b0;
 #pragma unroll
     for (int c = 0; c < BN / 128; ++c)
@@ -742,7 +733,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, args.err)) { ok = false; break; }
           uint8_t* sA = smem + stage * kPairStageBytes;
-          if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
+          // both CTAs' copies: A (64 rows each in a folded item) and half of B
+          if (leader)
+            mbar_arrive_expect_tx(&full_bar[stage],
+                                  2 * ((ti.fold ? kPairABytes / 2 : kPairABytes) + kPairBBytes));
           issue_loads_pair<MODE>(maps, args, ti, kb, sA, sA + kPairABytes,
                                  cluster_addr(&full_bar[stage], 0), crank);
           issued_mask |= 1u << stage;
@@ -757,7 +751,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ---------------- MMA issuer (even CTA only) ----------------
-      constexpr uint32_t idesc = idesc_bf16(2 * BM, BN, Traits<MODE>::a_mn, Traits<MODE>::b_mn);
+      constexpr uint32_t idesc256 = idesc_bf16(2 * BM, BN, Traits<MODE>::a_mn, Traits<MODE>::b_mn);
+      constexpr uint32_t idesc128 = idesc_bf16(BM, BN, Traits<MODE>::a_mn, Traits<MODE>::b_mn);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -769,6 +764,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abortp, args.err)) break;
         tc_fence_after();
         const uint32_t dtmem = tmem_base + acc * BN;
+        const uint32_t idesc = ti.fold ? idesc128 : idesc256;
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abortp, args.err)) { ok = false; break; }
           tc_fence_after();
@@ -810,7 +806,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else if constexpr (MODE == WGRAD) {
         epilogue_wgrad(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
       } else {
-        epilogue<MODE>(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
+        epilogue<MODE, true>(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
       }
       tc_fence_before();
       __syncwarp();
@@ -968,33 +964,26 @@ moe_status launch_pair(const Maps& maps, const Args& args, int64_t units, cudaSt
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-// Token-row modes pair neighbouring N tiles when their count is even.
+// Token-row modes: the SM-pair kernel over the schedule's pair items (at most
+// one per 128-row tile).
 template <int MODE>
-moe_status launch_rows(const Maps& maps, const Args& args, cudaStream_t s) {
-  if (args.n_nt % 2 == 0)
-    return launch<MODE, 2>(maps, args, static_cast<int64_t>(args.max_mtiles) * (args.n_nt / 2), s);
-  return launch<MODE, 1>(maps, args, static_cast<int64_t>(args.max_mtiles) * args.n_nt, s);
+moe_status launch_tokens(const Maps& maps, const Args& args, cudaStream_t s) {
+  return launch_pair<MODE>(maps, args, static_cast<int64_t>(args.max_mtiles) * args.n_nt, s);
 }
 
-// Rows of the A box of the token-row modes: the CTA's whole 128-row tile (SM
-// pairs, or no pairing), or the 64-row half each CTA of a multicast pair loads.
-int a_box_rows(const Layout& L, int n_nt) {
-  return (L.T < 256 && n_nt % 2 == 0) ? BM / 2 : BM;
-}
-
-// Token-row modes: SM-pair kernels when every expert segment is a multiple of
-// 256 rows (T >= 256), otherwise CTA pairs sharing A by multicast, or single CTAs.
-template <int MODE>
-moe_status launch_tokens(const Layout& L, const Maps& maps, const Args& args, cudaStream_t s) {
-  if (L.T >= 256)
-    return launch_pair<MODE>(maps, args, static_cast<int64_t>(args.max_mtiles / 2) * args.n_nt, s);
-  return launch_rows<MODE>(maps, args, s);
+// A operand maps of the SM-pair token-row kernel: 128-row box (256-row items)
+// and 64-row box (128-row items).
+bool make_a_maps(CUtensorMap* full, CUtensorMap* half, const void* base, int64_t cols,
+                 int64_t rows) {
+  return make_map(full, base, cols, rows, BM) && make_map(half, base, cols, rows, BM / 2);
 }
 
 Args base_args(const Layout& L, const void* ws) {
   Args a{};
   a.tiles = at<int32_t>(ws, L.tiles);
   a.n_tiles = at<int32_t>(ws, L.n_tiles);
+  a.ptiles = at<int32_t>(ws, L.ptiles);
+  a.n_ptiles = at<int32_t>(ws, L.n_ptiles);
   a.pad_offsets = at<int32_t>(ws, L.pad_offsets);
   a.order = at<int32_t>(ws, L.expert_order);
   a.counts = at<int32_t>(ws, L.counts);
@@ -1037,11 +1026,12 @@ moe_status gemm_router(const Layout& L, const void* ws, const void* x, const voi
 moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const void* wg,
                         const void* wu, void* g, void* u, void* act, cudaStream_t s) {
   Maps m{};
-  if (!make_map(&m.a0, xe, L.H, L.R, a_box_rows(L, L.I / (BN / 2))) ||
-      !make_map(&m.b0, wg, L.H, static_cast<int64_t>(L.E) * L.I, BN / 2) ||
-      !make_map(&m.b1, wu, L.H, static_cast<int64_t>(L.E) * L.I, BN / 2))
+  if (!make_a_maps(&m.a0, &m.a0h, xe, L.H, L.R) ||
+      !make_map(&m.b0, wg, L.H, static_cast<int64_t>(L.E) * L.I, BN / 4) ||
+      !make_map(&m.b1, wu, L.H, static_cast<int64_t>(L.E) * L.I, BN / 4))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
+  m.a1h = m.a0h;
   if (!make_bf16_out_map(&m.o0, g, L.I, L.R) || !make_bf16_out_map(&m.o1, u, L.I, L.R) ||
       !make_bf16_out_map(&m.o2, act, L.I, L.R))
     return MOE_ERR_CUDA;
@@ -1055,7 +1045,7 @@ moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const v
   a.out1 = u;
   a.out2 = act;
   a.store_gu = 1;
-  return launch_tokens<GATE_UP>(L, m, a, s);
+  return launch_tokens<GATE_UP>(m, a, s);
 }
 
 moe_status gemm_gate_up_gather(const Layout& L, const void* ws, const void* x, const void* wg,
@@ -1093,10 +1083,11 @@ moe_status gemm_gate_up_gather(const Layout& L, const void* ws, const void* x, c
 moe_status gemm_down(const Layout& L, const void* ws, const void* act, const void* wd, void* ye,
                      cudaStream_t s) {
   Maps m{};
-  if (!make_map(&m.a0, act, L.I, L.R, a_box_rows(L, L.H / BN)) ||
-      !make_map(&m.b0, wd, L.I, static_cast<int64_t>(L.E) * L.H, L.T >= 256 ? BN / 2 : BN))
+  if (!make_a_maps(&m.a0, &m.a0h, act, L.I, L.R) ||
+      !make_map(&m.b0, wd, L.I, static_cast<int64_t>(L.E) * L.H, BN / 2))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
+  m.a1h = m.a0h;
   m.b1 = m.b0;
   if (!make_bf16_out_map(&m.o0, ye, L.H, L.R)) return MOE_ERR_CUDA;
   Args a = base_args(L, ws);
@@ -1106,16 +1097,17 @@ moe_status gemm_down(const Layout& L, const void* ws, const void* act, const voi
   a.b_rows = L.H;
   a.ld_out = L.H;
   a.out0 = ye;
-  return launch_tokens<DOWN>(L, m, a, s);
+  return launch_tokens<DOWN>(m, a, s);
 }
 
 moe_status gemm_down_dgrad(const Layout& L, const void* ws, const void* dye, const void* g,
                            const void* u, const void* wd, void* dg, void* du, cudaStream_t s) {
   Maps m{};
-  if (!make_map(&m.a0, dye, L.H, L.R, a_box_rows(L, L.I / BN)) ||
+  if (!make_a_maps(&m.a0, &m.a0h, dye, L.H, L.R) ||
       !make_map(&m.b0, wd, L.I, static_cast<int64_t>(L.E) * L.H, 64))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
+  m.a1h = m.a0h;
   m.b1 = m.b0;
   Args a = base_args(L, ws);
   a.n_nt = L.I / BN;
@@ -1127,7 +1119,7 @@ moe_status gemm_down_dgrad(const Layout& L, const void* ws, const void* dye, con
   a.out1 = du;
   a.in0 = g;
   a.in1 = u;
-  return launch_tokens<DACT>(L, m, a, s);
+  return launch_tokens<DACT>(m, a, s);
 }
 
 moe_status gemm_down_wgrad(const Layout& L, const void* ws, const void* dye, const void* act,
@@ -1153,8 +1145,7 @@ moe_status gemm_down_wgrad(const Layout& L, const void* ws, const void* dye, con
 moe_status gemm_gate_up_dgrad(const Layout& L, const void* ws, const void* dg, const void* du,
                               const void* wg, const void* wu, void* dxe, cudaStream_t s) {
   Maps m{};
-  if (!make_map(&m.a0, dg, L.I, L.R, a_box_rows(L, L.H / BN)) ||
-      !make_map(&m.a1, du, L.I, L.R, a_box_rows(L, L.H / BN)) ||
+  if (!make_a_maps(&m.a0, &m.a0h, dg, L.I, L.R) || !make_a_maps(&m.a1, &m.a1h, du, L.I, L.R) ||
       !make_map(&m.b0, wg, L.H, static_cast<int64_t>(L.E) * L.I, 64) ||
       !make_map(&m.b1, wu, L.H, static_cast<int64_t>(L.E) * L.I, 64))
     return MOE_ERR_CUDA;
@@ -1166,7 +1157,7 @@ moe_status gemm_gate_up_dgrad(const Layout& L, const void* ws, const void* dg, c
   a.b_rows = L.I;
   a.ld_out = L.H;
   a.out0 = dxe;
-  return launch_tokens<DXE>(L, m, a, s);
+  return launch_tokens<DXE>(m, a, s);
 }
 
 moe_status gemm_gate_up_wgrad(const Layout& L, const void* ws, const void* dg, const void* du,

@@ -55,6 +55,8 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   L->src_of_row = take(sizeof(int32_t) * R);
   L->tiles = take(sizeof(int32_t) * 3 * (R / kTileM));
   L->n_tiles = take(sizeof(int32_t));
+  L->ptiles = take(sizeof(int32_t) * 3 * (R / kTileM));  // SM-pair items (at most one per tile)
+  L->n_ptiles = take(sizeof(int32_t));
   L->warp_counts = take(sizeof(int32_t) * p->E * std::max<int64_t>(L->n_warps, 1));
   L->expert_order = take(sizeof(int32_t) * p->E);
   L->router_logits = take(sizeof(float) * std::max<int64_t>(p->N, 1) * p->E);

@@ -24,7 +24,8 @@ struct Layout {
   int32_t dtype;          // MOE_BF16 or MOE_MXFP8
   int64_t n_warps;        // schedule warps = ceil(A / kSchedSub)
   // workspace byte offsets
-  size_t err, counts, offsets, pad_offsets, slot_of, src_of_row, tiles, n_tiles, warp_counts,
+  size_t err, counts, offsets, pad_offsets, slot_of, src_of_row, tiles, n_tiles, ptiles, n_ptiles,
+      warp_counts,
       expert_order,
       mx_rh, mx_ri1, mx_ri2, mx_ch, mx_ci1, mx_ci2,  // MXFP8 quantised operands (bf16 values)
       // MXFP8 E4M3 codes + scale chunks (tensor-core path): token rows [R, H] and

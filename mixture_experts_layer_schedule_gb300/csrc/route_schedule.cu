@@ -174,23 +174,38 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int32_t* __restrict__ 
   if (threadIdx.x == 0) counts[e] = carry;
 }
 
-// Kernel 3: offsets, padded offsets, tile list, padding rows.
+// Kernel 3: offsets, padded offsets, tile list, padding rows; optionally the
+// SM-pair item list: each expert's segment cut front to back into 256-row
+// items, the last one 128 rows when the segment holds an odd number of
+// 128-row tiles (ptiles [n][3] = expert, first row, rows; n in *n_ptiles).
 __global__ void __launch_bounds__(1024) sched_final_kernel(const int32_t* __restrict__ counts,
                                                            int E, int T,
                                                            int32_t* __restrict__ offsets,
                                                            int32_t* __restrict__ pad_offsets,
                                                            int32_t* __restrict__ src_of_row,
                                                            int32_t* __restrict__ tiles,
-                                                           int32_t* __restrict__ n_tiles) {
+                                                           int32_t* __restrict__ n_tiles,
+                                                           int32_t* __restrict__ ptiles,
+                                                           int32_t* __restrict__ n_ptiles) {
   __shared__ int32_t sm[32];
   __shared__ int32_t s_pad[kMaxE + 1];
   __shared__ int32_t s_cnt[kMaxE];
   const int e = threadIdx.x;
   const int32_t c = e < E ? counts[e] : 0;
   const int32_t cp = (c + T - 1) / T * T;
-  int32_t tot_c, tot_p;
+  int32_t tot_c, tot_p, tot_i;
   const int32_t off = block_exclusive_scan(c, sm, &tot_c);
   const int32_t poff = block_exclusive_scan(cp, sm, &tot_p);
+  const int32_t n_items = (cp / kTileM + 1) / 2;  // SM-pair items of this segment
+  const int32_t ioff = block_exclusive_scan(n_items, sm, &tot_i);
+  if (ptiles) {
+    for (int32_t j = 0; j < n_items; ++j) {
+      ptiles[3 * (ioff + j) + 0] = e;
+      ptiles[3 * (ioff + j) + 1] = poff + 2 * kTileM * j;
+      ptiles[3 * (ioff + j) + 2] = min(2 * kTileM, cp - 2 * kTileM * j);
+    }
+    if (e == 0) *n_ptiles = tot_i;
+  }
   if (e < E) {
     offsets[e] = off;
     pad_offsets[e] = poff;
@@ -309,7 +324,8 @@ cudaError_t launch_build_schedule_with_scratch(const Layout& L, const int32_t* i
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  sched_final_kernel<<<1, 1024, 0, s>>>(counts, L.E, L.T, offsets, pad, src, tiles, n_tiles);
+  sched_final_kernel<<<1, 1024, 0, s>>>(counts, L.E, L.T, offsets, pad, src, tiles, n_tiles,
+                                        at<int32_t>(ws, L.ptiles), at<int32_t>(ws, L.n_ptiles));
   note_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess || L.n_warps == 0) return e;
@@ -402,7 +418,8 @@ extern "C" moe_status moe_build_schedule_noalloc(const moe_problem* p, const int
   }
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   sched_final_kernel<<<1, 1024, 0, s>>>(out->counts, L.E, L.T, out->offsets, out->pad_offsets,
-                                        out->src_of_row, out->tiles, out->n_tiles);
+                                        out->src_of_row, out->tiles, out->n_tiles, nullptr,
+                                        nullptr);
   note_launch();
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   if (L.n_warps == 0) return MOE_OK;
