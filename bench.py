@@ -74,13 +74,12 @@ def dist_env():
 GEMM_SRC = ("mixture_experts_layer_schedule_gb300/csrc/grouped_gemm.cu",
             "mixture_experts_layer_schedule_gb300/csrc/moe_common.cuh")
 MEASURED_TRAFFIC = {
-    "src_sha256": "358267911035ed314553f1572f090d46dae56cb26c26550ef34319c6bc4a3d3f",
+    "src_sha256": "72d50f6a654669987dda0fd1bbbc94947eedf653d6bfa6d7382fffb62d388aa4",
     "workload": "skewed_fwd_bwd_N16384_H4096_I1536_E128_k8_zipf1.2",
-    "bytes": {"gate_up": 5.0780e9 + 1.3023e9, "down": 2.0481e9 + 1.1501e9,
-              "down_dgrad": 3.9648e9 + 0.8519e9, "down_wgrad": 2.3490e9 + 3.1561e9,
-              "gate_up_dgrad": 4.4882e9 + 1.1556e9, "gate_up_wgrad": 5.0709e9 + 6.3776e9},
+    "bytes": {"gate_up": 5.0185e9 + 1.2999e9, "down": 2.0361e9 + 1.1493e9,
+              "down_dgrad": 3.9674e9 + 0.8551e9, "down_wgrad": 2.3616e9 + 3.1569e9,
+              "gate_up_dgrad": 4.4326e9 + 1.1576e9, "gate_up_wgrad": 5.0993e9 + 6.3781e9},
 }
-
 
 def measured_traffic(workload_name, phase):
     import hashlib
