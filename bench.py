@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--sweep-T", action="store_true",
                     help="the minibatch knob sweep: run the workload at minibatch_rows T = 128, "
                          "256, 512, 1024 and print one line with every T's result and the best")
+    ap.add_argument("--overlap", action="store_true",
+                    help="bf16 backward through moe_backward_overlap (the reverse-combine run "
+                         "by side warps of the down data-gradient GEMM), timed as one phase")
     ap.add_argument("--inference", action="store_true",
                     help="forward-only workloads: time the context-free forward (dispatch "
                          "fused into gate/up) instead of the training forward")
@@ -240,6 +243,8 @@ def run_ours(args, ws_, rank, local, shape=None):
         phases = ["route", "schedule", "gate_up_gather", "down", "combine"]
     if mx:  # MXFP8: the composite passes (they add the activation quantisations)
         phases = ["route", "schedule", "forward"] + (["backward"] if backward else [])
+    elif backward and args.overlap:
+        phases += ["backward"]
     elif backward:
         phases += ["reverse_combine", "down_dgrad", "down_wgrad", "gate_up_dgrad",
                    "gate_up_wgrad", "reverse_dispatch"]
@@ -274,9 +279,9 @@ def run_ours(args, ws_, rank, local, shape=None):
         "reverse_dispatch": lambda: _lib.moe_reverse_dispatch(p, wsb, dyxe, g.dx),
         "forward": lambda: _lib.moe_forward(p, inp["x"], w, layer.topk_w, layer.y, layer.saved,
                                             wsb),
-        "backward": lambda: _lib.moe_backward(p, layer.saved, wfull, layer.topk_w, inp["dy"],
-                                              g.dx, g.dw_gate, g.dw_up, g.dw_down, g.d_topk_w,
-                                              wsb),
+        "backward": lambda: (_lib.moe_backward_overlap if args.overlap else _lib.moe_backward)(
+            p, layer.saved, wfull, layer.topk_w, inp["dy"], g.dx, g.dw_gate, g.dw_up, g.dw_down,
+            g.d_topk_w, wsb),
     }
 
     def step(events=None):
@@ -353,7 +358,8 @@ def run_ours(args, ws_, rank, local, shape=None):
                 return
             lay.forward(din["x"], inp["wg"], inp["wu"], inp["wd"], mx=mxw)
             if backward:
-                lay.backward(din["dy"], inp["wg"], inp["wu"], inp["wd"], bwd=wbwd, mx=mxw)
+                lay.backward(din["dy"], inp["wg"], inp["wu"], inp["wd"], bwd=wbwd, mx=mxw,
+                             overlap=args.overlap)
                 lay.router_backward(inp["w_router"], dwr)
         elif inference:
             lay.route(din["logits"], inp["bias"])
@@ -361,7 +367,7 @@ def run_ours(args, ws_, rank, local, shape=None):
             lay.forward_inference(din["x"], inp["wg"], inp["wu"], inp["wd"], mx=mxw)
         else:
             lay.step(din["x"], din["logits"], inp["bias"], inp["wg"], inp["wu"], inp["wd"],
-                     din.get("dy"), backward=backward, bwd=wbwd, mx=mxw)
+                     din.get("dy"), backward=backward, bwd=wbwd, mx=mxw, overlap=args.overlap)
 
     def upload(b):
         with torch.cuda.stream(copy_s):
@@ -464,6 +470,9 @@ def run_ours(args, ws_, rank, local, shape=None):
         "clocks": clocks,
         "phases": phase_report,
     }
+    if args.overlap and backward and not mx:
+        rec["config"]["backward"] = ("moe_backward_overlap: reverse-combine run by side warps of "
+                                     "the down data-gradient GEMM")
     return rec, shape, inp
 
 

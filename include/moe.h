@@ -289,6 +289,21 @@ moe_status moe_backward(const moe_problem* p, const void* saved, const moe_weigh
                         const float* topk_w, const void* dy, void* dx, float* dw_gate,
                         float* dw_up, float* dw_down, float* d_topk_w, void* ws, void* stream);
 
+/* moe_backward with the reverse-combine overlapped with the down
+ * data-gradient GEMM ([Clip] key point 2: the backward rounds mirror the
+ * forward ones and reuse one schedule; overlapping a round's data movement
+ * with the next round's GEMM tile by tile): the GEMM kernel's side warps claim
+ * 8-row chunks of the expert-grouped buffer in row order, write dYe and
+ * d_topk_w exactly as moe_reverse_combine does, and count the finished rows
+ * of each 128-row tile; the GEMM loads a tile's dYe only after its count is
+ * complete (bounded wait; on expiry MOE_DEVERR_TIMEOUT). Same arguments and
+ * bit-identical results as moe_backward. MOE_BF16 only; for MOE_MXFP8 it runs
+ * moe_backward (its quantisation sits between the two rounds). */
+moe_status moe_backward_overlap(const moe_problem* p, const void* saved, const moe_weights* w,
+                                const float* topk_w, const void* dy, void* dx, float* dw_gate,
+                                float* dw_up, float* dw_down, float* d_topk_w, void* ws,
+                                void* stream);
+
 /* Router ([Clip] key flowchart, Router node: the router picks the top-k
  * experts of each token from its logits). logits = x . w_router^T with x bf16
  * [N, H], w_router bf16 [E][H] (K contiguous), fp32 accumulation on the

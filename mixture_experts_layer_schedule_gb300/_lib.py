@@ -89,6 +89,7 @@ _SIGS = {
     "moe_expert_gate_up_wgrad": ([c_vp] * 8, c_i32),
     "moe_reverse_dispatch": ([c_vp] * 5, c_i32),
     "moe_backward": ([c_vp] * 12, c_i32),
+    "moe_backward_overlap": ([c_vp] * 12, c_i32),
     "mxfp8_quantize": ([c_vp, c_i64, c_i64, c_vp, c_vp, c_vp], c_i32),
     "mxfp8_qdq": ([c_vp, c_vp, c_i64, c_i64, c_i32, c_vp], c_i32),
     "mxfp8_quantize_mma": ([c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, c_vp], c_i32),
@@ -284,6 +285,13 @@ def moe_backward(p, saved, w: Weights, topk_w, dy, dx, dw_gate, dw_up, dw_down, 
                  stream=None):
     _call("moe_backward", ctypes.byref(p), _ptr(saved), ctypes.byref(w), _ptr(topk_w), _ptr(dy),
           _ptr(dx), _ptr(dw_gate), _ptr(dw_up), _ptr(dw_down), _ptr(d_topk_w), _ptr(ws),
+          _stream(stream))
+
+
+def moe_backward_overlap(p, saved, w: Weights, topk_w, dy, dx, dw_gate, dw_up, dw_down, d_topk_w,
+                         ws, stream=None):
+    _call("moe_backward_overlap", ctypes.byref(p), _ptr(saved), ctypes.byref(w), _ptr(topk_w),
+          _ptr(dy), _ptr(dx), _ptr(dw_gate), _ptr(dw_up), _ptr(dw_down), _ptr(d_topk_w), _ptr(ws),
           _stream(stream))
 
 

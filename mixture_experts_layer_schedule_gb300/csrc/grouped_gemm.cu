@@ -88,6 +88,18 @@ struct Args {
   int store_gu;                // GATE_UP(_GATHER): also store G and U
   void *out0, *out1, *out2;
   const void *in0, *in1;
+  // DACT with the reverse-combine fused in (rc_* set): dYe[row] = w[a] * dY[a / k]
+  // and dw[a] = <dY[a / k], Ye[row]> for every row (a = src_of_row[row]),
+  // claimed by side warps 8 rows at a time through rc_sync[0]; rc_sync[1 + tile]
+  // counts the finished rows of each 128-row tile.
+  const uint4* rc_dy;
+  const uint4* rc_ye;
+  const float* rc_w;
+  uint4* rc_dye;
+  float* rc_dw;
+  int32_t* rc_sync;
+  int hv;     // H / 8
+  int64_t A;  // assignments
 };
 
 template <int MODE>
@@ -637,6 +649,103 @@ __device__ __forceinline__ int64_t total_pair_tiles(const Args& a) {
   }
 }
 
+// Reverse-combine fused into the down-dgrad GEMM: side warps claim 8-row
+// chunks of the expert-grouped buffer in row order (the order the GEMM's pair
+// items consume them) and publish per-tile row counts; the GEMM producer waits
+// for its tile's count before loading dYe. Same arithmetic and summation
+// order as reverse_combine_kernel (256 threads per token: thread i covers
+// vectors i, i + 256, ...; per-warp shuffle trees; warp sums in order).
+constexpr int kRcWarps = 4, kRcRows = 8;
+
+__device__ __forceinline__ void reverse_combine_rows(const Args& a, int lane) {
+  int32_t* ticket = a.rc_sync;
+  int32_t* done = a.rc_sync + 1;
+  int64_t rows = a.pad_offsets[a.E];
+  rows = rows < 0 ? 0 : (rows > a.rows ? a.rows : rows);
+  const int32_t n_chunks = static_cast<int32_t>(rows / kRcRows);
+  while (true) {
+    int32_t c = 0;
+    if (lane == 0) c = atomicAdd(ticket, 1);
+    c = __shfl_sync(0xffffffffu, c, 0);
+    if (c >= n_chunks) break;
+    for (int r = 0; r < kRcRows; ++r) {
+      const int64_t row = static_cast<int64_t>(c) * kRcRows + r;
+      const int32_t as = a.src_of_row[row];
+      uint4* drow = a.rc_dye + row * a.hv;
+      if (as < 0 || as >= a.A) {  // padding row
+        for (int v = lane; v < a.hv; v += 32) drow[v] = make_uint4(0u, 0u, 0u, 0u);
+        continue;
+      }
+      const float wj = a.rc_w[as];
+      const uint4* gy = a.rc_dy + static_cast<int64_t>(as / a.k) * a.hv;
+      const uint4* ey = a.rc_ye + row * a.hv;
+      float part[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+      for (int base = 0; base < a.hv; base += 256) {
+        uint4 gv[8], ev[8];  // all loads of the step first: 16 in flight per lane
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int v = base + 32 * q + lane;
+          if (v < a.hv) {
+            gv[q] = __ldg(gy + v);
+            ev[q] = __ldg(ey + v);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int v = base + 32 * q + lane;
+          if (v < a.hv) {
+            float g[8], e8[8], sc[8];
+            unpack8(gv[q], g);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sc[i] = wj * g[i];
+            drow[v] = pack8(sc);
+            unpack8(ev[q], e8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) part[q] = fmaf(g[i], e8[i], part[q]);
+          }
+        }
+      }
+      float tot = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float p = part[q];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) p += __shfl_down_sync(0xffffffffu, p, off);
+        tot += p;
+      }
+      if (lane == 0) a.rc_dw[as] = tot;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // rows seen by the TMA loads
+      __threadfence();
+      atomicAdd(done + (static_cast<int64_t>(c) * kRcRows) / BM, kRcRows);
+    }
+  }
+}
+
+// Bounded wait until *p >= target (acquire), then order the caller's later
+// TMA loads after it.
+__device__ __forceinline__ bool wait_count(const int32_t* p, int32_t target, volatile int* abort,
+                                           int32_t* err) {
+  const long long t0 = clock64();
+  while (true) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return true;
+    }
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitBudgetCycles) {
+      set_dev_error(err, MOE_DEVERR_TIMEOUT);
+      *abort = 1;
+      return false;
+    }
+    __nanosleep(100);
+  }
+}
+
 template <int MODE>
 __device__ __forceinline__ void issue_loads_pair(const Maps& m, const Args& a, const TileInfo& ti,
                                                  int kb, uint8_t* sA, uint8_t* sB, uint32_t bar,
@@ -675,9 +784,10 @@ __device__ __forceinline__ void issue_loads_pair(const Maps& m, const Args& a, c
   }
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <int MODE, bool RC>
+__global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
     grouped_gemm_pair_kernel(const __grid_constant__ Maps maps, const Args args) {
+  static_assert(!RC || MODE == DACT, "the reverse-combine is fused into DACT only");
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kPairStages], empty_bar[kPairStages], tfull_bar[2], tempty_bar[2],
       drain_bar;
@@ -730,6 +840,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int64_t t;
       for (TileSeq q(first, stride, total, kInterleave); ok && q.next(t);) {
         const TileInfo ti = decode_pair_tile<MODE>(args, t, crank);
+        if constexpr (RC) {  // this CTA's dYe rows come from the side warps
+          if (ti.nkb > 0 && !wait_count(args.rc_sync + 1 + ti.row0 / BM, BM, abortp, args.err)) {
+            ok = false;
+            break;
+          }
+        }
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, args.err)) { ok = false; break; }
           uint8_t* sA = smem + stage * kPairStageBytes;
@@ -789,6 +905,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       umma_commit_pair(&drain_bar);
       wait_drain(&drain_bar, 0, args.err);
     }
+  } else if (warp >= 6) {
+    // ---------------- reverse-combine side warps 6.. (fused DACT only) ----------------
+    if constexpr (RC) reverse_combine_rows(args, lane);
   } else {
     // ---------------- epilogue warps 2..5 (both CTAs) ----------------
     const int quad = warp & 3;
@@ -926,7 +1045,7 @@ moe_status launch(const Maps& maps, const Args& args, int64_t units, cudaStream_
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-template <int MODE>
+template <int MODE, bool RC = false>
 moe_status launch_pair(const Maps& maps, const Args& args, int64_t units, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -937,19 +1056,19 @@ moe_status launch_pair(const Maps& maps, const Args& args, int64_t units, cudaSt
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * clusters);
-    cfg.blockDim = dim3(kGemmThreads);
+    cfg.blockDim = dim3(kGemmThreads + (RC ? 32 * kRcWarps : 0));
     cfg.dynamicSmemBytes = kPairSmemBytes;
     cfg.attrs = at;
     cfg.numAttrs = 1;
   };
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<MODE>,
+    attr_err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<MODE, RC>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
     if (attr_err != cudaSuccess) return;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
     config(cfg, at, 64);
-    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_pair_kernel<MODE>, &cfg);
+    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_pair_kernel<MODE, RC>, &cfg);
     if (attr_err == cudaSuccess && max_clusters <= 0) attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
@@ -958,7 +1077,7 @@ moe_status launch_pair(const Maps& maps, const Args& args, int64_t units, cudaSt
   cudaLaunchAttribute at[1];
   config(cfg, at, static_cast<int>(std::min<int64_t>(max_clusters, units)));
   cfg.stream = s;
-  if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, maps, args) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE, RC>, maps, args) != cudaSuccess)
     return MOE_ERR_CUDA;
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -1102,6 +1221,13 @@ moe_status gemm_down(const Layout& L, const void* ws, const void* act, const voi
 
 moe_status gemm_down_dgrad(const Layout& L, const void* ws, const void* dye, const void* g,
                            const void* u, const void* wd, void* dg, void* du, cudaStream_t s) {
+  return gemm_down_dgrad_rc(L, ws, nullptr, nullptr, nullptr, dye, nullptr, g, u, wd, dg, du, s);
+}
+
+moe_status gemm_down_dgrad_rc(const Layout& L, const void* ws, const void* dy, const void* ye,
+                              const float* topk_w, const void* dye, float* d_topk_w,
+                              const void* g, const void* u, const void* wd, void* dg, void* du,
+                              cudaStream_t s) {
   Maps m{};
   if (!make_a_maps(&m.a0, &m.a0h, dye, L.H, L.R) ||
       !make_map(&m.b0, wd, L.I, static_cast<int64_t>(L.E) * L.H, 64))
@@ -1119,7 +1245,25 @@ moe_status gemm_down_dgrad(const Layout& L, const void* ws, const void* dye, con
   a.out1 = du;
   a.in0 = g;
   a.in1 = u;
-  return launch_tokens<DACT>(m, a, s);
+  const int64_t units = static_cast<int64_t>(a.max_mtiles) * a.n_nt;
+  if (!dy) return launch_pair<DACT>(m, a, units, s);
+  // fused reverse-combine: dYe and dw come from the kernel's side warps
+  a.rc_dy = static_cast<const uint4*>(dy);
+  a.rc_ye = static_cast<const uint4*>(ye);
+  a.rc_w = topk_w;
+  a.rc_dye = static_cast<uint4*>(const_cast<void*>(dye));
+  a.rc_dw = d_topk_w;
+  a.rc_sync = const_cast<int32_t*>(at<int32_t>(ws, L.rc_sync));
+  a.src_of_row = at<int32_t>(ws, L.src_of_row);
+  a.k = L.k;
+  a.hv = L.H / 8;
+  a.A = L.A;
+  if (cudaMemsetAsync(a.rc_sync, 0, sizeof(int32_t) * (1 + L.R / BM), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  // assignments without a row (rejected expert ids) keep dw = 0, as in the unfused kernel
+  if (L.A > 0 && cudaMemsetAsync(d_topk_w, 0, sizeof(float) * L.A, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return launch_pair<DACT, true>(m, a, std::max<int64_t>(units, 1), s);
 }
 
 moe_status gemm_down_wgrad(const Layout& L, const void* ws, const void* dye, const void* act,

@@ -57,6 +57,7 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   L->n_tiles = take(sizeof(int32_t));
   L->ptiles = take(sizeof(int32_t) * 3 * (R / kTileM));  // SM-pair items (at most one per tile)
   L->n_ptiles = take(sizeof(int32_t));
+  L->rc_sync = take(sizeof(int32_t) * (1 + R / kTileM));
   L->warp_counts = take(sizeof(int32_t) * p->E * std::max<int64_t>(L->n_warps, 1));
   L->expert_order = take(sizeof(int32_t) * p->E);
   L->router_logits = take(sizeof(float) * std::max<int64_t>(p->N, 1) * p->E);
@@ -213,6 +214,82 @@ moe_status mx_backward_gemms(const Layout& L, void* ws, const moe_mxfp8_weights&
   MOE_TRY(gemm_mx_gate_up_dgrad(L, ws, ri, ri2, mx.gate_t, mx.up_t, dyxe, s));
   MOE_TRY(quantize_forms(v.xe, L.R, L.H, nullptr, &th, s));
   return gemm_mx_gate_up_wgrad(L, ws, ti, ti2, th, dw_gate, dw_up, s);
+}
+
+}  // namespace
+
+namespace {
+
+moe_status backward_impl(const moe_problem* p, const void* saved, const moe_weights* w,
+                         const float* topk_w, const void* dy, void* dx, float* dw_gate,
+                         float* dw_up, float* dw_down, float* d_topk_w, void* ws, void* stream,
+                         bool overlap) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  moe_saved_view v;
+  MOE_TRY(moe_saved_layout(p, const_cast<void*>(saved), &v));
+  void* dyxe = at<char>(ws, L.dyxe);
+  void* dg = at<char>(ws, L.dg);
+  void* du = at<char>(ws, L.du);
+  if (p->dtype == MOE_MXFP8 && w && w->mx && w->mx->gate_t.q) {
+    if (!mx_backward_ok(w) || !aligned(dw_gate, 16) || !aligned(dw_up, 16) ||
+        !aligned(dw_down, 16))
+      return MOE_ERR_INVALID_ARG;
+    MOE_TRY(moe_reverse_combine(p, ws, dy, v.ye, topk_w, dyxe, d_topk_w, stream));
+    MOE_TRY(mx_backward_gemms(L, ws, *w->mx, v, dyxe, dg, du, dw_gate, dw_up, dw_down,
+                              S(stream)));
+    return moe_reverse_dispatch(p, ws, dyxe, dx, stream);
+  }
+  if (p->dtype == MOE_MXFP8) {
+    // Each GEMM operand quantised along that GEMM's K: rows of dYe along H,
+    // rows of dG/dU along I; for the weight gradients both operands along the
+    // token axis (blocks of 32 rows; expert segments start at multiples of T).
+    // The backward weight pointers hold Wd quantised along H, Wg/Wu along I.
+    if (!w || !w->w_gate_bwd || !w->w_up_bwd || !w->w_down_bwd) return MOE_ERR_INVALID_ARG;
+    moe_weights wb = *w;
+    wb.w_gate = w->w_gate_bwd;
+    wb.w_up = w->w_up_bwd;
+    wb.w_down = w->w_down_bwd;
+    void* rh = at<char>(ws, L.mx_rh);
+    void* ri1 = at<char>(ws, L.mx_ri1);
+    void* ri2 = at<char>(ws, L.mx_ri2);
+    void* ch = at<char>(ws, L.mx_ch);
+    void* ci1 = at<char>(ws, L.mx_ci1);
+    void* ci2 = at<char>(ws, L.mx_ci2);
+    MOE_TRY(moe_reverse_combine(p, ws, dy, v.ye, topk_w, dyxe, d_topk_w, stream));
+    MOE_TRY(mxfp8_qdq(dyxe, rh, L.R, L.H, 0, stream));
+    MOE_TRY(moe_expert_down_dgrad(p, ws, rh, v.g, v.u, &wb, dg, du, stream));
+    MOE_TRY(mxfp8_qdq(dyxe, ch, L.R, L.H, 1, stream));
+    MOE_TRY(mxfp8_qdq(v.act, ci1, L.R, L.I, 1, stream));
+    MOE_TRY(moe_expert_down_wgrad(p, ws, ch, ci1, dw_down, stream));
+    MOE_TRY(mxfp8_qdq(dg, ri1, L.R, L.I, 0, stream));
+    MOE_TRY(mxfp8_qdq(du, ri2, L.R, L.I, 0, stream));
+    MOE_TRY(moe_expert_gate_up_dgrad(p, ws, ri1, ri2, &wb, dyxe, stream));
+    MOE_TRY(mxfp8_qdq(dg, ci1, L.R, L.I, 1, stream));
+    MOE_TRY(mxfp8_qdq(du, ci2, L.R, L.I, 1, stream));
+    MOE_TRY(mxfp8_qdq(v.xe, ch, L.R, L.H, 1, stream));
+    MOE_TRY(moe_expert_gate_up_wgrad(p, ws, ci1, ci2, ch, dw_gate, dw_up, stream));
+    return moe_reverse_dispatch(p, ws, dyxe, dx, stream);
+  }
+  if (overlap) {
+    // reverse-combine (dYe, d_topk_w) run by side warps of the down
+    // data-gradient GEMM, which consumes dYe tile by tile as it is finished
+    if (!aligned(v.ye, 16) || !aligned(dyxe, 16) || !weights_ok(w) || !aligned(dg, 16) ||
+        !aligned(du, 16))
+      return MOE_ERR_INVALID_ARG;
+    if (L.N > 0 && (!aligned(dy, 16) || !aligned(topk_w, 4) || !aligned(d_topk_w, 4)))
+      return MOE_ERR_INVALID_ARG;
+    MOE_TRY(gemm_down_dgrad_rc(L, ws, dy, v.ye, topk_w, dyxe, d_topk_w, v.g, v.u, w->w_down, dg,
+                               du, S(stream)));
+  } else {
+    MOE_TRY(moe_reverse_combine(p, ws, dy, v.ye, topk_w, dyxe, d_topk_w, stream));
+    MOE_TRY(moe_expert_down_dgrad(p, ws, dyxe, v.g, v.u, w, dg, du, stream));
+  }
+  MOE_TRY(moe_expert_down_wgrad(p, ws, dyxe, v.act, dw_down, stream));
+  // dXe overwrites dYe in the shared buffer: dYe's last reader ran above.
+  MOE_TRY(moe_expert_gate_up_dgrad(p, ws, dg, du, w, dyxe, stream));
+  MOE_TRY(moe_expert_gate_up_wgrad(p, ws, dg, du, v.xe, dw_gate, dw_up, stream));
+  return moe_reverse_dispatch(p, ws, dyxe, dx, stream);
 }
 
 }  // namespace
@@ -482,60 +559,16 @@ moe_status moe_reverse_dispatch(const moe_problem* p, const void* ws, const void
 moe_status moe_backward(const moe_problem* p, const void* saved, const moe_weights* w,
                         const float* topk_w, const void* dy, void* dx, float* dw_gate,
                         float* dw_up, float* dw_down, float* d_topk_w, void* ws, void* stream) {
-  Layout L;
-  MOE_TRY(prep(p, ws, &L));
-  moe_saved_view v;
-  MOE_TRY(moe_saved_layout(p, const_cast<void*>(saved), &v));
-  void* dyxe = at<char>(ws, L.dyxe);
-  void* dg = at<char>(ws, L.dg);
-  void* du = at<char>(ws, L.du);
-  if (p->dtype == MOE_MXFP8 && w && w->mx && w->mx->gate_t.q) {
-    if (!mx_backward_ok(w) || !aligned(dw_gate, 16) || !aligned(dw_up, 16) ||
-        !aligned(dw_down, 16))
-      return MOE_ERR_INVALID_ARG;
-    MOE_TRY(moe_reverse_combine(p, ws, dy, v.ye, topk_w, dyxe, d_topk_w, stream));
-    MOE_TRY(mx_backward_gemms(L, ws, *w->mx, v, dyxe, dg, du, dw_gate, dw_up, dw_down,
-                              S(stream)));
-    return moe_reverse_dispatch(p, ws, dyxe, dx, stream);
-  }
-  if (p->dtype == MOE_MXFP8) {
-    // Each GEMM operand quantised along that GEMM's K: rows of dYe along H,
-    // rows of dG/dU along I; for the weight gradients both operands along the
-    // token axis (blocks of 32 rows; expert segments start at multiples of T).
-    // The backward weight pointers hold Wd quantised along H, Wg/Wu along I.
-    if (!w || !w->w_gate_bwd || !w->w_up_bwd || !w->w_down_bwd) return MOE_ERR_INVALID_ARG;
-    moe_weights wb = *w;
-    wb.w_gate = w->w_gate_bwd;
-    wb.w_up = w->w_up_bwd;
-    wb.w_down = w->w_down_bwd;
-    void* rh = at<char>(ws, L.mx_rh);
-    void* ri1 = at<char>(ws, L.mx_ri1);
-    void* ri2 = at<char>(ws, L.mx_ri2);
-    void* ch = at<char>(ws, L.mx_ch);
-    void* ci1 = at<char>(ws, L.mx_ci1);
-    void* ci2 = at<char>(ws, L.mx_ci2);
-    MOE_TRY(moe_reverse_combine(p, ws, dy, v.ye, topk_w, dyxe, d_topk_w, stream));
-    MOE_TRY(mxfp8_qdq(dyxe, rh, L.R, L.H, 0, stream));
-    MOE_TRY(moe_expert_down_dgrad(p, ws, rh, v.g, v.u, &wb, dg, du, stream));
-    MOE_TRY(mxfp8_qdq(dyxe, ch, L.R, L.H, 1, stream));
-    MOE_TRY(mxfp8_qdq(v.act, ci1, L.R, L.I, 1, stream));
-    MOE_TRY(moe_expert_down_wgrad(p, ws, ch, ci1, dw_down, stream));
-    MOE_TRY(mxfp8_qdq(dg, ri1, L.R, L.I, 0, stream));
-    MOE_TRY(mxfp8_qdq(du, ri2, L.R, L.I, 0, stream));
-    MOE_TRY(moe_expert_gate_up_dgrad(p, ws, ri1, ri2, &wb, dyxe, stream));
-    MOE_TRY(mxfp8_qdq(dg, ci1, L.R, L.I, 1, stream));
-    MOE_TRY(mxfp8_qdq(du, ci2, L.R, L.I, 1, stream));
-    MOE_TRY(mxfp8_qdq(v.xe, ch, L.R, L.H, 1, stream));
-    MOE_TRY(moe_expert_gate_up_wgrad(p, ws, ci1, ci2, ch, dw_gate, dw_up, stream));
-    return moe_reverse_dispatch(p, ws, dyxe, dx, stream);
-  }
-  MOE_TRY(moe_reverse_combine(p, ws, dy, v.ye, topk_w, dyxe, d_topk_w, stream));
-  MOE_TRY(moe_expert_down_dgrad(p, ws, dyxe, v.g, v.u, w, dg, du, stream));
-  MOE_TRY(moe_expert_down_wgrad(p, ws, dyxe, v.act, dw_down, stream));
-  // dXe overwrites dYe in the shared buffer: dYe's last reader ran above.
-  MOE_TRY(moe_expert_gate_up_dgrad(p, ws, dg, du, w, dyxe, stream));
-  MOE_TRY(moe_expert_gate_up_wgrad(p, ws, dg, du, v.xe, dw_gate, dw_up, stream));
-  return moe_reverse_dispatch(p, ws, dyxe, dx, stream);
+  return backward_impl(p, saved, w, topk_w, dy, dx, dw_gate, dw_up, dw_down, d_topk_w, ws, stream,
+                       false);
+}
+
+moe_status moe_backward_overlap(const moe_problem* p, const void* saved, const moe_weights* w,
+                                const float* topk_w, const void* dy, void* dx, float* dw_gate,
+                                float* dw_up, float* dw_down, float* d_topk_w, void* ws,
+                                void* stream) {
+  return backward_impl(p, saved, w, topk_w, dy, dx, dw_gate, dw_up, dw_down, d_topk_w, ws, stream,
+                       p && p->dtype == MOE_BF16);
 }
 
 moe_status mxfp8_qdq(const void* src_bf16, void* dst_bf16, int64_t rows, int64_t cols, int axis,

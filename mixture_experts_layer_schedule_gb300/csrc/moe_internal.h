@@ -32,6 +32,7 @@ struct Layout {
       // [R, I] x2 quantised along K; transposed [H, R] and [I, R] x2 along tokens
       mq_rh, ms_rh, mq_ri, ms_ri, mq_ri2, ms_ri2, mq_th, ms_th, mq_ti, ms_ti, mq_ti2, ms_ti2,
       router_logits, router_dz, router_partial,  // router: logits scratch [N,E], dz [A], tile partials
+      rc_sync,  // fused reverse-combine: chunk ticket + finished rows per 128-row tile
       dyxe, dg, du, ws_bytes;
   // forward-context byte offsets
   size_t xe, g, u, act, ye, saved_bytes;
@@ -86,6 +87,13 @@ moe_status gemm_down(const Layout& L, const void* ws, const void* act, const voi
                      cudaStream_t s);
 moe_status gemm_down_dgrad(const Layout& L, const void* ws, const void* dye, const void* g,
                            const void* u, const void* wd, void* dg, void* du, cudaStream_t s);
+// DACT with the reverse-combine fused in: dYe (written here, then read by the
+// GEMM) and d_topk_w from dY, Ye and the routing weights, as
+// launch_reverse_combine computes them.
+moe_status gemm_down_dgrad_rc(const Layout& L, const void* ws, const void* dy, const void* ye,
+                              const float* topk_w, const void* dye, float* d_topk_w,
+                              const void* g, const void* u, const void* wd, void* dg, void* du,
+                              cudaStream_t s);
 moe_status gemm_down_wgrad(const Layout& L, const void* ws, const void* dye, const void* act,
                            float* dw_down, cudaStream_t s);
 moe_status gemm_gate_up_dgrad(const Layout& L, const void* ws, const void* dg, const void* du,

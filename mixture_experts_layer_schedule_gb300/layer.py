@@ -159,25 +159,28 @@ class MoELayer:
                                    self.y, self.ws, stream)
         return self.y
 
-    def backward(self, dy, wg, wu, wd, topk_w=None, stream=None, bwd=None, mx=None) -> Grads:
+    def backward(self, dy, wg, wu, wd, topk_w=None, stream=None, bwd=None, mx=None,
+                 overlap=False) -> Grads:
         """MXFP8: mx (MXFP8MMAWeights with the transposed copies) runs the GEMMs on
         the FP8 tensor cores; otherwise bwd (the backward-direction bf16 MXFP8
-        values) feeds bf16 MMAs."""
+        values) feeds bf16 MMAs. overlap: the reverse-combine runs inside the
+        down data-gradient GEMM (moe_backward_overlap; same results)."""
         g = self.grads
         w = _lib.weights(wg, wu, wd, *(bwd if bwd is not None else (None, None, None)),
                          mx=mx.struct if mx is not None else None)
-        _lib.moe_backward(self.p, self.saved, w, self.topk_w if topk_w is None else topk_w, dy,
-                          g.dx, g.dw_gate, g.dw_up, g.dw_down, g.d_topk_w, self.ws, stream)
+        fn = _lib.moe_backward_overlap if overlap else _lib.moe_backward
+        fn(self.p, self.saved, w, self.topk_w if topk_w is None else topk_w, dy, g.dx, g.dw_gate,
+           g.dw_up, g.dw_down, g.d_topk_w, self.ws, stream)
         return g
 
     def step(self, x, logits, bias, wg, wu, wd, dy, stream=None, backward=True, bwd=None,
-             mx=None):
+             mx=None, overlap=False):
         """Route, schedule, forward and (optionally) backward: one layer pass."""
         self.route(logits, bias, stream)
         self.build_schedule(None, stream)
         y = self.forward(x, wg, wu, wd, None, stream, mx=mx)
         if backward:
-            self.backward(dy, wg, wu, wd, None, stream, bwd=bwd, mx=mx)
+            self.backward(dy, wg, wu, wd, None, stream, bwd=bwd, mx=mx, overlap=overlap)
         return y
 
     def device_error(self, stream=None) -> int:

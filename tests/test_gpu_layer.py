@@ -226,3 +226,48 @@ def test_reruns_are_bitwise_identical():
         assert torch.equal(t[:rows], b.saved_tensors()[key][:rows]), key
     for f in ("dx", "dw_gate", "dw_up", "dw_down", "d_topk_w"):
         assert torch.equal(getattr(a.grads, f), getattr(b.grads, f)), f
+
+
+CHAIN_SHAPES = [RAGGED, RAGGED.with_(name="ragged_skewed_T256", minibatch_rows=256),
+                custom_shape(2048, 1024, 512, 16, 4, zipf_s=1.2, name="many_tiles_skewed")]
+
+
+@pytest.mark.parametrize("overlap", [False, True], ids=["moe_backward", "moe_backward_overlap"])
+@pytest.mark.parametrize("shape", CHAIN_SHAPES, ids=lambda s: s.name)
+def test_backward_equals_phase_chain(shape, overlap):
+    """moe_backward, and moe_backward_overlap (the reverse-combine inside the
+    down data-gradient GEMM: side warps publish finished tiles, the GEMM waits
+    for each tile it loads), must equal, bit for bit, the chain of the
+    separate phase entry points on the same inputs."""
+    inp = to_dev(inputs.make_inputs(shape, seed=5, device="cpu"))
+    layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev(),
+                     minibatch_rows=shape.minibatch_rows)
+    layer.step(inp["x"], inp["logits"], inp["bias"], inp["wg"], inp["wu"], inp["wd"], inp["dy"],
+               overlap=overlap)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    p, ws = layer.p, layer.ws
+    w = _lib.weights(inp["wg"], inp["wu"], inp["wd"])
+    sv = layer.saved_tensors()
+    dye = torch.empty_like(sv["xe"])
+    dtw = torch.empty_like(layer.topk_w)
+    dg = torch.empty_like(sv["g"])
+    du = torch.empty_like(sv["u"])
+    dxe = torch.empty_like(sv["xe"])
+    dwg = torch.empty_like(layer.grads.dw_gate)
+    dwu = torch.empty_like(layer.grads.dw_up)
+    dwd = torch.empty_like(layer.grads.dw_down)
+    dx = torch.empty_like(inp["x"])
+    _lib.moe_reverse_combine(p, ws, inp["dy"], sv["ye"], layer.topk_w, dye, dtw)
+    _lib.moe_expert_down_dgrad(p, ws, dye, sv["g"], sv["u"], w, dg, du)
+    _lib.moe_expert_down_wgrad(p, ws, dye, sv["act"], dwd)
+    _lib.moe_expert_gate_up_dgrad(p, ws, dg, du, w, dxe)
+    _lib.moe_expert_gate_up_wgrad(p, ws, dg, du, sv["xe"], dwg, dwu)
+    _lib.moe_reverse_dispatch(p, ws, dxe, dx)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    g = layer.grads
+    for name, got, want in (("d_topk_w", g.d_topk_w, dtw), ("dx", g.dx, dx),
+                            ("dw_gate", g.dw_gate, dwg), ("dw_up", g.dw_up, dwu),
+                            ("dw_down", g.dw_down, dwd)):
+        assert torch.equal(got, want), name
