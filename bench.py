@@ -77,12 +77,13 @@ def dist_env():
 GEMM_SRC = ("mixture_experts_layer_schedule_gb300/csrc/grouped_gemm.cu",
             "mixture_experts_layer_schedule_gb300/csrc/moe_common.cuh")
 MEASURED_TRAFFIC = {
-    "src_sha256": "72d50f6a654669987dda0fd1bbbc94947eedf653d6bfa6d7382fffb62d388aa4",
+    "src_sha256": "2301a7bb325c6698c9895c28cc230cb22f83359308d643b7b1967308e0b53052",
     "workload": "skewed_fwd_bwd_N16384_H4096_I1536_E128_k8_zipf1.2",
-    "bytes": {"gate_up": 5.0185e9 + 1.2999e9, "down": 2.0361e9 + 1.1493e9,
-              "down_dgrad": 3.9674e9 + 0.8551e9, "down_wgrad": 2.3616e9 + 3.1569e9,
-              "gate_up_dgrad": 4.4326e9 + 1.1576e9, "gate_up_wgrad": 5.0993e9 + 6.3781e9},
+    "bytes": {"gate_up": 5.2534e9 + 1.3010e9, "down": 2.0415e9 + 1.1489e9,
+              "down_dgrad": 4.0517e9 + 0.8554e9, "down_wgrad": 2.5610e9 + 3.1564e9,
+              "gate_up_dgrad": 4.5056e9 + 1.1577e9, "gate_up_wgrad": 5.9166e9 + 6.3780e9},
 }
+
 
 def measured_traffic(workload_name, phase):
     import hashlib
