@@ -749,6 +749,98 @@ __device__ __forceinline__ bool wait_count(const int32_t* p, int32_t target, vol
   }
 }
 
+// Work items of one CTA pair: a run of k-blocks [kb0, kb1) of tile t on
+// accumulator acc, `commit` when it ends the tile.
+// The producer, the MMA issuer and the epilogue walk the same items.
+//  * Token-row modes: whole tiles in order on alternating accumulators.
+//  * WGRAD: the pair's tiles come alternately from the front (largest
+//    experts, long K) and the back (smallest experts, short K) of the
+//    size-ordered list, on alternating accumulators, so the MMAs of one tile
+//    overlap the epilogue (fp32 stores) of the previous. A front tile of more
+//    than kWgChunkMin k-blocks is issued in chunks of kWgChunk with one whole back
+//    tile, on the other accumulator, after each chunk, and the next front
+//    tile's first chunk comes before the next back tile: the short tiles'
+//    epilogues then run under the long tile's MMAs instead of the MMAs
+//    waiting for them.
+constexpr int kWgChunk = 24, kWgChunkMin = 48;
+
+struct PairItem {
+  int64_t t;
+  int acc, kb0, kb1;
+  bool commit;
+};
+
+template <int MODE>
+struct PairPlan {
+  int64_t fi, bi, half, total, stride;
+  int64_t lt;         // open front tile
+  TileInfo lti;       // its decoded tile
+  int lkb, lnk, la;   // its next k-block, k-blocks, accumulator
+  int nxt;            // accumulator of the next tile opened without a front tile open
+  bool has_l, chunked, short_next;
+  __device__ __forceinline__ PairPlan(int64_t first, int64_t stride_, int64_t total_)
+      : fi(first), bi(first), half(MODE == WGRAD ? (total_ + 1) / 2 : total_), total(total_),
+        stride(stride_), lt(0), lkb(0), lnk(0), la(0), nxt(0), has_l(false), chunked(false),
+        short_next(false) {}
+
+  __device__ __forceinline__ int take_acc() {
+    const int a = nxt;
+    nxt ^= 1;
+    return a;
+  }
+
+  // The next item and its decoded tile (decoded once per tile).
+  __device__ __forceinline__ bool next(PairItem& it, TileInfo& ti, const Args& a, int crank) {
+    if constexpr (MODE != WGRAD) {
+      if (fi >= total) return false;
+      it.t = fi;
+      fi += stride;
+      ti = decode_pair_tile<MODE>(a, it.t, crank);
+      it.acc = take_acc();
+      it.kb0 = 0;
+      it.kb1 = ti.nkb;
+      it.commit = true;
+      return true;
+    } else {
+      const bool f_ok = fi < half, b_ok = bi < total - half;
+      if ((short_next || (!has_l && !f_ok)) && b_ok) {  // a whole back tile
+        it.t = total - 1 - bi;
+        bi += stride;
+        ti = decode_pair_tile<MODE>(a, it.t, crank);
+        it.acc = has_l ? (la ^ 1) : take_acc();
+        it.kb0 = 0;
+        it.kb1 = ti.nkb;
+        it.commit = true;
+        short_next = false;
+        return true;
+      }
+      if (!has_l) {  // open the next front tile
+        if (!f_ok) return false;
+        lt = fi;
+        fi += stride;
+        lti = decode_pair_tile<MODE>(a, lt, crank);
+        lkb = 0;
+        lnk = lti.nkb;
+        la = take_acc();
+        chunked = lnk > kWgChunkMin;
+        has_l = true;
+      }
+      ti = lti;
+      it.t = lt;
+      it.acc = la;
+      it.kb0 = lkb;
+      it.kb1 = chunked ? min(lkb + kWgChunk, lnk) : lnk;
+      it.commit = it.kb1 == lnk;
+      lkb = it.kb1;
+      if (it.commit) has_l = false;
+      // after a chunk, or a short front tile, a back tile; after a chunked
+      // front tile's last chunk, the next front tile's first chunk
+      short_next = !(it.commit && chunked);
+      return true;
+    }
+  }
+};
+
 template <int MODE>
 __device__ __forceinline__ void issue_loads_pair(const Maps& m, const Args& a, const TileInfo& ti,
                                                  int kb, uint8_t* sA, uint8_t* sB, uint32_t bar,
@@ -830,7 +922,6 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
   const uint32_t tmem_base = tmem_base_slot;
   volatile int* abortp = &abort_flag;
   const int64_t total = total_pair_tiles<MODE>(args);
-  constexpr bool kInterleave = (MODE == WGRAD);
   const int64_t first = blockIdx.x / 2, stride = gridDim.x / 2;
 
   if (warp == 0) {
@@ -840,16 +931,16 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;
       bool ok = true;
-      int64_t t;
-      for (TileSeq q(first, stride, total, kInterleave); ok && q.next(t);) {
-        const TileInfo ti = decode_pair_tile<MODE>(args, t, crank);
+      PairItem it;
+      TileInfo ti;
+      for (PairPlan<MODE> plan(first, stride, total); ok && plan.next(it, ti, args, crank);) {
         if constexpr (RC) {  // this CTA's dYe rows come from the side warps
           if (ti.nkb > 0 && !wait_count(args.rc_sync + 1 + ti.row0 / BM, BM, abortp, args.err)) {
             ok = false;
             break;
           }
         }
-        for (int kb = 0; kb < ti.nkb; ++kb) {
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, args.err)) { ok = false; break; }
           uint8_t* sA = smem + stage * kPairStageBytes;
           // both CTAs' copies: A (64 rows each in a folded item) and half of B
@@ -874,17 +965,20 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
       constexpr uint32_t idesc128 = idesc_bf16(BM, BN, Traits<MODE>::a_mn, Traits<MODE>::b_mn);
       int stage = 0;
       uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
+      uint32_t uses0 = 0u, uses1 = 0u;  // tiles committed on each accumulator
       bool ok = true;
-      int64_t t;
-      for (TileSeq q(first, stride, total, kInterleave); ok && q.next(t);) {
-        const TileInfo ti = decode_pair_tile<MODE>(args, t, crank);
-        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abortp, args.err)) break;
-        tc_fence_after();
+      PairItem it;
+      TileInfo ti;
+      for (PairPlan<MODE> plan(first, stride, total); ok && plan.next(it, ti, args, crank);) {
+        const int acc = it.acc;
+        if (it.kb0 == 0) {  // a new tile: its accumulator's last tile has been read out
+          if (!mbar_wait(&tempty_bar[acc], ((acc ? uses1 : uses0) & 1u) ^ 1u, abortp, args.err))
+            break;
+          tc_fence_after();
+        }
         const uint32_t dtmem = tmem_base + acc * BN;
         const uint32_t idesc = ti.fold ? idesc128 : idesc256;
-        for (int kb = 0; kb < ti.nkb; ++kb) {
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abortp, args.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + stage * kPairStageBytes);
@@ -902,8 +996,10 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
           if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        umma_commit_pair_mc(&tfull_bar[acc], 0x3);  // both halves of the tile are ready
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (it.commit) {
+          umma_commit_pair_mc(&tfull_bar[acc], 0x3);  // both halves of the tile are ready
+          if (acc) ++uses1; else ++uses0;
+        }
       }
       umma_commit_pair(&drain_bar);
       wait_drain(&drain_bar, 0, args.err);
@@ -916,12 +1012,13 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
     const int quad = warp & 3;
     uint8_t* stage_out = smem + kPairStages * kPairStageBytes + (warp - 2) * 2 * kStageOutBytes;
     uint32_t nstore = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    int64_t t;
-    for (TileSeq q(first, stride, total, kInterleave); q.next(t);) {
-      const TileInfo ti = decode_pair_tile<MODE>(args, t, crank);
-      if (!mbar_wait(&tfull_bar[acc], acc_phase, abortp, args.err)) break;
+    uint32_t uses0 = 0u, uses1 = 0u;
+    PairItem it;
+    TileInfo ti;
+    for (PairPlan<MODE> plan(first, stride, total); plan.next(it, ti, args, crank);) {
+      if (!it.commit) continue;
+      const int acc = it.acc;
+      if (!mbar_wait(&tfull_bar[acc], (acc ? uses1 : uses0) & 1u, abortp, args.err)) break;
       tc_fence_after();
       if (ti.skip) {
         if (lane == 0) set_dev_error(args.err, MOE_DEVERR_BAD_EXPERT);
@@ -936,7 +1033,7 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
         if (leader) mbar_arrive(&tempty_bar[acc]);
         else mbar_arrive_cluster(cluster_addr(&tempty_bar[acc], 0));
       }
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (acc) ++uses1; else ++uses0;
     }
     if (lane == 0) bulk_wait_all();
   }
