@@ -271,3 +271,22 @@ def test_backward_equals_phase_chain(shape, overlap):
                             ("dw_gate", g.dw_gate, dwg), ("dw_up", g.dw_up, dwu),
                             ("dw_down", g.dw_down, dwd)):
         assert torch.equal(got, want), name
+
+
+def test_weight_gradient_of_a_dominant_expert():
+    """One expert takes every token (K = 4096 rows = 64 k-blocks): its weight-
+    gradient tiles are long enough to be issued in chunks with the other
+    experts' tiles between them. Gradients match the oracle and reruns are
+    bitwise identical."""
+    shape = custom_shape(4096, 256, 512, 8, 2, name="dominant_expert")
+    inp = inputs.make_inputs(shape, seed=6, device="cpu")
+    inp["bias"] = torch.zeros(8)
+    inp["bias"][0] = 1e4  # always selected
+    a = run_layer(shape, to_dev(inp))
+    assert a.device_error() == 0
+    counts = a.schedule_tensors()["counts"].cpu().numpy()
+    assert counts[0] == shape.N
+    _oracle_compare(shape, inp, a)
+    b = run_layer(shape, to_dev(inp))
+    for f in ("dw_gate", "dw_up", "dw_down"):
+        assert torch.equal(getattr(a.grads, f), getattr(b.grads, f)), f
