@@ -77,11 +77,11 @@ def dist_env():
 GEMM_SRC = ("mixture_experts_layer_schedule_gb300/csrc/grouped_gemm.cu",
             "mixture_experts_layer_schedule_gb300/csrc/moe_common.cuh")
 MEASURED_TRAFFIC = {
-    "src_sha256": "2301a7bb325c6698c9895c28cc230cb22f83359308d643b7b1967308e0b53052",
+    "src_sha256": "9034480f30475debe3a71950d5aabd70dc144465d3a598faa65248de3aa50cb5",
     "workload": "skewed_fwd_bwd_N16384_H4096_I1536_E128_k8_zipf1.2",
-    "bytes": {"gate_up": 5.2534e9 + 1.3010e9, "down": 2.0415e9 + 1.1489e9,
-              "down_dgrad": 4.0517e9 + 0.8554e9, "down_wgrad": 2.5610e9 + 3.1564e9,
-              "gate_up_dgrad": 4.5056e9 + 1.1577e9, "gate_up_wgrad": 5.9166e9 + 6.3780e9},
+    "bytes": {"gate_up": 4.9867e9 + 1.2999e9, "down": 2.0371e9 + 1.1496e9,
+              "down_dgrad": 3.9952e9 + 0.8550e9, "down_wgrad": 2.4752e9 + 3.1562e9,
+              "gate_up_dgrad": 4.4480e9 + 1.1576e9, "gate_up_wgrad": 4.9630e9 + 6.3775e9},
 }
 
 
