@@ -166,6 +166,9 @@ LAYER_SHAPES = [
     custom_shape(300, 512, 768, 16, 4, zipf_s=1.2, name="ragged_skewed_T256", T=256),
     custom_shape(129, 256, 512, 4, 2, name="one_over_tile_T1024", T=1024),
     custom_shape(64, 1024, 512, 32, 8, name="many_empty_experts_T512", T=512),
+    custom_shape(1, 256, 256, 4, 1, name="one_token_k1"),
+    custom_shape(100, 256, 512, 4, 4, name="k_equals_E"),
+    custom_shape(77, 512, 256, 1, 1, name="single_expert"),
 ]
 
 
@@ -290,3 +293,19 @@ def test_weight_gradient_of_a_dominant_expert():
     b = run_layer(shape, to_dev(inp))
     for f in ("dw_gate", "dw_up", "dw_down"):
         assert torch.equal(getattr(a.grads, f), getattr(b.grads, f)), f
+
+
+def test_empty_batch():
+    """N = 0: every phase is a no-op; the weight gradients are written as zeros."""
+    shape = custom_shape(0, 256, 512, 8, 2, name="empty")
+    inp = to_dev(inputs.make_inputs(custom_shape(4, 256, 512, 8, 2), seed=7, device="cpu"))
+    layer = MoELayer(0, 256, 512, 8, 2, device=dev())
+    for t in (layer.grads.dw_gate, layer.grads.dw_up, layer.grads.dw_down):
+        t.fill_(3.0)
+    empty = {k: v[:0] for k, v in inp.items() if k in ("x", "logits", "dy")}
+    layer.step(empty["x"], empty["logits"], None, inp["wg"], inp["wu"], inp["wd"], empty["dy"])
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert layer.y.shape == (0, 256) and layer.grads.dx.shape == (0, 256)
+    for t in (layer.grads.dw_gate, layer.grads.dw_up, layer.grads.dw_down):
+        assert torch.all(t == 0)
