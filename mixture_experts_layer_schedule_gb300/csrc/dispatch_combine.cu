@@ -10,8 +10,8 @@
 //   reverse-dispatch dx[t] = sum_j dxe[slot(t,j)]                  (fp32, j order)
 // Each CTA owns one token and walks its row in 16-byte vectors, so every row
 // of x / dy / y / dx is read or written exactly once and each expert row is
-// touched by exactly one CTA. Extra CTAs (one per expert) zero the padding
-// rows that round each expert segment up to the tile height. Slots are
+// touched by exactly one CTA. Extra CTAs at the front of the grid (kPadSplit per
+// expert) zero the padding rows that round each expert segment up to T rows. Slots are
 // bounds-checked: an unplaced assignment (bad expert id) is skipped.
 #include "moe_common.cuh"
 #include "moe_internal.h"
@@ -20,27 +20,31 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
+// CTAs per expert that zero its padding rows. They come first in the grid so
+// that their writes overlap the token CTAs instead of forming a tail.
+constexpr int kPadSplit = 8;
 
-
-// Zero the padding rows of expert e's segment (CTA index >= N).
-__device__ __forceinline__ void zero_padding(int e, const int32_t* __restrict__ counts,
+// Zero every kPadSplit-th padding row of expert e's segment, from the part-th.
+__device__ __forceinline__ void zero_padding(int e, int part, const int32_t* __restrict__ counts,
                                              const int32_t* __restrict__ pad_offsets,
                                              int64_t R, int hv, uint4* __restrict__ buf) {
   const int64_t r0 = static_cast<int64_t>(pad_offsets[e]) + counts[e];
   const int64_t r1 = pad_offsets[e + 1];
-  for (int64_t r = r0; r < r1 && r < R; ++r)
+  for (int64_t r = r0 + part; r < r1 && r < R; r += kPadSplit)
     for (int v = threadIdx.x; v < hv; v += blockDim.x) buf[r * hv + v] = make_uint4(0, 0, 0, 0);
 }
 
 __global__ void __launch_bounds__(kThreads) dispatch_kernel(
     const uint4* __restrict__ x, const int32_t* __restrict__ slot_of,
     const int32_t* __restrict__ counts, const int32_t* __restrict__ pad_offsets, int64_t N, int k,
-    int hv, int64_t R, uint4* __restrict__ xe) {
-  const int64_t t = blockIdx.x;
-  if (t >= N) {
-    zero_padding(static_cast<int>(t - N), counts, pad_offsets, R, hv, xe);
+    int hv, int64_t R, int E, uint4* __restrict__ xe) {
+  const int64_t b = blockIdx.x;
+  if (b < static_cast<int64_t>(E) * kPadSplit) {
+    zero_padding(static_cast<int>(b / kPadSplit), static_cast<int>(b % kPadSplit), counts,
+                 pad_offsets, R, hv, xe);
     return;
   }
+  const int64_t t = b - static_cast<int64_t>(E) * kPadSplit;
   __shared__ int32_t slots[kMaxK];
   if (threadIdx.x < k) slots[threadIdx.x] = slot_of[t * k + threadIdx.x];
   __syncthreads();
@@ -79,13 +83,15 @@ __global__ void __launch_bounds__(kThreads) reverse_combine_kernel(
     const uint4* __restrict__ dy, const uint4* __restrict__ ye, const float* __restrict__ w,
     const int32_t* __restrict__ slot_of, const int32_t* __restrict__ counts,
     const int32_t* __restrict__ pad_offsets, int64_t N, int k, int hv, int64_t R,
-    uint4* __restrict__ dye, float* __restrict__ dw) {
+    int E, uint4* __restrict__ dye, float* __restrict__ dw) {
   __shared__ float red[kThreads / 32][kMaxK];
-  const int64_t t = blockIdx.x;
-  if (t >= N) {
-    zero_padding(static_cast<int>(t - N), counts, pad_offsets, R, hv, dye);
+  const int64_t b = blockIdx.x;
+  if (b < static_cast<int64_t>(E) * kPadSplit) {
+    zero_padding(static_cast<int>(b / kPadSplit), static_cast<int>(b % kPadSplit), counts,
+                 pad_offsets, R, hv, dye);
     return;
   }
+  const int64_t t = b - static_cast<int64_t>(E) * kPadSplit;
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   for (int j = 0; j < k; ++j) {
     const int32_t slot = slot_of[t * k + j];
@@ -121,10 +127,10 @@ __global__ void __launch_bounds__(kThreads) reverse_combine_kernel(
 
 cudaError_t launch_dispatch(const Layout& L, const void* ws, const void* x, void* xe,
                             cudaStream_t s) {
-  const int64_t blocks = L.N + L.E;
+  const int64_t blocks = L.N + static_cast<int64_t>(L.E) * kPadSplit;
   dispatch_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
       static_cast<const uint4*>(x), at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.counts),
-      at<int32_t>(ws, L.pad_offsets), L.N, L.k, L.H / 8, L.R, static_cast<uint4*>(xe));
+      at<int32_t>(ws, L.pad_offsets), L.N, L.k, L.H / 8, L.R, L.E, static_cast<uint4*>(xe));
   note_launch();
   return cudaGetLastError();
 }
@@ -142,11 +148,11 @@ cudaError_t launch_combine(const Layout& L, const void* ws, const void* ye, cons
 cudaError_t launch_reverse_combine(const Layout& L, const void* ws, const void* dy,
                                    const void* ye, const float* w, void* dye, float* dw,
                                    cudaStream_t s) {
-  const int64_t blocks = L.N + L.E;
+  const int64_t blocks = L.N + static_cast<int64_t>(L.E) * kPadSplit;
   reverse_combine_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
       static_cast<const uint4*>(dy), static_cast<const uint4*>(ye), w,
       at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.counts), at<int32_t>(ws, L.pad_offsets), L.N,
-      L.k, L.H / 8, L.R, static_cast<uint4*>(dye), dw);
+      L.k, L.H / 8, L.R, L.E, static_cast<uint4*>(dye), dw);
   note_launch();
   return cudaGetLastError();
 }
