@@ -58,8 +58,12 @@ def parse():
                     help="bf16 backward through moe_backward_overlap (the reverse-combine run "
                          "by side warps of the down data-gradient GEMM), timed as one phase")
     ap.add_argument("--inference", action="store_true",
-                    help="forward-only workloads: time the context-free forward (dispatch "
-                         "fused into gate/up) instead of the training forward")
+                    help="forward-only workloads: time the context-free forward (no G, U or "
+                         "context stored) instead of the training forward; --gather fuses the "
+                         "dispatch into the gate/up producer")
+    ap.add_argument("--gather", action="store_true",
+                    help="with --inference: time the gate/up GEMM with the dispatch fused into "
+                         "its producer (moe_expert_gate_up_gather)")
     return ap.parse_args()
 
 
@@ -169,6 +173,7 @@ def phase_flops(shape):
     """Algorithmic flops of each GEMM phase (padding rows excluded)."""
     A, H, I = shape.N * shape.k, shape.H, shape.I
     return {"gate_up": 4 * A * H * I, "gate_up_gather": 4 * A * H * I,
+            "gate_up_act": 4 * A * H * I,
             "down": 2 * A * H * I, "down_dgrad": 2 * A * H * I,
             "down_wgrad": 2 * A * H * I, "gate_up_dgrad": 4 * A * H * I,
             "gate_up_wgrad": 4 * A * H * I, "forward": 6 * A * H * I, "backward": 12 * A * H * I}
@@ -241,7 +246,8 @@ def run_ours(args, ws_, rank, local, shape=None):
     inference = args.inference and not backward
     phases = ["route", "schedule", "dispatch", "gate_up", "down", "combine"]
     if inference:
-        phases = ["route", "schedule", "gate_up_gather", "down", "combine"]
+        phases = (["route", "schedule", "gate_up_gather", "down", "combine"] if args.gather else
+                  ["route", "schedule", "dispatch", "gate_up_act", "down", "combine"])
     if mx:  # MXFP8: the composite passes (they add the activation quantisations)
         phases = ["route", "schedule", "forward"] + (["backward"] if backward else [])
     elif backward and args.overlap:
@@ -267,6 +273,7 @@ def run_ours(args, ws_, rank, local, shape=None):
                                                    sv["act"]),
         "gate_up_gather": lambda: _lib.moe_expert_gate_up_gather(p, wsb, inp["x"], w, None, None,
                                                                  sv["act"]),
+        "gate_up_act": lambda: _lib.moe_expert_gate_up(p, wsb, sv["xe"], w, None, None, sv["act"]),
         "down": lambda: _lib.moe_expert_down(p, wsb, sv["act"], w, sv["ye"]),
         "combine": lambda: _lib.moe_combine(p, wsb, sv["ye"], layer.topk_w, layer.y),
         "reverse_combine": lambda: _lib.moe_reverse_combine(p, wsb, inp["dy"], sv["ye"],

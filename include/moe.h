@@ -209,7 +209,8 @@ moe_status moe_dispatch(const moe_problem* p, const void* ws, const void* x, voi
 
 /* Expert gate/up GEMM with the SwiGLU epilogue ([Clip] key point 5): per
  * expert e and its rows, G = Xe Wg[e]^T, U = Xe Wu[e]^T (fp32 accumulation on
- * the tensor cores), Act = silu(G) * U. Writes G, U, Act bf16 [R,I]. */
+ * the tensor cores), Act = silu(G) * U. Writes G, U, Act bf16 [R,I]; g and u
+ * both NULL skip G and U (inference). */
 moe_status moe_expert_gate_up(const moe_problem* p, const void* ws, const void* xe,
                               const moe_weights* w, void* g, void* u, void* act, void* stream);
 
@@ -234,9 +235,10 @@ moe_status moe_expert_gate_up_gather(const moe_problem* p, const void* ws, const
                                      const moe_weights* w, void* g, void* u, void* act,
                                      void* stream);
 
-/* Forward without a context (inference): gathered gate/up (Act only), down,
- * combine. Uses the workspace's backward buffers as scratch for Act and Ye,
- * so it must not run between a moe_forward and its moe_backward. */
+/* Forward without a context (inference): dispatch into scratch, gate/up
+ * (Act only), down over the same scratch, combine; same y as moe_forward.
+ * Uses the workspace's backward buffers as scratch for Xe/Ye and Act, so it
+ * must not run between a moe_forward and its moe_backward. */
 moe_status moe_forward_inference(const moe_problem* p, const void* x, const moe_weights* w,
                                  const float* topk_w, void* y, void* ws, void* stream);
 

@@ -1251,8 +1251,9 @@ moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const v
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
   m.a1h = m.a0h;
-  if (!make_bf16_out_map(&m.o0, g, L.I, L.R) || !make_bf16_out_map(&m.o1, u, L.I, L.R) ||
-      !make_bf16_out_map(&m.o2, act, L.I, L.R))
+  const bool store_gu = g != nullptr && u != nullptr;  // G and U are skipped for inference
+  if (!make_bf16_out_map(&m.o2, act, L.I, L.R)) return MOE_ERR_CUDA;
+  if (store_gu && (!make_bf16_out_map(&m.o0, g, L.I, L.R) || !make_bf16_out_map(&m.o1, u, L.I, L.R)))
     return MOE_ERR_CUDA;
   Args a = base_args(L, ws);
   a.n_nt = L.I / (BN / 2);
@@ -1263,7 +1264,7 @@ moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const v
   a.out0 = g;
   a.out1 = u;
   a.out2 = act;
-  a.store_gu = 1;
+  a.store_gu = store_gu ? 1 : 0;
   return launch_tokens<GATE_UP>(m, a, s);
 }
 
