@@ -207,6 +207,16 @@ moe_status moe_build_schedule_noalloc(const moe_problem* p, const int32_t* topk_
 moe_status moe_dispatch(const moe_problem* p, const void* ws, const void* x, void* xe,
                         void* stream);
 
+/* moe_dispatch with the MXFP8 row quantisation of Xe fused in (the MXFP8
+ * forward's first step): xe as moe_dispatch writes it, plus q_e4m3 [R, H] and
+ * s_e8m0 (R*H/32 bytes) exactly as mxfp8_quantize_mma(xe, R, H, 0, ...) writes
+ * them on every row of the used expert segments (padding rows: codes and
+ * scales 0; rows past the last segment are not written). x is read once and
+ * each token's blocks are quantised once for its k copies. All pointers
+ * 16-byte aligned. */
+moe_status moe_dispatch_mxfp8(const moe_problem* p, const void* ws, const void* x, void* xe,
+                              uint8_t* q_e4m3, uint8_t* s_e8m0, void* stream);
+
 /* Expert gate/up GEMM with the SwiGLU epilogue ([Clip] key point 5): per
  * expert e and its rows, G = Xe Wg[e]^T, U = Xe Wu[e]^T (fp32 accumulation on
  * the tensor cores), Act = silu(G) * U. Writes G, U, Act bf16 [R,I]; g and u

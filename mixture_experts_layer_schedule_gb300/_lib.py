@@ -89,6 +89,7 @@ _SIGS = {
     "moe_expert_gate_up_wgrad": ([c_vp] * 8, c_i32),
     "moe_reverse_dispatch": ([c_vp] * 5, c_i32),
     "moe_backward": ([c_vp] * 12, c_i32),
+    "moe_dispatch_mxfp8": ([c_vp] * 7, c_i32),
     "moe_backward_overlap": ([c_vp] * 12, c_i32),
     "mxfp8_quantize": ([c_vp, c_i64, c_i64, c_vp, c_vp, c_vp], c_i32),
     "mxfp8_qdq": ([c_vp, c_vp, c_i64, c_i64, c_i32, c_vp], c_i32),
@@ -219,6 +220,11 @@ def moe_build_schedule_noalloc(p, topk_ids, out: Schedule, err_word, stream=None
 
 def moe_dispatch(p, ws, x, xe, stream=None):
     _call("moe_dispatch", ctypes.byref(p), _ptr(ws), _ptr(x), _ptr(xe), _stream(stream))
+
+
+def moe_dispatch_mxfp8(p, ws, x, xe, q, s, stream=None):
+    _call("moe_dispatch_mxfp8", ctypes.byref(p), _ptr(ws), _ptr(x), _ptr(xe), _ptr(q), _ptr(s),
+          _stream(stream))
 
 
 def moe_expert_gate_up(p, ws, xe, w: Weights, g, u, act, stream=None):

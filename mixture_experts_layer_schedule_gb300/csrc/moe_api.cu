@@ -178,12 +178,21 @@ moe_status quantize_forms(const void* src, int64_t rows, int64_t cols,
 
 // MXFP8 forward on the block-scaled tensor cores: Xe quantised along H feeds
 // gate/up, Act quantised along I feeds down. g/u may be NULL (inference).
-moe_status mx_forward_gemms(const Layout& L, void* ws, const moe_mxfp8_weights& mx,
-                            const void* xe, void* g, void* u, void* act, void* ye,
-                            cudaStream_t s) {
+// The dispatch with the row quantisation of Xe fused in: Xe bf16 and its
+// E4M3 codes + scales (the gate/up GEMM's A operand, in the workspace) from
+// one read of x.
+moe_status mx_dispatch(const Layout& L, void* ws, const void* x, void* xe, cudaStream_t s) {
+  if ((L.N > 0 && !aligned(x, 16)) || !aligned(xe, 16)) return MOE_ERR_INVALID_ARG;
+  const moe_mxfp8_operand xq = ws_operand(ws, L.mq_rh, L.ms_rh);
+  return cu(launch_dispatch_quant(L, ws, x, xe, const_cast<uint8_t*>(xq.q),
+                                  const_cast<uint8_t*>(xq.s), s));
+}
+
+// After mx_dispatch: gate/up reads Xe's codes, Act is quantised for down.
+moe_status mx_forward_gemms(const Layout& L, void* ws, const moe_mxfp8_weights& mx, void* g,
+                            void* u, void* act, void* ye, cudaStream_t s) {
   const moe_mxfp8_operand xq = ws_operand(ws, L.mq_rh, L.ms_rh);
   const moe_mxfp8_operand aq = ws_operand(ws, L.mq_ri, L.ms_ri);
-  MOE_TRY(quantize_into(xe, L.R, L.H, 0, xq, s));
   MOE_TRY(gemm_mx_gate_up(L, ws, xq, mx.gate, mx.up, g, u, act, s));
   MOE_TRY(quantize_into(act, L.R, L.I, 0, aq, s));
   return gemm_mx_down(L, ws, aq, mx.down, ye, s);
@@ -399,6 +408,16 @@ moe_status moe_dispatch(const moe_problem* p, const void* ws, const void* x, voi
   return cu(launch_dispatch(L, ws, x, xe, S(stream)));
 }
 
+moe_status moe_dispatch_mxfp8(const moe_problem* p, const void* ws, const void* x, void* xe,
+                              uint8_t* q_e4m3, uint8_t* s_e8m0, void* stream) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if ((L.N > 0 && !aligned(x, 16)) || !aligned(xe, 16) || !aligned(q_e4m3, 16) ||
+      !aligned(s_e8m0, 16))
+    return MOE_ERR_INVALID_ARG;
+  return cu(launch_dispatch_quant(L, ws, x, xe, q_e4m3, s_e8m0, S(stream)));
+}
+
 moe_status moe_expert_gate_up(const moe_problem* p, const void* ws, const void* xe,
                               const moe_weights* w, void* g, void* u, void* act, void* stream) {
   Layout L;
@@ -448,10 +467,11 @@ moe_status moe_forward_inference(const moe_problem* p, const void* x, const moe_
   if (p->dtype == MOE_MXFP8) {
     // Xe must exist to be quantised along H: dispatch into scratch first.
     void* xe = at<char>(ws, L.mx_ch);
-    MOE_TRY(moe_dispatch(p, ws, x, xe, stream));
     if (mx_forward_ok(w)) {
-      MOE_TRY(mx_forward_gemms(L, ws, *w->mx, xe, nullptr, nullptr, act, ye, S(stream)));
+      MOE_TRY(mx_dispatch(L, ws, x, xe, S(stream)));
+      MOE_TRY(mx_forward_gemms(L, ws, *w->mx, nullptr, nullptr, act, ye, S(stream)));
     } else {
+      MOE_TRY(moe_dispatch(p, ws, x, xe, stream));
       void* xq = at<char>(ws, L.mx_rh);
       void* aq = at<char>(ws, L.mx_ri1);
       MOE_TRY(mxfp8_qdq(xe, xq, L.R, L.H, 0, stream));
@@ -476,14 +496,15 @@ moe_status moe_forward(const moe_problem* p, const void* x, const moe_weights* w
                        const float* topk_w, void* y, void* saved, void* ws, void* stream) {
   moe_saved_view v;
   MOE_TRY(moe_saved_layout(p, saved, &v));
-  MOE_TRY(moe_dispatch(p, ws, x, v.xe, stream));
   if (p->dtype == MOE_MXFP8 && w && w->mx) {
     Layout L;
     MOE_TRY(prep(p, ws, &L));
     if (!mx_forward_ok(w)) return MOE_ERR_INVALID_ARG;
-    MOE_TRY(mx_forward_gemms(L, ws, *w->mx, v.xe, v.g, v.u, v.act, v.ye, S(stream)));
+    MOE_TRY(mx_dispatch(L, ws, x, v.xe, S(stream)));
+    MOE_TRY(mx_forward_gemms(L, ws, *w->mx, v.g, v.u, v.act, v.ye, S(stream)));
     return moe_combine(p, ws, v.ye, topk_w, y, stream);
   }
+  MOE_TRY(moe_dispatch(p, ws, x, v.xe, stream));
   if (p->dtype == MOE_MXFP8) {
     // MXFP8 on bf16 MMAs: gate/up reads Xe quantised along H, down reads Act
     // quantised along I, as exact bf16 values

@@ -58,6 +58,11 @@ cudaError_t launch_build_schedule_with_scratch(const Layout& L, const int32_t* i
                                                int32_t* warp_counts, cudaStream_t s);
 cudaError_t launch_dispatch(const Layout& L, const void* ws, const void* x, void* xe,
                             cudaStream_t s);
+// Dispatch plus the MXFP8 row quantisation of Xe (codes q [R, H], scales sf in
+// the tensor-memory chunk layout), as launch_mxfp8_quantize_mma(xe, R, H, 0)
+// would write them on every row of a used expert segment.
+cudaError_t launch_dispatch_quant(const Layout& L, const void* ws, const void* x, void* xe,
+                                  uint8_t* q, uint8_t* sf, cudaStream_t s);
 cudaError_t launch_combine(const Layout& L, const void* ws, const void* ye, const float* w,
                            void* y, cudaStream_t s);
 cudaError_t launch_reverse_combine(const Layout& L, const void* ws, const void* dy,

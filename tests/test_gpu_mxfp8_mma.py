@@ -53,6 +53,48 @@ def test_quantize_mma_matches_oracle(transpose, rows, cols):
     np.testing.assert_array_equal(untile_scales(s.cpu().numpy(), R, K), ref_s)
 
 
+@pytest.mark.parametrize("shape", [custom_shape(300, 512, 768, 16, 4, zipf_s=1.2, name="ragged"),
+                                   custom_shape(300, 512, 768, 16, 4, name="ragged_T256", T=256),
+                                   custom_shape(64, 1024, 512, 32, 8, name="many_empty")],
+                         ids=lambda s: s.name)
+def test_dispatch_mxfp8_equals_dispatch_then_quantise(shape):
+    """The fused dispatch + row quantiser writes Xe, its codes and its scales
+    exactly as moe_dispatch followed by mxfp8_quantize_mma on every row of the
+    used expert segments; padding rows get zero codes and scales."""
+    inp_cpu = inputs.make_inputs(shape, seed=8, device="cpu")
+    g = torch.Generator().manual_seed(8)
+    spread = torch.exp(torch.empty((shape.N, 1)).uniform_(-8, 8, generator=g))
+    inp_cpu["x"] = (inp_cpu["x"].float() * spread).bfloat16()
+    inp_cpu["x"][0, :64] = 0.0
+    inp = to_dev(inp_cpu)
+    layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev(),
+                     minibatch_rows=shape.minibatch_rows)
+    layer.route(inp["logits"], inp["bias"])
+    layer.build_schedule()
+    p, ws, R, H = layer.p, layer.ws, layer.R, shape.H
+    xe1 = torch.full((R, H), 5.0, dtype=torch.bfloat16, device=dev())
+    xe2 = torch.full((R, H), 7.0, dtype=torch.bfloat16, device=dev())
+    q1 = torch.empty(R * H, dtype=torch.uint8, device=dev())
+    s1 = torch.empty(R * H // 32, dtype=torch.uint8, device=dev())
+    q2 = torch.full((R * H,), 0x55, dtype=torch.uint8, device=dev())
+    s2 = torch.full((R * H // 32,), 0x55, dtype=torch.uint8, device=dev())
+    _lib.moe_dispatch(p, ws, inp["x"], xe1)
+    _lib.mxfp8_quantize_mma(xe1, R, H, 0, q1, s1)
+    _lib.moe_dispatch_mxfp8(p, ws, inp["x"], xe2, q2, s2)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    used = int(layer.schedule_tensors()["pad_offsets"][shape.E])
+    assert torch.equal(xe2[:used], xe1[:used])
+    qa, qb = q1.view(R, H)[:used], q2.view(R, H)[:used]
+    assert torch.equal(qa, qb)
+    sa = untile_scales(s1.cpu().numpy(), R, H)[:used]
+    sb = untile_scales(s2.cpu().numpy(), R, H)[:used]
+    np.testing.assert_array_equal(sb, sa)
+    src = layer.schedule_tensors()["src_of_row"][:used].cpu().numpy()
+    pad = np.nonzero(src < 0)[0]
+    assert np.all(sb[pad] == 0) and torch.all(qb[torch.as_tensor(pad, device=dev())] == 0)
+
+
 def test_quantize_mma_rejects_unaligned_sizes():
     x = torch.zeros((128, 96), dtype=torch.bfloat16, device=dev())
     q = torch.empty(128 * 96, dtype=torch.uint8, device=dev())
