@@ -217,6 +217,16 @@ moe_status moe_dispatch(const moe_problem* p, const void* ws, const void* x, voi
 moe_status moe_dispatch_mxfp8(const moe_problem* p, const void* ws, const void* x, void* xe,
                               uint8_t* q_e4m3, uint8_t* s_e8m0, void* stream);
 
+/* The workspace buffers that the MXFP8 tensor-core forward quantises its
+ * activations into (host-only, no GPU work): xe_rows = Xe's row form (the
+ * gate/up GEMM's A, written by the dispatch), act_rows = Act's row form (the
+ * down GEMM's A, written by the gate/up epilogue), both [R, K] E4M3 codes with
+ * scales in the mxfp8_quantize_mma chunk layout. Valid after moe_forward or
+ * moe_forward_inference until the next call that reuses the workspace.
+ * MOE_MXFP8 problems only. */
+moe_status moe_mxfp8_forward_operands(const moe_problem* p, void* ws, moe_mxfp8_operand* xe_rows,
+                                      moe_mxfp8_operand* act_rows);
+
 /* Expert gate/up GEMM with the SwiGLU epilogue ([Clip] key point 5): per
  * expert e and its rows, G = Xe Wg[e]^T, U = Xe Wu[e]^T (fp32 accumulation on
  * the tensor cores), Act = silu(G) * U. Writes G, U, Act bf16 [R,I]; g and u

@@ -89,6 +89,7 @@ _SIGS = {
     "moe_expert_gate_up_wgrad": ([c_vp] * 8, c_i32),
     "moe_reverse_dispatch": ([c_vp] * 5, c_i32),
     "moe_backward": ([c_vp] * 12, c_i32),
+    "moe_mxfp8_forward_operands": ([c_vp] * 4, c_i32),
     "moe_dispatch_mxfp8": ([c_vp] * 7, c_i32),
     "moe_backward_overlap": ([c_vp] * 12, c_i32),
     "mxfp8_quantize": ([c_vp, c_i64, c_i64, c_vp, c_vp, c_vp], c_i32),
@@ -220,6 +221,14 @@ def moe_build_schedule_noalloc(p, topk_ids, out: Schedule, err_word, stream=None
 
 def moe_dispatch(p, ws, x, xe, stream=None):
     _call("moe_dispatch", ctypes.byref(p), _ptr(ws), _ptr(x), _ptr(xe), _stream(stream))
+
+
+def moe_mxfp8_forward_operands(p, ws):
+    """Device addresses (q, s) of Xe's and Act's row-form MXFP8 operands in ws."""
+    xe, act = MXFP8Operand(), MXFP8Operand()
+    _call("moe_mxfp8_forward_operands", ctypes.byref(p), _ptr(ws), ctypes.byref(xe),
+          ctypes.byref(act))
+    return (xe.q, xe.s), (act.q, act.s)
 
 
 def moe_dispatch_mxfp8(p, ws, x, xe, q, s, stream=None):

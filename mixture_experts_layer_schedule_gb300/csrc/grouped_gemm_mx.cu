@@ -64,6 +64,7 @@ enum QMode { Q_GATE_UP = 0, Q_DOWN = 1, Q_DACT = 2, Q_DXE = 3, Q_WGRAD = 4 };
 struct QMaps {
   CUtensorMap a0, a1, b0, b1;
   CUtensorMap o0, o1, o2;  // outputs (TMA stores): 32 rows x 32 bytes, no swizzle
+  CUtensorMap o3;          // GATE_UP: Act's E4M3 codes (row form, the down GEMM's A)
 };
 
 struct QArgs {
@@ -88,6 +89,7 @@ struct QArgs {
   int64_t b_rblocks;           // rows of B / 128
   int ld_out;                  // output row length (elements)
   int store_gu;                // GATE_UP: also store G and U
+  uint8_t* act_sf;             // GATE_UP: Act's scale chunks (row form), with o3; NULL: none
   const void *in0, *in1;       // DACT: the saved G, U
 };
 
@@ -498,6 +500,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
       } else if constexpr (MODE == Q_GATE_UP) {
         const int32_t x0 = ti.nt * (QN / 2) + 64 * half;
+        // Act's MXFP8 row form, from its bf16 values: the thread's 64 columns
+        // are two 32-value blocks (blocks 4 nt + 2 half + {0, 1} of the row)
+        float blk[32];
+        uint8_t codes[2] = {0, 0};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint32_t w[8];
@@ -512,6 +518,24 @@ __global__ void __launch_bounds__(kQThreads, 1)
           for (int i = 0; i < 16; ++i) act[i] = q_silu(v[16 * j + i]) * v[64 + 16 * j + i];
           pack16(act, w);
           q_store(&maps.o2, w, x0 + 16 * j, y, lane, out_bufs, nstore);
+          if (args.act_sf) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              blk[16 * (j & 1) + 2 * i] = bf16lo(w[i]);
+              blk[16 * (j & 1) + 2 * i + 1] = bf16hi(w[i]);
+            }
+            if (j & 1) {
+              uint32_t cq[8];
+              codes[j >> 1] = quant32(blk, cq);
+              q_store(&maps.o3, cq, x0 + 32 * (j >> 1), y, lane, out_bufs, nstore);
+            }
+          }
+        }
+        if (args.act_sf) {
+          const int64_t r = static_cast<int64_t>(y) + lane;
+          const int64_t kb = x0 / 32;  // first of the two blocks; kb % 4 == 2 * half
+          *reinterpret_cast<uint16_t*>(args.act_sf + sf_mma_index(r, kb, args.rows)) =
+              static_cast<uint16_t>(codes[0] | (codes[1] << 8));
         }
       } else {  // DOWN, DXE
         const int32_t x0 = ti.nt * QN + 128 * half;
@@ -636,7 +660,7 @@ moe_status q_launch_wgrad(const QMaps& maps, const QArgs& args, cudaStream_t s) 
 
 moe_status gemm_mx_gate_up(const Layout& L, const void* ws, moe_mxfp8_operand xe,
                            const moe_mxfp8_operand& wg, const moe_mxfp8_operand& wu, void* g,
-                           void* u, void* act, cudaStream_t s) {
+                           void* u, void* act, const moe_mxfp8_operand* act_q, cudaStream_t s) {
   const int n_nt = L.I / (QN / 2);
   QMaps m{};
   if (!fp8_map(&m.a0, xe.q, L.H, L.R, a_box(n_nt)) ||
@@ -657,6 +681,12 @@ moe_status gemm_mx_gate_up(const Layout& L, const void* ws, moe_mxfp8_operand xe
   if (!out_map_bf16(&m.o2, act, L.I, L.R)) return MOE_ERR_CUDA;
   if (a.store_gu && (!out_map_bf16(&m.o0, g, L.I, L.R) || !out_map_bf16(&m.o1, u, L.I, L.R)))
     return MOE_ERR_CUDA;
+  if (act_q) {  // the epilogue also writes Act's row-form codes and scales
+    if (!tma_map_2d(&m.o3, act_q->q, L.I, L.R, 32, 32, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+      return MOE_ERR_CUDA;
+    a.act_sf = const_cast<uint8_t*>(act_q->s);
+  }
   return q_launch_rows<Q_GATE_UP>(m, a, s);
 }
 

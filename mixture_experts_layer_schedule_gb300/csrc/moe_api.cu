@@ -158,12 +158,6 @@ moe_mxfp8_operand ws_operand(void* ws, size_t q, size_t s) {
   return moe_mxfp8_operand{at<uint8_t>(ws, q), at<uint8_t>(ws, s)};
 }
 
-// Quantise bf16 [rows, cols] into a workspace operand (transpose: along rows).
-moe_status quantize_into(const void* src, int64_t rows, int64_t cols, int transpose,
-                         moe_mxfp8_operand o, cudaStream_t s) {
-  return cu(launch_mxfp8_quantize_mma(src, rows, cols, transpose, const_cast<uint8_t*>(o.q),
-                                      const_cast<uint8_t*>(o.s), s));
-}
 
 // Quantise bf16 [rows, cols] into the row form (K = cols) and/or the
 // transposed form (K = rows) in one pass; a NULL operand is skipped.
@@ -193,8 +187,8 @@ moe_status mx_forward_gemms(const Layout& L, void* ws, const moe_mxfp8_weights& 
                             void* u, void* act, void* ye, cudaStream_t s) {
   const moe_mxfp8_operand xq = ws_operand(ws, L.mq_rh, L.ms_rh);
   const moe_mxfp8_operand aq = ws_operand(ws, L.mq_ri, L.ms_ri);
-  MOE_TRY(gemm_mx_gate_up(L, ws, xq, mx.gate, mx.up, g, u, act, s));
-  MOE_TRY(quantize_into(act, L.R, L.I, 0, aq, s));
+  // the gate/up epilogue also quantises Act's rows for the down GEMM
+  MOE_TRY(gemm_mx_gate_up(L, ws, xq, mx.gate, mx.up, g, u, act, &aq, s));
   return gemm_mx_down(L, ws, aq, mx.down, ye, s);
 }
 
@@ -406,6 +400,16 @@ moe_status moe_dispatch(const moe_problem* p, const void* ws, const void* x, voi
   MOE_TRY(prep(p, ws, &L));
   if ((L.N > 0 && !aligned(x, 16)) || !aligned(xe, 16)) return MOE_ERR_INVALID_ARG;
   return cu(launch_dispatch(L, ws, x, xe, S(stream)));
+}
+
+moe_status moe_mxfp8_forward_operands(const moe_problem* p, void* ws, moe_mxfp8_operand* xe_rows,
+                                      moe_mxfp8_operand* act_rows) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (p->dtype != MOE_MXFP8 || !xe_rows || !act_rows) return MOE_ERR_INVALID_ARG;
+  *xe_rows = ws_operand(ws, L.mq_rh, L.ms_rh);
+  *act_rows = ws_operand(ws, L.mq_ri, L.ms_ri);
+  return MOE_OK;
 }
 
 moe_status moe_dispatch_mxfp8(const moe_problem* p, const void* ws, const void* x, void* xe,

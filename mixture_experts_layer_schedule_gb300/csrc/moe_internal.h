@@ -116,7 +116,7 @@ moe_status launch_expert_order(const Layout& L, const void* ws, cudaStream_t s);
 // weights, or transposed activations [C, R] quantised along the token axis.
 moe_status gemm_mx_gate_up(const Layout& L, const void* ws, moe_mxfp8_operand xe,
                            const moe_mxfp8_operand& wg, const moe_mxfp8_operand& wu, void* g,
-                           void* u, void* act, cudaStream_t s);
+                           void* u, void* act, const moe_mxfp8_operand* act_q, cudaStream_t s);
 moe_status gemm_mx_down(const Layout& L, const void* ws, moe_mxfp8_operand act,
                         const moe_mxfp8_operand& wd, void* ye, cudaStream_t s);
 // dG, dU = SwiGLU backward of dYe . Wd[e] (B = Wd transposed, [I, E*H]).

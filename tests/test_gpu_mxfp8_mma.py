@@ -114,6 +114,43 @@ def _layer(shape):
                     minibatch_rows=shape.minibatch_rows, dtype="mxfp8")
 
 
+class _DevBytes:
+    """A raw device buffer of n bytes as a CUDA-array-interface object."""
+
+    def __init__(self, ptr, n):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "|u1", "data": (ptr, False),
+                                         "version": 3}
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: s.name)
+def test_fp8_forward_operands_equal_the_quantiser(shape):
+    """The MXFP8 forward quantises Xe's rows in the dispatch and Act's rows in
+    the gate/up epilogue. Both must equal, bit for bit, mxfp8_quantize_mma of
+    the saved bf16 Xe and Act on every row of the used expert segments."""
+    inp = to_dev(inputs.make_inputs(shape, seed=9, device="cpu"))
+    fwd, _ = MoELayer.prepare_mxfp8_weights(inp["wg"], inp["wu"], inp["wd"])
+    mx = MoELayer.prepare_mxfp8_mma_weights(inp["wg"], inp["wu"], inp["wd"], backward=False)
+    layer = _layer(shape)
+    layer.route(inp["logits"], inp["bias"])
+    layer.build_schedule()
+    layer.forward(inp["x"], *fwd, mx=mx)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    R, used = layer.R, int(layer.schedule_tensors()["pad_offsets"][shape.E])
+    sv = layer.saved_tensors()
+    ops = _lib.moe_mxfp8_forward_operands(layer.p, layer.ws)
+    for (q_ptr, s_ptr), src, K in zip(ops, (sv["xe"], sv["act"]), (shape.H, shape.I)):
+        q_ref = torch.empty(R * K, dtype=torch.uint8, device=dev())
+        s_ref = torch.empty(R * K // 32, dtype=torch.uint8, device=dev())
+        _lib.mxfp8_quantize_mma(src, R, K, 0, q_ref, s_ref)
+        q_got = torch.as_tensor(_DevBytes(q_ptr, R * K), device=dev()).clone()
+        s_got = torch.as_tensor(_DevBytes(s_ptr, R * K // 32), device=dev()).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(q_got.view(R, K)[:used], q_ref.view(R, K)[:used]), K
+        np.testing.assert_array_equal(untile_scales(s_got.cpu().numpy(), R, K)[:used],
+                                      untile_scales(s_ref.cpu().numpy(), R, K)[:used])
+
+
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: s.name)
 def test_fp8_forward_matches_bf16_mma_forward(shape):
     inp = to_dev(inputs.make_inputs(shape, seed=5, device="cpu"))
