@@ -371,36 +371,6 @@ __device__ __forceinline__ uint8_t quant32(const float (&f)[32], uint32_t (&pack
   return static_cast<uint8_t>(code);
 }
 
-// ---- tile order of the weight-gradient GEMMs --------------------------------
-
-// Order in which one CTA (pair) visits the size-ordered WGRAD tiles: it
-// alternates between the front of the list (largest experts, long K: tensor
-// work) and the back (smallest experts, short K: mostly fp32 output stores), so
-// the two kinds of tile overlap instead of the store-bound tail running alone.
-// Front tiles are still visited in list order by all CTAs together, which
-// keeps the CTAs on one large expert in step for L2 reuse.
-struct TileSeq {
-  int64_t fi, bi, half, total, stride;
-  int turn;
-  __device__ __forceinline__ TileSeq(int64_t first, int64_t stride_, int64_t total_,
-                                     bool interleave)
-      : fi(first), bi(first), half(interleave ? (total_ + 1) / 2 : total_), total(total_),
-        stride(stride_), turn(0) {}
-  __device__ __forceinline__ bool next(int64_t& t) {
-    const bool f_ok = fi < half, b_ok = bi < total - half;
-    if (!f_ok && !b_ok) return false;
-    if ((turn == 0 && f_ok) || !b_ok) {
-      t = fi;
-      fi += stride;
-    } else {
-      t = total - 1 - bi;
-      bi += stride;
-    }
-    turn ^= 1;
-    return true;
-  }
-};
-
 // ---- bf16 helpers ------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
