@@ -74,6 +74,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x, ws_, device):
+    """The largest x over all ranks: the slowest replica sets the job's time."""
+    if ws_ <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(tokens_per_step, steps, ws_, elapsed_ms):
+    """Whole-job tokens/s of ws_ replicas that each process tokens_per_step
+    tokens per step (weak scaling), over the slowest replica's time."""
+    return tokens_per_step * steps * ws_ / (elapsed_ms * 1e-3)
+
+
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # grouped-GEMM phases, from one single-pass ncu capture of the default
 # workload (summary in profiles/). A value is reported only while the GEMM
@@ -221,7 +237,8 @@ def run_ours(args, ws_, rank, local, shape=None):
     shape = shape or workload(args.config)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    inp = inputs.make_inputs(shape, seed=rank, device=dev)
+    # replicas: the same parameters, their own tokens and upstream gradients
+    inp = inputs.make_inputs(shape, seed=rank, device=dev, weight_seed=0)
     mx = shape.dtype == "mxfp8"
     layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev,
                      minibatch_rows=shape.minibatch_rows, dtype=shape.dtype)
@@ -324,11 +341,7 @@ def run_ours(args, ws_, rank, local, shape=None):
         torch.distributed.barrier()
     clocks = clk.stop()
     launches = _lib.moe_launch_count() - n0
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if ws_ > 1:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), ws_, dev)
     ph_ms = {ph: statistics.mean(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(K))
              for i, ph in enumerate(phases)}
     assert layer.device_error() == 0, "device error in the timed region"
@@ -411,11 +424,7 @@ def run_ours(args, ws_, rank, local, shape=None):
     stream.wait_stream(copy_s)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
-    if ws_ > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, ws_, dev)
     del layers[1]
 
     # ---- roofline of the dominant kernel ----
@@ -452,7 +461,7 @@ def run_ours(args, ws_, rank, local, shape=None):
         phase_report[ph] = d
 
     step_ms = elapsed_ms / K
-    value = shape.N * K * ws_ / (elapsed_ms * 1e-3)
+    value = replica_throughput(shape.N, K, ws_, elapsed_ms)
     rec = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws_, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
@@ -472,7 +481,7 @@ def run_ours(args, ws_, rank, local, shape=None):
         "gemm_tflops": round(gemm_flops / (gemm_ms * 1e-3) / 1e12, 1),
         "gemm_frac_of_peak": round(gemm_flops / (gemm_ms * 1e-3) / 1e12 / t_peak, 4),
         "roofline": roof,
-        "e2e": {"value": round(shape.N * ws_ / (e2e_ms * 1e-3), 1), "unit": UNIT,
+        "e2e": {"value": round(replica_throughput(shape.N, 1, ws_, e2e_ms), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "clocks": clocks,

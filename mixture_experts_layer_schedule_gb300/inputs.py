@@ -94,20 +94,25 @@ def _expert_stack(E, rows, cols, std, gen, device):
     return out
 
 
-def make_inputs(shape: LayerShape, seed: int = 0, device="cpu", with_dy: bool = True) -> dict:
-    """Draw every input of one layer call. Returns torch tensors on `device`."""
+def make_inputs(shape: LayerShape, seed: int = 0, device="cpu", with_dy: bool = True,
+                weight_seed: int = None) -> dict:
+    """Draw every input of one layer call. Returns torch tensors on `device`.
+    weight_seed (default: seed) draws the parameters -- router and expert
+    weights, expert bias -- so data-parallel replicas can share them while
+    their tokens and upstream gradients (seed) differ."""
     N, H, I, E = shape.N, shape.H, shape.I, shape.E
     dev = torch.device(device)
     std = 1.0 / math.sqrt(H)
+    pseed = seed if weight_seed is None else weight_seed
     x = _normal((N, H), 1.0, _gen(seed, "x", dev), dev)
-    wr = _normal((H, E), std, _gen(seed, "wr", dev), dev, dtype=torch.float32)
-    wg = _expert_stack(E, I, H, std, _gen(seed, "wg", dev), dev)
-    wu = _expert_stack(E, I, H, std, _gen(seed, "wu", dev), dev)
-    wd = _expert_stack(E, H, I, std, _gen(seed, "wd", dev), dev)
+    wr = _normal((H, E), std, _gen(pseed, "wr", dev), dev, dtype=torch.float32)
+    wg = _expert_stack(E, I, H, std, _gen(pseed, "wg", dev), dev)
+    wu = _expert_stack(E, I, H, std, _gen(pseed, "wu", dev), dev)
+    wd = _expert_stack(E, H, I, std, _gen(pseed, "wd", dev), dev)
     logits = (x.double() @ wr.double()).float().contiguous()
     bias = None
     if shape.zipf_s is not None:
-        g = _gen(seed, "bias", torch.device("cpu"))
+        g = _gen(pseed, "bias", torch.device("cpu"))
         r = torch.randperm(E, generator=g).double() + 1.0
         bias = (-shape.zipf_s * torch.log(r)).float().to(dev)
     # the same router weights as the device router GEMM reads them: bf16 [E, H]
