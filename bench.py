@@ -97,11 +97,11 @@ def replica_throughput(tokens_per_step, steps, ws_, elapsed_ms):
 GEMM_SRC = ("mixture_experts_layer_schedule_gb300/csrc/grouped_gemm.cu",
             "mixture_experts_layer_schedule_gb300/csrc/moe_common.cuh")
 MEASURED_TRAFFIC = {
-    "src_sha256": "9034480f30475debe3a71950d5aabd70dc144465d3a598faa65248de3aa50cb5",
+    "src_sha256": "ba0730e49c01efdaf26c2a031ab73a0643ccd05f992a2088fb448ada46757419",
     "workload": "skewed_fwd_bwd_N16384_H4096_I1536_E128_k8_zipf1.2",
-    "bytes": {"gate_up": 4.9867e9 + 1.2999e9, "down": 2.0371e9 + 1.1496e9,
-              "down_dgrad": 3.9952e9 + 0.8550e9, "down_wgrad": 2.4752e9 + 3.1562e9,
-              "gate_up_dgrad": 4.4480e9 + 1.1576e9, "gate_up_wgrad": 4.9630e9 + 6.3775e9},
+    "bytes": {"gate_up": 4.9147e9 + 1.3004e9, "down": 2.0368e9 + 1.1491e9,
+              "down_dgrad": 3.9430e9 + 0.8543e9, "down_wgrad": 2.3642e9 + 3.1560e9,
+              "gate_up_dgrad": 4.4273e9 + 1.1575e9, "gate_up_wgrad": 4.6220e9 + 6.3774e9},
 }
 
 
