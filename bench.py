@@ -365,7 +365,9 @@ def run_ours(args, ws_, rank, local, shape=None):
             for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in pin.values())
     d2h = shape.N * shape.H * 2 * (2 if backward else 1)
+    # uploads and read-backs on streams of their own: the two directions overlap
     copy_s = torch.cuda.Stream(device=dev)
+    read_s = torch.cuda.Stream(device=dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_comp = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
@@ -415,13 +417,14 @@ def run_ours(args, ws_, rank, local, shape=None):
             stream.wait_event(ev_out[b])  # step i-2's outputs have been read back
         run_one(layers[b], dev_in[b])
         ev_comp[b].record(stream)
-        with torch.cuda.stream(copy_s):
-            copy_s.wait_event(ev_comp[b])
+        with torch.cuda.stream(read_s):
+            read_s.wait_event(ev_comp[b])
             outs[b]["y"].copy_(layers[b].y, non_blocking=True)
             if backward:
                 outs[b]["dx"].copy_(layers[b].grads.dx, non_blocking=True)
-            ev_out[b].record(copy_s)
+            ev_out[b].record(read_s)
     stream.wait_stream(copy_s)
+    stream.wait_stream(read_s)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, ws_, dev)
