@@ -90,6 +90,62 @@ def replica_throughput(tokens_per_step, steps, ws_, elapsed_ms):
     return tokens_per_step * steps * ws_ / (elapsed_ms * 1e-3)
 
 
+def output_tensors(layer, backward, dw_router=None):
+    """The step's outputs, in the fixed order the digest reads them."""
+    out = {"y": layer.y}
+    if backward:
+        g = layer.grads
+        out.update(dx=g.dx, dw_gate=g.dw_gate, dw_up=g.dw_up, dw_down=g.dw_down,
+                   d_topk_w=g.d_topk_w)
+        if dw_router is not None:
+            out["dw_router"] = dw_router
+    return out
+
+
+def output_digest(tensors, chunk_bytes=1 << 28):
+    """SHA-256 over the bytes of every tensor (in dict order), read back in
+    chunks so the host never holds more than one chunk."""
+    import hashlib
+
+    import torch
+    h = hashlib.sha256()
+    for t in tensors.values():
+        b = t.detach().reshape(-1).view(torch.uint8)
+        for i in range(0, b.numel(), chunk_bytes):
+            h.update(b[i:i + chunk_bytes].cpu().numpy().tobytes())
+    return h.hexdigest()
+
+
+def rerun_check(step, outputs, digest_keys=("y", "dx", "d_topk_w")):
+    """Run one more step on the same inputs and compare every output with the
+    previous step's, byte for byte (the combine and every reduction have a
+    fixed order, so reruns must be identical). The SHA-256 fingerprint covers
+    the token-sized outputs only (the fp32 weight gradients are compared on
+    the device but not read back)."""
+    import torch
+    first = {k: v.clone() for k, v in outputs.items()}
+    digest = output_digest({k: first[k] for k in digest_keys if k in first})
+    step()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
+    same = {k: bool(torch.equal(first[k].reshape(-1).view(torch.uint8),
+                                v.reshape(-1).view(torch.uint8))) for k, v in outputs.items()}
+    del first
+    return {"rerun_bitwise_equal": all(same.values()), "compared": list(outputs),
+            "sha256": digest, "sha256_of": [k for k in digest_keys if k in outputs]}
+
+
+def expert_loads(counts, tile_rows=128):
+    """Tokens per expert (m_e) and the share of grouped-GEMM rows that are
+    padding when each expert's rows are rounded up to whole tiles."""
+    m = [int(c) for c in counts]
+    A = sum(m)
+    padded = sum(-(-c // tile_rows) * tile_rows for c in m)
+    return {"m_e_max": max(m), "m_e_mean": A / len(m), "m_e_min": min(m),
+            "empty_experts": sum(c == 0 for c in m), "tile_rows": tile_rows,
+            "padded_row_frac": round((padded - A) / padded, 4) if padded else 0.0}
+
+
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # grouped-GEMM phases, from one single-pass ncu capture of the default
 # workload (summary in profiles/). A value is reported only while the GEMM
@@ -345,6 +401,8 @@ def run_ours(args, ws_, rank, local, shape=None):
     ph_ms = {ph: statistics.mean(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(K))
              for i, ph in enumerate(phases)}
     assert layer.device_error() == 0, "device error in the timed region"
+    determinism = rerun_check(step, output_tensors(layer, backward, dwr))
+    loads = expert_loads(layer.schedule_tensors()["counts"].cpu(), shape.minibatch_rows)
 
     # ---- end to end through the public API with host buffers ----
     # Every step copies its inputs (x, logits, dy) from pinned host memory and
@@ -489,6 +547,8 @@ def run_ours(args, ws_, rank, local, shape=None):
         "gpu_launches": int(launches),
         "clocks": clocks,
         "phases": phase_report,
+        "determinism": determinism,
+        "expert_loads": loads,
     }
     if args.overlap and backward and not mx:
         rec["config"]["backward"] = ("moe_backward_overlap: reverse-combine run by side warps of "

@@ -1,0 +1,44 @@
+"""Host-side bookkeeping of bench.py that needs no GPU: the expert-load
+statistics, the output fingerprint and the rerun comparison."""
+import hashlib
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import bench  # noqa: E402
+
+
+def test_expert_loads_padding_by_hand():
+    # m_e = 0, 1, 128, 129, 300 with 128-row tiles: padded rows 0, 128, 128, 256, 384
+    loads = bench.expert_loads(torch.tensor([0, 1, 128, 129, 300]), tile_rows=128)
+    A, padded = 558, 896
+    assert loads["m_e_max"] == 300 and loads["m_e_min"] == 0
+    assert loads["m_e_mean"] == pytest.approx(A / 5)
+    assert loads["empty_experts"] == 1
+    assert loads["padded_row_frac"] == pytest.approx(round((padded - A) / padded, 4))
+
+
+def test_expert_loads_whole_tiles_have_no_padding():
+    loads = bench.expert_loads([256, 128, 384], tile_rows=128)
+    assert loads["padded_row_frac"] == 0.0 and loads["empty_experts"] == 0
+    assert bench.expert_loads([0, 0], tile_rows=128)["padded_row_frac"] == 0.0
+
+
+def test_digest_is_sha256_of_the_bytes_in_order():
+    a = torch.arange(1000, dtype=torch.float32)
+    b = torch.arange(77, dtype=torch.int16)
+    want = hashlib.sha256(a.numpy().tobytes() + b.numpy().tobytes()).hexdigest()
+    # chunk boundaries inside a tensor do not change the digest
+    assert bench.output_digest({"a": a, "b": b}, chunk_bytes=96) == want
+    assert bench.output_digest({"b": b, "a": a}) != want
+
+
+def test_rerun_check_sees_a_changed_bit():
+    out = {"y": torch.ones(64, dtype=torch.bfloat16), "dx": torch.zeros(8, dtype=torch.float32)}
+    same = bench.rerun_check(lambda: None, out)
+    assert same["rerun_bitwise_equal"] and same["compared"] == ["y", "dx"]
+    assert same["sha256_of"] == ["y", "dx"]
+
+    def flip_sign_of_zero():  # -0.0 == 0.0 as floats, not as bytes
+        out["dx"][3] = -0.0
+    assert not bench.rerun_check(flip_sign_of_zero, out)["rerun_bitwise_equal"]
