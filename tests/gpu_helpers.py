@@ -43,14 +43,3 @@ def run_layer(shape, inp_dev, backward=True):
                inp_dev["wd"], inp_dev.get("dy"), backward=backward)
     torch.cuda.synchronize()
     return layer
-
-
-def oracle_route(inp):
-    logits = inp["logits"].cpu().numpy()
-    bias = None if inp["bias"] is None else inp["bias"].cpu().numpy()
-    k = None
-    return logits, bias
-
-
-def np_i32(t):
-    return t.cpu().numpy().astype(np.int32)

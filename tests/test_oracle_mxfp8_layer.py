@@ -103,3 +103,35 @@ def test_weight_copies_are_the_quantiser_s_values_and_the_two_halves_compose():
     r2 = oracle.layer_mxfp8_prepared(x, pw, ids, w, dy)
     for key in r1:
         np.testing.assert_array_equal(r1[key], r2[key])
+
+
+def test_token_rows_and_expert_segments_are_local():
+    """What the full-size sampled MXFP8 parity test relies on. Every forward
+    and dX-path operand is quantised along K one row at a time, so a token
+    run alone against its own k experts gives its y, dx and d(routing
+    weights) exactly. An expert's weight-gradient operands are quantised in
+    32-token blocks from the start of its segment (tokens ascending), so that
+    expert run alone on exactly its tokens (k = 1) gives its dW exactly --
+    and the same tokens in another order do not (the blocks regroup)."""
+    N, H, I, E, k = 80, 64, 96, 3, 2  # ~53 tokens per expert: a ragged 32-token block
+    x, wg, wu, wd, ids, w, dy = _layer(N, H, I, E, k, 5)
+    full = oracle.layer_mxfp8(x, wg, wu, wd, ids, w, dy)
+    own = np.arange(k, dtype=np.int32)[None]
+    for t in (0, 41, N - 1):
+        ex = ids[t]
+        r = oracle.layer_mxfp8(x[t:t + 1], wg[ex], wu[ex], wd[ex], own, w[t:t + 1], dy[t:t + 1])
+        for key in ("y", "dx", "dw"):
+            np.testing.assert_array_equal(r[key][0], full[key][t])
+    for e in range(E):
+        hit = ids == e
+        toks = np.flatnonzero(hit.any(axis=1))
+        assert len(toks) % 32 != 0
+        one = np.zeros((len(toks), 1), np.int32)
+        r = oracle.layer_mxfp8(x[toks], wg[e:e + 1], wu[e:e + 1], wd[e:e + 1], one,
+                               w[hit][:, None], dy[toks])
+        for key in ("dwg", "dwu", "dwd"):
+            np.testing.assert_array_equal(r[key][0], full[key][e])
+        rev = toks[::-1]
+        r = oracle.layer_mxfp8(x[rev], wg[e:e + 1], wu[e:e + 1], wd[e:e + 1], one,
+                               w[hit][::-1, None], dy[rev])
+        assert not np.array_equal(r["dwd"][0], full["dwd"][e])
