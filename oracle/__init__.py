@@ -69,6 +69,9 @@ def lib():
             L.orc_expert_wgrad_bf16.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp,
                                                 vp, vp, vp, i32, i64, vp, i64, vp, vp, vp,
                                                 vp, ctypes.c_int]
+            L.orc_expert_wgrad_mxfp8.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+                                                 vp, vp, i32, i64, vp, i64, vp, ctypes.c_int,
+                                                 vp, vp, vp, ctypes.c_int]
             L.orc_mxfp8_quantize.argtypes = [i64, i64, vp, vp, vp]
             L.orc_layer_mxfp8.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp,
                                           ctypes.c_int, vp, vp, vp, vp, vp, vp, ctypes.c_int]
@@ -276,6 +279,23 @@ def layer_mxfp8(x, wg, wu, wd, ids, w, dy, quantize=True, threads=0):
                                  _p(dy), 1 if quantize else 0, _p(y), _p(dx), _p(dwg), _p(dwu),
                                  _p(dwd), _p(dw), threads))
     return dict(y=y, dx=dx, dwg=dwg, dwu=dwu, dwd=dwd, dw=dw)
+
+
+def expert_wgrad_mxfp8(x, wg, wu, wd, ids, w, dy, e, i_list, h_list, quantize=True, threads=0):
+    """Entries of expert e's MXFP8 weight gradients (those of layer_mxfp8):
+    dwg, dwu [len(i_list), len(h_list)] and dwd [len(h_list), len(i_list)]."""
+    x, wg, wu, wd, dy = (as_bf16_bits(a) for a in (x, wg, wu, wd, dy))
+    ids, w = _c(ids, np.int32), _c(w, np.float64)
+    il, hl = _c(i_list, np.int32), _c(h_list, np.int32)
+    N, H = x.shape
+    E, I, _ = wg.shape
+    k = ids.shape[1]
+    dwg, dwu = np.empty((len(il), len(hl))), np.empty((len(il), len(hl)))
+    dwd = np.empty((len(hl), len(il)))
+    _check(lib().orc_expert_wgrad_mxfp8(N, H, I, E, k, _p(x), _p(wg), _p(wu), _p(wd), _p(ids),
+                                        _p(w), _p(dy), int(e), len(il), _p(il), len(hl), _p(hl),
+                                        1 if quantize else 0, _p(dwg), _p(dwu), _p(dwd), threads))
+    return dict(dwg=dwg, dwu=dwu, dwd=dwd)
 
 
 MXFP8_WEIGHT_COPIES = ("wg_h", "wu_h", "wd_i", "wd_h", "wg_i", "wu_i")

@@ -786,4 +786,106 @@ extern "C" int orc_layer_mxfp8_prepared(int64_t N, int32_t H, int32_t I, int32_t
   return ORC_OK;
 }
 
+// The MXFP8 weight gradients of expert e at sampled entries, by the steps of
+// orc_layer_mxfp8 restricted to what those entries read. Each of e's
+// assignments (ascending token) needs its Xe and dYe rows quantised along H
+// (whole rows) and, for each listed i, G, U, Act, dAct, dG and dU; each
+// listed column then goes through the token-axis quantisation of its own
+// column (blocks of 32 assignments from the start of e's list), and the
+// contraction runs over the assignments in the same order. Results equal
+// orc_layer_mxfp8's dwg[e][i][h], dwu[e][i][h] and dwd[e][h][i] at
+// i = i_list[r], h = h_list[c]: dwg, dwu [n_i][n_h], dwd [n_h][n_i].
+int orc_expert_wgrad_mxfp8(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k,
+                           const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
+                           const uint16_t* wd, const int32_t* ids, const double* w,
+                           const uint16_t* dy, int32_t e, int64_t n_i, const int32_t* i_list,
+                           int64_t n_h, const int32_t* h_list, int quantize, double* dwg,
+                           double* dwu, double* dwd, int threads) {
+  if (N < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || k > E || e < 0 || e >= E)
+    return ORC_ERR_ARG;
+  for (int64_t r = 0; r < n_i; ++r)
+    if (i_list[r] < 0 || i_list[r] >= I) return ORC_ERR_ARG;
+  for (int64_t c = 0; c < n_h; ++c)
+    if (h_list[c] < 0 || h_list[c] >= H) return ORC_ERR_ARG;
+  auto q = [quantize](double* v, int64_t n) { if (quantize) qdq_vec(v, n); };
+  auto rb = [quantize](double v) { return quantize ? round_bf16(v) : v; };
+  const int64_t o = static_cast<int64_t>(e) * H * I;
+  // the weight rows and columns the listed i read, quantised as the layer reads them
+  std::vector<double> wgr(n_i * H), wur(n_i * H), wdc(n_i * H);
+  for (int64_t r = 0; r < n_i; ++r) {
+    const int64_t i = i_list[r];
+    for (int32_t h = 0; h < H; ++h) {
+      wgr[r * H + h] = bf16_to_double(wg[o + i * H + h]);               // Wg[e][i][:]
+      wur[r * H + h] = bf16_to_double(wu[o + i * H + h]);
+      wdc[r * H + h] = bf16_to_double(wd[o + static_cast<int64_t>(h) * I + i]);  // Wd[e][:][i]
+    }
+    q(&wgr[r * H], H);
+    q(&wur[r * H], H);
+    q(&wdc[r * H], H);
+  }
+  std::vector<int64_t> as;  // e's assignments in slot order
+  for (int64_t a = 0; a < N * k; ++a) {
+    if (ids[a] < 0 || ids[a] >= E) return ORC_ERR_ARG;
+    if (ids[a] == e) as.push_back(a);
+  }
+  const int64_t M = static_cast<int64_t>(as.size());
+  std::vector<double> Ab(M * n_i), DG(M * n_i), DU(M * n_i), DYe(M * n_h), Xb(M * n_h);
+  parallel_for(M, threads, [&](int64_t m) {
+    const int64_t a = as[m], t = a / k;
+    std::vector<double> xq(H), dq(H);
+    for (int32_t h = 0; h < H; ++h) {
+      xq[h] = bf16_to_double(x[t * H + h]);
+      dq[h] = rb(w[a] * bf16_to_double(dy[t * H + h]));              // dYe, stored bf16
+    }
+    for (int64_t c = 0; c < n_h; ++c) {
+      DYe[m * n_h + c] = dq[h_list[c]];
+      Xb[m * n_h + c] = xq[h_list[c]];
+    }
+    q(xq.data(), H);                                                  // Xe rows along H
+    q(dq.data(), H);                                                  // dYe rows along H
+    for (int64_t r = 0; r < n_i; ++r) {
+      double gs = 0.0, us = 0.0, da = 0.0;
+      for (int32_t h = 0; h < H; ++h) {
+        gs += wgr[r * H + h] * xq[h];
+        us += wur[r * H + h] * xq[h];
+      }
+      for (int32_t h = 0; h < H; ++h) da += wdc[r * H + h] * dq[h];
+      const double sg = sigmoid(gs);
+      Ab[m * n_i + r] = rb(gs * sg * us);                             // Act, stored bf16
+      DG[m * n_i + r] = rb(da * us * sg * (1.0 + gs * (1.0 - sg)));   // dG, dU stored bf16
+      DU[m * n_i + r] = rb(da * gs * sg);
+    }
+  });
+  // token-axis quantisation, one listed column at a time
+  auto column = [&](const std::vector<double>& src, int64_t stride, int64_t col) {
+    std::vector<double> v(M);
+    for (int64_t m = 0; m < M; ++m) v[m] = src[m * stride + col];
+    q(v.data(), M);
+    return v;
+  };
+  std::vector<std::vector<double>> actT(n_i), dgT(n_i), duT(n_i), dyeT(n_h), xeT(n_h);
+  for (int64_t r = 0; r < n_i; ++r) {
+    actT[r] = column(Ab, n_i, r);
+    dgT[r] = column(DG, n_i, r);
+    duT[r] = column(DU, n_i, r);
+  }
+  for (int64_t c = 0; c < n_h; ++c) {
+    dyeT[c] = column(DYe, n_h, c);
+    xeT[c] = column(Xb, n_h, c);
+  }
+  for (int64_t r = 0; r < n_i; ++r)
+    for (int64_t c = 0; c < n_h; ++c) {
+      double ag = 0.0, au = 0.0, ad = 0.0;
+      for (int64_t m = 0; m < M; ++m) {
+        ag += dgT[r][m] * xeT[c][m];
+        au += duT[r][m] * xeT[c][m];
+        ad += dyeT[c][m] * actT[r][m];
+      }
+      dwg[r * n_h + c] = ag;
+      dwu[r * n_h + c] = au;
+      dwd[c * n_i + r] = ad;
+    }
+  return ORC_OK;
+}
+
 }  // extern "C"

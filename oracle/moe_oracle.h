@@ -177,6 +177,20 @@ int orc_layer_mxfp8_prepared(int64_t N, int32_t H, int32_t I, int32_t E, int32_t
                              const uint16_t* dy, int quantize, double* y, double* dx, double* dwg,
                              double* dwu, double* dwd, double* dw, int threads);
 
+/* The weight gradients of orc_layer_mxfp8 for expert e at sampled entries
+ * (sampled parity where the whole layer is too large for the oracle):
+ * dwg[r][c] = dWg[e][i_list[r]][h_list[c]], dwu likewise (both [n_i, n_h]),
+ * dwd[c][r] = dWd[e][h_list[c]][i_list[r]] ([n_h, n_i]). Same steps, same
+ * token-axis blocks and same summation order as orc_layer_mxfp8, so the
+ * values are equal to its entries; cost grows with e's assignments times
+ * (n_i + n_h) rows, not with H * I. */
+int orc_expert_wgrad_mxfp8(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k,
+                           const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
+                           const uint16_t* wd, const int32_t* ids, const double* w,
+                           const uint16_t* dy, int32_t e, int64_t n_i, const int32_t* i_list,
+                           int64_t n_h, const int32_t* h_list, int quantize, double* dwg,
+                           double* dwu, double* dwd, int threads);
+
 /* MXFP8 quantiser (OCP MX v1.0, MXFP8 E4M3): for each block of 32
  * consecutive values along a row, X = 2^(floor(log2(amax)) - 8) (8 = the
  * largest E4M3 exponent), scale code = that exponent + 127 clamped to

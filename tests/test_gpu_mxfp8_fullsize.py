@@ -9,11 +9,16 @@ The oracle cannot run this whole layer, but most of it is local:
     alone against just those k experts;
   * an expert's weight gradients quantise their operands along the token
     axis in 32-row blocks that restart at the expert's segment (its tokens in
-    ascending order), so the oracle runs exactly that expert's tokens against
-    that expert alone (k = 1, each token's own routing weight) and the whole
-    dW_gate[e], dW_up[e], dW_down[e] are compared.
+    ascending order), each column on its own, so sampled entries of dW need
+    only the sampled rows and columns of that expert's operands
+    (oracle.expert_wgrad_mxfp8) -- cheap even for the expert that takes
+    almost every token.
 Tolerance: the MXFP8 bound, max|err| <= 6e-2 * max|ref| over the sampled
-elements of each tensor; the routing ids are exact."""
+elements of each tensor (all sampled experts together, as the bound is per
+tensor); the routing ids are exact. A single expert's slice is not the
+tensor: with few tokens, one E4M3 code that flips between the two sides
+(an intermediate next to a rounding boundary, fp32 against fp64) moves a
+small expert's dW by several percent of that expert's own maximum."""
 import numpy as np
 import pytest
 import torch
@@ -63,21 +68,37 @@ def test_mxfp8_full_size_sampled_parity():
     assert_close("dx", g.dx[sel], np.stack(ref["dx"]), MX_TOL)
     assert_close("d_topk_w", g.d_topk_w[sel], np.stack(ref["dw"]), MX_TOL)
 
-    # whole weight gradients of three experts: one token; 33 tokens (a ragged
-    # 32-row block); the first with more than 128 (a second 128-row tile)
+    # weight gradients: sampled entries of five experts, from one token to the
+    # dominant expert (its long tiles go through the chunked weight-gradient
+    # plan): 1, 33 (a ragged 32-token block), the first above 128 (a second
+    # 128-row tile), the median and the largest expert
     counts = np.bincount(ids.reshape(-1), minlength=shape.E)
-    picks = []
-    for lo in (1, 33, 129):
+    nz = np.flatnonzero(counts)
+    picks = {int(nz[np.argmin(counts[nz])]), int(np.argmax(counts)),
+             int(nz[np.argsort(counts[nz], kind="stable")[len(nz) // 2]])}
+    for lo in (33, 129):
         cand = np.flatnonzero(counts >= lo)
-        picks.append(int(cand[np.argmin(counts[cand])]))
-    for e in sorted(set(picks)):
-        hit = ids == e
-        toks = np.flatnonzero(hit.any(axis=1))
-        we = w[hit][:, None]  # row-major order of hit = ascending tokens
-        r = oracle.layer_mxfp8(x[toks], wg[e:e + 1], wu[e:e + 1], wd[e:e + 1],
-                               np.zeros((len(toks), 1), np.int32), we, dy[toks])
-        assert_close(f"dw_gate[{e}] (m_e={len(toks)})", g.dw_gate[e], r["dwg"][0], MX_TOL)
-        assert_close(f"dw_up[{e}] (m_e={len(toks)})", g.dw_up[e], r["dwu"][0], MX_TOL)
-        assert_close(f"dw_down[{e}] (m_e={len(toks)})", g.dw_down[e], r["dwd"][0], MX_TOL)
+        picks.add(int(cand[np.argmin(counts[cand])]))
+    il = np.sort(rng.choice(shape.I, 16, replace=False)).astype(np.int32)
+    hl = np.sort(rng.choice(shape.H, 32, replace=False)).astype(np.int32)
+    il_t, hl_t = torch.as_tensor(il, device=d).long(), torch.as_tensor(hl, device=d).long()
+    got = {n: [] for n in ("dwg", "dwu", "dwd")}
+    want = {n: [] for n in got}
+    for e in sorted(picks):
+        r = oracle.expert_wgrad_mxfp8(x, wg, wu, wd, ids, w, dy, e, il, hl)
+        got["dwg"].append(g.dw_gate[e][il_t][:, hl_t])
+        got["dwu"].append(g.dw_up[e][il_t][:, hl_t])
+        got["dwd"].append(g.dw_down[e][hl_t][:, il_t])
+        for n in want:
+            want[n].append(r[n])
+            # gross-error screen per expert: a flipped E4M3 code moves a
+            # product by at most 2^-3 of itself, so two flips on the dominant
+            # product stay under a quarter of the expert's own maximum
+            assert_close(f"{n}[{e}] (m_e={counts[e]})", got[n][-1], r[n], 0.25)
+    # the bound is per tensor: max|err| over the sampled entries of all five
+    # experts against max|ref| over the same entries
+    for n, name in (("dwg", "dw_gate"), ("dwu", "dw_up"), ("dwd", "dw_down")):
+        assert_close(f"{name} (experts {sorted(picks)}, m_e {sorted(counts[list(picks)])})",
+                     torch.cat(got[n]), np.concatenate(want[n]), MX_TOL)
     del layer, inp
     torch.cuda.empty_cache()

@@ -135,3 +135,28 @@ def test_token_rows_and_expert_segments_are_local():
         r = oracle.layer_mxfp8(x[rev], wg[e:e + 1], wu[e:e + 1], wd[e:e + 1], one,
                                w[hit][::-1, None], dy[rev])
         assert not np.array_equal(r["dwd"][0], full["dwd"][e])
+
+
+@pytest.mark.parametrize("quantize", [True, False])
+def test_sampled_expert_wgrad_equals_the_layer_entries(quantize):
+    """expert_wgrad_mxfp8 (sampled entries, any expert size) against the
+    whole-layer oracle: equal entries, bit for bit, on ragged experts and on
+    lists that repeat, reorder and reach the last row and column."""
+    N, H, I, E, k = 90, 64, 96, 3, 2
+    x, wg, wu, wd, ids, w, dy = _layer(N, H, I, E, k, 8)
+    full = oracle.layer_mxfp8(x, wg, wu, wd, ids, w, dy, quantize=quantize)
+    il = np.array([95, 0, 31, 32, 7, 7], np.int32)
+    hl = np.array([63, 1, 32, 0, 40], np.int32)
+    for e in range(E):
+        r = oracle.expert_wgrad_mxfp8(x, wg, wu, wd, ids, w, dy, e, il, hl, quantize=quantize)
+        np.testing.assert_array_equal(r["dwg"], full["dwg"][e][np.ix_(il, hl)])
+        np.testing.assert_array_equal(r["dwu"], full["dwu"][e][np.ix_(il, hl)])
+        np.testing.assert_array_equal(r["dwd"], full["dwd"][e][np.ix_(hl, il)])
+
+
+def test_sampled_expert_wgrad_rejects_bad_lists():
+    x, wg, wu, wd, ids, w, dy = _layer(8, 64, 96, 3, 2, 1)
+    with pytest.raises(oracle.OracleError):
+        oracle.expert_wgrad_mxfp8(x, wg, wu, wd, ids, w, dy, 0, [96], [0])
+    with pytest.raises(oracle.OracleError):
+        oracle.expert_wgrad_mxfp8(x, wg, wu, wd, ids, w, dy, 3, [0], [0])
