@@ -153,11 +153,11 @@ def expert_loads(counts, tile_rows=128):
 GEMM_SRC = ("mixture_experts_layer_schedule_gb300/csrc/grouped_gemm.cu",
             "mixture_experts_layer_schedule_gb300/csrc/moe_common.cuh")
 MEASURED_TRAFFIC = {
-    "src_sha256": "ba0730e49c01efdaf26c2a031ab73a0643ccd05f992a2088fb448ada46757419",
+    "src_sha256": "28b7168831838b2ece08b683c1b3444283bdf29095e2692851dfead2dc83713c",
     "workload": "skewed_fwd_bwd_N16384_H4096_I1536_E128_k8_zipf1.2",
-    "bytes": {"gate_up": 4.9147e9 + 1.3004e9, "down": 2.0368e9 + 1.1491e9,
-              "down_dgrad": 3.9430e9 + 0.8543e9, "down_wgrad": 2.3642e9 + 3.1560e9,
-              "gate_up_dgrad": 4.4273e9 + 1.1575e9, "gate_up_wgrad": 4.6220e9 + 6.3774e9},
+    "bytes": {"gate_up": 4.9579e9 + 1.3012e9, "down": 2.0358e9 + 1.1494e9,
+              "down_dgrad": 3.9836e9 + 0.8549e9, "down_wgrad": 2.4080e9 + 3.1563e9,
+              "gate_up_dgrad": 4.3366e9 + 1.1572e9, "gate_up_wgrad": 4.8683e9 + 6.3782e9},
 }
 
 

@@ -210,10 +210,12 @@ __device__ __forceinline__ void issue_loads(const Maps& m, const Args& a, const 
   // GATE_UP_GATHER: loaded by the whole producer warp (see the kernel)
 }
 
-// silu with the fast exponential and division intrinsics (__expf: at most
-// 2 + floor(1.16 |x|) ulp; __fdividef: 2 ulp), far below the bf16 rounding of
-// Act; with the IEEE forms the gate/up epilogue's arithmetic cost 3% of that GEMM.
+// silu and the sigmoid with the fast exponential and division intrinsics
+// (__expf: at most 2 + floor(1.16 |x|) ulp; __fdividef: 2 ulp), far below the
+// bf16 rounding of Act, dG and dU; with the IEEE forms the gate/up epilogue's
+// arithmetic cost 3% of that GEMM and the down data-gradient epilogue's 5-7%.
 __device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+__device__ __forceinline__ float sigmoid(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 
 // One 32-row x 64-column bf16 block of a warp's output: 64 fp32 values per
 // thread (its row) -> bf16 -> shared staging buffer (128-byte swizzle: one
@@ -329,7 +331,7 @@ __device__ __forceinline__ void epilogue(const Maps& m, const Args& a, const Til
             const float da = __uint_as_float(d[8 * v + 2 * q + h]);
             const float g = h ? bf16hi(gw[q]) : bf16lo(gw[q]);
             const float u = h ? bf16hi(uw[q]) : bf16lo(uw[q]);
-            const float sg = 1.0f / (1.0f + expf(-g));
+            const float sg = sigmoid(g);
             dg2[h] = da * u * sg * (1.0f + g * (1.0f - sg));
             du2[h] = da * g * sg;
           }
