@@ -251,6 +251,23 @@ def phase_flops(shape):
             "gate_up_wgrad": 4 * A * H * I, "forward": 6 * A * H * I, "backward": 12 * A * H * I}
 
 
+def gemm_bytes(shape):
+    """Least HBM bytes of each bf16 GEMM phase: every operand read once and
+    every output written once (padding rows excluded). Set against the
+    phase's time this places a GEMM on the bandwidth roofline too, which
+    matters where few tokens per expert meet large weights."""
+    N, A, H, I, E = shape.N, shape.N * shape.k, shape.H, shape.I, shape.E
+    W = 2 * E * H * I  # one bf16 weight tensor
+    return {"gate_up": 2 * A * H + 2 * W + 3 * 2 * A * I,
+            "gate_up_act": 2 * A * H + 2 * W + 2 * A * I,
+            "gate_up_gather": 2 * N * H + 4 * A + 2 * W + 2 * A * I,
+            "down": 2 * A * I + W + 2 * A * H,
+            "down_dgrad": 2 * A * H + W + 2 * 2 * A * I + 2 * 2 * A * I,
+            "down_wgrad": 2 * A * H + 2 * A * I + 2 * W,
+            "gate_up_dgrad": 2 * 2 * A * I + 2 * W + 2 * A * H,
+            "gate_up_wgrad": 2 * 2 * A * I + 2 * A * H + 4 * W}
+
+
 def phase_bytes(shape, R, router=False):
     """Algorithmic HBM bytes of the data-movement phases."""
     N, A, H, E, k = shape.N, shape.N * shape.k, shape.H, shape.E, shape.k
@@ -512,12 +529,16 @@ def run_ours(args, ws_, rank, local, shape=None):
                 "traffic": None}
     gemm_ms = sum(ph_ms[k] for k in fl if k in ph_ms)
     gemm_flops = sum(fl[k] for k in fl if k in ph_ms)
+    gb_min = gemm_bytes(shape)
     phase_report = {}
     for ph in phases:
         d = {"ms": round(ph_ms[ph], 4)}
         if ph in fl:
             tf = fl[ph] / (ph_ms[ph] * 1e-3) / 1e12
             d.update(tflops=round(tf, 1), frac=round(tf / t_peak, 3))
+            if ph in gb_min and not mx:  # the same phase on the bandwidth roofline
+                gb = gb_min[ph] / (ph_ms[ph] * 1e-3) / 1e9
+                d.update(min_gbs=round(gb, 1), hbm_frac=round(gb / peaks["hbm_gbs"], 3))
         elif ph in by:
             gb = by[ph] / (ph_ms[ph] * 1e-3) / 1e9
             d.update(gbs=round(gb, 1), frac=round(gb / peaks["hbm_gbs"], 3))
