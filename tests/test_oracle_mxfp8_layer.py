@@ -8,7 +8,16 @@ along that GEMM's K; the MXFP8 workload of the pages' benchmark set).
 * quantisation axis of one GEMM operand: a huge outlier in one column of the
   down weights flushes the small values sharing its 1x32 blocks to zero only
   when the blocks run along H (the K of the down backward), which changes the
-  data gradient by a predictable, large amount.
+  data gradient by a predictable, large amount;
+* the six weight copies equal the quantiser's values along their axes;
+* every activation operand, by a flush pin of its own: Xe, Act, dYe, dG/dU
+  row blocks along K (forward and data-gradient GEMMs) and the token-axis
+  blocks of dYe, Act, Xe, dG, dU (weight-gradient GEMMs). Dropping any one of
+  those quantisations from the oracle fails its pin (checked by planting each
+  omission in a copy of the oracle);
+* locality: a token run alone, or an expert run on exactly its tokens,
+  reproduces the whole run's rows; the sampled weight-gradient entries equal
+  the whole run's.
 """
 import math
 
@@ -160,3 +169,171 @@ def test_sampled_expert_wgrad_rejects_bad_lists():
         oracle.expert_wgrad_mxfp8(x, wg, wu, wd, ids, w, dy, 0, [96], [0])
     with pytest.raises(oracle.OracleError):
         oracle.expert_wgrad_mxfp8(x, wg, wu, wd, ids, w, dy, 3, [0], [0])
+
+
+# Flush pins for the activation operands. Each plants an outlier 2^40 times
+# the typical magnitude at position 0 of a 32-value block of one operand; with
+# that operand quantised along the block's axis the other 31 values of the
+# block round to zero (E4M3 keeps values down to 2^-17 of the block maximum),
+# so zeroing their sources leaves the watched output bit-identical -- and
+# without quantisation the same edit changes it. Zeroing in one place only
+# (the operand's own inputs) keeps every other operand's blocks unchanged.
+BIG = 2.0 ** 40
+
+
+def _flush_pair(make, watch):
+    x, wg, wu, wd, ids, w, dy = _layer(3, 64, 64, 1, 1, 11)
+    args_a, args_b = make(x, wg, wu, wd, dy)
+    for quantize, same in ((True, True), (False, False)):
+        ra = oracle.layer_mxfp8(*args_a[:4], ids, w, args_a[4], quantize=quantize)
+        rb = oracle.layer_mxfp8(*args_b[:4], ids, w, args_b[4], quantize=quantize)
+        assert np.array_equal(watch(ra), watch(rb)) == same, quantize
+
+
+def test_xe_rows_are_quantised_along_h():
+    """y[t] sees x[t] only through Xe's rows, 32-blocks along H. Column h = 0
+    of Wg and Wu is zero, so the outlier x[t, 0] sets its block's scale but
+    adds nothing to G and U (else it would swamp the neighbours' share below
+    the bf16 rounding of Act and hide a missing quantisation)."""
+    def make(x, wg, wu, wd, dy):
+        wgf, wuf = oracle.bf16_bits_to_f64(wg), oracle.bf16_bits_to_f64(wu)
+        wgf[:, :, 0] = 0.0
+        wuf[:, :, 0] = 0.0
+        xf = oracle.bf16_bits_to_f64(x)
+        xf[1, 0] = BIG
+        xz = xf.copy()
+        xz[1, 1:32] = 0.0
+        wg0, wu0 = _bits(wgf), _bits(wuf)
+        return (_bits(xf), wg0, wu0, wd, dy), (_bits(xz), wg0, wu0, wd, dy)
+    _flush_pair(make, lambda r: r["y"][1])
+
+
+def test_act_rows_are_quantised_along_i():
+    """Wu[0][0][:] scaled by 2^40 makes Act[:, 0] the outlier of block
+    i = 0..31; zeroing Wg and Wu rows 1..31 (their own row blocks along H are
+    independent) makes Act[:, 1:32] exactly 0 instead of flushed."""
+    def make(x, wg, wu, wd, dy):
+        wuf = oracle.bf16_bits_to_f64(wu)
+        wuf[0, 0, :] *= BIG
+        wgz, wuz = oracle.bf16_bits_to_f64(wg), wuf.copy()
+        wgz[0, 1:32, :] = 0.0
+        wuz[0, 1:32, :] = 0.0
+        return (x, wg, _bits(wuf), wd, dy), (x, _bits(wgz), _bits(wuz), wd, dy)
+    _flush_pair(make, lambda r: r["y"])
+
+
+def test_dye_rows_are_quantised_along_h():
+    """dx[t] sees dY[t] only through dYe's rows, 32-blocks along H (dw, the
+    routing-weight gradient, reads dY unquantised and is not watched). Row
+    h = 0 of Wd is zero, so the outlier dY[t, 0] sets its block's scale but
+    adds nothing to dAct."""
+    def make(x, wg, wu, wd, dy):
+        wdf = oracle.bf16_bits_to_f64(wd)
+        wdf[0, 0, :] = 0.0
+        wd0 = _bits(wdf)
+        df = oracle.bf16_bits_to_f64(dy)
+        df[2, 0] = BIG
+        dz = df.copy()
+        dz[2, 1:32] = 0.0
+        return (x, wg, wu, wd0, _bits(df)), (x, wg, wu, wd0, _bits(dz))
+    _flush_pair(make, lambda r: r["dx"][2])
+
+
+def test_dg_du_rows_are_quantised_along_i():
+    """Wd[0][:][0] scaled by 2^40 makes dAct[:, 0], hence dG[:, 0] and
+    dU[:, 0], the outliers of block i = 0..31; zeroing Wd columns 1..31 makes
+    dAct, dG, dU exactly 0 there instead of flushed. The forward's Wd row
+    blocks along I already flush those columns, and Wd's column blocks along H
+    are per column, so nothing else changes."""
+    def make(x, wg, wu, wd, dy):
+        wdf = oracle.bf16_bits_to_f64(wd)
+        wdf[0, :, 0] *= BIG
+        wdz = wdf.copy()
+        wdz[0, :, 1:32] = 0.0
+        return (x, wg, wu, _bits(wdf), dy), (x, wg, wu, _bits(wdz), dy)
+    _flush_pair(make, lambda r: r["dx"])
+
+
+# The same flush pins for the weight-gradient operands, whose 32-value blocks
+# run along the token axis of an expert's segment (E = 1, k = 1, 40 tokens:
+# tokens 0..31 form the first block). The outlier sits at token 0; zeroing
+# the sources of tokens 1..31 leaves the watched gradient bit-identical only
+# if that operand is quantised along tokens. Sums of the weight gradients are
+# fp64 with no rounding, so an unquantised operand's O(1) terms beside the
+# 2^40-scale one would show.
+def _wgrad_pair(make, watch):
+    x, wg, wu, wd, ids, w, dy = _layer(40, 64, 64, 1, 1, 12)
+    args_a, args_b = make(x, wg, wu, wd, dy)
+    for quantize, same in ((True, True), (False, False)):
+        ra = oracle.layer_mxfp8(*args_a[:4], ids, w, args_a[4], quantize=quantize)
+        rb = oracle.layer_mxfp8(*args_b[:4], ids, w, args_b[4], quantize=quantize)
+        assert np.array_equal(watch(ra), watch(rb)) == same, quantize
+
+
+def test_dye_columns_are_quantised_along_tokens():
+    """dWd[h0, :] = sum over tokens of dYe[:, h0] * Act: dY[0, h0] is the
+    outlier of dYe's first token block in column h0. Zeroing dY[1:32, h0]
+    changes only dYe (and, through its row blocks, dAct, which dWd does not
+    read)."""
+    h0 = 5
+
+    def make(x, wg, wu, wd, dy):
+        df = oracle.bf16_bits_to_f64(dy)
+        df[0, h0] = BIG
+        dz = df.copy()
+        dz[1:32, h0] = 0.0
+        return (x, wg, wu, wd, _bits(df)), (x, wg, wu, wd, _bits(dz))
+    _wgrad_pair(make, lambda r: r["dwd"][0, h0])
+
+
+def test_act_columns_are_quantised_along_tokens():
+    """x[0] scaled by 2^12 makes Act[0, i0] (i0 with G and U well away from 0
+    for token 0) the outlier of Act's first token block in column i0; zeroing
+    x rows 1..31 makes their Act exactly 0. dYe is untouched, so dWd[:, i0]
+    can change only through Act's column blocks."""
+    def make(x, wg, wu, wd, dy):
+        xf = oracle.bf16_bits_to_f64(x)
+        g = oracle.bf16_bits_to_f64(wg)[0] @ xf[0]
+        u = oracle.bf16_bits_to_f64(wu)[0] @ xf[0]
+        i0 = int(np.argmax(np.where(g > 0, g * np.abs(u), -np.inf)))
+        make.i0 = i0
+        xf[0] *= 2.0 ** 12
+        xz = xf.copy()
+        xz[1:32] = 0.0
+        return (_bits(xf), wg, wu, wd, dy), (_bits(xz), wg, wu, wd, dy)
+    _wgrad_pair(make, lambda r: r["dwd"][0][:, make.i0])
+
+
+def test_xe_columns_are_quantised_along_tokens():
+    """dWg[:, h0], dWu[:, h0] read x[:, h0] through Xe's token blocks.
+    Column h0 of Wg and Wu is zero, so x[:, h0] changes no G or U; the values
+    x[1:32, h0] are made small so they never set their row block's scale."""
+    h0 = 7
+
+    def make(x, wg, wu, wd, dy):
+        wgf, wuf = oracle.bf16_bits_to_f64(wg), oracle.bf16_bits_to_f64(wu)
+        wgf[:, :, h0] = 0.0
+        wuf[:, :, h0] = 0.0
+        xf = oracle.bf16_bits_to_f64(x)
+        xf[0, h0] = BIG
+        xf[1:32, h0] = 2.0 ** -6
+        xz = xf.copy()
+        xz[1:32, h0] = 0.0
+        wg0, wu0 = _bits(wgf), _bits(wuf)
+        return (_bits(xf), wg0, wu0, wd, dy), (_bits(xz), wg0, wu0, wd, dy)
+    _wgrad_pair(make, lambda r: np.concatenate([r["dwg"][0][:, h0], r["dwu"][0][:, h0]]))
+
+
+def test_dg_du_columns_are_quantised_along_tokens():
+    """dY[0] scaled by 2^40 scales dYe, dAct, dG and dU of token 0 by 2^40
+    (a power of two passes through every rounding unchanged), making token 0
+    the outlier of every dG and dU column's first token block; zeroing dY
+    rows 1..31 makes their dG and dU exactly 0. x is untouched, so dWg and dWu
+    can change only through dG's and dU's column blocks."""
+    def make(x, wg, wu, wd, dy):
+        df = oracle.bf16_bits_to_f64(dy)
+        df[0] *= BIG
+        dz = df.copy()
+        dz[1:32] = 0.0
+        return (x, wg, wu, wd, _bits(df)), (x, wg, wu, wd, _bits(dz))
+    _wgrad_pair(make, lambda r: np.concatenate([r["dwg"].ravel(), r["dwu"].ravel()]))
