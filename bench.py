@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--gather", action="store_true",
                     help="with --inference: time the gate/up GEMM with the dispatch fused into "
                          "its producer (moe_expert_gate_up_gather)")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured once in a CUDA graph and replayed "
+                         "(reported as \"graph\"; the headline stays the eager step)")
     return ap.parse_args()
 
 
@@ -133,6 +136,34 @@ def rerun_check(step, outputs, digest_keys=("y", "dx", "d_topk_w")):
     del first
     return {"rerun_bitwise_equal": all(same.values()), "compared": list(outputs),
             "sha256": digest, "sha256_of": [k for k in digest_keys if k in outputs]}
+
+
+def graph_timing(step, warmup, K, ws_, tokens, dev):
+    """The same step captured once in a CUDA graph, replayed warmup + K times;
+    the K replays timed with CUDA events like the eager steps. The library
+    enqueues everything on the capturing stream and never allocates or
+    synchronises, so the capture holds the whole pass."""
+    import torch
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if ws_ > 1:
+        torch.distributed.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    s = torch.cuda.current_stream()
+    t0.record(s)
+    for _ in range(K):
+        graph.replay()
+    t1.record(s)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1), ws_, dev)
+    del graph
+    return {"ms_per_step": round(ms / K, 4),
+            "value": round(replica_throughput(tokens, K, ws_, ms), 1)}
 
 
 def expert_loads(counts, tile_rows=128):
@@ -419,6 +450,8 @@ def run_ours(args, ws_, rank, local, shape=None):
              for i, ph in enumerate(phases)}
     assert layer.device_error() == 0, "device error in the timed region"
 
+    graph = graph_timing(step, args.warmup, K, ws_, shape.N, dev) if args.graph else None
+
     # ---- end to end through the public API with host buffers ----
     # Every step copies its inputs (x, logits, dy) from pinned host memory and
     # reads its outputs (y, dx) back. Two buffer sets (two MoELayer objects)
@@ -573,6 +606,8 @@ def run_ours(args, ws_, rank, local, shape=None):
         "determinism": determinism,
         "expert_loads": loads,
     }
+    if graph is not None:
+        rec["graph"] = graph
     if args.overlap and backward and not mx:
         rec["config"]["backward"] = ("moe_backward_overlap: reverse-combine run by side warps of "
                                      "the down data-gradient GEMM")
