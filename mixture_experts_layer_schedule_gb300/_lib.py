@@ -129,10 +129,26 @@ def _check(name, status):
 
 
 def _ptr(t):
+    """Device address of a tensor argument (None -> NULL; an int is taken as a
+    raw address). The kernels read and write dense row-major device buffers,
+    so a strided view or a host tensor raises here, before the library sees
+    it: a host address would fault on the GPU instead of failing cleanly."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_contiguous():
+        raise ValueError(f"expected a contiguous tensor, got strides {tuple(t.stride())} "
+                         f"for shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
+    return t.data_ptr()
+
+
+def _host_ptr(t):
+    """Address of a pinned host tensor (the library's host-side outputs)."""
+    if not t.is_pinned():
+        raise ValueError("expected a pinned host tensor")
     return t.data_ptr()
 
 
@@ -338,7 +354,7 @@ def mxfp8_qdq(src, dst, rows, cols, axis, stream=None):
 def moe_get_device_error(p, ws, stream=None) -> int:
     """Reads the device error word (synchronises the stream)."""
     out = torch.zeros(1, dtype=torch.int32, pin_memory=True)
-    _call("moe_get_device_error", ctypes.byref(p), _ptr(ws), _ptr(out), _stream(stream))
+    _call("moe_get_device_error", ctypes.byref(p), _ptr(ws), _host_ptr(out), _stream(stream))
     (torch.cuda.current_stream() if stream is None else stream).synchronize() \
         if not isinstance(stream, int) else torch.cuda.synchronize()
     return int(out.item())

@@ -73,3 +73,19 @@ def test_null_and_misaligned_pointers_are_rejected_before_any_launch(lib):
     st = lib.mxfp8_quantize(16, 4, 48, 16, 16, None)  # cols not a multiple of 32
     assert st == _lib.MOE_ERR_INVALID_ARG
     assert lib.moe_status_string(_lib.MOE_ERR_CUDA) == b"CUDA runtime or driver error"
+
+
+def test_binding_rejects_host_and_strided_tensors_before_the_library():
+    """A host tensor would hand the kernels a host address (a GPU fault, not an
+    error status), and a strided view the wrong layout: the binding raises on
+    both before any library call."""
+    torch = pytest.importorskip("torch")
+    p = _lib.problem(64, 256, 256, 4, 2)
+    host = torch.zeros(64, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        _lib.moe_dispatch(p, 256, host, 512)
+    with pytest.raises(ValueError, match="contiguous"):
+        _lib.moe_dispatch(p, 256, host.t(), 512)
+    with pytest.raises(ValueError, match="contiguous"):
+        _lib.mxfp8_quantize(host[:, ::2], 64, 128, 256, 512)
+    assert _lib._ptr(None) is None and _lib._ptr(4096) == 4096
