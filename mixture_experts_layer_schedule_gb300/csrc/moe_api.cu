@@ -28,9 +28,12 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   if (p->dtype != MOE_BF16 && p->dtype != MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
   const int32_t T = p->minibatch_rows == 0 ? kTileM : p->minibatch_rows;
   if (T != 128 && T != 256 && T != 512 && T != 1024) return MOE_ERR_UNSUPPORTED;
+  // rows, slots and tile coordinates are int32 on the device; bound N before
+  // forming N * k so that the product cannot overflow
+  if (p->N > (1LL << 31) / p->k) return MOE_ERR_UNSUPPORTED;
   const int64_t A = p->N * p->k;
   const int64_t R = (A + static_cast<int64_t>(p->E) * (T - 1) + T - 1) / T * T;
-  if (R >= (1LL << 31) - 1 || p->N > (1LL << 31) / p->k) return MOE_ERR_UNSUPPORTED;
+  if (R >= (1LL << 31) - 1) return MOE_ERR_UNSUPPORTED;
   L->N = p->N;
   L->A = A;
   L->R = R;

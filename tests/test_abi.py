@@ -47,10 +47,17 @@ def test_sizes_and_validation(lib):
     for bad, status in (((256, 200, 512, 8, 2), _lib.MOE_ERR_UNSUPPORTED),
                         ((256, 256, 512, 8, 9), _lib.MOE_ERR_INVALID_ARG),
                         ((256, 256, 512, 2048, 2), _lib.MOE_ERR_UNSUPPORTED),
-                        ((-1, 256, 512, 8, 2), _lib.MOE_ERR_INVALID_ARG)):
+                        ((-1, 256, 512, 8, 2), _lib.MOE_ERR_INVALID_ARG),
+                        # int32 rows on the device: N * k (+ padding) must fit
+                        ((2 ** 62, 256, 512, 8, 8), _lib.MOE_ERR_UNSUPPORTED),
+                        ((2 ** 28, 256, 512, 8, 8), _lib.MOE_ERR_UNSUPPORTED),
+                        # N * k = 2^31 - 512 fits, but not with E * (T - 1) padding rows
+                        ((2 ** 28 - 64, 256, 512, 8, 8), _lib.MOE_ERR_UNSUPPORTED)):
         with pytest.raises(_lib.MoEError) as ei:
             _lib.moe_workspace_bytes(_lib.problem(*bad))
         assert ei.value.status == status
+    # the largest sizes below the bound are accepted (host-side sizing only)
+    assert _lib.moe_workspace_bytes(_lib.problem(2 ** 28 - 2 ** 16, 256, 512, 8, 8)) > 0
     for bad_kw in (dict(dtype=7), dict(minibatch_rows=192), dict(minibatch_rows=2048)):
         with pytest.raises(_lib.MoEError) as ei:
             _lib.moe_workspace_bytes(_lib.problem(256, 256, 512, 8, 2, **bad_kw))
