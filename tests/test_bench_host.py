@@ -42,3 +42,43 @@ def test_rerun_check_sees_a_changed_bit():
     def flip_sign_of_zero():  # -0.0 == 0.0 as floats, not as bytes
         out["dx"][3] = -0.0
     assert not bench.rerun_check(flip_sign_of_zero, out)["rerun_bitwise_equal"]
+
+
+def _run_bench(args, env_extra=None):
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ)
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        env.pop(k, None)
+    env.update(env_extra or {})
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py")] + args, env=env,
+                       capture_output=True, text=True, timeout=600, cwd=root)
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    return r.returncode, [json.loads(ln) for ln in lines]
+
+
+def test_reference_arm_prints_one_complete_line():
+    """The oracle arm's JSON line carries the keys of the bench line, on the
+    workload it is given (a tiny one here, so this runs in seconds)."""
+    rc, lines = _run_bench(["--impl", "reference", "--config", "256,256,512,8,2",
+                            "--steps", "1", "--warmup", "0"])
+    assert rc == 0 and len(lines) == 1
+    r = lines[0]
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in r, key
+    assert r["impl"] == "reference" and r["unit"] == "tokens/s" and r["value"] > 0
+    assert r["e2e"]["value"] == r["value"] and r["e2e"]["h2d_bytes_per_step"] == 0
+    assert r["cpu_baseline"]["kind"] == "oracle" and r["cpu_baseline"]["cores"] >= 1
+    assert r["config"]["workload"] == "custom_N256_H256_I512_E8_k2_T128"
+
+
+def test_reference_arm_on_a_non_zero_rank_exits_quietly():
+    rc, lines = _run_bench(["--impl", "reference", "--config", "256,256,512,8,2",
+                            "--steps", "1", "--warmup", "0"],
+                           {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert rc == 0 and lines == []
