@@ -6,9 +6,11 @@ CPU-baseline leg of ``bench.py`` may import this package; the product path
 the CUDA path: it is a plain C++ library (``moe_oracle.cpp``) loaded with
 ctypes, plus the numpy marshalling below.
 
-Parity status: every function here is pinned by ``tests/test_oracle_*.py``
-(brute force, closed forms, finite differences, library routines, published
-E4M3 code points); none is "parity unpinned".
+Parity status: every function here is pinned by ``tests/test_oracle_*.py`` and
+``tests/test_golden.py`` (brute force, closed forms, finite differences,
+library routines, code points fixed by the OCP MXFP8 specifications, a flush
+pin for every MXFP8 quantisation point, and bit-exact agreement of the
+sampled functions with the whole-layer ones); none is "parity unpinned".
 """
 from __future__ import annotations
 
