@@ -96,3 +96,37 @@ def test_binding_rejects_host_and_strided_tensors_before_the_library():
     with pytest.raises(ValueError, match="contiguous"):
         _lib.mxfp8_quantize(host[:, ::2], 64, 128, 256, 512)
     assert _lib._ptr(None) is None and _lib._ptr(4096) == 4096
+
+
+@pytest.mark.parametrize("N,H,I,E,k,dtype,T", [(256, 256, 512, 8, 2, 0, 128),
+                                               (300, 512, 768, 16, 4, 1, 256),
+                                               (16384, 4096, 1536, 128, 8, 1, 128),
+                                               (0, 256, 256, 4, 2, 0, 1024)])
+def test_workspace_and_context_regions_are_disjoint_and_aligned(lib, N, H, I, E, k, dtype, T):
+    """The host-side carving of the workspace (schedule tables) and of the
+    saved context (Xe, G, U, Act, Ye): every region 256-byte aligned, inside
+    its buffer and disjoint from the others, at the documented sizes. Pure
+    address arithmetic on a fake base address; nothing is launched."""
+    p = _lib.problem(N, H, I, E, k, dtype=dtype, minibatch_rows=T)
+    R = _lib.moe_grouped_rows(p)
+    base = 1 << 40
+    ws_bytes, sv_bytes = _lib.moe_workspace_bytes(p), _lib.moe_saved_bytes(p)
+
+    def check(regions, total):
+        spans = sorted((addr - base, n, name) for name, addr, n in regions)
+        for off, n, name in spans:
+            assert off % 256 == 0 and 0 <= off and off + n <= total, name
+        for (o1, n1, a), (o2, _, b) in zip(spans, spans[1:]):
+            assert o1 + n1 <= o2, (a, b)
+
+    sched = _lib.Schedule()
+    assert lib.moe_schedule_view(ctypes.byref(p), base, ctypes.byref(sched)) == _lib.MOE_OK
+    A = N * k
+    check([("counts", sched.counts, 4 * E), ("offsets", sched.offsets, 4 * (E + 1)),
+           ("pad_offsets", sched.pad_offsets, 4 * (E + 1)), ("slot_of", sched.slot_of, 4 * A),
+           ("src_of_row", sched.src_of_row, 4 * R), ("tiles", sched.tiles, 12 * (R // 128)),
+           ("n_tiles", sched.n_tiles, 4)], ws_bytes)
+    sv = _lib.SavedView()
+    assert lib.moe_saved_layout(ctypes.byref(p), base, ctypes.byref(sv)) == _lib.MOE_OK
+    check([("xe", sv.xe, 2 * R * H), ("g", sv.g, 2 * R * I), ("u", sv.u, 2 * R * I),
+           ("act", sv.act, 2 * R * I), ("ye", sv.ye, 2 * R * H)], sv_bytes)
