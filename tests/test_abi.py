@@ -122,10 +122,15 @@ def test_workspace_and_context_regions_are_disjoint_and_aligned(lib, N, H, I, E,
     sched = _lib.Schedule()
     assert lib.moe_schedule_view(ctypes.byref(p), base, ctypes.byref(sched)) == _lib.MOE_OK
     A = N * k
-    check([("counts", sched.counts, 4 * E), ("offsets", sched.offsets, 4 * (E + 1)),
-           ("pad_offsets", sched.pad_offsets, 4 * (E + 1)), ("slot_of", sched.slot_of, 4 * A),
-           ("src_of_row", sched.src_of_row, 4 * R), ("tiles", sched.tiles, 12 * (R // 128)),
-           ("n_tiles", sched.n_tiles, 4)], ws_bytes)
+    regions = [("counts", sched.counts, 4 * E), ("offsets", sched.offsets, 4 * (E + 1)),
+               ("pad_offsets", sched.pad_offsets, 4 * (E + 1)), ("slot_of", sched.slot_of, 4 * A),
+               ("src_of_row", sched.src_of_row, 4 * R), ("tiles", sched.tiles, 12 * (R // 128)),
+               ("n_tiles", sched.n_tiles, 4)]
+    if dtype == _lib.MOE_MXFP8:  # the forward's row-form MXFP8 operands of Xe and Act
+        (xq, xs), (aq, as_) = _lib.moe_mxfp8_forward_operands(p, base)
+        regions += [("xe_q", xq, R * H), ("xe_s", xs, R * H // 32), ("act_q", aq, R * I),
+                    ("act_s", as_, R * I // 32)]
+    check(regions, ws_bytes)
     sv = _lib.SavedView()
     assert lib.moe_saved_layout(ctypes.byref(p), base, ctypes.byref(sv)) == _lib.MOE_OK
     check([("xe", sv.xe, 2 * R * H), ("g", sv.g, 2 * R * I), ("u", sv.u, 2 * R * I),
