@@ -655,6 +655,14 @@ def cpu_sample(shape, inp, n_tok, threads, router=False):
     return time.perf_counter() - t0 + (t_router if router else 0.0), n_tok
 
 
+def one_core(shape, inp, router=False, n_tok=8):
+    """The oracle on one host thread, on the first n_tok tokens: the baseline's
+    single-core rate beside its all-cores one."""
+    secs, n = cpu_sample(shape, inp, n_tok, 1, router)
+    return {"value": round(n / secs, 3), "unit": UNIT, "cores": 1,
+            "sample": f"first {n} tokens, {secs:.1f} s"}
+
+
 def run_reference(args, ws_, rank):
     """The oracle, timed on the host cores, on bounded samples of the workload."""
     if rank != 0:
@@ -685,7 +693,8 @@ def run_reference(args, ws_, rank):
                          "sample": f"first {n_tok} tokens of the workload per step "
                                    f"(full expert weights, fwd+bwd with weight gradients"
                                    f"{MX_NOTE if shape.dtype == 'mxfp8' else ''}"
-                                   f"{ROUTER_NOTE if args.router else ''})"},
+                                   f"{ROUTER_NOTE if args.router else ''})",
+                         "one_core": one_core(shape, inp, args.router)},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -739,6 +748,7 @@ def main():
                                          f"{MX_NOTE if shape.dtype == 'mxfp8' else ''}"
                                          f"{ROUTER_NOTE if args.router else ''}), "
                                          f"{secs:.1f} s"}
+        rec["cpu_baseline"]["one_core"] = one_core(shape, inp, args.router)
     if rank == 0:
         if not args.phase_report:
             rec.pop("phases", None)

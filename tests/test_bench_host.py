@@ -74,6 +74,8 @@ def test_reference_arm_prints_one_complete_line():
     assert r["impl"] == "reference" and r["unit"] == "tokens/s" and r["value"] > 0
     assert r["e2e"]["value"] == r["value"] and r["e2e"]["h2d_bytes_per_step"] == 0
     assert r["cpu_baseline"]["kind"] == "oracle" and r["cpu_baseline"]["cores"] >= 1
+    one = r["cpu_baseline"]["one_core"]
+    assert one["cores"] == 1 and one["value"] > 0 and one["unit"] == "tokens/s"
     assert r["config"]["workload"] == "custom_N256_H256_I512_E8_k2_T128"
 
 
