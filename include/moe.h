@@ -31,6 +31,14 @@
  *  - Determinism: identical inputs give bitwise-identical outputs. No
  *    floating-point atomics are used; every reduction has a fixed order.
  *  - Pointers to device buffers must be 16-byte aligned; row-major layouts.
+ *  - Stream capture: the first call of each kernel family on a device does
+ *    one-time host setup (shared-memory attributes, cluster occupancy query,
+ *    the scratch address of moe_build_schedule_noalloc). After one eager call
+ *    of the same entry points, a sequence of calls can be captured into a
+ *    CUDA graph and replayed; the graph reads its buffers at replay time.
+ *    The schedule is rebuilt on the device, so new routing needs no new
+ *    capture. moe_get_device_error copies to host memory, so call it outside
+ *    a capture.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
