@@ -193,3 +193,46 @@ def test_expert_with_no_tokens_has_zero_gradient():
     r = oracle.backward_f64(x, wg, wu, wd, ids, w, dy)
     assert np.all(r["dwg"][[0, 2]] == 0) and np.all(r["dwd"][[0, 2]] == 0)
     assert np.any(r["dwg"][1] != 0)
+
+
+def test_forward_and_backward_equal_torch_autograd():
+    """An independent library routine: the layer written with torch CPU fp64
+    ops (F.silu for the activation, index_add for the weighted combine) and
+    differentiated by autograd gives the oracle's y and every gradient, at
+    the tiny workload's shape (N=256, H=256, I=512, E=8, top-2)."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    N, H, I, E, k = 256, 256, 512, 8, 2
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((N, H))
+    wg, wu, wd = (rng.standard_normal(s) / np.sqrt(H) for s in ((E, I, H), (E, I, H), (E, H, I)))
+    dy = rng.standard_normal((N, H))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(N)]).astype(np.int32)
+    w = rng.random((N, k)) + 0.05
+    w /= w.sum(1, keepdims=True)
+    y_ref = oracle.forward_f64(x, wg, wu, wd, ids, w)
+    g_ref = oracle.backward_f64(x, wg, wu, wd, ids, w, dy)
+
+    X, WG, WU, WD, W = (torch.tensor(a, requires_grad=True) for a in (x, wg, wu, wd, w))
+    y = torch.zeros(N, H, dtype=torch.float64)
+    ids_t = torch.as_tensor(ids, dtype=torch.long)
+    for j in range(k):
+        for e in range(E):
+            sel = torch.nonzero(ids_t[:, j] == e).flatten()
+            if len(sel) == 0:
+                continue
+            xs = X[sel]
+            act = F.silu(xs @ WG[e].T) * (xs @ WU[e].T)
+            y = y.index_add(0, sel, W[sel, j:j + 1] * (act @ WD[e].T))
+    (y * torch.as_tensor(dy)).sum().backward()
+
+    def close(got, ref):
+        scale = np.max(np.abs(ref))
+        np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12 * scale)
+
+    close(y.detach().numpy(), y_ref)
+    close(X.grad.numpy(), g_ref["dx"])
+    close(WG.grad.numpy(), g_ref["dwg"])
+    close(WU.grad.numpy(), g_ref["dwu"])
+    close(WD.grad.numpy(), g_ref["dwd"])
+    close(W.grad.numpy(), g_ref["dw"])
