@@ -119,11 +119,10 @@ struct TileInfo {
   bool fold;  // SM-pair item of 128 rows: M=128 pair MMA, 64 rows per CTA
 };
 
-// Tile t of this CTA. With CL = 2 (a cluster of two CTAs), t numbers pair
-// tiles and `crank` (the CTA's rank in the cluster) picks the member: the
-// two members share the A tile (token-row modes: neighbouring N tiles) or the
-// B tile (WGRAD: neighbouring M tiles), which they load once, half each,
-// multicast to both.
+// Tile t of this CTA. With CL = 2 (the two CTAs of an SM pair), t numbers
+// pair tiles and `crank` (the CTA's rank in the pair) picks the member: in
+// WGRAD the members take neighbouring M tiles of one expert, which share the
+// B tile of the pair MMA.
 template <int MODE, int CL>
 __device__ __forceinline__ TileInfo decode_tile(const Args& a, int64_t t, int crank) {
   TileInfo ti;
@@ -198,10 +197,9 @@ __device__ __forceinline__ int64_t total_tiles(const Args& a) {
 }
 
 // Loads of one k-block for the single-CTA kernel's modes.
-template <int MODE, int CL>
+template <int MODE>
 __device__ __forceinline__ void issue_loads(const Maps& m, const Args& a, const TileInfo& ti,
-                                            int kb, uint8_t* sA, uint8_t* sB, uint64_t* bar,
-                                            int crank) {
+                                            int kb, uint8_t* sA, uint8_t* sB, uint64_t* bar) {
   static_assert(MODE == GATE_UP_GATHER || MODE == ROUTER, "single-CTA kernel modes");
   if constexpr (MODE == ROUTER) {
     tma_load_2d(sA, &m.a0, bar, kb * BK, ti.row0);
@@ -400,7 +398,7 @@ __device__ __forceinline__ void epilogue_router(const Maps& m, const Args& a, co
                stage_out, nstore);
 }
 
-template <int MODE, int CL>
+template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ Maps maps, const Args args) {
   static_assert(MODE == GATE_UP_GATHER || MODE == ROUTER, "single-CTA kernel modes");
@@ -415,7 +413,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], CL);  // both CTAs of a pair must have read the stage
+      mbar_init(&empty_bar[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
@@ -435,35 +433,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (CL > 1) cluster_sync();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_slot;
   volatile int* abortp = &abort_flag;
-  const int64_t total = total_tiles<MODE, CL>(args);
-  const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int64_t first = blockIdx.x / CL, stride = gridDim.x / CL;
+  const int64_t total = total_tiles<MODE, 1>(args);
+  const int64_t first = blockIdx.x, stride = gridDim.x;
 
   if (warp == 0 && MODE == GATE_UP_GATHER) {
    if constexpr (MODE == GATE_UP_GATHER) {
     // ---------------- TMA producer, gathering A rows (whole warp) ----------------
-    // Lane l owns rows 4l..4l+3 of the CTA's share of the 128-row tile (all of
-    // it, or with CL = 2 one 64-row half, multicast to both CTAs of the pair,
-    // which compute neighbouring N tiles of the same rows): it looks up their
-    // tokens once per tile and issues one gather4 per k-block; lane 0 arms the
-    // stage barrier and loads the gate/up weight rows.
-    constexpr int kRowsPerCta = BM / CL;
-    const bool gathers = lane < kRowsPerCta / 4;
-    const int rbase = crank * kRowsPerCta + 4 * lane;
+    // Lane l owns rows 4l..4l+3 of the 128-row tile: it looks up their tokens
+    // once per tile and issues one gather4 per k-block into this CTA's own
+    // stage; lane 0 arms the stage barrier and loads the gate/up weight rows.
+    const int rbase = 4 * lane;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
     bool ok = true;
     for (int64_t t = first; t < total && ok; t += stride) {
-      const TileInfo ti = decode_tile<MODE, CL>(args, t, crank);
+      const TileInfo ti = decode_tile<MODE, 1>(args, t, 0);
       int32_t tok[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int32_t src = (ti.nkb > 0 && gathers) ? args.src_of_row[ti.row0 + rbase + r] : -1;
+        const int32_t src = ti.nkb > 0 ? args.src_of_row[ti.row0 + rbase + r] : -1;
         tok[r] = src >= 0 ? src / args.k : 0;  // padding rows read token 0 (finite, unused)
       }
       for (int kb = 0; kb < ti.nkb; ++kb) {
@@ -474,14 +466,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint8_t* sA = smem + stage * kStageBytes;
         if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
         __syncwarp();
-        if (gathers) {
-          if constexpr (CL == 1)
-            tma_gather4(sA + rbase * (BK * 2), &maps.a0, &full_bar[stage], kb * BK, tok[0],
-                        tok[1], tok[2], tok[3]);
-          else
-            tma_gather4_mc(sA + rbase * (BK * 2), &maps.a0, &full_bar[stage], kb * BK, tok[0],
-                           tok[1], tok[2], tok[3], (1u << CL) - 1);
-        }
+        tma_gather4(sA + rbase * (BK * 2), &maps.a0, &full_bar[stage], kb * BK, tok[0], tok[1],
+                    tok[2], tok[3]);
         if (lane == 0) {
           const int brow = ti.e * args.b_rows + ti.nt * (BN / 2);
           tma_load_2d(sA + kABytes, &maps.b0, &full_bar[stage], kb * BK, brow);
@@ -504,12 +490,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t issued_mask = 0, issued_parity = 0;
       bool ok = true;
       for (int64_t t = first; t < total && ok; t += stride) {
-        const TileInfo ti = decode_tile<MODE, CL>(args, t, crank);
+        const TileInfo ti = decode_tile<MODE, 1>(args, t, 0);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, args.err)) { ok = false; break; }
           uint8_t* sA = smem + stage * kStageBytes;
           mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
-          issue_loads<MODE, CL>(maps, args, ti, kb, sA, sA + kABytes, &full_bar[stage], crank);
+          issue_loads<MODE>(maps, args, ti, kb, sA, sA + kABytes, &full_bar[stage]);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -529,7 +515,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int64_t t = first; t < total && ok; t += stride) {
-        const TileInfo ti = decode_tile<MODE, CL>(args, t, crank);
+        const TileInfo ti = decode_tile<MODE, 1>(args, t, 0);
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abortp, args.err)) break;
         tc_fence_after();
         const uint32_t dtmem = tmem_base + acc * BN;
@@ -547,8 +533,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             else bd = sdesc_sw128(b_addr + ks * 32, 16, 1024);
             umma_bf16(dtmem, ad, bd, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
           }
-          if constexpr (CL == 1) umma_commit(&empty_bar[stage]);  // stage free once read
-          else umma_commit_mc(&empty_bar[stage], (1u << CL) - 1);  // ... in every CTA's view
+          umma_commit(&empty_bar[stage]);  // stage free once read
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -566,7 +551,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = first; t < total; t += stride) {
-      const TileInfo ti = decode_tile<MODE, CL>(args, t, crank);
+      const TileInfo ti = decode_tile<MODE, 1>(args, t, 0);
       if (!mbar_wait(&tfull_bar[acc], acc_phase, abortp, args.err)) break;
       tc_fence_after();
       if (ti.skip) {
@@ -590,7 +575,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
-  if constexpr (CL > 1) cluster_sync();  // no CTA leaves while its peer may still write to it
 }
 
 // ---------------------------------------------------------------------------
@@ -1094,55 +1078,20 @@ int sm_count() {
   return n > 0 ? n : 148;
 }
 
-// Launch a persistent grid: one CTA per SM (CL = 1), or as many co-resident
-// CTA pairs as the GPU holds (CL = 2, clusters of two), capped by the work
-// units (tiles, or pair tiles) available.
-template <int MODE, int CL>
+// Launch the single-CTA kernel as a persistent grid: one CTA per SM,
+// capped by the tiles available.
+template <int MODE>
 moe_status launch(const Maps& maps, const Args& args, int64_t units, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  static int max_clusters = 0;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, CL>,
+    attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (attr_err == cudaSuccess && CL > 1) {
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute at[1];
-      at[0].id = cudaLaunchAttributeClusterDimension;
-      at[0].val.clusterDim.x = CL;
-      at[0].val.clusterDim.y = 1;
-      at[0].val.clusterDim.z = 1;
-      cfg.gridDim = dim3(CL * 64);
-      cfg.blockDim = dim3(kGemmThreads);
-      cfg.dynamicSmemBytes = kSmemBytes;
-      cfg.attrs = at;
-      cfg.numAttrs = 1;
-      attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_kernel<MODE, CL>, &cfg);
-      if (attr_err == cudaSuccess && max_clusters <= 0) attr_err = cudaErrorInvalidConfiguration;
-    }
   });
   if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
   if (units <= 0) return MOE_OK;
-  if constexpr (CL == 1) {
-    const int grid = static_cast<int>(std::min<int64_t>(sm_count(), units));
-    grouped_gemm_kernel<MODE, 1><<<grid, kGemmThreads, kSmemBytes, s>>>(maps, args);
-  } else {
-    const int clusters = static_cast<int>(std::min<int64_t>(max_clusters, units));
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = CL;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(CL * clusters);
-    cfg.blockDim = dim3(kGemmThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = s;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, CL>, maps, args) != cudaSuccess)
-      return MOE_ERR_CUDA;
-  }
+  const int grid = static_cast<int>(std::min<int64_t>(sm_count(), units));
+  grouped_gemm_kernel<MODE><<<grid, kGemmThreads, kSmemBytes, s>>>(maps, args);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -1241,7 +1190,7 @@ moe_status gemm_router(const Layout& L, const void* ws, const void* x, const voi
   a.kb1 = L.H / BK;
   a.kb2 = 0;
   a.ld_out = L.E;
-  return launch<ROUTER, 1>(m, a, a.max_mtiles, s);
+  return launch<ROUTER>(m, a, a.max_mtiles, s);
 }
 
 moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const void* wg,
@@ -1292,14 +1241,7 @@ moe_status gemm_gate_up_gather(const Layout& L, const void* ws, const void* x, c
   a.src_of_row = at<int32_t>(ws, L.src_of_row);
   a.k = L.k;
   a.store_gu = store_gu ? 1 : 0;
-  // clusters of four CTAs (neighbouring N tiles of the same rows) gather a
-  // quarter of the rows each and multicast them: the gather instruction count
-  // per CTA, not bandwidth, limits a gathering producer
-  if (a.n_nt % 4 == 0)
-    return launch<GATE_UP_GATHER, 4>(m, a, static_cast<int64_t>(a.max_mtiles) * (a.n_nt / 4), s);
-  if (a.n_nt % 2 == 0)
-    return launch<GATE_UP_GATHER, 2>(m, a, static_cast<int64_t>(a.max_mtiles) * (a.n_nt / 2), s);
-  return launch<GATE_UP_GATHER, 1>(m, a, static_cast<int64_t>(a.max_mtiles) * a.n_nt, s);
+  return launch<GATE_UP_GATHER>(m, a, static_cast<int64_t>(a.max_mtiles) * a.n_nt, s);
 }
 
 moe_status gemm_down(const Layout& L, const void* ws, const void* act, const void* wd, void* ye,

@@ -8,8 +8,7 @@
 // op); the activations are quantised per 1x32 block along each GEMM's K, so
 // every product the MMA forms is a product of two MXFP8 numbers.
 //
-// Structure (one persistent CTA per SM, clusters of two CTAs that share the A
-// tile by multicast, as in the bf16 kernels):
+// Structure (one persistent CTA per SM, each loading its own tiles):
 //   warp 0      producer: TMA loads of the A (token rows) and B (weight rows)
 //               tiles, 128 K values per stage, and 1-D bulk copies of the
 //               matching scale chunks (512 bytes per 128 rows);
@@ -153,23 +152,20 @@ struct QTile {
   bool skip;
 };
 
-// Tile t of this CTA. With CL = 2 the two CTAs of a cluster take neighbouring
-// N tiles of the same A rows (token rows, or dW rows of one expert and
-// problem) and load that A tile once, half each, multicast to both.
-template <int MODE, int CL>
-__device__ __forceinline__ QTile q_decode(const QArgs& a, int64_t t, int crank) {
+// Tile t of this CTA.
+template <int MODE>
+__device__ __forceinline__ QTile q_decode(const QArgs& a, int64_t t) {
   QTile ti;
   ti.skip = false;
   if constexpr (MODE == Q_WGRAD) {
     // Largest experts first; within an expert (mt, N tile pair, problem), the
     // problem fastest, so dWg and dWu tiles reading one Xe panel run together.
-    const int w_ntp = a.w_nt / CL;
-    const int64_t per_e = static_cast<int64_t>(a.w_mt) * w_ntp * a.n_probs;
+    const int64_t per_e = static_cast<int64_t>(a.w_mt) * a.w_nt * a.n_probs;
     const int rank = static_cast<int>(t / per_e);
     int64_t r = t % per_e;
-    ti.mt = static_cast<int>(r / (w_ntp * a.n_probs));
-    r %= (w_ntp * a.n_probs);
-    ti.nt = static_cast<int>(r / a.n_probs) * CL + crank;
+    ti.mt = static_cast<int>(r / (a.w_nt * a.n_probs));
+    r %= (a.w_nt * a.n_probs);
+    ti.nt = static_cast<int>(r / a.n_probs);
     ti.prob = static_cast<int>(r % a.n_probs);
     ti.e = a.order[rank];
     if (ti.e < 0 || ti.e >= a.E) ti.e = 0;
@@ -184,9 +180,8 @@ __device__ __forceinline__ QTile q_decode(const QArgs& a, int64_t t, int crank) 
       ti.skip = true;
     }
   } else {
-    const int n_ntp = a.n_nt / CL;
-    const int mtile = static_cast<int>(t / n_ntp);
-    ti.nt = static_cast<int>(t % n_ntp) * CL + crank;
+    const int mtile = static_cast<int>(t / a.n_nt);
+    ti.nt = static_cast<int>(t % a.n_nt);
     ti.mt = mtile;
     ti.prob = 0;
     ti.kstart = 0;
@@ -203,23 +198,22 @@ __device__ __forceinline__ QTile q_decode(const QArgs& a, int64_t t, int crank) 
   return ti;
 }
 
-template <int MODE, int CL>
+template <int MODE>
 __device__ __forceinline__ int64_t q_total(const QArgs& a) {
   if constexpr (MODE == Q_WGRAD) {
-    return static_cast<int64_t>(a.n_probs) * a.E * a.w_mt * (a.w_nt / CL);
+    return static_cast<int64_t>(a.n_probs) * a.E * a.w_mt * a.w_nt;
   } else {
     int n = *a.n_tiles;
     n = n < 0 ? 0 : (n > a.max_mtiles ? a.max_mtiles : n);
-    return static_cast<int64_t>(n) * (a.n_nt / CL);
+    return static_cast<int64_t>(n) * a.n_nt;
   }
 }
 
-// The copies of one stage: A (whole, or this CTA's multicast half), B, and
-// the scale chunks of both. Coordinates are (K element, row).
-template <int MODE, int CL>
+// The copies of one stage: A, B, and the scale chunks of both. Coordinates
+// are (K element, row).
+template <int MODE>
 __device__ __forceinline__ void q_issue_loads(const QMaps& m, const QArgs& a, const QTile& ti,
-                                              int kb, uint8_t* sA, uint8_t* sSa, uint64_t* bar,
-                                              int crank) {
+                                              int kb, uint8_t* sA, uint8_t* sSa, uint64_t* bar) {
   uint8_t* sB = sA + kQA;
   uint8_t* sSb = sSa + kQSfa;
   const CUtensorMap* ma = &m.a0;
@@ -257,8 +251,7 @@ __device__ __forceinline__ void q_issue_loads(const QMaps& m, const QArgs& a, co
     by = MODE == Q_GATE_UP ? ti.e * a.b_rows + ti.nt * (QN / 2) : ti.e * a.b_rows + ti.nt * QN;
     b_chunk = static_cast<int64_t>(kb) * a.b_rblocks + by / 128;
   }
-  if constexpr (CL == 1) tma_load_2d(sA, ma, bar, ax, ay);
-  else tma_load_2d_mc(sA + crank * (kQA / 2), ma, bar, ax, ay + crank * (QM / 2), 0x3);
+  tma_load_2d(sA, ma, bar, ax, ay);
   bulk_load(sSa, sfa + a_chunk * 512, kQSfa, bar);
   if constexpr (MODE == Q_GATE_UP) {
     // the N tile is 128 gate rows then 128 up rows of the same expert
@@ -309,7 +302,7 @@ __device__ __forceinline__ void q_store(const CUtensorMap* om, const uint32_t (&
   ++n;
 }
 
-template <int MODE, int CL>
+template <int MODE>
 __global__ void __launch_bounds__(kQThreads, 1)
     grouped_gemm_mx_kernel(const __grid_constant__ QMaps maps, const QArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -323,7 +316,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], CL);  // both CTAs of a pair must have read the stage
+      mbar_init(&empty_bar[s], 1);
     }
     mbar_init(&tfull_bar, 1);
     mbar_init(&tempty_bar, 8);  // one arrive per epilogue warp
@@ -341,13 +334,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (CL > 1) cluster_sync();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_slot;
   volatile int* abortp = &abort_flag;
-  const int64_t total = q_total<MODE, CL>(args);
-  const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int64_t first = blockIdx.x / CL, stride = gridDim.x / CL;
+  const int64_t total = q_total<MODE>(args);
+  const int64_t first = blockIdx.x, stride = gridDim.x;
   uint8_t* sf_ring = smem + kQStages * kQStageBytes;
 
   if (warp == 0) {
@@ -358,13 +349,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
       uint32_t issued_mask = 0, issued_parity = 0;
       bool ok = true;
       for (int64_t t = first; t < total && ok; t += stride) {
-        const QTile ti = q_decode<MODE, CL>(args, t, crank);
+        const QTile ti = q_decode<MODE>(args, t);
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, args.err)) { ok = false; break; }
           uint64_t* bar = &full_bar[stage];
           mbar_arrive_expect_tx(bar, kQStageTx);
-          q_issue_loads<MODE, CL>(maps, args, ti, kb, smem + stage * kQStageBytes,
-                                  sf_ring + stage * kQSfBytes, bar, crank);
+          q_issue_loads<MODE>(maps, args, ti, kb, smem + stage * kQStageBytes,
+                              sf_ring + stage * kQSfBytes, bar);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kQStages) { stage = 0; phase ^= 1u; }
@@ -382,7 +373,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int64_t t = first; t < total && ok; t += stride) {
-        const QTile ti = q_decode<MODE, CL>(args, t, crank);
+        const QTile ti = q_decode<MODE>(args, t);
         if (!mbar_wait(&tempty_bar, acc_phase ^ 1u, abortp, args.err)) break;
         tc_fence_after();
         for (int kb = 0; kb < ti.nkb; ++kb) {
@@ -403,8 +394,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
             umma_mx(tmem_base, ad, bd, idesc_mx(QM, QN, static_cast<uint32_t>(ks)), sf_t,
                     sf_t + 4, (kb > 0 || ks > 0) ? 1u : 0u);
           }
-          if constexpr (CL == 1) umma_commit(&empty_bar[stage]);
-          else umma_commit_mc(&empty_bar[stage], (1u << CL) - 1);
+          umma_commit(&empty_bar[stage]);
           if (++stage == kQStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -422,7 +412,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     uint32_t nstore = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = first; t < total; t += stride) {
-      const QTile ti = q_decode<MODE, CL>(args, t, crank);
+      const QTile ti = q_decode<MODE>(args, t);
       if (!mbar_wait(&tfull_bar, acc_phase, abortp, args.err)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
@@ -557,7 +547,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kQTmemCols);
   }
-  if constexpr (CL > 1) cluster_sync();  // no CTA leaves while its peer may still write to it
 }
 
 int q_sm_count() {
@@ -567,54 +556,26 @@ int q_sm_count() {
   return n > 0 ? n : 148;
 }
 
-template <int MODE, int CL>
+// One persistent CTA per SM, capped by the tiles available.
+template <int MODE>
 moe_status q_launch(const QMaps& maps, const QArgs& args, int64_t units, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  static int max_clusters = 0;
-  auto config = [](cudaLaunchConfig_t& cfg, cudaLaunchAttribute* at, int clusters) {
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = CL;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(CL * clusters);
-    cfg.blockDim = dim3(kQThreads);
-    cfg.dynamicSmemBytes = kQSmem;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-  };
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(grouped_gemm_mx_kernel<MODE, CL>,
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(grouped_gemm_mx_kernel<MODE>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
-    if (attr_err != cudaSuccess || CL == 1) return;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
-    config(cfg, at, 64);
-    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_mx_kernel<MODE, CL>, &cfg);
-    if (attr_err == cudaSuccess && max_clusters <= 0) attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
   if (units <= 0) return MOE_OK;
-  if constexpr (CL == 1) {
-    const int grid = static_cast<int>(std::min<int64_t>(q_sm_count(), units));
-    grouped_gemm_mx_kernel<MODE, 1><<<grid, kQThreads, kQSmem, s>>>(maps, args);
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
-    config(cfg, at, static_cast<int>(std::min<int64_t>(max_clusters, units)));
-    cfg.stream = s;
-    if (cudaLaunchKernelEx(&cfg, grouped_gemm_mx_kernel<MODE, CL>, maps, args) != cudaSuccess)
-      return MOE_ERR_CUDA;
-  }
+  const int grid = static_cast<int>(std::min<int64_t>(q_sm_count(), units));
+  grouped_gemm_mx_kernel<MODE><<<grid, kQThreads, kQSmem, s>>>(maps, args);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 template <int MODE>
 moe_status q_launch_rows(const QMaps& maps, const QArgs& args, cudaStream_t s) {
-  if (args.n_nt % 2 == 0)
-    return q_launch<MODE, 2>(maps, args, static_cast<int64_t>(args.max_mtiles) * (args.n_nt / 2), s);
-  return q_launch<MODE, 1>(maps, args, static_cast<int64_t>(args.max_mtiles) * args.n_nt, s);
+  return q_launch<MODE>(maps, args, static_cast<int64_t>(args.max_mtiles) * args.n_nt, s);
 }
 
 bool fp8_map(CUtensorMap* m, const void* base, int64_t k, int64_t rows, int box_rows) {
@@ -646,14 +607,10 @@ QArgs q_base(const Layout& L, const void* ws) {
   return a;
 }
 
-// A box of the token-row modes: the CTA's half (CTA pairs) or the whole tile.
-int a_box(int n_nt) { return n_nt % 2 == 0 ? QM / 2 : QM; }
-
 template <int MODE>
 moe_status q_launch_wgrad(const QMaps& maps, const QArgs& args, cudaStream_t s) {
-  const int64_t per = static_cast<int64_t>(args.n_probs) * args.E * args.w_mt;
-  if (args.w_nt % 2 == 0) return q_launch<MODE, 2>(maps, args, per * (args.w_nt / 2), s);
-  return q_launch<MODE, 1>(maps, args, per * args.w_nt, s);
+  return q_launch<MODE>(maps, args,
+                        static_cast<int64_t>(args.n_probs) * args.E * args.w_mt * args.w_nt, s);
 }
 
 }  // namespace
@@ -663,7 +620,7 @@ moe_status gemm_mx_gate_up(const Layout& L, const void* ws, moe_mxfp8_operand xe
                            void* u, void* act, const moe_mxfp8_operand* act_q, cudaStream_t s) {
   const int n_nt = L.I / (QN / 2);
   QMaps m{};
-  if (!fp8_map(&m.a0, xe.q, L.H, L.R, a_box(n_nt)) ||
+  if (!fp8_map(&m.a0, xe.q, L.H, L.R, QM) ||
       !fp8_map(&m.b0, wg.q, L.H, static_cast<int64_t>(L.E) * L.I, QN / 2) ||
       !fp8_map(&m.b1, wu.q, L.H, static_cast<int64_t>(L.E) * L.I, QN / 2))
     return MOE_ERR_CUDA;
@@ -694,7 +651,7 @@ moe_status gemm_mx_down(const Layout& L, const void* ws, moe_mxfp8_operand act,
                         const moe_mxfp8_operand& wd, void* ye, cudaStream_t s) {
   const int n_nt = L.H / QN;
   QMaps m{};
-  if (!fp8_map(&m.a0, act.q, L.I, L.R, a_box(n_nt)) ||
+  if (!fp8_map(&m.a0, act.q, L.I, L.R, QM) ||
       !fp8_map(&m.b0, wd.q, L.I, static_cast<int64_t>(L.E) * L.H, QN))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
@@ -716,7 +673,7 @@ moe_status gemm_mx_down_dgrad(const Layout& L, const void* ws, moe_mxfp8_operand
                               void* dg, void* du, cudaStream_t s) {
   const int n_nt = L.I / QN;
   QMaps m{};
-  if (!fp8_map(&m.a0, dye.q, L.H, L.R, a_box(n_nt)) ||
+  if (!fp8_map(&m.a0, dye.q, L.H, L.R, QM) ||
       !fp8_map(&m.b0, wd_t.q, static_cast<int64_t>(L.E) * L.H, L.I, QN))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
@@ -741,8 +698,8 @@ moe_status gemm_mx_gate_up_dgrad(const Layout& L, const void* ws, moe_mxfp8_oper
                                  const moe_mxfp8_operand& wu_t, void* dxe, cudaStream_t s) {
   const int n_nt = L.H / QN;
   QMaps m{};
-  if (!fp8_map(&m.a0, dg.q, L.I, L.R, a_box(n_nt)) ||
-      !fp8_map(&m.a1, du.q, L.I, L.R, a_box(n_nt)) ||
+  if (!fp8_map(&m.a0, dg.q, L.I, L.R, QM) ||
+      !fp8_map(&m.a1, du.q, L.I, L.R, QM) ||
       !fp8_map(&m.b0, wg_t.q, static_cast<int64_t>(L.E) * L.I, L.H, QN) ||
       !fp8_map(&m.b1, wu_t.q, static_cast<int64_t>(L.E) * L.I, L.H, QN))
     return MOE_ERR_CUDA;
@@ -765,7 +722,7 @@ moe_status gemm_mx_down_wgrad(const Layout& L, const void* ws, moe_mxfp8_operand
                               moe_mxfp8_operand act_t, float* dw_down, cudaStream_t s) {
   const int w_nt = L.I / QN;
   QMaps m{};
-  if (!fp8_map(&m.a0, dye_t.q, L.R, L.H, w_nt % 2 == 0 ? QM / 2 : QM) ||
+  if (!fp8_map(&m.a0, dye_t.q, L.R, L.H, QM) ||
       !fp8_map(&m.b0, act_t.q, L.R, L.I, QN))
     return MOE_ERR_CUDA;
   m.a1 = m.a0;
@@ -790,8 +747,8 @@ moe_status gemm_mx_gate_up_wgrad(const Layout& L, const void* ws, moe_mxfp8_oper
                                  float* dw_up, cudaStream_t s) {
   const int w_nt = L.H / QN;
   QMaps m{};
-  if (!fp8_map(&m.a0, dg_t.q, L.R, L.I, w_nt % 2 == 0 ? QM / 2 : QM) ||
-      !fp8_map(&m.a1, du_t.q, L.R, L.I, w_nt % 2 == 0 ? QM / 2 : QM) ||
+  if (!fp8_map(&m.a0, dg_t.q, L.R, L.I, QM) ||
+      !fp8_map(&m.a1, du_t.q, L.R, L.I, QM) ||
       !fp8_map(&m.b0, xe_t.q, L.R, L.H, QN))
     return MOE_ERR_CUDA;
   m.b1 = m.b0;

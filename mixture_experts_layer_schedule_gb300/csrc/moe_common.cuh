@@ -93,18 +93,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, ui
       : "memory");
 }
 
-// Same copy, delivered to the same shared-memory offset of every CTA in
-// cta_mask (thread-block cluster), each destination's mbarrier at `bar`'s
-// offset receiving the bytes that land in that CTA.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* tm, uint64_t* bar,
-                                               int32_t c0, int32_t c1, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask)
-      : "memory");
-}
-
 // Four rows (row0..row3, any order) of a 2-D tensor, each box-width wide from
 // column c0, gathered into four consecutive shared-memory rows (the map's box
 // is one row high).
@@ -116,18 +104,6 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tm, ui
       " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2),
       "r"(r3)
-      : "memory");
-}
-
-// gather4 delivered to the same offset of every CTA in cta_mask.
-__device__ __forceinline__ void tma_gather4_mc(void* dst, const CUtensorMap* tm, uint64_t* bar,
-                                               int32_t c0, int32_t r0, int32_t r1, int32_t r2,
-                                               int32_t r3, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2),
-      "r"(r3), "h"(cta_mask)
       : "memory");
 }
 
@@ -211,16 +187,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-
-// As umma_commit, arriving on the mbarrier at `bar`'s offset in every CTA of
-// cta_mask (so a cluster peer learns when this CTA's MMAs have read a stage).
-__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 
