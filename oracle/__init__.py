@@ -82,6 +82,9 @@ def lib():
             L.orc_layer_mxfp8_prepared.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp,
                                                    vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp,
                                                    vp, vp, vp, ctypes.c_int]
+            L.orc_layer_mxfp8_trace.argtypes = [i64, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+                                                vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int,
+                                                vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int]
             L.orc_router_logits.argtypes = [i64, i32, i32, vp, vp, vp, ctypes.c_int]
             L.orc_router_backward.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                               ctypes.c_int]
@@ -327,6 +330,26 @@ def layer_mxfp8_prepared(x, prepared, ids, w, dy, quantize=True, threads=0):
         N, H, I, E, k, _p(x), *(_p(prepared[n]) for n in MXFP8_WEIGHT_COPIES), _p(ids), _p(w),
         _p(dy), 1 if quantize else 0, _p(y), _p(dx), _p(dwg), _p(dwu), _p(dwd), _p(dw), threads))
     return dict(y=y, dx=dx, dwg=dwg, dwu=dwu, dwd=dwd, dw=dw)
+
+
+def layer_mxfp8_trace(x, prepared, ids, w, dy, gu_bf16=False, threads=0):
+    """layer_mxfp8_prepared (quantisation on) plus the quantised dG and dU rows
+    [N*k, I] the gate/up data gradient reads; gu_bf16 rounds G and U to bf16
+    before the SwiGLU backward (an error-accounting diagnostic, not a parity
+    reference)."""
+    x, dy = as_bf16_bits(x), as_bf16_bits(dy)
+    ids, w = _c(ids, np.int32), _c(w, np.float64)
+    N, H = x.shape
+    E, I, _ = prepared["wg_h"].shape
+    k = ids.shape[1]
+    y = np.empty((N, H))
+    dx, dwg, dwu, dwd, dw = _bw_out(N, H, I, E, k)
+    dg_rows, du_rows = np.empty((N * k, I)), np.empty((N * k, I))
+    _check(lib().orc_layer_mxfp8_trace(
+        N, H, I, E, k, _p(x), *(_p(prepared[n]) for n in MXFP8_WEIGHT_COPIES), _p(ids), _p(w),
+        _p(dy), 1, 1 if gu_bf16 else 0, _p(y), _p(dx), _p(dwg), _p(dwu), _p(dwd), _p(dw),
+        _p(dg_rows), _p(du_rows), threads))
+    return dict(y=y, dx=dx, dwg=dwg, dwu=dwu, dwd=dwd, dw=dw, dg_rows=dg_rows, du_rows=du_rows)
 
 
 def mxfp8_quantize(src_bits):

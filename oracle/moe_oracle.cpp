@@ -671,6 +671,17 @@ extern "C" int orc_layer_mxfp8_prepared(int64_t N, int32_t H, int32_t I, int32_t
                                         const uint16_t* dy, int quantize, double* y, double* dx,
                                         double* dwg, double* dwu, double* dwd, double* dw,
                                         int threads) {
+  return orc_layer_mxfp8_trace(N, H, I, E, k, x, wg_h, wu_h, wd_i, wd_h, wg_i, wu_i, ids, w, dy,
+                               quantize, 0, y, dx, dwg, dwu, dwd, dw, nullptr, nullptr, threads);
+}
+
+extern "C" int orc_layer_mxfp8_trace(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k,
+                                     const uint16_t* x, const double* wg_h, const double* wu_h,
+                                     const double* wd_i, const double* wd_h, const double* wg_i,
+                                     const double* wu_i, const int32_t* ids, const double* w,
+                                     const uint16_t* dy, int quantize, int gu_bf16, double* y,
+                                     double* dx, double* dwg, double* dwu, double* dwd, double* dw,
+                                     double* dg_rows, double* du_rows, int threads) {
   if (N < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || k > E) return ORC_ERR_ARG;
   const int64_t A = N * k;
   for (int64_t a = 0; a < A; ++a)
@@ -720,7 +731,11 @@ extern "C" int orc_layer_mxfp8_prepared(int64_t N, int32_t H, int32_t I, int32_t
         da[i] = acc;
       }
       for (int32_t i = 0; i < I; ++i) {
-        const double g = G[a * I + i], u = U[a * I + i], sg = sigmoid(g);
+        // gu_bf16 (diagnostic, off in every parity test): G and U as the
+        // bf16 values a layer that stores them reads back
+        const double g = gu_bf16 ? round_bf16(G[a * I + i]) : G[a * I + i];
+        const double u = gu_bf16 ? round_bf16(U[a * I + i]) : U[a * I + i];
+        const double sg = sigmoid(g);
         DG[a * I + i] = rb(da[i] * u * sg * (1.0 + g * (1.0 - sg)));  // dG, dU stored bf16
         DU[a * I + i] = rb(da[i] * g * sg);
         gq[i] = DG[a * I + i];
@@ -728,6 +743,11 @@ extern "C" int orc_layer_mxfp8_prepared(int64_t N, int32_t H, int32_t I, int32_t
       }
       q(gq.data(), I);                                                 // dG, dU rows along I
       q(uq.data(), I);
+      if (dg_rows && du_rows)
+        for (int32_t i = 0; i < I; ++i) {
+          dg_rows[a * I + i] = gq[i];
+          du_rows[a * I + i] = uq[i];
+        }
       for (int32_t h = 0; h < H; ++h) {
         double acc = 0.0;
         for (int32_t i = 0; i < I; ++i)

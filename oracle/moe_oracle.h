@@ -177,6 +177,21 @@ int orc_layer_mxfp8_prepared(int64_t N, int32_t H, int32_t I, int32_t E, int32_t
                              const uint16_t* dy, int quantize, double* y, double* dx, double* dwg,
                              double* dwu, double* dwd, double* dw, int threads);
 
+/* orc_layer_mxfp8_prepared with two diagnostics for error accounting (never
+ * used by a parity check): gu_bf16 = 1 rounds G and U to bf16 before the
+ * SwiGLU backward reads them (as a layer that stores G and U in bf16 reads
+ * them back; 0 keeps the fp64 values, which is orc_layer_mxfp8_prepared), and
+ * dg_rows / du_rows (NULL: not written) receive the quantised dG and dU rows
+ * [N*k, I] that the data-gradient GEMM of gate/up reads, in assignment order
+ * t*k + j. */
+int orc_layer_mxfp8_trace(int64_t N, int32_t H, int32_t I, int32_t E, int32_t k,
+                          const uint16_t* x, const double* wg_h, const double* wu_h,
+                          const double* wd_i, const double* wd_h, const double* wg_i,
+                          const double* wu_i, const int32_t* ids, const double* w,
+                          const uint16_t* dy, int quantize, int gu_bf16, double* y, double* dx,
+                          double* dwg, double* dwu, double* dwd, double* dw, double* dg_rows,
+                          double* du_rows, int threads);
+
 /* The weight gradients of orc_layer_mxfp8 for expert e at sampled entries
  * (sampled parity where the whole layer is too large for the oracle):
  * dwg[r][c] = dWg[e][i_list[r]][h_list[c]], dwu likewise (both [n_i, n_h]),

@@ -337,3 +337,48 @@ def test_dg_du_columns_are_quantised_along_tokens():
         dz[1:32] = 0.0
         return (x, wg, wu, wd, _bits(df)), (x, wg, wu, wd, _bits(dz))
     _wgrad_pair(make, lambda r: np.concatenate([r["dwg"].ravel(), r["dwu"].ravel()]))
+
+
+def test_trace_without_the_diagnostic_equals_the_layer_and_exposes_dg_du():
+    """The error-accounting entry (layer_mxfp8_trace): with gu_bf16 off every
+    output equals layer_mxfp8 bit for bit; the dG/dU rows it exposes are the
+    operands of the gate/up data gradient (dx recomputed from them and the
+    transposed weight copies matches), and each is an MXFP8 number along I
+    (a fixed point of the quantiser)."""
+    x, wg, wu, wd, ids, w, dy = _layer(24, 64, 96, 5, 2, 7)
+    prep = oracle.mxfp8_weights(wg, wu, wd)
+    r = oracle.layer_mxfp8(x, wg, wu, wd, ids, w, dy, quantize=True)
+    t = oracle.layer_mxfp8_trace(x, prep, ids, w, dy, gu_bf16=False)
+    for key in ("y", "dx", "dwg", "dwu", "dwd", "dw"):
+        np.testing.assert_array_equal(t[key], r[key], err_msg=key)
+    N, k = ids.shape
+    dx = np.zeros_like(r["dx"])
+    for a in range(N * k):
+        e = ids.reshape(-1)[a]
+        dx[a // k] += prep["wg_i"][e].T @ t["dg_rows"][a] + prep["wu_i"][e].T @ t["du_rows"][a]
+    np.testing.assert_allclose(dx, r["dx"], rtol=0, atol=1e-12 * np.max(np.abs(r["dx"])))
+    for rows in (t["dg_rows"], t["du_rows"]):
+        q = _qdq_rows(rows)
+        np.testing.assert_array_equal(q, rows)
+
+
+def _qdq_rows(v):
+    """Quantise-dequantise rows of exact bf16 values along the row (blocks of
+    32) with the oracle's element and scale rules."""
+    q, s = oracle.mxfp8_quantize(_bits(v.astype(np.float32)))
+    table = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    return table[q] * np.repeat(2.0 ** (s.astype(np.float64) - 127), 32, axis=1)
+
+
+def test_trace_bf16_gu_changes_only_the_swiglu_backward_outputs():
+    """gu_bf16 rounds G and U before the SwiGLU backward: y, dWd and d(routing
+    weights) do not depend on it; dx, dWg and dWu move by a small amount."""
+    x, wg, wu, wd, ids, w, dy = _layer(24, 64, 96, 5, 2, 8)
+    prep = oracle.mxfp8_weights(wg, wu, wd)
+    a = oracle.layer_mxfp8_trace(x, prep, ids, w, dy, gu_bf16=False)
+    b = oracle.layer_mxfp8_trace(x, prep, ids, w, dy, gu_bf16=True)
+    for key in ("y", "dwd", "dw"):
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    for key in ("dx", "dwg", "dwu"):
+        d = np.max(np.abs(a[key] - b[key])) / np.max(np.abs(a[key]))
+        assert 0 < d < 0.1, (key, d)
