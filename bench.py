@@ -59,11 +59,13 @@ def parse():
                          "by side warps of the down data-gradient GEMM), timed as one phase")
     ap.add_argument("--inference", action="store_true",
                     help="forward-only workloads: time the context-free forward (no G, U or "
-                         "context stored) instead of the training forward; --gather fuses the "
-                         "dispatch into the gate/up producer")
-    ap.add_argument("--gather", action="store_true",
-                    help="with --inference: time the gate/up GEMM with the dispatch fused into "
-                         "its producer (moe_expert_gate_up_gather)")
+                         "context stored) instead of the training forward")
+    ap.add_argument("--fused", action="store_true",
+                    help="bf16 training forward: time dispatch, gate/up and down as one "
+                         "persistent launch (moe_dispatch_expert_ffn) instead of three")
+    ap.add_argument("--unfused", action="store_true",
+                    help="bf16 context-free forward (--inference): time dispatch, gate/up and "
+                         "down as three launches instead of moe_dispatch_expert_ffn")
     ap.add_argument("--tensor-peaks", action="store_true",
                     help="measure the dense bf16 and FP8 (E4M3) tensor-core peaks with library "
                          "GEMMs of 8192^3 (best of 10, and back to back for 4 s) and print them")
@@ -352,8 +354,9 @@ class ClockSampler:
 def phase_flops(shape):
     """Algorithmic flops of each GEMM phase (padding rows excluded)."""
     A, H, I = shape.N * shape.k, shape.H, shape.I
-    return {"gate_up": 4 * A * H * I, "gate_up_gather": 4 * A * H * I,
-            "gate_up_act": 4 * A * H * I,
+    return {"gate_up": 4 * A * H * I,
+            "gate_up_act": 4 * A * H * I, "experts_fwd": 6 * A * H * I,
+            "experts_fwd_inf": 6 * A * H * I,
             "down": 2 * A * H * I, "down_dgrad": 2 * A * H * I,
             "down_wgrad": 2 * A * H * I, "gate_up_dgrad": 4 * A * H * I,
             "gate_up_wgrad": 4 * A * H * I, "forward": 6 * A * H * I, "backward": 12 * A * H * I}
@@ -366,9 +369,10 @@ def gemm_bytes(shape):
     matters where few tokens per expert meet large weights."""
     N, A, H, I, E = shape.N, shape.N * shape.k, shape.H, shape.I, shape.E
     W = 2 * E * H * I  # one bf16 weight tensor
-    return {"gate_up": 2 * A * H + 2 * W + 3 * 2 * A * I,
+    return {"experts_fwd": 2 * N * H + 2 * A * H + 3 * W + 3 * 2 * A * I + 2 * A * H,
+            "experts_fwd_inf": 2 * N * H + 3 * W + 2 * A * H,
+            "gate_up": 2 * A * H + 2 * W + 3 * 2 * A * I,
             "gate_up_act": 2 * A * H + 2 * W + 2 * A * I,
-            "gate_up_gather": 2 * N * H + 4 * A + 2 * W + 2 * A * I,
             "down": 2 * A * I + W + 2 * A * H,
             "down_dgrad": 2 * A * H + W + 2 * 2 * A * I + 2 * 2 * A * I,
             "down_wgrad": 2 * A * H + 2 * A * I + 2 * W,
@@ -442,10 +446,11 @@ def run_ours(args, ws_, rank, local, shape=None):
     backward = shape.backward
 
     inference = args.inference and not backward
-    phases = ["route", "schedule", "dispatch", "gate_up", "down", "combine"]
+    fwd = ["experts_fwd"] if args.fused else ["dispatch", "gate_up", "down"]
+    phases = ["route", "schedule"] + fwd + ["combine"]
     if inference:
-        phases = (["route", "schedule", "gate_up_gather", "down", "combine"] if args.gather else
-                  ["route", "schedule", "dispatch", "gate_up_act", "down", "combine"])
+        phases = (["route", "schedule", "dispatch", "gate_up_act", "down", "combine"] if args.unfused
+                  else ["route", "schedule", "experts_fwd_inf", "combine"])
     if mx:  # MXFP8: the composite passes (they add the activation quantisations)
         phases = ["route", "schedule", "forward"] + (["backward"] if backward else [])
     elif backward and args.overlap:
@@ -467,10 +472,13 @@ def run_ours(args, ws_, rank, local, shape=None):
             wsb),
         "schedule": lambda: _lib.moe_build_schedule(p, layer.topk_ids, wsb),
         "dispatch": lambda: _lib.moe_dispatch(p, wsb, inp["x"], sv["xe"]),
+        "experts_fwd": lambda: _lib.moe_dispatch_expert_ffn(p, wsb, inp["x"], w, sv["xe"], sv["g"],
+                                                            sv["u"], sv["act"], sv["ye"]),
+        # context-free: Xe and Ye share the Ye rows the combine reads
+        "experts_fwd_inf": lambda: _lib.moe_dispatch_expert_ffn(p, wsb, inp["x"], w, sv["ye"], None,
+                                                                None, sv["act"], sv["ye"]),
         "gate_up": lambda: _lib.moe_expert_gate_up(p, wsb, sv["xe"], w, sv["g"], sv["u"],
                                                    sv["act"]),
-        "gate_up_gather": lambda: _lib.moe_expert_gate_up_gather(p, wsb, inp["x"], w, None, None,
-                                                                 sv["act"]),
         "gate_up_act": lambda: _lib.moe_expert_gate_up(p, wsb, sv["xe"], w, None, None, sv["act"]),
         "down": lambda: _lib.moe_expert_down(p, wsb, sv["act"], w, sv["ye"]),
         "combine": lambda: _lib.moe_combine(p, wsb, sv["ye"], layer.topk_w, layer.y),

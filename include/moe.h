@@ -192,18 +192,25 @@ moe_status moe_build_schedule(const moe_problem* p, const int32_t* topk_ids, voi
  * cannot allocate device memory -- e.g. a plugin whose host application owns
  * the whole device memory pool, or a loop that must never call the
  * allocator -- and so cannot provide the scan scratch moe_build_schedule
- * takes from the workspace. The tables are the same as moe_build_schedule's,
- * written to the caller's arrays in *out (device pointers, 4-byte aligned):
- * counts[E], offsets[E+1], pad_offsets[E+1], slot_of[N*k],
+ * takes from the workspace. It writes these tables, with the same values as
+ * moe_build_schedule, to the caller's arrays in *out (device pointers,
+ * 4-byte aligned): counts[E], offsets[E+1], pad_offsets[E+1], slot_of[N*k],
  * src_of_row[moe_grouped_rows(p)], tiles[3 * moe_grouped_rows(p) / 128],
- * n_tiles[1]; device-detected errors go to *err_word (device int32).
+ * n_tiles[1]; device-detected errors go to *err_word (device int32). It does
+ * NOT build the SM-pair work list that moe_build_schedule also writes into the
+ * workspace for the expert GEMMs, so its output cannot stand in for a
+ * workspace schedule in moe_forward, moe_backward or the expert-GEMM phase
+ * calls: it serves callers that consume the routing tables themselves.
  * The scratch is a static device array owned by the library: 524288 int32
  * (2 MiB), held on every device that loads the library until the process
  * exits. Problems needing more than E * ceil(N*k / 256) = 524288 entries
  * return MOE_ERR_UNSUPPORTED. Allocates and frees nothing. The first call on
- * a device looks up the array's device address (cudaGetSymbolAddress); make
- * that first call before any stream capture. Every call shares the array, so
- * calls whose kernels overlap on the GPU (e.g. on two streams) race. */
+ * a device looks up the array's device address (cudaGetSymbolAddress); the
+ * address is cached with the id of the device's context and looked up again
+ * in a new context (after cudaDeviceReset). Make the first call on a device,
+ * and the first after a reset, before any stream capture. Every call shares
+ * the array, so calls whose kernels overlap on the GPU (e.g. on two streams)
+ * race. */
 moe_status moe_build_schedule_noalloc(const moe_problem* p, const int32_t* topk_ids,
                                       const moe_schedule* out, int32_t* err_word, void* stream);
 
@@ -235,6 +242,15 @@ moe_status moe_dispatch_mxfp8(const moe_problem* p, const void* ws, const void* 
 moe_status moe_mxfp8_forward_operands(const moe_problem* p, void* ws, moe_mxfp8_operand* xe_rows,
                                       moe_mxfp8_operand* act_rows);
 
+/* The workspace buffers holding the row forms of dG and dU (E4M3 codes
+ * [R, I] with scales in the mxfp8_quantize_mma chunk layout) that the MXFP8
+ * tensor-core backward quantises for the gate/up data-gradient GEMM
+ * (host-only address arithmetic, no GPU work). Valid after moe_backward on the
+ * FP8 tensor cores until the next call that reuses the workspace. For
+ * inspecting the quantised operands (error accounting); MOE_MXFP8 only. */
+moe_status moe_mxfp8_backward_operands(const moe_problem* p, void* ws, moe_mxfp8_operand* dg_rows,
+                                       moe_mxfp8_operand* du_rows);
+
 /* Expert gate/up GEMM with the SwiGLU epilogue ([Clip] key point 5): per
  * expert e and its rows, G = Xe Wg[e]^T, U = Xe Wu[e]^T (fp32 accumulation on
  * the tensor cores), Act = silu(G) * U. Writes G, U, Act bf16 [R,I]; g and u
@@ -252,19 +268,26 @@ moe_status moe_expert_down(const moe_problem* p, const void* ws, const void* act
 moe_status moe_combine(const moe_problem* p, const void* ws, const void* ye, const float* topk_w,
                        void* y, void* stream);
 
-/* Gate/up GEMM with the dispatch fused into its producer ([Clip] flowchart:
- * dispatch feeding the expert FFN through a token buffer): the rows of each
- * expert tile are gathered from the token-ordered x (bf16 [N,H]) by TMA
- * straight into the shared-memory stage ring, so Xe is never written. Same
- * G, U, Act as moe_dispatch + moe_expert_gate_up on every real row; padding
- * rows hold finite values of another row instead of zeros (they are never
- * read by the combine). g and u may both be NULL: then only Act is stored. */
-moe_status moe_expert_gate_up_gather(const moe_problem* p, const void* ws, const void* x,
-                                     const moe_weights* w, void* g, void* u, void* act,
-                                     void* stream);
+/* Dispatch + expert FFN in one persistent launch ([Clip] key point 5 and the
+ * key flowchart: the producer pulls a minibatch of token rows and local
+ * counters wake the expert FFN): side warps of every CTA copy token rows into
+ * xe (as moe_dispatch) and count the finished rows of each 128-row tile; the
+ * SM-pair GEMM roles run gate/up + SwiGLU (as moe_expert_gate_up) on a tile
+ * once its rows are there, and the down GEMM (as moe_expert_down) on a group
+ * of rows once all of its Act columns are stored. Bit-identical to
+ * moe_dispatch, moe_expert_gate_up and moe_expert_down in sequence. x bf16
+ * [N,H] -> xe [R,H], g, u, act [R,I], ye [R,H]; g and u both NULL skip G and
+ * U (inference). xe and ye may be the same buffer (a row group's Xe is read
+ * completely before its Ye is written). MOE_BF16 only; the grid holds only
+ * co-resident CTA pairs, and every wait is bounded (MOE_DEVERR_TIMEOUT). */
+moe_status moe_dispatch_expert_ffn(const moe_problem* p, const void* ws, const void* x,
+                                   const moe_weights* w, void* xe, void* g, void* u, void* act,
+                                   void* ye, void* stream);
 
-/* Forward without a context (inference): dispatch into scratch, gate/up
- * (Act only), down over the same scratch, combine; same y as moe_forward.
+/* Forward without a context (inference): dispatch, gate/up (Act only) and
+ * down in one launch (moe_dispatch_expert_ffn; MOE_MXFP8: separate launches)
+ * with Xe and Ye sharing one scratch buffer, then the combine; same y as
+ * moe_forward.
  * Uses the workspace's backward buffers as scratch for Xe/Ye and Act, so it
  * must not run between a moe_forward and its moe_backward. */
 moe_status moe_forward_inference(const moe_problem* p, const void* x, const moe_weights* w,

@@ -10,7 +10,7 @@ from ._lib import (EXPORTED, MoEError, Problem, Weights, load, moe_backward,
                    moe_build_schedule, moe_clear_device_error, moe_combine, moe_dispatch,
                    moe_expert_down, moe_expert_down_dgrad, moe_expert_down_wgrad,
                    moe_expert_gate_up, moe_expert_gate_up_dgrad, moe_expert_gate_up_wgrad,
-                   moe_launch_count, moe_forward, moe_forward_inference, moe_expert_gate_up_gather, moe_get_device_error,
+                   moe_launch_count, moe_forward, moe_forward_inference, moe_get_device_error,
                    moe_grouped_rows, moe_reverse_combine, moe_reverse_dispatch, moe_route_topk,
                    moe_saved_bytes, moe_saved_layout, moe_schedule_view, moe_workspace_bytes,
                    mxfp8_quantize, problem, weights)

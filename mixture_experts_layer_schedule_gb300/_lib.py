@@ -80,7 +80,6 @@ _SIGS = {
     "moe_expert_down": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_vp], c_i32),
     "moe_combine": ([c_vp, c_vp, c_vp, c_vp, c_vp, c_vp], c_i32),
     "moe_forward": ([c_vp] * 8, c_i32),
-    "moe_expert_gate_up_gather": ([c_vp] * 8, c_i32),
     "moe_forward_inference": ([c_vp] * 7, c_i32),
     "moe_reverse_combine": ([c_vp] * 8, c_i32),
     "moe_expert_down_dgrad": ([c_vp] * 9, c_i32),
@@ -90,6 +89,8 @@ _SIGS = {
     "moe_reverse_dispatch": ([c_vp] * 5, c_i32),
     "moe_backward": ([c_vp] * 12, c_i32),
     "moe_mxfp8_forward_operands": ([c_vp] * 4, c_i32),
+    "moe_mxfp8_backward_operands": ([c_vp] * 4, c_i32),
+    "moe_dispatch_expert_ffn": ([c_vp] * 10, c_i32),
     "moe_dispatch_mxfp8": ([c_vp] * 7, c_i32),
     "moe_backward_overlap": ([c_vp] * 12, c_i32),
     "mxfp8_quantize": ([c_vp, c_i64, c_i64, c_vp, c_vp, c_vp], c_i32),
@@ -247,6 +248,20 @@ def moe_mxfp8_forward_operands(p, ws):
     return (xe.q, xe.s), (act.q, act.s)
 
 
+def moe_mxfp8_backward_operands(p, ws):
+    """Device addresses (q, s) of dG's and dU's row-form MXFP8 operands in ws."""
+    dg, du = MXFP8Operand(), MXFP8Operand()
+    _call("moe_mxfp8_backward_operands", ctypes.byref(p), _ptr(ws), ctypes.byref(dg),
+          ctypes.byref(du))
+    return (dg.q, dg.s), (du.q, du.s)
+
+
+def moe_dispatch_expert_ffn(p, ws, x, w: Weights, xe, g, u, act, ye, stream=None):
+    """Dispatch + gate/up + SwiGLU + down in one persistent launch."""
+    _call("moe_dispatch_expert_ffn", ctypes.byref(p), _ptr(ws), _ptr(x), ctypes.byref(w), _ptr(xe),
+          _ptr(g), _ptr(u), _ptr(act), _ptr(ye), _stream(stream))
+
+
 def moe_dispatch_mxfp8(p, ws, x, xe, q, s, stream=None):
     _call("moe_dispatch_mxfp8", ctypes.byref(p), _ptr(ws), _ptr(x), _ptr(xe), _ptr(q), _ptr(s),
           _stream(stream))
@@ -270,11 +285,6 @@ def moe_combine(p, ws, ye, topk_w, y, stream=None):
 def moe_forward(p, x, w: Weights, topk_w, y, saved, ws, stream=None):
     _call("moe_forward", ctypes.byref(p), _ptr(x), ctypes.byref(w), _ptr(topk_w), _ptr(y),
           _ptr(saved), _ptr(ws), _stream(stream))
-
-
-def moe_expert_gate_up_gather(p, ws, x, w: Weights, g, u, act, stream=None):
-    _call("moe_expert_gate_up_gather", ctypes.byref(p), _ptr(ws), _ptr(x), ctypes.byref(w),
-          _ptr(g), _ptr(u), _ptr(act), _stream(stream))
 
 
 def moe_forward_inference(p, x, w: Weights, topk_w, y, ws, stream=None):

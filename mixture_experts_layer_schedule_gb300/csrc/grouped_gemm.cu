@@ -7,11 +7,12 @@
 // key flowchart node "expert FFN + SwiGLU"). The backward rounds (key point
 // 2) need the matching data-gradient and weight-gradient GEMMs.
 //
-// Two persistent kernel templates serve the GEMMs of the layer: the SM-pair
+// Persistent kernel templates serve the GEMMs of the layer: the SM-pair
 // kernel (tcgen05 cta_group::2, further below) runs the four token-row modes
-// and the weight gradients; the single-CTA kernel runs the router GEMM and
-// the gate/up GEMM with the dispatch fused into its producer. In both, each
-// CTA (one per SM) runs three roles that hand work over through mbarriers:
+// and the weight gradients, the fused forward kernel runs dispatch, gate/up
+// and down in one launch, and the single-CTA kernel runs the router GEMM. In
+// each, every CTA (one per SM) runs three roles that hand work over through
+// mbarriers:
 //   warp 0      TMA producer: streams 64-wide K slices of the A and B tiles
 //               into a ring of shared-memory stages (128-byte swizzle);
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256,
@@ -54,12 +55,9 @@ constexpr int kSmemBytes = kStages * kStageBytes + kOutBytes + 1024;  // + align
 constexpr int kGemmThreads = 192;
 constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
 
-// GATE_UP_GATHER: GATE_UP with the dispatch fused into the producer -- the A
-// rows are gathered from the token-ordered x by TMA (tile::gather4), so the
-// expert-grouped Xe never exists in HBM; G and U may be skipped (inference).
 // ROUTER: the dense router GEMM in front of the routing, logits = x . Wr^T
 // (M tiles over the N tokens, one N tile of up to 256 experts, fp32 out).
-enum Mode { GATE_UP = 0, DOWN = 1, DACT = 2, DXE = 3, WGRAD = 4, GATE_UP_GATHER = 5, ROUTER = 6 };
+enum Mode { GATE_UP = 0, DOWN = 1, DACT = 2, DXE = 3, WGRAD = 4, ROUTER = 6 };
 
 struct Maps {
   CUtensorMap a0, a1, b0, b1;
@@ -83,9 +81,9 @@ struct Args {
   int b_rows;                  // rows per expert in B's 2-D view
   int E, w_mt, w_nt, n_probs;  // WGRAD tiling
   int ld_out;                  // output row length (elements)
-  const int32_t* src_of_row;   // GATE_UP_GATHER: assignment index of each row (-1: padding)
-  int k;                       // GATE_UP_GATHER: experts per token
-  int store_gu;                // GATE_UP(_GATHER): also store G and U
+  const int32_t* src_of_row;   // fused reverse-combine: assignment index of each row (-1: padding)
+  int k;                       // fused reverse-combine: experts per token
+  int store_gu;                // GATE_UP: also store G and U
   void *out0, *out1, *out2;
   const void *in0, *in1;
   // DACT with the reverse-combine fused in (rc_* set): dYe[row] = w[a] * dY[a / k]
@@ -196,16 +194,13 @@ __device__ __forceinline__ int64_t total_tiles(const Args& a) {
   }
 }
 
-// Loads of one k-block for the single-CTA kernel's modes.
+// Loads of one k-block for the single-CTA kernel (the router GEMM).
 template <int MODE>
 __device__ __forceinline__ void issue_loads(const Maps& m, const Args& a, const TileInfo& ti,
                                             int kb, uint8_t* sA, uint8_t* sB, uint64_t* bar) {
-  static_assert(MODE == GATE_UP_GATHER || MODE == ROUTER, "single-CTA kernel modes");
-  if constexpr (MODE == ROUTER) {
-    tma_load_2d(sA, &m.a0, bar, kb * BK, ti.row0);
-    tma_load_2d(sB, &m.b0, bar, kb * BK, 0);  // all E router rows; rows past E read as zeros
-  }
-  // GATE_UP_GATHER: loaded by the whole producer warp (see the kernel)
+  static_assert(MODE == ROUTER, "single-CTA kernel modes");
+  tma_load_2d(sA, &m.a0, bar, kb * BK, ti.row0);
+  tma_load_2d(sB, &m.b0, bar, kb * BK, 0);  // all E router rows; rows past E read as zeros
 }
 
 // silu and the sigmoid with the fast exponential and division intrinsics
@@ -277,7 +272,7 @@ __device__ __forceinline__ void epilogue(const Maps& m, const Args& a, const Til
   const int32_t y = ti.row0 + (ti.fold ? (quad & 1) : quad) * 32;
   const int dc0 = ti.fold ? (quad >> 1) * (BN / 2) : 0;  // first D column held
   const int ncol = ti.fold ? BN / 2 : BN;                // D columns held
-  if constexpr (MODE == GATE_UP || MODE == GATE_UP_GATHER) {
+  if constexpr (MODE == GATE_UP) {
     const int32_t x0 = ti.nt * (BN / 2);
     for (int c = 0; c < ncol / 2; c += 64) {
       float g[64], u[64];
@@ -401,7 +396,7 @@ __device__ __forceinline__ void epilogue_router(const Maps& m, const Args& a, co
 template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ Maps maps, const Args args) {
-  static_assert(MODE == GATE_UP_GATHER || MODE == ROUTER, "single-CTA kernel modes");
+  static_assert(MODE == ROUTER, "single-CTA kernel modes");
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], drain_bar;
   __shared__ uint32_t tmem_base_slot;
@@ -439,51 +434,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int64_t total = total_tiles<MODE, 1>(args);
   const int64_t first = blockIdx.x, stride = gridDim.x;
 
-  if (warp == 0 && MODE == GATE_UP_GATHER) {
-   if constexpr (MODE == GATE_UP_GATHER) {
-    // ---------------- TMA producer, gathering A rows (whole warp) ----------------
-    // Lane l owns rows 4l..4l+3 of the 128-row tile: it looks up their tokens
-    // once per tile and issues one gather4 per k-block into this CTA's own
-    // stage; lane 0 arms the stage barrier and loads the gate/up weight rows.
-    const int rbase = 4 * lane;
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t issued_mask = 0, issued_parity = 0;
-    bool ok = true;
-    for (int64_t t = first; t < total && ok; t += stride) {
-      const TileInfo ti = decode_tile<MODE, 1>(args, t, 0);
-      int32_t tok[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int32_t src = ti.nkb > 0 ? args.src_of_row[ti.row0 + rbase + r] : -1;
-        tok[r] = src >= 0 ? src / args.k : 0;  // padding rows read token 0 (finite, unused)
-      }
-      for (int kb = 0; kb < ti.nkb; ++kb) {
-        int ready = 1;
-        if (lane == 0) ready = mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, args.err) ? 1 : 0;
-        ready = __shfl_sync(0xffffffffu, ready, 0);
-        if (!ready) { ok = false; break; }
-        uint8_t* sA = smem + stage * kStageBytes;
-        if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
-        __syncwarp();
-        tma_gather4(sA + rbase * (BK * 2), &maps.a0, &full_bar[stage], kb * BK, tok[0], tok[1],
-                    tok[2], tok[3]);
-        if (lane == 0) {
-          const int brow = ti.e * args.b_rows + ti.nt * (BN / 2);
-          tma_load_2d(sA + kABytes, &maps.b0, &full_bar[stage], kb * BK, brow);
-          tma_load_2d(sA + kABytes + kBBytes / 2, &maps.b1, &full_bar[stage], kb * BK, brow);
-        }
-        issued_mask |= 1u << stage;
-        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
-      }
-    }
-    if (lane == 0)
-      for (int s = 0; s < kStages; ++s)
-        if ((issued_mask >> s) & 1u) wait_drain(&full_bar[s], (issued_parity >> s) & 1u, args.err);
-   }
-  } else if (warp == 0) {
-    if (lane == 0 && MODE != GATE_UP_GATHER) {
+  if (warp == 0) {
+    if (lane == 0) {
       // ---------------- TMA producer ----------------
       int stage = 0;
       uint32_t phase = 0;
@@ -1035,6 +987,288 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
   cluster_sync();  // no CTA leaves while its peer may still signal it
 }
 
+// ---------------------------------------------------------------------------
+// Fused forward: dispatch, gate/up + SwiGLU and down in one persistent launch
+// ("Mixture-of-Kittens: Cursor open-sources an MoE training megakernel", key
+// point 5 and the key flowchart: a producer pulls a minibatch of token rows,
+// local counters wake the expert FFN, which runs gate/up, SwiGLU and down).
+//
+// On one GPU the pull dispatch is an HBM copy, done by side warps of every
+// CTA: they claim 8-row chunks of the expert-grouped buffer in row order
+// through a ticket, copy each row's token from x (zero rows for padding) and
+// count the finished rows of each 128-row tile. The SM-pair GEMM roles walk
+// one list of units: every pair item (256 rows of one expert, or its last 128)
+// contributes G gate/up units (one per 128 I columns of gate and up) and D
+// down units (one per 256 H columns), the down units of item p placed `lag`
+// items after its gate/up units. A gate/up unit's producer waits (bounded)
+// until the rows of its tile are dispatched; a down unit's producer waits
+// until all G gate/up units of its item have stored Act (each epilogue warp
+// counts its stores once they have landed). Every unit depends only on units
+// earlier in the list and on the dispatch, which waits on nothing, and the
+// grid holds only co-resident CTA pairs, so every wait is satisfied in time.
+// The arithmetic of each tile is that of the separate gate/up and down
+// launches (same MMAs in the same order, same epilogues), so the results are
+// bit-identical to dispatch + gate/up + down.
+constexpr int kFfDispWarps = 4;
+
+struct FusedArgs {
+  const uint4* x;            // token rows [N][H/8]
+  uint4* xe;                 // expert-grouped rows [R][H/8]
+  const int32_t* src_of_row;  // assignment of each row, -1 on padding
+  const int32_t* pad_offsets;
+  int32_t* ticket;           // dispatch chunk ticket
+  int32_t* disp_done;        // [R/128] rows dispatched per 128-row tile
+  int32_t* gu_done;          // [R/128] finished gate/up epilogue-warp units per item
+  int64_t A, rows;
+  int E, k, hv;
+  int G, D, lag;             // units per item (gate/up, down); item lag of the down units
+};
+
+struct FusedUnit {
+  bool valid, down;
+  int item, nt;
+};
+
+__device__ __forceinline__ FusedUnit fused_unit(const FusedArgs& f, int64_t u, int n_items) {
+  const int per = f.G + f.D;
+  const int64_t step = u / per;
+  const int r = static_cast<int>(u % per);
+  FusedUnit x;
+  x.down = r >= f.G;
+  x.nt = x.down ? r - f.G : r;
+  const int64_t item = x.down ? step - f.lag : step;
+  x.valid = item >= 0 && item < n_items;
+  x.item = x.valid ? static_cast<int>(item) : 0;
+  return x;
+}
+
+// Dispatch side warps: xe[row] = x[src_of_row[row] / k], padding rows 0.
+// They claim chunks from the front as fast as they can: making them wait for
+// the gate/up progress (a bounded window of items ahead, so rows are still in
+// L2 when read) measured slower, the producers then waiting for rows.
+__device__ __forceinline__ void dispatch_rows(const FusedArgs& f, int lane) {
+  int64_t rows = f.pad_offsets[f.E];
+  rows = rows < 0 ? 0 : (rows > f.rows ? f.rows : rows);
+  const int32_t n_chunks = static_cast<int32_t>(rows / kRcRows);
+  while (true) {
+    int32_t c = 0;
+    if (lane == 0) c = atomicAdd(f.ticket, 1);
+    c = __shfl_sync(0xffffffffu, c, 0);
+    if (c >= n_chunks) break;
+    for (int r = 0; r < kRcRows; ++r) {
+      const int64_t row = static_cast<int64_t>(c) * kRcRows + r;
+      const int32_t as = f.src_of_row[row];
+      uint4* drow = f.xe + row * f.hv;
+      if (as < 0 || as >= f.A) {
+        for (int v = lane; v < f.hv; v += 32) drow[v] = make_uint4(0u, 0u, 0u, 0u);
+        continue;
+      }
+      const uint4* srow = f.x + static_cast<int64_t>(as / f.k) * f.hv;
+      for (int base = 0; base < f.hv; base += 256) {
+        uint4 v8[8];  // all loads of the step first: 8 in flight per lane
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int v = base + 32 * q + lane;
+          if (v < f.hv) v8[q] = __ldg(srow + v);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int v = base + 32 * q + lane;
+          if (v < f.hv) drow[v] = v8[q];
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // rows seen by the TMA loads
+      __threadfence();
+      atomicAdd(f.disp_done + (static_cast<int64_t>(c) * kRcRows) / BM, kRcRows);
+    }
+  }
+}
+
+__device__ __forceinline__ TileInfo fused_tile(const FusedArgs& f, const Args& gu, const Args& dn,
+                                               const FusedUnit& fu, int crank) {
+  return fu.down ? decode_pair_tile<DOWN>(dn, static_cast<int64_t>(fu.item) * dn.n_nt + fu.nt, crank)
+                 : decode_pair_tile<GATE_UP>(gu, static_cast<int64_t>(fu.item) * gu.n_nt + fu.nt,
+                                             crank);
+}
+
+__global__ void __launch_bounds__(kGemmThreads + 32 * kFfDispWarps, 1)
+    fused_forward_kernel(const __grid_constant__ Maps mgu, const __grid_constant__ Maps mdn,
+                         const Args gu, const Args dn, const FusedArgs f) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[kPairStages], empty_bar[kPairStages], tfull_bar[2], tempty_bar[2],
+      drain_bar;
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ int abort_flag;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int crank = static_cast<int>(cluster_ctarank());
+  const bool leader = crank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 8);  // one arrive per epilogue warp of both CTAs
+    }
+    mbar_init(&drain_bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mgu.a0);
+    tma_prefetch_desc(&mgu.b0);
+    tma_prefetch_desc(&mdn.a0);
+    tma_prefetch_desc(&mdn.b0);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&tmem_base_slot, kTmemCols);  // one warp of each CTA, collectively
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_slot;
+  volatile int* abortp = &abort_flag;
+  int n_items = *gu.n_ptiles;
+  n_items = n_items < 0 ? 0 : (n_items > gu.max_mtiles ? gu.max_mtiles : n_items);
+  const int64_t total = static_cast<int64_t>(n_items + f.lag) * (f.G + f.D);
+  const int64_t first = blockIdx.x / 2, stride = gridDim.x / 2;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs) ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      for (int64_t u = first; u < total && ok; u += stride) {
+        const FusedUnit fu = fused_unit(f, u, n_items);
+        if (!fu.valid) continue;
+        const TileInfo ti = fused_tile(f, gu, dn, fu, crank);
+        if (ti.nkb > 0) {
+          const bool ready = fu.down ? wait_count(f.gu_done + fu.item, 8 * f.G, abortp, gu.err)
+                                     : wait_count(f.disp_done + ti.row0 / BM, BM, abortp, gu.err);
+          if (!ready) break;
+        }
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, gu.err)) { ok = false; break; }
+          uint8_t* sA = smem + stage * kPairStageBytes;
+          if (leader)
+            mbar_arrive_expect_tx(&full_bar[stage],
+                                  2 * ((ti.fold ? kPairABytes / 2 : kPairABytes) + kPairBBytes));
+          if (fu.down)
+            issue_loads_pair<DOWN>(mdn, dn, ti, kb, sA, sA + kPairABytes,
+                                   cluster_addr(&full_bar[stage], 0), crank);
+          else
+            issue_loads_pair<GATE_UP>(mgu, gu, ti, kb, sA, sA + kPairABytes,
+                                      cluster_addr(&full_bar[stage], 0), crank);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (leader)  // the even CTA's full barriers count both CTAs' copies
+        for (int s = 0; s < kPairStages; ++s)
+          if ((issued_mask >> s) & 1u) wait_drain(&full_bar[s], (issued_parity >> s) & 1u, gu.err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (even CTA only) ----------------
+      constexpr uint32_t idesc256 = idesc_bf16(2 * BM, BN, false, false);
+      constexpr uint32_t idesc128 = idesc_bf16(BM, BN, false, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t uses0 = 0u, uses1 = 0u;
+      bool ok = true;
+      for (int64_t u = first; u < total && ok; u += stride) {
+        const FusedUnit fu = fused_unit(f, u, n_items);
+        if (!fu.valid) continue;
+        const TileInfo ti = fused_tile(f, gu, dn, fu, crank);
+        if (!mbar_wait(&tempty_bar[acc], ((acc ? uses1 : uses0) & 1u) ^ 1u, abortp, gu.err)) break;
+        tc_fence_after();
+        const uint32_t dtmem = tmem_base + acc * BN;
+        const uint32_t idesc = ti.fold ? idesc128 : idesc256;
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abortp, gu.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * kPairStageBytes);
+          const uint32_t b_addr = a_addr + kPairABytes;
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks)
+            umma_bf16_pair(dtmem, sdesc_sw128(a_addr + ks * 32, 16, 1024),
+                           sdesc_sw128(b_addr + ks * 32, 16, 1024), idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+          umma_commit_pair_mc(&empty_bar[stage], 0x3);  // both CTAs may refill the stage
+          if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(&tfull_bar[acc], 0x3);  // both halves of the tile are ready
+        if (acc) ++uses1; else ++uses0;
+        acc ^= 1;
+      }
+      umma_commit_pair(&drain_bar);
+      wait_drain(&drain_bar, 0, gu.err);
+    }
+  } else if (warp >= 6) {
+    // ---------------- dispatch side warps 6.. ----------------
+    dispatch_rows(f, lane);
+  } else {
+    // ---------------- epilogue warps 2..5 (both CTAs) ----------------
+    const int quad = warp & 3;
+    uint8_t* stage_out = smem + kPairStages * kPairStageBytes + (warp - 2) * 2 * kStageOutBytes;
+    uint32_t nstore = 0;
+    int acc = 0;
+    uint32_t uses0 = 0u, uses1 = 0u;
+    for (int64_t u = first; u < total; u += stride) {
+      const FusedUnit fu = fused_unit(f, u, n_items);
+      if (!fu.valid) continue;
+      const TileInfo ti = fused_tile(f, gu, dn, fu, crank);
+      if (!mbar_wait(&tfull_bar[acc], (acc ? uses1 : uses0) & 1u, abortp, gu.err)) break;
+      tc_fence_after();
+      if (ti.skip) {
+        if (lane == 0) set_dev_error(gu.err, MOE_DEVERR_BAD_EXPERT);
+      } else if (fu.down) {
+        epilogue<DOWN, true>(mdn, dn, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
+      } else {
+        epilogue<GATE_UP, true>(mgu, gu, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&tempty_bar[acc]);
+        else mbar_arrive_cluster(cluster_addr(&tempty_bar[acc], 0));
+        if (!fu.down) {  // this warp's Act rows are in global memory: count them
+          bulk_wait_all();
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __threadfence();
+          atomicAdd(f.gu_done + fu.item, 1);
+        }
+      }
+      if (acc) ++uses1; else ++uses0;
+      acc ^= 1;
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the even CTA's MMAs into this CTA's TMEM have retired
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+  cluster_sync();  // no CTA leaves while its peer may still signal it
+}
+
 // Experts ranked by row count, descending; equal counts keep ascending
 // expert index. One CTA; each thread ranks its experts against all others.
 __global__ void __launch_bounds__(1024) expert_order_kernel(const int32_t* __restrict__ counts,
@@ -1219,31 +1453,6 @@ moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const v
   return launch_tokens<GATE_UP>(m, a, s);
 }
 
-moe_status gemm_gate_up_gather(const Layout& L, const void* ws, const void* x, const void* wg,
-                               const void* wu, void* g, void* u, void* act, cudaStream_t s) {
-  if (L.N == 0) return MOE_OK;
-  Maps m{};
-  if (!make_map(&m.a0, x, L.H, L.N, 1) ||
-      !make_map(&m.b0, wg, L.H, static_cast<int64_t>(L.E) * L.I, BN / 2) ||
-      !make_map(&m.b1, wu, L.H, static_cast<int64_t>(L.E) * L.I, BN / 2) ||
-      !make_bf16_out_map(&m.o2, act, L.I, L.R))
-    return MOE_ERR_CUDA;
-  const bool store_gu = g != nullptr && u != nullptr;
-  if (store_gu && (!make_bf16_out_map(&m.o0, g, L.I, L.R) || !make_bf16_out_map(&m.o1, u, L.I, L.R)))
-    return MOE_ERR_CUDA;
-  m.a1 = m.a0;
-  Args a = base_args(L, ws);
-  a.n_nt = L.I / (BN / 2);
-  a.kb1 = L.H / BK;
-  a.kb2 = 0;
-  a.b_rows = L.I;
-  a.ld_out = L.I;
-  a.src_of_row = at<int32_t>(ws, L.src_of_row);
-  a.k = L.k;
-  a.store_gu = store_gu ? 1 : 0;
-  return launch<GATE_UP_GATHER>(m, a, static_cast<int64_t>(a.max_mtiles) * a.n_nt, s);
-}
-
 moe_status gemm_down(const Layout& L, const void* ws, const void* act, const void* wd, void* ye,
                      cudaStream_t s) {
   Maps m{};
@@ -1368,6 +1577,99 @@ moe_status gemm_gate_up_wgrad(const Layout& L, const void* ws, const void* dg, c
   a.out0 = dw_gate;
   a.out1 = dw_up;
   return launch_pair<WGRAD>(m, a, 2LL * L.E * (a.w_mt / 2) * a.w_nt, s);
+}
+
+moe_status gemm_fused_forward(const Layout& L, const void* ws, const void* x, const void* wg,
+                              const void* wu, const void* wd, void* xe, void* g, void* u,
+                              void* act, void* ye, cudaStream_t s) {
+  Maps mg{}, md{};
+  if (!make_a_maps(&mg.a0, &mg.a0h, xe, L.H, L.R) ||
+      !make_map(&mg.b0, wg, L.H, static_cast<int64_t>(L.E) * L.I, BN / 4) ||
+      !make_map(&mg.b1, wu, L.H, static_cast<int64_t>(L.E) * L.I, BN / 4) ||
+      !make_bf16_out_map(&mg.o2, act, L.I, L.R) ||
+      !make_a_maps(&md.a0, &md.a0h, act, L.I, L.R) ||
+      !make_map(&md.b0, wd, L.I, static_cast<int64_t>(L.E) * L.H, BN / 2) ||
+      !make_bf16_out_map(&md.o0, ye, L.H, L.R))
+    return MOE_ERR_CUDA;
+  const bool store_gu = g != nullptr && u != nullptr;
+  if (store_gu && (!make_bf16_out_map(&mg.o0, g, L.I, L.R) || !make_bf16_out_map(&mg.o1, u, L.I, L.R)))
+    return MOE_ERR_CUDA;
+  mg.a1 = mg.a0;
+  mg.a1h = mg.a0h;
+  md.a1 = md.a0;
+  md.a1h = md.a0h;
+  md.b1 = md.b0;
+  Args ag = base_args(L, ws);
+  ag.n_nt = L.I / (BN / 2);
+  ag.kb1 = L.H / BK;
+  ag.b_rows = L.I;
+  ag.ld_out = L.I;
+  ag.store_gu = store_gu ? 1 : 0;
+  Args ad = base_args(L, ws);
+  ad.n_nt = L.H / BN;
+  ad.kb1 = L.I / BK;
+  ad.b_rows = L.H;
+  ad.ld_out = L.H;
+  int32_t* sync = const_cast<int32_t*>(at<int32_t>(ws, L.ff_sync));
+  const int64_t n_tiles = L.R / BM;
+  FusedArgs f{};
+  f.x = static_cast<const uint4*>(x);
+  f.xe = static_cast<uint4*>(xe);
+  f.src_of_row = at<int32_t>(ws, L.src_of_row);
+  f.pad_offsets = at<int32_t>(ws, L.pad_offsets);
+  f.ticket = sync;
+  f.disp_done = sync + 1;
+  f.gu_done = sync + 1 + n_tiles;
+  f.A = L.A;
+  f.rows = L.R;
+  f.E = L.E;
+  f.k = L.k;
+  f.hv = L.H / 8;
+  f.G = ag.n_nt;
+  f.D = ad.n_nt;
+
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;
+  auto config = [](cudaLaunchConfig_t& cfg, cudaLaunchAttribute* att, int clusters) {
+    att[0].id = cudaLaunchAttributeClusterDimension;
+    att[0].val.clusterDim.x = 2;
+    att[0].val.clusterDim.y = 1;
+    att[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(kGemmThreads + 32 * kFfDispWarps);
+    cfg.dynamicSmemBytes = kPairSmemBytes;
+    cfg.attrs = att;
+    cfg.numAttrs = 1;
+  };
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(fused_forward_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+    if (attr_err != cudaSuccess) return;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute att[1];
+    config(cfg, att, 64);
+    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, fused_forward_kernel, &cfg);
+    if (attr_err == cudaSuccess && max_clusters <= 0) attr_err = cudaErrorInvalidConfiguration;
+  });
+  if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
+  // every CTA pair of the grid is resident at once (the waits rely on it):
+  // the grid is the occupancy query's cluster count, never more
+  const int clusters = max_clusters;
+  // the down units of an item follow its gate/up units by about three waves
+  // of units, so they rarely find its Act unfinished
+  f.lag = std::max(2, (3 * clusters + f.G + f.D - 1) / (f.G + f.D));
+  if (cudaMemsetAsync(sync, 0, sizeof(int32_t) * (1 + 2 * n_tiles), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (L.R == 0) return MOE_OK;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute att[1];
+  config(cfg, att, clusters);
+  cfg.stream = s;
+  if (cudaLaunchKernelEx(&cfg, fused_forward_kernel, mg, md, ag, ad, f) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace moe

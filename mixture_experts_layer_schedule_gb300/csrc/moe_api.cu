@@ -61,6 +61,7 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   L->ptiles = take(sizeof(int32_t) * 3 * (R / kTileM));  // SM-pair items (at most one per tile)
   L->n_ptiles = take(sizeof(int32_t));
   L->rc_sync = take(sizeof(int32_t) * (1 + R / kTileM));
+  L->ff_sync = take(sizeof(int32_t) * (1 + 2 * (R / kTileM)));
   L->warp_counts = take(sizeof(int32_t) * p->E * std::max<int64_t>(L->n_warps, 1));
   L->expert_order = take(sizeof(int32_t) * p->E);
   L->router_logits = take(sizeof(float) * std::max<int64_t>(p->N, 1) * p->E);
@@ -415,6 +416,16 @@ moe_status moe_mxfp8_forward_operands(const moe_problem* p, void* ws, moe_mxfp8_
   return MOE_OK;
 }
 
+moe_status moe_mxfp8_backward_operands(const moe_problem* p, void* ws, moe_mxfp8_operand* dg_rows,
+                                       moe_mxfp8_operand* du_rows) {
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  if (p->dtype != MOE_MXFP8 || !dg_rows || !du_rows) return MOE_ERR_INVALID_ARG;
+  *dg_rows = ws_operand(ws, L.mq_ri, L.ms_ri);  // written by mx_backward_gemms
+  *du_rows = ws_operand(ws, L.mq_ri2, L.ms_ri2);
+  return MOE_OK;
+}
+
 moe_status moe_dispatch_mxfp8(const moe_problem* p, const void* ws, const void* x, void* xe,
                               uint8_t* q_e4m3, uint8_t* s_e8m0, void* stream) {
   Layout L;
@@ -453,16 +464,17 @@ moe_status moe_combine(const moe_problem* p, const void* ws, const void* ye, con
   return cu(launch_combine(L, ws, ye, topk_w, y, S(stream)));
 }
 
-moe_status moe_expert_gate_up_gather(const moe_problem* p, const void* ws, const void* x,
-                                     const moe_weights* w, void* g, void* u, void* act,
-                                     void* stream) {
+moe_status moe_dispatch_expert_ffn(const moe_problem* p, const void* ws, const void* x,
+                                   const moe_weights* w, void* xe, void* g, void* u, void* act,
+                                   void* ye, void* stream) {
   Layout L;
   MOE_TRY(prep(p, ws, &L));
-  if ((L.N > 0 && !aligned(x, 16)) || !weights_ok(w) || !aligned(act, 16))
+  if (p->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const bool no_gu = g == nullptr && u == nullptr;
+  if ((L.N > 0 && !aligned(x, 16)) || !weights_ok(w) || !aligned(xe, 16) || !aligned(act, 16) ||
+      !aligned(ye, 16) || (!no_gu && (!aligned(g, 16) || !aligned(u, 16))))
     return MOE_ERR_INVALID_ARG;
-  if ((g == nullptr) != (u == nullptr)) return MOE_ERR_INVALID_ARG;
-  if (g && (!aligned(g, 16) || !aligned(u, 16))) return MOE_ERR_INVALID_ARG;
-  return gemm_gate_up_gather(L, ws, x, w->w_gate, w->w_up, g, u, act, S(stream));
+  return gemm_fused_forward(L, ws, x, w->w_gate, w->w_up, w->w_down, xe, g, u, act, ye, S(stream));
 }
 
 moe_status moe_forward_inference(const moe_problem* p, const void* x, const moe_weights* w,
@@ -489,13 +501,9 @@ moe_status moe_forward_inference(const moe_problem* p, const void* x, const moe_
     }
     return moe_combine(p, ws, ye, topk_w, y, stream);
   }
-  // Dispatch into the Ye scratch, gate/up on SM pairs without storing G and U,
-  // then down overwrites Xe with Ye (Xe's last reader ran). Measured faster
-  // than the gate/up GEMM with the dispatch fused into its producer
-  // (moe_expert_gate_up_gather), whose gathers run on single-CTA tiles.
-  MOE_TRY(moe_dispatch(p, ws, x, ye, stream));
-  MOE_TRY(moe_expert_gate_up(p, ws, ye, w, nullptr, nullptr, act, stream));
-  MOE_TRY(moe_expert_down(p, ws, act, w, ye, stream));
+  // Dispatch, gate/up (Act only) and down in one launch; Xe and Ye share the
+  // scratch rows (a row group's Xe is consumed before its Ye is written).
+  MOE_TRY(moe_dispatch_expert_ffn(p, ws, x, w, ye, nullptr, nullptr, act, ye, stream));
   return moe_combine(p, ws, ye, topk_w, y, stream);
 }
 
@@ -511,22 +519,26 @@ moe_status moe_forward(const moe_problem* p, const void* x, const moe_weights* w
     MOE_TRY(mx_forward_gemms(L, ws, *w->mx, v.g, v.u, v.act, v.ye, S(stream)));
     return moe_combine(p, ws, v.ye, topk_w, y, stream);
   }
-  MOE_TRY(moe_dispatch(p, ws, x, v.xe, stream));
-  if (p->dtype == MOE_MXFP8) {
-    // MXFP8 on bf16 MMAs: gate/up reads Xe quantised along H, down reads Act
-    // quantised along I, as exact bf16 values
-    Layout L;
-    MOE_TRY(prep(p, ws, &L));
-    void* xq = at<char>(ws, L.mx_rh);
-    void* aq = at<char>(ws, L.mx_ri1);
-    MOE_TRY(mxfp8_qdq(v.xe, xq, L.R, L.H, 0, stream));
-    MOE_TRY(moe_expert_gate_up(p, ws, xq, w, v.g, v.u, v.act, stream));
-    MOE_TRY(mxfp8_qdq(v.act, aq, L.R, L.I, 0, stream));
-    MOE_TRY(moe_expert_down(p, ws, aq, w, v.ye, stream));
+  if (p->dtype == MOE_BF16) {
+    // Four launches: measured faster than moe_dispatch_expert_ffn (the same
+    // work in one persistent launch), whose dispatch competes with the GEMMs
+    // for the same memory system instead of overlapping a separate resource.
+    MOE_TRY(moe_dispatch(p, ws, x, v.xe, stream));
+    MOE_TRY(moe_expert_gate_up(p, ws, v.xe, w, v.g, v.u, v.act, stream));
+    MOE_TRY(moe_expert_down(p, ws, v.act, w, v.ye, stream));
     return moe_combine(p, ws, v.ye, topk_w, y, stream);
   }
-  MOE_TRY(moe_expert_gate_up(p, ws, v.xe, w, v.g, v.u, v.act, stream));
-  MOE_TRY(moe_expert_down(p, ws, v.act, w, v.ye, stream));
+  // MXFP8 on bf16 MMAs: gate/up reads Xe quantised along H, down reads Act
+  // quantised along I, as exact bf16 values
+  Layout L;
+  MOE_TRY(prep(p, ws, &L));
+  MOE_TRY(moe_dispatch(p, ws, x, v.xe, stream));
+  void* xq = at<char>(ws, L.mx_rh);
+  void* aq = at<char>(ws, L.mx_ri1);
+  MOE_TRY(mxfp8_qdq(v.xe, xq, L.R, L.H, 0, stream));
+  MOE_TRY(moe_expert_gate_up(p, ws, xq, w, v.g, v.u, v.act, stream));
+  MOE_TRY(mxfp8_qdq(v.act, aq, L.R, L.I, 0, stream));
+  MOE_TRY(moe_expert_down(p, ws, aq, w, v.ye, stream));
   return moe_combine(p, ws, v.ye, topk_w, y, stream);
 }
 

@@ -93,20 +93,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, ui
       : "memory");
 }
 
-// Four rows (row0..row3, any order) of a 2-D tensor, each box-width wide from
-// column c0, gathered into four consecutive shared-memory rows (the map's box
-// is one row high).
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tm, uint64_t* bar,
-                                            int32_t c0, int32_t r0, int32_t r1, int32_t r2,
-                                            int32_t r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2),
-      "r"(r3)
-      : "memory");
-}
-
 // ---- thread-block clusters ----------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -33,6 +33,7 @@ struct Layout {
       mq_rh, ms_rh, mq_ri, ms_ri, mq_ri2, ms_ri2, mq_th, ms_th, mq_ti, ms_ti, mq_ti2, ms_ti2,
       router_logits, router_dz, router_partial,  // router: logits scratch [N,E], dz [A], tile partials
       rc_sync,  // fused reverse-combine: chunk ticket + finished rows per 128-row tile
+      ff_sync,  // fused forward: dispatch ticket, rows per 128-row tile, gate/up units per item
       dyxe, dg, du, ws_bytes;
   // forward-context byte offsets
   size_t xe, g, u, act, ye, saved_bytes;
@@ -86,10 +87,14 @@ cudaError_t launch_mxfp8_quantize(const void* src, int64_t rows, int64_t cols, u
 // Grouped GEMMs (tcgen05). Return MOE_ERR_CUDA on a driver/launch failure.
 moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const void* wg,
                         const void* wu, void* g, void* u, void* act, cudaStream_t s);
-moe_status gemm_gate_up_gather(const Layout& L, const void* ws, const void* x, const void* wg,
-                               const void* wu, void* g, void* u, void* act, cudaStream_t s);
 moe_status gemm_down(const Layout& L, const void* ws, const void* act, const void* wd, void* ye,
                      cudaStream_t s);
+// Dispatch + gate/up + SwiGLU + down in one persistent launch (bit-identical
+// to launch_dispatch, gemm_gate_up and gemm_down in sequence). g, u may both
+// be NULL (inference: Act only).
+moe_status gemm_fused_forward(const Layout& L, const void* ws, const void* x, const void* wg,
+                              const void* wu, const void* wd, void* xe, void* g, void* u,
+                              void* act, void* ye, cudaStream_t s);
 moe_status gemm_down_dgrad(const Layout& L, const void* ws, const void* dye, const void* g,
                            const void* u, const void* wd, void* dg, void* du, cudaStream_t s);
 // DACT with the reverse-combine fused in: dYe (written here, then read by the

@@ -362,24 +362,60 @@ __device__ __align__(256) int32_t g_sched_scratch[kNoAllocScratchInts];
 
 constexpr int kMaxDevices = 256;
 std::mutex g_scratch_mu;
-int32_t* g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+  unsigned long long ctx_id;  // unique id of the context the address belongs to (0: none)
+  int32_t* ptr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
+
+// Unique id of the calling thread's current context (driver entry points
+// looked up once through the runtime, no libcuda link); 0 if none is current.
+unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 // Device address of g_sched_scratch on the current device. In host code the
-// array's name is only a host-side stand-in, so the address is looked up once
-// per device (the first call on a device does this) and cached.
+// array's name is only a host-side stand-in, so the address is looked up with
+// the device current and cached per device together with the id of the
+// context it was taken in: the first call on a device does the lookup, and so
+// does the first call after the device's context was destroyed and created
+// again (cudaDeviceReset), where the old address would be stale.
 cudaError_t scratch_for_current_device(int32_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchAddr& c = g_scratch_addr[dev];
+  if (ctx == 0 || c.ctx_id != ctx || !c.ptr) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_sched_scratch);
+    e = cudaGetSymbolAddress(&p, g_sched_scratch);  // also makes the device's context current
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = static_cast<int32_t*>(p);
+    c.ptr = static_cast<int32_t*>(p);
+    c.ctx_id = current_context_id();
   }
-  *out = g_scratch_addr[dev];
+  *out = c.ptr;
   return cudaSuccess;
 }
 

@@ -153,7 +153,8 @@ class MoELayer:
         return self.y
 
     def forward_inference(self, x, wg, wu, wd, topk_w=None, stream=None, mx=None):
-        """Forward without a saved context; the dispatch is fused into gate/up (bf16)."""
+        """Forward without a saved context (inference): dispatch into workspace
+        scratch, gate/up storing Act only, down, combine; same y as forward()."""
         w = _lib.weights(wg, wu, wd, mx=mx.struct if mx is not None else None)
         _lib.moe_forward_inference(self.p, x, w, self.topk_w if topk_w is None else topk_w,
                                    self.y, self.ws, stream)

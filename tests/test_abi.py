@@ -128,8 +128,14 @@ def test_workspace_and_context_regions_are_disjoint_and_aligned(lib, N, H, I, E,
                ("n_tiles", sched.n_tiles, 4)]
     if dtype == _lib.MOE_MXFP8:  # the forward's row-form MXFP8 operands of Xe and Act
         (xq, xs), (aq, as_) = _lib.moe_mxfp8_forward_operands(p, base)
-        regions += [("xe_q", xq, R * H), ("xe_s", xs, R * H // 32), ("act_q", aq, R * I),
-                    ("act_s", as_, R * I // 32)]
+        fwd = [("xe_q", xq, R * H), ("xe_s", xs, R * H // 32), ("act_q", aq, R * I),
+               ("act_s", as_, R * I // 32)]
+        # the backward's dG / dU row operands (dG reuses Act's buffer after the
+        # forward's last reader): checked beside the tables, apart from the forward's
+        (gq, gs), (uq, us) = _lib.moe_mxfp8_backward_operands(p, base)
+        check(regions + [("dg_q", gq, R * I), ("dg_s", gs, R * I // 32), ("du_q", uq, R * I),
+                         ("du_s", us, R * I // 32)], ws_bytes)
+        regions += fwd
     check(regions, ws_bytes)
     sv = _lib.SavedView()
     assert lib.moe_saved_layout(ctypes.byref(p), base, ctypes.byref(sv)) == _lib.MOE_OK

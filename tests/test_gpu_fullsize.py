@@ -8,8 +8,10 @@ At these sizes the oracle cannot run the whole layer, so:
   * y, dx and d(routing weights) are compared on a seeded sample of tokens,
     each computed by the oracle from that token's own assignments;
   * weight-gradient rows are compared for sampled experts (the smallest
-    non-empty one and the median one) and sampled rows, each computed by the
-    oracle over every token routed to that expert;
+    non-empty one, the median one and the largest one, whose long token
+    panels run the chunked weight-gradient plan on the skewed workload) and
+    sampled rows, each computed by the oracle over every token routed to that
+    expert;
   * the tolerance is the bf16 bound, max|err| <= 2e-2 * max|ref| over the
     sampled elements of each tensor; ids and tables are exact.
 """
@@ -73,11 +75,11 @@ def test_full_size_sampled_parity(shape):
     assert_close("dx", g.dx[torch.as_tensor(tok)], s["dx"])
     assert_close("d_topk_w", g.d_topk_w[torch.as_tensor(tok)], s["dw"])
 
-    # sampled weight-gradient rows of two experts
+    # sampled weight-gradient rows of three experts: smallest, median, largest
     counts = ref["counts"]
     nonzero = np.flatnonzero(counts)
     by_size = nonzero[np.argsort(counts[nonzero], kind="stable")]
-    experts = sorted({int(by_size[0]), int(by_size[len(by_size) // 2])})
+    experts = sorted({int(by_size[0]), int(by_size[len(by_size) // 2]), int(by_size[-1])})
     il = np.sort(rng.choice(shape.I, 4, replace=False)).astype(np.int32)
     hl = np.sort(rng.choice(shape.H, 4, replace=False)).astype(np.int32)
     for e in experts:

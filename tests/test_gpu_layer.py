@@ -276,6 +276,76 @@ def test_backward_equals_phase_chain(shape, overlap):
         assert torch.equal(got, want), name
 
 
+FUSED_SHAPES = CHAIN_SHAPES + [LAYER_SHAPES[i] for i in (2, 3, 5, 7, 8, 9)] + [
+    custom_shape(3000, 1024, 768, 16, 8, zipf_s=1.2, name="fused_skewed_odd_items")]
+
+
+@pytest.mark.parametrize("inference", [False, True], ids=["training", "inference"])
+@pytest.mark.parametrize("shape", FUSED_SHAPES, ids=lambda s: s.name)
+def test_fused_forward_equals_phase_chain(shape, inference):
+    """moe_dispatch_expert_ffn (dispatch, gate/up + SwiGLU and down in one
+    persistent launch) followed by the combine must equal, bit for bit,
+    moe_dispatch + moe_expert_gate_up + moe_expert_down + moe_combine on the
+    same inputs: Xe (padding rows zero), G, U, Act, Ye and y. The context-free
+    forward (moe_forward_inference: the fused launch with Xe and Ye sharing one
+    scratch buffer) gives the same y."""
+    inp = to_dev(inputs.make_inputs(shape, seed=4, device="cpu"))
+    layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev(),
+                     minibatch_rows=shape.minibatch_rows, allocate_grads=False)
+    layer.route(inp["logits"], inp["bias"])
+    layer.build_schedule()
+    sv = layer.saved_tensors()
+    for t in sv.values():
+        t.fill_(float("nan"))  # rows the fused launch must write
+    p, ws = layer.p, layer.ws
+    w = _lib.weights(inp["wg"], inp["wu"], inp["wd"])
+    if inference:
+        y = layer.forward_inference(inp["x"], inp["wg"], inp["wu"], inp["wd"]).clone()
+    else:
+        _lib.moe_dispatch_expert_ffn(p, ws, inp["x"], w, sv["xe"], sv["g"], sv["u"], sv["act"],
+                                     sv["ye"])
+        _lib.moe_combine(p, ws, sv["ye"], layer.topk_w, layer.y)
+        y = layer.y.clone()
+        got = {k: v.clone() for k, v in sv.items()}
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    ref = {k: torch.empty_like(v) for k, v in sv.items()}
+    y_ref = torch.empty_like(y)
+    _lib.moe_dispatch(p, ws, inp["x"], ref["xe"])
+    _lib.moe_expert_gate_up(p, ws, ref["xe"], w, ref["g"], ref["u"], ref["act"])
+    _lib.moe_expert_down(p, ws, ref["act"], w, ref["ye"])
+    _lib.moe_combine(p, ws, ref["ye"], layer.topk_w, y_ref)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert torch.equal(y, y_ref)
+    if inference:
+        return
+    rows = int(layer.schedule_tensors()["pad_offsets"][shape.E])
+    for name in ("xe", "g", "u", "act", "ye"):
+        assert torch.equal(got[name][:rows].view(torch.int16), ref[name][:rows].view(torch.int16)), name
+
+
+def test_fused_forward_reruns_are_bitwise_identical():
+    shape = custom_shape(3000, 1024, 768, 16, 8, zipf_s=1.2, name="fused_rerun")
+    inp = to_dev(inputs.make_inputs(shape, seed=8, device="cpu"))
+    layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev(), allocate_grads=False)
+    layer.route(inp["logits"], inp["bias"])
+    layer.build_schedule()
+    w = _lib.weights(inp["wg"], inp["wu"], inp["wd"])
+    sv = layer.saved_tensors()
+    outs = []
+    for _ in range(3):
+        _lib.moe_dispatch_expert_ffn(layer.p, layer.ws, inp["x"], w, sv["xe"], sv["g"], sv["u"],
+                                     sv["act"], sv["ye"])
+        _lib.moe_combine(layer.p, layer.ws, sv["ye"], layer.topk_w, layer.y)
+        outs.append((layer.y.clone(), layer.saved.clone()))
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    for y, s in outs[1:]:
+        assert torch.equal(y.view(torch.int16), outs[0][0].view(torch.int16))
+        assert torch.equal(s, outs[0][1])
+
+
 def test_weight_gradient_of_a_dominant_expert():
     """One expert takes every token (K = 4096 rows = 64 k-blocks): its weight-
     gradient tiles are long enough to be issued in chunks with the other

@@ -284,3 +284,63 @@ def test_fp8_layer_empty_batch():
     torch.cuda.synchronize()
     assert layer.device_error() == 0
     assert torch.all(layer.grads.dw_gate == 0) and torch.all(layer.grads.dw_down == 0)
+
+
+def _decode_rows(q_ptr, s_ptr, rows, k):
+    """Values [rows, k] of a row-form MXFP8 operand in device memory."""
+    q = torch.as_tensor(_DevBytes(q_ptr, rows * k), device=dev()).cpu().numpy().reshape(rows, k)
+    s = torch.as_tensor(_DevBytes(s_ptr, rows * k // 32), device=dev()).cpu().numpy()
+    table = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    scale = 2.0 ** (untile_scales(s, rows, k).astype(np.float64) - 127)
+    return table[q] * np.repeat(scale, 32, axis=1)
+
+
+def test_fp8_error_budget_at_the_tiny_shape():
+    """Where the MXFP8 error against the oracle comes from, on the tiny
+    workload (seed 0, as in smoke): the GPU forms dG and dU from the G and U it
+    saved in bf16, the oracle from fp64 G and U; the two sides can then round
+    a dG or dU value to a neighbouring bf16 value and quantise it to a
+    neighbouring E4M3 code (or, through the block maximum, another scale).
+    The oracle's diagnostic switch that reads G and U as bf16 values (never
+    a parity reference) shows how much of the dx / dWg / dWu error that
+    explains: the GPU's quantised dG/dU rows (read back from the workspace)
+    disagree with it in far fewer codes, and the errors shrink."""
+    shape = SHAPES[0]
+    inp_cpu = inputs.make_inputs(shape, seed=0, device="cpu")
+    inp = to_dev(inp_cpu)
+    fwd, bwd = MoELayer.prepare_mxfp8_weights(inp["wg"], inp["wu"], inp["wd"])
+    mx = MoELayer.prepare_mxfp8_mma_weights(inp["wg"], inp["wu"], inp["wd"])
+    layer = _layer(shape)
+    layer.step(inp["x"], inp["logits"], inp["bias"], *fwd, inp["dy"], bwd=bwd, mx=mx)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    ids, w = oracle.route_topk(inp_cpu["logits"].numpy(), None, shape.k)
+    np.testing.assert_array_equal(layer.topk_ids.cpu().numpy(), ids)
+    prep = oracle.mxfp8_weights(inp_cpu["wg"], inp_cpu["wu"], inp_cpu["wd"])
+    ref = {gb: oracle.layer_mxfp8_trace(inp_cpu["x"], prep, ids, w, inp_cpu["dy"], gu_bf16=gb)
+           for gb in (False, True)}
+    slot = layer.schedule_tensors()["slot_of"].cpu().numpy().reshape(-1)
+    (gq, gs), (uq, us) = _lib.moe_mxfp8_backward_operands(layer.p, layer.ws)
+    got_rows = {"dg": _decode_rows(gq, gs, layer.R, shape.I)[slot],
+                "du": _decode_rows(uq, us, layer.R, shape.I)[slot]}
+    g = layer.grads
+    report = {}
+    for gb, r in ref.items():
+        key = "oracle_bf16_gu" if gb else "oracle"
+        report[key] = {
+            "dg_code_mismatch": float(np.mean(got_rows["dg"] != r["dg_rows"])),
+            "du_code_mismatch": float(np.mean(got_rows["du"] != r["du_rows"])),
+            **{n: max_rel(t, r[k]) for n, t, k in (("dx", g.dx, "dx"), ("dw_gate", g.dw_gate, "dwg"),
+                                                    ("dw_up", g.dw_up, "dwu"),
+                                                    ("dw_down", g.dw_down, "dwd"))}}
+    print("error budget", report)
+    # measured on a GB300 (seed 0): against the fp64 reference 4.3% / 1.5% of
+    # the dG / dU codes differ and dWg is off by 4.7e-2, dx by 3.7e-2; against
+    # the diagnostic one code in 262144 differs, dWg is off by 8e-6, dWu by
+    # 6e-4, dx by 4e-3. The checks keep a margin above those figures.
+    a, b = report["oracle"], report["oracle_bf16_gu"]
+    for n in ("dx", "dw_gate", "dw_up", "dw_down"):
+        assert a[n] <= MX_TOL, n
+    assert b["dg_code_mismatch"] <= 1e-4 and b["du_code_mismatch"] <= 1e-4
+    assert b["dw_gate"] <= 5e-3 and b["dw_up"] <= 5e-3 and b["dx"] <= 1.5e-2
+    assert b["dw_gate"] < a["dw_gate"] / 5 and b["dx"] < a["dx"] / 5
