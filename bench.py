@@ -51,6 +51,11 @@ def parse():
     ap.add_argument("--router", action="store_true",
                     help="start from x: the router GEMM (x . Wr^T) and its backward run on the "
                          "GPU inside the step (default: the step starts from router logits)")
+    ap.add_argument("--stages", type=int, default=0, choices=[0, 4, 5, 6],
+                    help="ring stages of the bf16 SM-pair GEMMs (0: the library's per-shape choice)")
+    ap.add_argument("--sweep-stages", action="store_true",
+                    help="time the workload with 4, 5 and 6 GEMM ring stages and print every "
+                         "GEMM phase's time at each and its best stage count")
     ap.add_argument("--sweep-T", action="store_true",
                     help="the minibatch knob sweep: run the workload at minibatch_rows T = 128, "
                          "256, 512, 1024 and print one line with every T's result and the best")
@@ -415,7 +420,7 @@ def workload(name):
                              zipf_s=z, minibatch_rows=T, dtype=dtype)
 
 
-def run_ours(args, ws_, rank, local, shape=None):
+def run_ours(args, ws_, rank, local, shape=None, stages=None):
     import torch
     from mixture_experts_layer_schedule_gb300 import MoELayer, _lib, inputs
 
@@ -425,8 +430,10 @@ def run_ours(args, ws_, rank, local, shape=None):
     # replicas: the same parameters, their own tokens and upstream gradients
     inp = inputs.make_inputs(shape, seed=rank, device=dev, weight_seed=0)
     mx = shape.dtype == "mxfp8"
+    stages = args.stages if stages is None else stages
     layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev,
-                     minibatch_rows=shape.minibatch_rows, dtype=shape.dtype)
+                     minibatch_rows=shape.minibatch_rows, dtype=shape.dtype,
+                     pipeline_stages=stages)
     p, wsb = layer.p, layer.ws
     wbwd = mxw = None
     if mx:  # weights pre-quantised once, outside the timed steps
@@ -549,7 +556,7 @@ def run_ours(args, ws_, rank, local, shape=None):
         pin.pop("dy", None)
     layers = [layer, MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev,
                               allocate_grads=backward, minibatch_rows=shape.minibatch_rows,
-                              dtype=shape.dtype)]
+                              dtype=shape.dtype, pipeline_stages=stages)]
     dev_in = [{k: torch.empty_like(v, device=dev) for k, v in pin.items()} for _ in range(2)]
     outs = [{"y": torch.empty((shape.N, shape.H), dtype=torch.bfloat16).pin_memory(),
              "dx": torch.empty((shape.N, shape.H), dtype=torch.bfloat16).pin_memory()}
@@ -674,6 +681,7 @@ def run_ours(args, ws_, rank, local, shape=None):
         "config": {"workload": shape.name, "N": shape.N, "H": shape.H, "I": shape.I,
                    "E": shape.E, "k": shape.k, "zipf_bias": shape.zipf_s,
                    "minibatch_rows": shape.minibatch_rows,
+                   "pipeline_stages": stages or "library choice",
                    "passes": "fwd+bwd" if backward else ("fwd (inference)" if inference
                                                            else "fwd"),
                    "l2": "inputs larger than L2 (expert weights alone "
@@ -704,13 +712,35 @@ MX_NOTE = "; MXFP8 weight copies quantised once before the sample, as on the GPU
 ROUTER_NOTE = "; router GEMM and router backward included"
 
 
+# fp64 weight gradients above this many bytes do not fit the oracle's host run
+# beside everything else; such shapes are timed per token and extrapolated.
+ORACLE_DW_BYTES_MAX = 16 << 30
+
+
+def oracle_extrapolates(shape):
+    return shape.backward and 3 * 8 * shape.E * shape.H * shape.I > ORACLE_DW_BYTES_MAX
+
+
 def cpu_sample(shape, inp, n_tok, threads, router=False):
     """Run the oracle on the first n_tok tokens of the workload (fwd+bwd with
     weight gradients; with router, the router GEMM and its backward too).
-    Returns (seconds, tokens)."""
+    Returns (seconds, tokens). Where the fp64 weight gradients would not fit
+    (oracle_extrapolates), the oracle runs the tokens' forward and data
+    gradients (tokens_bf16: 12 of the 18 H*I multiply-adds per assignment) and
+    the returned time is scaled by 18/12 for the weight gradients' share."""
     import numpy as np
 
     import oracle
+    if oracle_extrapolates(shape) and not router:
+        ids, w = oracle.route_topk(inp["logits"][:n_tok].cpu().numpy(),
+                                   None if inp["bias"] is None else inp["bias"].cpu().numpy(),
+                                   shape.k)
+        x = oracle.as_bf16_bits(inp["x"][:n_tok])
+        dy = oracle.as_bf16_bits(inp["dy"][:n_tok])
+        wg, wu, wd = (oracle.as_bf16_bits(t) for t in (inp["wg"], inp["wu"], inp["wd"]))
+        t0 = time.perf_counter()
+        oracle.tokens_bf16(x, wg, wu, wd, ids, w, dy, np.arange(n_tok), threads=threads)
+        return (time.perf_counter() - t0) * 18.0 / 12.0, n_tok
     logits = inp["logits"][:n_tok].cpu().numpy()
     if router:
         t0 = time.perf_counter()
@@ -808,6 +838,27 @@ def main():
         if rec is not None:
             print(json.dumps(rec), flush=True)
         return
+    if args.sweep_stages:
+        import torch
+        base = workload(args.config)
+        res = {}
+        for S in (4, 5, 6):
+            args.phase_report = True
+            r, _, _ = run_ours(args, ws_, rank, local, base, stages=S)
+            res[S] = {"value": r["value"], "ms_per_step": r["ms_per_step"],
+                      "phases": {k: v["ms"] for k, v in r["phases"].items()},
+                      "clocks": r["clocks"]}
+            del r
+            torch.cuda.empty_cache()
+        gemm = [k for k in res[6]["phases"] if k in phase_flops(base)]
+        best = {k: min(res, key=lambda S: res[S]["phases"][k]) for k in gemm}
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "unit": UNIT, "sweep": "pipeline_stages",
+                              "workload": base.name, "steps": args.steps, "warmup": args.warmup,
+                              "results": res, "best_stages_per_phase": best,
+                              "best_stages_step": max(res, key=lambda S: res[S]["value"])}),
+                  flush=True)
+        return
     if args.sweep_T:
         import torch
         base = workload(args.config)
@@ -831,15 +882,24 @@ def main():
     if rank == 0 and ws_ == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
         n_tok = args.cpu_tokens or 256
+        ext = oracle_extrapolates(shape) and not args.router
+        if ext:
+            n_tok = min(n_tok, 16)
         secs, n = cpu_sample(shape, inp, n_tok, threads, args.router)
         rec["cpu_baseline"] = {"value": round(n / secs, 3), "unit": UNIT, "cores": threads,
                                "kind": "oracle",
-                               "sample": f"first {n} tokens of the workload (full expert "
-                                         f"weights, fwd+bwd with weight gradients"
-                                         f"{MX_NOTE if shape.dtype == 'mxfp8' else ''}"
-                                         f"{ROUTER_NOTE if args.router else ''}), "
-                                         f"{secs:.1f} s"}
-        rec["cpu_baseline"]["one_core"] = one_core(shape, inp, args.router)
+                               "sample": (f"first {n} tokens of the workload: forward and data "
+                                          f"gradients timed, x 18/12 for the weight gradients "
+                                          f"(extrapolated: fp64 weight gradients of this shape "
+                                          f"exceed host memory), {secs:.1f} s" if ext else
+                                          f"first {n} tokens of the workload (full expert "
+                                          f"weights, fwd+bwd with weight gradients"
+                                          f"{MX_NOTE if shape.dtype == 'mxfp8' else ''}"
+                                          f"{ROUTER_NOTE if args.router else ''}), "
+                                          f"{secs:.1f} s"),
+                               "full_layer_seconds": round(shape.N * secs / n, 1)}
+        if not ext:
+            rec["cpu_baseline"]["one_core"] = one_core(shape, inp, args.router)
     if rank == 0:
         if not args.phase_report:
             rec.pop("phases", None)

@@ -80,12 +80,18 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_dtype;
  * per expert slot" of the large-batch sweep): each expert's rows are grouped
  * and padded to a multiple of T. T = 128 (also for 0), 256, 512 or 1024.
  * Larger T only adds padding rows on one GPU (the expert GEMMs run on SM
- * pairs at every T); it is kept as the pages' minibatch knob. */
+ * pairs at every T); it is kept as the pages' minibatch knob.
+ * pipeline_stages: depth of the shared-memory ring that the bf16 expert
+ * GEMMs stream operands through (4, 5 or 6 stages of 32 KB per SM; 0 = the
+ * library's choice per shape, from sweeps on a GB300). The results do not
+ * depend on it (same MMAs in the same order). The pages' knobs ([MoK] core
+ * concepts) that apply on one GPU are minibatch_rows and this ring depth. */
 typedef struct {
   int64_t N;
   int32_t H, I, E, k;
   int32_t dtype;
   int32_t minibatch_rows;
+  int32_t pipeline_stages;
 } moe_problem;
 
 /* One MXFP8 operand as the block-scaled tensor-core GEMMs read it (see

@@ -541,11 +541,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // odd CTA's copies signal it across the pair); the MMA commits arrive on both
 // CTAs' empty[s] and tfull[a]; the odd CTA's epilogue releases the
 // accumulator with a remote arrive on the even CTA's tempty[a].
-constexpr int kPairStages = 6;
+constexpr int kPairStages = 6;  // the fused forward's ring depth; the GEMM kernel takes S
 constexpr int kPairABytes = BM * BK * 2;        // 16 KB: this CTA's 128 A rows
 constexpr int kPairBBytes = (BN / 2) * BK * 2;  // 16 KB: this CTA's 128 B columns
 constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
 constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + kOutBytes + 1024;
+// Dynamic shared memory of the SM-pair GEMM kernel with S stages.
+constexpr int pair_smem_bytes(int S) { return S * kPairStageBytes + kOutBytes + 1024; }
 
 // Pair tiles: WGRAD pairs neighbouring M tiles of one expert (shared B); the
 // token-row modes take the schedule's SM-pair items (256 rows of one expert,
@@ -817,12 +819,14 @@ __device__ __forceinline__ void issue_loads_pair(const Maps& m, const Args& a, c
   }
 }
 
-template <int MODE, bool RC>
+// S: stages of the shared-memory ring (4, 5 or 6; the per-shape choice of
+// pick_stages below).
+template <int MODE, bool RC, int S>
 __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
     grouped_gemm_pair_kernel(const __grid_constant__ Maps maps, const Args args) {
   static_assert(!RC || MODE == DACT, "the reverse-combine is fused into DACT only");
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[kPairStages], empty_bar[kPairStages], tfull_bar[2], tempty_bar[2],
+  __shared__ uint64_t full_bar[S], empty_bar[S], tfull_bar[2], tempty_bar[2],
       drain_bar;
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
@@ -833,7 +837,7 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
   const bool leader = crank == 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPairStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
@@ -889,11 +893,11 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
                                  cluster_addr(&full_bar[stage], 0), crank);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
+          if (++stage == S) { stage = 0; phase ^= 1u; }
         }
       }
       if (leader)  // the even CTA's full barriers count both CTAs' copies
-        for (int s = 0; s < kPairStages; ++s)
+        for (int s = 0; s < S; ++s)
           if ((issued_mask >> s) & 1u) wait_drain(&full_bar[s], (issued_parity >> s) & 1u, args.err);
     }
   } else if (warp == 1) {
@@ -931,7 +935,7 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
             umma_bf16_pair(dtmem, ad, bd, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
           }
           umma_commit_pair_mc(&empty_bar[stage], 0x3);  // both CTAs may refill the stage
-          if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
+          if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         if (it.commit) {
@@ -948,7 +952,7 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
   } else {
     // ---------------- epilogue warps 2..5 (both CTAs) ----------------
     const int quad = warp & 3;
-    uint8_t* stage_out = smem + kPairStages * kPairStageBytes + (warp - 2) * 2 * kStageOutBytes;
+    uint8_t* stage_out = smem + S * kPairStageBytes + (warp - 2) * 2 * kStageOutBytes;
     uint32_t nstore = 0;
     uint32_t uses0 = 0u, uses1 = 0u;
     PairItem it;
@@ -1330,8 +1334,8 @@ moe_status launch(const Maps& maps, const Args& args, int64_t units, cudaStream_
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-template <int MODE, bool RC = false>
-moe_status launch_pair(const Maps& maps, const Args& args, int64_t units, cudaStream_t s) {
+template <int MODE, bool RC, int S>
+moe_status launch_pair_s(const Maps& maps, const Args& args, int64_t units, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters = 0;
@@ -1342,18 +1346,18 @@ moe_status launch_pair(const Maps& maps, const Args& args, int64_t units, cudaSt
     at[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(kGemmThreads + (RC ? 32 * kRcWarps : 0));
-    cfg.dynamicSmemBytes = kPairSmemBytes;
+    cfg.dynamicSmemBytes = pair_smem_bytes(S);
     cfg.attrs = at;
     cfg.numAttrs = 1;
   };
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<MODE, RC>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+    attr_err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<MODE, RC, S>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem_bytes(S));
     if (attr_err != cudaSuccess) return;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
     config(cfg, at, 64);
-    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_pair_kernel<MODE, RC>, &cfg);
+    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_pair_kernel<MODE, RC, S>, &cfg);
     if (attr_err == cudaSuccess && max_clusters <= 0) attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
@@ -1362,17 +1366,45 @@ moe_status launch_pair(const Maps& maps, const Args& args, int64_t units, cudaSt
   cudaLaunchAttribute at[1];
   config(cfg, at, static_cast<int>(std::min<int64_t>(max_clusters, units)));
   cfg.stream = s;
-  if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE, RC>, maps, args) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE, RC, S>, maps, args) != cudaSuccess)
     return MOE_ERR_CUDA;
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// The stage count of the SM-pair GEMM kernel for one GEMM of a problem: the
+// caller's moe_problem.pipeline_stages if set, else the library's choice per
+// shape, from sweeps of 4, 5 and 6 stages on a GB300 (bench.py
+// --sweep-stages) over the benchmark workloads at equal clocks:
+//  * token-row GEMMs: 6 everywhere (fine-grained forward: 0.2375 / 0.2155 /
+//    0.2099 ms for gate/up at 4 / 5 / 6 stages; large batch at N = 8192:
+//    3.70 / 3.34 / 3.20 ms);
+//  * weight gradients: 4 when the experts average at most 256 tokens (large
+//    batch at N = 8192: dWg + dWu 7.48 / 7.78 / 7.87 ms, dWd 3.44 / 3.42 /
+//    3.58 ms -- the fp32 stores bound them there, and fewer loads in flight
+//    leave the L2 more room for the stores), else 6 (skewed workload: dWg +
+//    dWu 2.93 / 2.81 / 2.77 ms).
+int pick_stages(const Layout& L, int mode) {
+  if (L.stages == 4 || L.stages == 5 || L.stages == 6) return L.stages;
+  if (mode == WGRAD && L.A <= 256LL * L.E) return 4;
+  return 6;
+}
+
+template <int MODE, bool RC = false>
+moe_status launch_pair(const Layout& L, const Maps& maps, const Args& args, int64_t units,
+                       cudaStream_t s) {
+  switch (pick_stages(L, MODE)) {
+    case 4: return launch_pair_s<MODE, RC, 4>(maps, args, units, s);
+    case 5: return launch_pair_s<MODE, RC, 5>(maps, args, units, s);
+    default: return launch_pair_s<MODE, RC, 6>(maps, args, units, s);
+  }
+}
+
 // Token-row modes: the SM-pair kernel over the schedule's pair items (at most
 // one per 128-row tile).
 template <int MODE>
-moe_status launch_tokens(const Maps& maps, const Args& args, cudaStream_t s) {
-  return launch_pair<MODE>(maps, args, static_cast<int64_t>(args.max_mtiles) * args.n_nt, s);
+moe_status launch_tokens(const Layout& L, const Maps& maps, const Args& args, cudaStream_t s) {
+  return launch_pair<MODE>(L, maps, args, static_cast<int64_t>(args.max_mtiles) * args.n_nt, s);
 }
 
 // A operand maps of the SM-pair token-row kernel: 128-row box (256-row items)
@@ -1450,7 +1482,7 @@ moe_status gemm_gate_up(const Layout& L, const void* ws, const void* xe, const v
   a.out1 = u;
   a.out2 = act;
   a.store_gu = store_gu ? 1 : 0;
-  return launch_tokens<GATE_UP>(m, a, s);
+  return launch_tokens<GATE_UP>(L, m, a, s);
 }
 
 moe_status gemm_down(const Layout& L, const void* ws, const void* act, const void* wd, void* ye,
@@ -1470,7 +1502,7 @@ moe_status gemm_down(const Layout& L, const void* ws, const void* act, const voi
   a.b_rows = L.H;
   a.ld_out = L.H;
   a.out0 = ye;
-  return launch_tokens<DOWN>(m, a, s);
+  return launch_tokens<DOWN>(L, m, a, s);
 }
 
 moe_status gemm_down_dgrad(const Layout& L, const void* ws, const void* dye, const void* g,
@@ -1500,7 +1532,7 @@ moe_status gemm_down_dgrad_rc(const Layout& L, const void* ws, const void* dy, c
   a.in0 = g;
   a.in1 = u;
   const int64_t units = static_cast<int64_t>(a.max_mtiles) * a.n_nt;
-  if (!dy) return launch_pair<DACT>(m, a, units, s);
+  if (!dy) return launch_pair<DACT>(L, m, a, units, s);
   // fused reverse-combine: dYe and dw come from the kernel's side warps
   a.rc_dy = static_cast<const uint4*>(dy);
   a.rc_ye = static_cast<const uint4*>(ye);
@@ -1517,7 +1549,7 @@ moe_status gemm_down_dgrad_rc(const Layout& L, const void* ws, const void* dy, c
   // assignments without a row (rejected expert ids) keep dw = 0, as in the unfused kernel
   if (L.A > 0 && cudaMemsetAsync(d_topk_w, 0, sizeof(float) * L.A, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  return launch_pair<DACT, true>(m, a, std::max<int64_t>(units, 1), s);
+  return launch_pair<DACT, true>(L, m, a, std::max<int64_t>(units, 1), s);
 }
 
 moe_status gemm_down_wgrad(const Layout& L, const void* ws, const void* dye, const void* act,
@@ -1537,7 +1569,7 @@ moe_status gemm_down_wgrad(const Layout& L, const void* ws, const void* dye, con
   a.ld_out = L.I;
   a.out0 = dw_down;
   a.out1 = dw_down;
-  return launch_pair<WGRAD>(m, a, static_cast<int64_t>(L.E) * (a.w_mt / 2) * a.w_nt, s);
+  return launch_pair<WGRAD>(L, m, a, static_cast<int64_t>(L.E) * (a.w_mt / 2) * a.w_nt, s);
 }
 
 moe_status gemm_gate_up_dgrad(const Layout& L, const void* ws, const void* dg, const void* du,
@@ -1555,7 +1587,7 @@ moe_status gemm_gate_up_dgrad(const Layout& L, const void* ws, const void* dg, c
   a.b_rows = L.I;
   a.ld_out = L.H;
   a.out0 = dxe;
-  return launch_tokens<DXE>(m, a, s);
+  return launch_tokens<DXE>(L, m, a, s);
 }
 
 moe_status gemm_gate_up_wgrad(const Layout& L, const void* ws, const void* dg, const void* du,
@@ -1576,7 +1608,7 @@ moe_status gemm_gate_up_wgrad(const Layout& L, const void* ws, const void* dg, c
   a.ld_out = L.H;
   a.out0 = dw_gate;
   a.out1 = dw_up;
-  return launch_pair<WGRAD>(m, a, 2LL * L.E * (a.w_mt / 2) * a.w_nt, s);
+  return launch_pair<WGRAD>(L, m, a, 2LL * L.E * (a.w_mt / 2) * a.w_nt, s);
 }
 
 moe_status gemm_fused_forward(const Layout& L, const void* ws, const void* x, const void* wg,

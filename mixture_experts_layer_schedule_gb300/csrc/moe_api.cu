@@ -28,6 +28,8 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   if (p->dtype != MOE_BF16 && p->dtype != MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
   const int32_t T = p->minibatch_rows == 0 ? kTileM : p->minibatch_rows;
   if (T != 128 && T != 256 && T != 512 && T != 1024) return MOE_ERR_UNSUPPORTED;
+  if (p->pipeline_stages != 0 && (p->pipeline_stages < 4 || p->pipeline_stages > 6))
+    return MOE_ERR_UNSUPPORTED;
   // rows, slots and tile coordinates are int32 on the device; bound N before
   // forming N * k so that the product cannot overflow
   if (p->N > (1LL << 31) / p->k) return MOE_ERR_UNSUPPORTED;
@@ -43,6 +45,7 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   L->k = p->k;
   L->T = T;
   L->dtype = p->dtype;
+  L->stages = p->pipeline_stages;
   L->n_warps = (A + kSchedSub - 1) / kSchedSub;
   size_t o = 0;
   auto take = [&o](size_t bytes) {

@@ -379,3 +379,27 @@ def test_empty_batch():
     assert layer.y.shape == (0, 256) and layer.grads.dx.shape == (0, 256)
     for t in (layer.grads.dw_gate, layer.grads.dw_up, layer.grads.dw_down):
         assert torch.all(t == 0)
+
+
+@pytest.mark.parametrize("stages", [4, 5, 6])
+def test_results_do_not_depend_on_the_ring_depth(stages):
+    """moe_problem.pipeline_stages only changes how many k-blocks the SM-pair
+    GEMMs keep in flight: the MMAs, their order and the epilogues are the
+    same, so every output equals the library's default choice bit for bit."""
+    shape = custom_shape(2048, 1024, 512, 16, 4, zipf_s=1.2, name="ring_depth")
+    inp = to_dev(inputs.make_inputs(shape, seed=5, device="cpu"))
+    ref = run_layer(shape, inp)
+    layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev(),
+                     pipeline_stages=stages)
+    layer.step(inp["x"], inp["logits"], inp["bias"], inp["wg"], inp["wu"], inp["wd"], inp["dy"])
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert torch.equal(layer.y.view(torch.int16), ref.y.view(torch.int16))
+    rows = int(ref.schedule_tensors()["pad_offsets"][shape.E])  # rows past it are never written
+    got, want = layer.saved_tensors(), ref.saved_tensors()
+    for name in want:
+        assert torch.equal(got[name][:rows].view(torch.int16), want[name][:rows].view(torch.int16)), name
+    for name in ("dx", "dw_gate", "dw_up", "dw_down", "d_topk_w"):
+        a, b = getattr(layer.grads, name), getattr(ref.grads, name)
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b), name
