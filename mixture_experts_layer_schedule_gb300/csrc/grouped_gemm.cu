@@ -212,13 +212,14 @@ __device__ __forceinline__ float sigmoid(float g) { return __fdividef(1.0f, 1.0f
 
 // One 32-row x 64-column bf16 block of a warp's output: 64 fp32 values per
 // thread (its row) -> bf16 -> shared staging buffer (128-byte swizzle: one
-// warp store covers all banks) -> one TMA store. Two staging buffers per warp
-// let a store overlap the next block.
+// warp store covers all banks) -> one TMA store. NB staging buffers per warp
+// let NB - 1 stores be in flight while the next block is staged.
+template <int NB>
 __device__ __forceinline__ void store_block_bf16(const CUtensorMap* om, const float (&v)[64],
                                                  int32_t x, int32_t y, int lane,
                                                  uint8_t* stage_out, uint32_t& nstore) {
-  uint8_t* buf = stage_out + (nstore & 1u) * kStageOutBytes;
-  if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
+  uint8_t* buf = stage_out + (nstore % NB) * kStageOutBytes;
+  if (lane == 0) bulk_wait_read<NB - 1>();  // the store that last used this buffer has read it
   __syncwarp();
   const uint32_t row = smem_u32(buf) + lane * 128;
 #pragma unroll
@@ -264,7 +265,7 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 // [BN/2, BN) of the same rows, both in TMEM columns [0, BN/2).
 // GATE_UP D column order: single CTA, 128 G then 128 U columns of the N tile;
 // SM pair, per half of the N tile (one CTA's B rows) 64 G then 64 U columns.
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIR, int NB = 2>
 __device__ __forceinline__ void epilogue(const Maps& m, const Args& a, const TileInfo& ti,
                                          uint32_t tmem_acc, int quad, int lane,
                                          uint8_t* stage_out, uint32_t& nstore) {
@@ -281,18 +282,18 @@ __device__ __forceinline__ void epilogue(const Maps& m, const Args& a, const Til
       tmem_ld64(taddr + tg, g);
       tmem_ld64(taddr + tu, u);
       if (a.store_gu) {
-        store_block_bf16(&m.o0, g, xo, y, lane, stage_out, nstore);
-        store_block_bf16(&m.o1, u, xo, y, lane, stage_out, nstore);
+        store_block_bf16<NB>(&m.o0, g, xo, y, lane, stage_out, nstore);
+        store_block_bf16<NB>(&m.o1, u, xo, y, lane, stage_out, nstore);
       }
 #pragma unroll
       for (int i = 0; i < 64; ++i) g[i] = silu(g[i]) * u[i];
-      store_block_bf16(&m.o2, g, xo, y, lane, stage_out, nstore);
+      store_block_bf16<NB>(&m.o2, g, xo, y, lane, stage_out, nstore);
     }
   } else if constexpr (MODE == DOWN || MODE == DXE) {
     for (int c = 0; c < ncol; c += 64) {
       float d[64];
       tmem_ld64(taddr + c, d);
-      store_block_bf16(&m.o0, d, ti.nt * BN + dc0 + c, y, lane, stage_out, nstore);
+      store_block_bf16<NB>(&m.o0, d, ti.nt * BN + dc0 + c, y, lane, stage_out, nstore);
     }
   } else {  // DACT: direct 16-byte stores, G and U read alongside in 32-column steps
     const int64_t row = static_cast<int64_t>(y) + lane;
@@ -343,6 +344,7 @@ __device__ __forceinline__ void epilogue(const Maps& m, const Args& a, const Til
 // blocks: TMEM -> registers -> shared staging buffer (the 128-byte swizzle
 // spreads one warp store over all banks) -> one TMA store at (x0 + c, y).
 // Two staging buffers per warp let the store of block i overlap block i+1.
+template <int NB>
 __device__ __forceinline__ void epilogue_f32(const CUtensorMap* om, const TileInfo& ti, int32_t x0,
                                              int32_t y, int ncols, uint32_t tmem_acc, int quad,
                                              int lane, uint8_t* stage_out, uint32_t& nstore) {
@@ -356,8 +358,8 @@ __device__ __forceinline__ void epilogue_f32(const CUtensorMap* om, const TileIn
 #pragma unroll
       for (int q = 0; q < 32; ++q) d[q] = 0u;
     }
-    uint8_t* buf = stage_out + (nstore & 1u) * kStageOutBytes;
-    if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
+    uint8_t* buf = stage_out + (nstore % NB) * kStageOutBytes;
+    if (lane == 0) bulk_wait_read<NB - 1>();  // the store that last used this buffer has read it
     __syncwarp();
     const uint32_t row = smem_u32(buf) + lane * 128;
 #pragma unroll
@@ -377,10 +379,11 @@ __device__ __forceinline__ void epilogue_f32(const CUtensorMap* om, const TileIn
   }
 }
 
+template <int NB>
 __device__ __forceinline__ void epilogue_wgrad(const Maps& m, const Args& a, const TileInfo& ti,
                                                uint32_t tmem_acc, int quad, int lane,
                                                uint8_t* stage_out, uint32_t& nstore) {
-  epilogue_f32(ti.prob ? &m.o1 : &m.o0, ti, ti.nt * BN, ti.e * (a.w_mt * BM) + ti.mt * BM + quad * 32,
+  epilogue_f32<NB>(ti.prob ? &m.o1 : &m.o0, ti, ti.nt * BN, ti.e * (a.w_mt * BM) + ti.mt * BM + quad * 32,
                BN, tmem_acc, quad, lane, stage_out, nstore);
 }
 
@@ -389,7 +392,7 @@ __device__ __forceinline__ void epilogue_wgrad(const Maps& m, const Args& a, con
 __device__ __forceinline__ void epilogue_router(const Maps& m, const Args& a, const TileInfo& ti,
                                                 uint32_t tmem_acc, int quad, int lane,
                                                 uint8_t* stage_out, uint32_t& nstore) {
-  epilogue_f32(&m.o0, ti, 0, ti.row0 + quad * 32, (a.ld_out + 31) / 32 * 32, tmem_acc, quad, lane,
+  epilogue_f32<2>(&m.o0, ti, 0, ti.row0 + quad * 32, (a.ld_out + 31) / 32 * 32, tmem_acc, quad, lane,
                stage_out, nstore);
 }
 
@@ -547,7 +550,16 @@ constexpr int kPairBBytes = (BN / 2) * BK * 2;  // 16 KB: this CTA's 128 B colum
 constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
 constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + kOutBytes + 1024;
 // Dynamic shared memory of the SM-pair GEMM kernel with S stages.
-constexpr int pair_smem_bytes(int S) { return S * kPairStageBytes + kOutBytes + 1024; }
+// Staging buffers per epilogue warp of the SM-pair GEMM kernel with S stages:
+// the shared memory the ring leaves free (2, 4 and 6 at 6, 5 and 4 stages;
+// 225 KB in every case) goes to more TMA stores in flight.
+constexpr int pair_out_bufs(int S) { return S >= 6 ? 2 : (S == 5 ? 4 : 6); }
+constexpr int pair_smem_bytes(int S) {
+  return S * kPairStageBytes + 4 * pair_out_bufs(S) * kStageOutBytes + 1024;
+}
+static_assert(pair_smem_bytes(4) <= 227 * 1024 && pair_smem_bytes(5) <= 227 * 1024 &&
+                  pair_smem_bytes(6) <= 227 * 1024,
+              "SM-pair ring plus staging within the shared memory of one CTA");
 
 // Pair tiles: WGRAD pairs neighbouring M tiles of one expert (shared B); the
 // token-row modes take the schedule's SM-pair items (256 rows of one expert,
@@ -952,7 +964,8 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
   } else {
     // ---------------- epilogue warps 2..5 (both CTAs) ----------------
     const int quad = warp & 3;
-    uint8_t* stage_out = smem + S * kPairStageBytes + (warp - 2) * 2 * kStageOutBytes;
+    constexpr int NB = pair_out_bufs(S);
+    uint8_t* stage_out = smem + S * kPairStageBytes + (warp - 2) * NB * kStageOutBytes;
     uint32_t nstore = 0;
     uint32_t uses0 = 0u, uses1 = 0u;
     PairItem it;
@@ -965,9 +978,10 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
       if (ti.skip) {
         if (lane == 0) set_dev_error(args.err, MOE_DEVERR_BAD_EXPERT);
       } else if constexpr (MODE == WGRAD) {
-        epilogue_wgrad(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
+        epilogue_wgrad<NB>(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
       } else {
-        epilogue<MODE, true>(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
+        epilogue<MODE, true, NB>(maps, args, ti, tmem_base + acc * BN, quad, lane, stage_out,
+                                 nstore);
       }
       tc_fence_before();
       __syncwarp();
@@ -1375,19 +1389,22 @@ moe_status launch_pair_s(const Maps& maps, const Args& args, int64_t units, cuda
 // The stage count of the SM-pair GEMM kernel for one GEMM of a problem: the
 // caller's moe_problem.pipeline_stages if set, else the library's choice per
 // shape, from sweeps of 4, 5 and 6 stages on a GB300 (bench.py
-// --sweep-stages) over the benchmark workloads at equal clocks:
-//  * token-row GEMMs: 6 everywhere (fine-grained forward: 0.2375 / 0.2155 /
-//    0.2099 ms for gate/up at 4 / 5 / 6 stages; large batch at N = 8192:
-//    3.70 / 3.34 / 3.20 ms);
-//  * weight gradients: 4 when the experts average at most 256 tokens (large
-//    batch at N = 8192: dWg + dWu 7.48 / 7.78 / 7.87 ms, dWd 3.44 / 3.42 /
-//    3.58 ms -- the fp32 stores bound them there, and fewer loads in flight
-//    leave the L2 more room for the stores), else 6 (skewed workload: dWg +
-//    dWu 2.93 / 2.81 / 2.77 ms).
+// --sweep-stages, all runs at 2070 MHz; fewer stages leave room for more
+// epilogue staging buffers, pair_out_bufs):
+//  * weight gradients: 4 stages when the experts average at most 256 tokens
+//    (large batch at N = 8192: dWg + dWu 7.48 ms at 4 stages against 7.87 at
+//    6 -- the fp32 stores bound them there), else 6 (skewed workload: 2.84
+//    at 6 against 2.92 at 5 and 2.98 at 4; uniform routing 2.66 / 2.79 /
+//    2.83);
+//  * token-row GEMMs: 5 stages when the experts average at least 1024 tokens
+//    (skewed and uniform workloads: gate/up 2.27 / 2.13 ms at 5 against
+//    2.30 / 2.18 at 6, gate/up dgrad 2.26 / 2.15 against 2.29 / 2.17), else 6
+//    (fine-grained forward: gate/up 0.211 at 6 against 0.216 at 5; large
+//    batch at N = 8192: 3.22 against 3.34).
 int pick_stages(const Layout& L, int mode) {
   if (L.stages == 4 || L.stages == 5 || L.stages == 6) return L.stages;
-  if (mode == WGRAD && L.A <= 256LL * L.E) return 4;
-  return 6;
+  if (mode == WGRAD) return L.A <= 256LL * L.E ? 4 : 6;
+  return L.A >= 1024LL * L.E ? 5 : 6;
 }
 
 template <int MODE, bool RC = false>
