@@ -13,7 +13,9 @@ At these sizes the oracle cannot run the whole layer, so:
     sampled rows, each computed by the oracle over every token routed to that
     expert;
   * the tolerance is the bf16 bound, max|err| <= 2e-2 * max|ref| over the
-    sampled elements of each tensor; ids and tables are exact.
+    sampled elements of each tensor; ids and tables are exact;
+  * the fused dispatch + expert FFN launch (moe_forward_inference) reproduces
+    the checked y bit for bit.
 """
 import numpy as np
 import pytest
@@ -61,6 +63,14 @@ def test_full_size_sampled_parity(shape):
     rows = int(ref["pad_offsets"][shape.E])
     np.testing.assert_array_equal(got["src_of_row"][:rows], ref["src_of_row"])
     np.testing.assert_array_equal(got["tiles"].reshape(-1, 3)[:ref["n_tiles"]], ref["tiles"])
+
+    # the fused dispatch + expert FFN launch (the context-free forward's path)
+    # gives the training forward's y bit for bit at this size as well
+    y_train = layer.y.clone()
+    layer.forward_inference(inp["x"], inp["wg"], inp["wu"], inp["wd"])
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert torch.equal(layer.y.view(torch.int16), y_train.view(torch.int16))
 
     # sampled tokens: y (and dx, d routing weights when the pass has a backward)
     x, wgt, wut, wdt = (_host(inp[k]) for k in ("x", "wg", "wu", "wd"))
