@@ -53,9 +53,12 @@ def parse():
                          "GPU inside the step (default: the step starts from router logits)")
     ap.add_argument("--stages", type=int, default=0, choices=[0, 4, 5, 6],
                     help="ring stages of the bf16 SM-pair GEMMs (0: the library's per-shape choice)")
+    ap.add_argument("--tile-n", type=int, default=0, choices=[0, 256, 512],
+                    help="pair-tile width of the bf16 token-row GEMMs (0: the library's choice)")
     ap.add_argument("--sweep-stages", action="store_true",
-                    help="time the workload with 4, 5 and 6 GEMM ring stages and print every "
-                         "GEMM phase's time at each and its best stage count")
+                    help="time the workload with 4, 5 and 6 GEMM ring stages (256-wide pair "
+                         "tiles) and with 512-wide token-row tiles, and print every GEMM "
+                         "phase's time at each and its best setting")
     ap.add_argument("--sweep-T", action="store_true",
                     help="the minibatch knob sweep: run the workload at minibatch_rows T = 128, "
                          "256, 512, 1024 and print one line with every T's result and the best")
@@ -422,7 +425,7 @@ def workload(name):
                              zipf_s=z, minibatch_rows=T, dtype=dtype)
 
 
-def run_ours(args, ws_, rank, local, shape=None, stages=None):
+def run_ours(args, ws_, rank, local, shape=None, stages=None, tile_n=None):
     import torch
     from mixture_experts_layer_schedule_gb300 import MoELayer, _lib, inputs
 
@@ -433,9 +436,10 @@ def run_ours(args, ws_, rank, local, shape=None, stages=None):
     inp = inputs.make_inputs(shape, seed=rank, device=dev, weight_seed=0)
     mx = shape.dtype == "mxfp8"
     stages = args.stages if stages is None else stages
+    tile_n = args.tile_n if tile_n is None else tile_n
     layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev,
                      minibatch_rows=shape.minibatch_rows, dtype=shape.dtype,
-                     pipeline_stages=stages)
+                     pipeline_stages=stages, tile_n=tile_n)
     p, wsb = layer.p, layer.ws
     wbwd = mxw = None
     if mx:  # weights pre-quantised once, outside the timed steps
@@ -558,7 +562,7 @@ def run_ours(args, ws_, rank, local, shape=None, stages=None):
         pin.pop("dy", None)
     layers = [layer, MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev,
                               allocate_grads=backward, minibatch_rows=shape.minibatch_rows,
-                              dtype=shape.dtype, pipeline_stages=stages)]
+                              dtype=shape.dtype, pipeline_stages=stages, tile_n=tile_n)]
     dev_in = [{k: torch.empty_like(v, device=dev) for k, v in pin.items()} for _ in range(2)]
     outs = [{"y": torch.empty((shape.N, shape.H), dtype=torch.bfloat16).pin_memory(),
              "dx": torch.empty((shape.N, shape.H), dtype=torch.bfloat16).pin_memory()}
@@ -684,6 +688,7 @@ def run_ours(args, ws_, rank, local, shape=None, stages=None):
                    "E": shape.E, "k": shape.k, "zipf_bias": shape.zipf_s,
                    "minibatch_rows": shape.minibatch_rows,
                    "pipeline_stages": stages or "library choice",
+                   "tile_n": tile_n or "library choice",
                    "passes": "fwd+bwd" if backward else ("fwd (inference)" if inference
                                                            else "fwd"),
                    "l2": "inputs larger than L2 (expert weights alone "
@@ -844,9 +849,10 @@ def main():
         import torch
         base = workload(args.config)
         res = {}
-        for S in (4, 5, 6):
+        for S in (4, 5, 6, "wide"):
             args.phase_report = True
-            r, _, _ = run_ours(args, ws_, rank, local, base, stages=S)
+            r, _, _ = run_ours(args, ws_, rank, local, base, stages=0 if S == "wide" else S,
+                               tile_n=512 if S == "wide" else 256)
             res[S] = {"value": r["value"], "ms_per_step": r["ms_per_step"],
                       "phases": {k: v["ms"] for k, v in r["phases"].items()},
                       "clocks": r["clocks"]}

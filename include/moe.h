@@ -84,14 +84,21 @@ typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_dtype;
  * pipeline_stages: depth of the shared-memory ring that the bf16 expert
  * GEMMs stream operands through (4, 5 or 6 stages of 32 KB per SM; 0 = the
  * library's choice per shape, from sweeps on a GB300). The results do not
- * depend on it (same MMAs in the same order). The pages' knobs ([MoK] core
- * concepts) that apply on one GPU are minibatch_rows and this ring depth. */
+ * depend on it (same MMAs in the same order).
+ * tile_n: width in N of the pair tiles of the token-row expert GEMMs (gate/up,
+ * down and their data gradients): 256, or 512 (two N tiles share each staged
+ * A k-block, one TMEM accumulator, a 4-stage ring of 48 KB; needs an even
+ * number of N tiles, else 256 is used); 0 = the library's choice per shape.
+ * The results do not depend on it either.
+ * The pages' knobs ([MoK] core concepts) that apply on one GPU are
+ * minibatch_rows, the ring depth and the tile width. */
 typedef struct {
   int64_t N;
   int32_t H, I, E, k;
   int32_t dtype;
   int32_t minibatch_rows;
   int32_t pipeline_stages;
+  int32_t tile_n;
 } moe_problem;
 
 /* One MXFP8 operand as the block-scaled tensor-core GEMMs read it (see

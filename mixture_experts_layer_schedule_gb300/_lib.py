@@ -25,7 +25,8 @@ c_i64, c_i32, c_vp, c_sz = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctyp
 
 class Problem(ctypes.Structure):
     _fields_ = [("N", c_i64), ("H", c_i32), ("I", c_i32), ("E", c_i32), ("k", c_i32),
-                ("dtype", c_i32), ("minibatch_rows", c_i32), ("pipeline_stages", c_i32)]
+                ("dtype", c_i32), ("minibatch_rows", c_i32), ("pipeline_stages", c_i32),
+                ("tile_n", c_i32)]
 
 
 class MXFP8Operand(ctypes.Structure):
@@ -161,9 +162,10 @@ def _stream(stream):
     return stream
 
 
-def problem(N, H, I, E, k, dtype=MOE_BF16, minibatch_rows=128, pipeline_stages=0) -> Problem:
+def problem(N, H, I, E, k, dtype=MOE_BF16, minibatch_rows=128, pipeline_stages=0,
+            tile_n=0) -> Problem:
     return Problem(int(N), int(H), int(I), int(E), int(k), int(dtype), int(minibatch_rows),
-                   int(pipeline_stages))
+                   int(pipeline_stages), int(tile_n))
 
 
 def mxfp8_weights(operands: dict) -> MXFP8Weights:

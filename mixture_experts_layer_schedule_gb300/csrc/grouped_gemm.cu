@@ -793,6 +793,43 @@ struct PairPlan {
   }
 };
 
+// Token-row modes: this CTA's A rows of k-block kb (both K phases of DXE).
+template <int MODE>
+__device__ __forceinline__ void load_a_pair(const Maps& m, const Args& a, const TileInfo& ti,
+                                            int kb, uint8_t* sA, uint32_t bar) {
+  if constexpr (MODE == DXE) {
+    const bool second = kb >= a.kb1;
+    const CUtensorMap* ma = second ? (ti.fold ? &m.a1h : &m.a1) : (ti.fold ? &m.a0h : &m.a0);
+    tma_load_2d_pair(sA, ma, bar, (second ? kb - a.kb1 : kb) * BK, ti.row0);
+  } else {
+    tma_load_2d_pair(sA, ti.fold ? &m.a0h : &m.a0, bar, kb * BK, ti.row0);
+  }
+}
+
+// Token-row modes: this CTA's half of the B tile of N tile nt at k-block kb.
+template <int MODE>
+__device__ __forceinline__ void load_b_pair(const Maps& m, const Args& a, const TileInfo& ti,
+                                            int nt, int kb, uint8_t* sB, uint32_t bar,
+                                            int crank) {
+  if constexpr (MODE == GATE_UP) {
+    // the N tile covers 128 gate and 128 up rows of the weights; each CTA
+    // stages 64 gate rows then the 64 up rows of the same I columns
+    const int brow = ti.e * a.b_rows + nt * (BN / 2) + crank * (BN / 4);
+    tma_load_2d_pair(sB, &m.b0, bar, kb * BK, brow);
+    tma_load_2d_pair(sB + (BN / 4) * BK * 2, &m.b1, bar, kb * BK, brow);
+  } else if constexpr (MODE == DOWN) {
+    tma_load_2d_pair(sB, &m.b0, bar, kb * BK, ti.e * a.b_rows + nt * BN + crank * (BN / 2));
+  } else {  // DACT, DXE: B is MN-major, two 64-column chunks per CTA
+    const bool second = (MODE == DXE) && kb >= a.kb1;
+    const int kk = second ? kb - a.kb1 : kb;
+    const CUtensorMap* mb = second ? &m.b1 : &m.b0;
+#pragma unroll
+    for (int c = 0; c < BN / 128; ++c)
+      tma_load_2d_pair(sB + c * (64 * BK * 2), mb, bar, nt * BN + crank * (BN / 2) + c * 64,
+                       ti.e * a.b_rows + kk * BK);
+  }
+}
+
 template <int MODE>
 __device__ __forceinline__ void issue_loads_pair(const Maps& m, const Args& a, const TileInfo& ti,
                                                  int kb, uint8_t* sA, uint8_t* sB, uint32_t bar,
@@ -808,26 +845,9 @@ __device__ __forceinline__ void issue_loads_pair(const Maps& m, const Args& a, c
     for (int c = 0; c < BN / 128; ++c)
       tma_load_2d_pair(sB + c * (64 * BK * 2), mb, bar, ti.nt * BN + crank * (BN / 2) + c * 64,
                        krow);
-  } else if constexpr (MODE == GATE_UP) {
-    // the N tile covers 128 gate and 128 up rows of the weights; each CTA
-    // stages 64 gate rows then the 64 up rows of the same I columns
-    tma_load_2d_pair(sA, ti.fold ? &m.a0h : &m.a0, bar, kb * BK, ti.row0);
-    const int brow = ti.e * a.b_rows + ti.nt * (BN / 2) + crank * (BN / 4);
-    tma_load_2d_pair(sB, &m.b0, bar, kb * BK, brow);
-    tma_load_2d_pair(sB + (BN / 4) * BK * 2, &m.b1, bar, kb * BK, brow);
-  } else if constexpr (MODE == DOWN) {
-    tma_load_2d_pair(sA, ti.fold ? &m.a0h : &m.a0, bar, kb * BK, ti.row0);
-    tma_load_2d_pair(sB, &m.b0, bar, kb * BK, ti.e * a.b_rows + ti.nt * BN + crank * (BN / 2));
-  } else {  // DACT, DXE: B is MN-major, two 64-column chunks per CTA
-    const bool second = (MODE == DXE) && kb >= a.kb1;
-    const int kk = second ? kb - a.kb1 : kb;
-    const CUtensorMap* ma = second ? (ti.fold ? &m.a1h : &m.a1) : (ti.fold ? &m.a0h : &m.a0);
-    tma_load_2d_pair(sA, ma, bar, kk * BK, ti.row0);
-    const CUtensorMap* mb = second ? &m.b1 : &m.b0;
-#pragma unroll
-    for (int c = 0; c < BN / 128; ++c)
-      tma_load_2d_pair(sB + c * (64 * BK * 2), mb, bar, ti.nt * BN + crank * (BN / 2) + c * 64,
-                       ti.e * a.b_rows + kk * BK);
+  } else {
+    load_a_pair<MODE>(m, a, ti, kb, sA, bar);
+    load_b_pair<MODE>(m, a, ti, ti.nt, kb, sB, bar, crank);
   }
 }
 
@@ -990,6 +1010,186 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
         else mbar_arrive_cluster(cluster_addr(&tempty_bar[acc], 0));
       }
       if (acc) ++uses1; else ++uses0;
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the even CTA's MMAs into this CTA's TMEM have retired
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+  cluster_sync();  // no CTA leaves while its peer may still signal it
+}
+
+// ---------------------------------------------------------------------------
+// Wide SM-pair tiles for the token-row modes: each unit of work is one pair
+// item and TWO neighbouring N tiles (256 x 512 per pair, 128 x 512 per CTA).
+// A k-block's A rows are staged once and feed two pair MMAs (N = 256 each)
+// into TMEM columns [0, 256) and [256, 512): per unit of MMA work each SM
+// stages 24 KB instead of 32, and the GEMMs are bound by the bytes an SM
+// moves through its L2 interface. The whole TMEM is one accumulator, so the
+// MMAs of the next unit start after the epilogue has read this one out; the
+// producer keeps the ring filled meanwhile. Each 256-column block gets the
+// same MMAs in the same order as a narrow tile, so the results are
+// bit-identical.
+constexpr int kWideStageBytes = kPairABytes + 2 * kPairBBytes;  // 48 KB
+constexpr int wide_smem_bytes(int S) { return S * kWideStageBytes + kOutBytes + 1024; }
+static_assert(wide_smem_bytes(4) <= 227 * 1024, "wide ring within one CTA's shared memory");
+
+template <int MODE>
+__device__ __forceinline__ int64_t total_wide_units(const Args& a) {
+  int n = *a.n_ptiles;
+  n = n < 0 ? 0 : (n > a.max_mtiles ? a.max_mtiles : n);
+  return static_cast<int64_t>(n) * (a.n_nt / 2);
+}
+
+// The first (lower) of the unit's two N tiles, as decode_pair_tile gives it.
+template <int MODE>
+__device__ __forceinline__ TileInfo decode_wide_unit(const Args& a, int64_t u, int crank) {
+  const int64_t pm = u / (a.n_nt / 2);
+  const int nt = static_cast<int>(u % (a.n_nt / 2)) * 2;
+  return decode_pair_tile<MODE>(a, pm * a.n_nt + nt, crank);
+}
+
+template <int MODE, int S>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    grouped_gemm_wide_kernel(const __grid_constant__ Maps maps, const Args args) {
+  static_assert(MODE == GATE_UP || MODE == DOWN || MODE == DACT || MODE == DXE,
+                "wide tiles serve the token-row modes");
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[S], empty_bar[S], tfull_bar, tempty_bar, drain_bar;
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ int abort_flag;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int crank = static_cast<int>(cluster_ctarank());
+  const bool leader = crank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&tfull_bar, 1);
+    mbar_init(&tempty_bar, 8);  // one arrive per epilogue warp of both CTAs
+    mbar_init(&drain_bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.a0);
+    tma_prefetch_desc(&maps.b0);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&tmem_base_slot, kTmemCols);  // one warp of each CTA, collectively
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_slot;
+  volatile int* abortp = &abort_flag;
+  const int64_t total = total_wide_units<MODE>(args);
+  const int64_t first = blockIdx.x / 2, stride = gridDim.x / 2;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs) ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      for (int64_t u = first; u < total && ok; u += stride) {
+        const TileInfo ti = decode_wide_unit<MODE>(args, u, crank);
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, args.err)) { ok = false; break; }
+          uint8_t* sA = smem + stage * kWideStageBytes;
+          const uint32_t bar = cluster_addr(&full_bar[stage], 0);
+          if (leader)
+            mbar_arrive_expect_tx(&full_bar[stage],
+                                  2 * ((ti.fold ? kPairABytes / 2 : kPairABytes) + 2 * kPairBBytes));
+          load_a_pair<MODE>(maps, args, ti, kb, sA, bar);
+          load_b_pair<MODE>(maps, args, ti, ti.nt, kb, sA + kPairABytes, bar, crank);
+          load_b_pair<MODE>(maps, args, ti, ti.nt + 1, kb, sA + kPairABytes + kPairBBytes, bar,
+                            crank);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (leader)  // the even CTA's full barriers count both CTAs' copies
+        for (int s = 0; s < S; ++s)
+          if ((issued_mask >> s) & 1u) wait_drain(&full_bar[s], (issued_parity >> s) & 1u, args.err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (even CTA only) ----------------
+      constexpr uint32_t idesc256 = idesc_bf16(2 * BM, BN, false, Traits<MODE>::b_mn);
+      constexpr uint32_t idesc128 = idesc_bf16(BM, BN, false, Traits<MODE>::b_mn);
+      int stage = 0;
+      uint32_t phase = 0, uses = 0;
+      bool ok = true;
+      for (int64_t u = first; u < total && ok; u += stride) {
+        const TileInfo ti = decode_wide_unit<MODE>(args, u, crank);
+        if (!mbar_wait(&tempty_bar, (uses & 1u) ^ 1u, abortp, args.err)) break;
+        tc_fence_after();
+        const uint32_t idesc = ti.fold ? idesc128 : idesc256;
+        for (int kb = 0; kb < ti.nkb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abortp, args.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * kWideStageBytes);
+          const uint32_t b_addr = a_addr + kPairABytes;
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks) {
+            const uint64_t ad = sdesc_sw128(a_addr + ks * 32, 16, 1024);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t bh = b_addr + h * kPairBBytes;
+              uint64_t bd;
+              if constexpr (Traits<MODE>::b_mn) bd = sdesc_sw128(bh + ks * 2048, 64 * BK * 2, 1024);
+              else bd = sdesc_sw128(bh + ks * 32, 16, 1024);
+              umma_bf16_pair(tmem_base + h * BN, ad, bd, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
+          umma_commit_pair_mc(&empty_bar[stage], 0x3);  // both CTAs may refill the stage
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(&tfull_bar, 0x3);  // both halves of the unit are ready
+        ++uses;
+      }
+      umma_commit_pair(&drain_bar);
+      wait_drain(&drain_bar, 0, args.err);
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 (both CTAs) ----------------
+    const int quad = warp & 3;
+    uint8_t* stage_out = smem + S * kWideStageBytes + (warp - 2) * 2 * kStageOutBytes;
+    uint32_t nstore = 0, uses = 0;
+    for (int64_t u = first; u < total; u += stride) {
+      TileInfo ti = decode_wide_unit<MODE>(args, u, crank);
+      if (!mbar_wait(&tfull_bar, uses & 1u, abortp, args.err)) break;
+      tc_fence_after();
+      if (ti.skip) {
+        if (lane == 0) set_dev_error(args.err, MOE_DEVERR_BAD_EXPERT);
+      } else {
+        epilogue<MODE, true>(maps, args, ti, tmem_base, quad, lane, stage_out, nstore);
+        ++ti.nt;
+        epilogue<MODE, true>(maps, args, ti, tmem_base + BN, quad, lane, stage_out, nstore);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&tempty_bar);
+        else mbar_arrive_cluster(cluster_addr(&tempty_bar, 0));
+      }
+      ++uses;
     }
     if (lane == 0) bulk_wait_all();
   }
@@ -1407,6 +1607,62 @@ int pick_stages(const Layout& L, int mode) {
   return L.A >= 1024LL * L.E ? 5 : 6;
 }
 
+template <int MODE, int S>
+moe_status launch_wide_s(const Maps& maps, const Args& args, int64_t units, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;
+  auto config = [](cudaLaunchConfig_t& cfg, cudaLaunchAttribute* at, int clusters) {
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = wide_smem_bytes(S);
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+  };
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(grouped_gemm_wide_kernel<MODE, S>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, wide_smem_bytes(S));
+    if (attr_err != cudaSuccess) return;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    config(cfg, at, 64);
+    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_wide_kernel<MODE, S>, &cfg);
+    if (attr_err == cudaSuccess && max_clusters <= 0) attr_err = cudaErrorInvalidConfiguration;
+  });
+  if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
+  if (units <= 0) return MOE_OK;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  config(cfg, at, static_cast<int>(std::min<int64_t>(max_clusters, units)));
+  cfg.stream = s;
+  if (cudaLaunchKernelEx(&cfg, grouped_gemm_wide_kernel<MODE, S>, maps, args) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Width of the token-row GEMMs' pair tiles in N: the caller's
+// moe_problem.tile_n if set, else the library's choice per shape, from
+// sweeps on a GB300 (bench.py --sweep-stages, 2070 MHz). The 512-wide tile
+// stages each A k-block once for two N tiles but keeps one accumulator, so its
+// epilogue stalls the MMAs: it pays only where K is long and the epilogue
+// light. The gate/up data gradient (K = 2 I) with experts of at least 1024
+// tokens on average: 2.11 against 2.30 ms narrow (skewed workload), 2.11
+// against 2.20 (uniform routing); at 256 tokens per expert (large batch,
+// N = 8192) 3.37 against 3.34. Not for gate/up and down (skewed -4%, uniform
+// +3%, fine-grained +10%), nor the down data gradient, whose epilogue reads G
+// and U back (+28% and +37%).
+bool pick_wide(const Layout& L, int mode, int n_nt) {
+  if (n_nt % 2 != 0) return false;
+  if (L.tile_n == 256) return false;
+  if (L.tile_n == 512) return true;
+  return mode == DXE && L.A >= 1024LL * L.E;
+}
+
 template <int MODE, bool RC = false>
 moe_status launch_pair(const Layout& L, const Maps& maps, const Args& args, int64_t units,
                        cudaStream_t s) {
@@ -1421,6 +1677,9 @@ moe_status launch_pair(const Layout& L, const Maps& maps, const Args& args, int6
 // one per 128-row tile).
 template <int MODE>
 moe_status launch_tokens(const Layout& L, const Maps& maps, const Args& args, cudaStream_t s) {
+  if (pick_wide(L, MODE, args.n_nt))
+    return launch_wide_s<MODE, 4>(maps, args, static_cast<int64_t>(args.max_mtiles) * (args.n_nt / 2),
+                                  s);
   return launch_pair<MODE>(L, maps, args, static_cast<int64_t>(args.max_mtiles) * args.n_nt, s);
 }
 
@@ -1549,7 +1808,7 @@ moe_status gemm_down_dgrad_rc(const Layout& L, const void* ws, const void* dy, c
   a.in0 = g;
   a.in1 = u;
   const int64_t units = static_cast<int64_t>(a.max_mtiles) * a.n_nt;
-  if (!dy) return launch_pair<DACT>(L, m, a, units, s);
+  if (!dy) return launch_tokens<DACT>(L, m, a, s);
   // fused reverse-combine: dYe and dw come from the kernel's side warps
   a.rc_dy = static_cast<const uint4*>(dy);
   a.rc_ye = static_cast<const uint4*>(ye);

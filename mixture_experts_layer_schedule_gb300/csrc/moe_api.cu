@@ -30,6 +30,7 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   if (T != 128 && T != 256 && T != 512 && T != 1024) return MOE_ERR_UNSUPPORTED;
   if (p->pipeline_stages != 0 && (p->pipeline_stages < 4 || p->pipeline_stages > 6))
     return MOE_ERR_UNSUPPORTED;
+  if (p->tile_n != 0 && p->tile_n != 256 && p->tile_n != 512) return MOE_ERR_UNSUPPORTED;
   // rows, slots and tile coordinates are int32 on the device; bound N before
   // forming N * k so that the product cannot overflow
   if (p->N > (1LL << 31) / p->k) return MOE_ERR_UNSUPPORTED;
@@ -46,6 +47,7 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   L->T = T;
   L->dtype = p->dtype;
   L->stages = p->pipeline_stages;
+  L->tile_n = p->tile_n;
   L->n_warps = (A + kSchedSub - 1) / kSchedSub;
   size_t o = 0;
   auto take = [&o](size_t bytes) {

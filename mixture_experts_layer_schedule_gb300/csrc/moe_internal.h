@@ -23,6 +23,7 @@ struct Layout {
   int32_t T;              // per-expert row granularity (minibatch rows)
   int32_t dtype;          // MOE_BF16 or MOE_MXFP8
   int32_t stages;         // SM-pair GEMM ring stages requested (0: the library's choice)
+  int32_t tile_n;         // token-row GEMM pair-tile width requested (0: the library's choice)
   int64_t n_warps;        // schedule warps = ceil(A / kSchedSub)
   // workspace byte offsets
   size_t err, counts, offsets, pad_offsets, slot_of, src_of_row, tiles, n_tiles, ptiles, n_ptiles,

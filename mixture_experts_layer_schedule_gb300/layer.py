@@ -36,14 +36,15 @@ class MoELayer:
     """Buffers of one problem size on one device, reused across calls."""
 
     def __init__(self, N, H, I, E, k, device="cuda", allocate_grads=True, minibatch_rows=128,
-                 dtype="bf16", pipeline_stages=0):
+                 dtype="bf16", pipeline_stages=0, tile_n=0):
         self.N, self.H, self.I, self.E, self.k = int(N), int(H), int(I), int(E), int(k)
         self.T = int(minibatch_rows)
         self.dtype = dtype
         self.device = torch.device(device)
         self.p = _lib.problem(N, H, I, E, k,
                               dtype=_lib.MOE_MXFP8 if dtype == "mxfp8" else _lib.MOE_BF16,
-                              minibatch_rows=self.T, pipeline_stages=pipeline_stages)
+                              minibatch_rows=self.T, pipeline_stages=pipeline_stages,
+                              tile_n=tile_n)
         self.R = _lib.moe_grouped_rows(self.p)
         dev = self.device
         self.ws = torch.empty(_lib.moe_workspace_bytes(self.p), dtype=torch.uint8, device=dev)

@@ -59,12 +59,15 @@ def test_sizes_and_validation(lib):
     # the largest sizes below the bound are accepted (host-side sizing only)
     assert _lib.moe_workspace_bytes(_lib.problem(2 ** 28 - 2 ** 16, 256, 512, 8, 8)) > 0
     for bad_kw in (dict(dtype=7), dict(minibatch_rows=192), dict(minibatch_rows=2048),
-                   dict(pipeline_stages=3), dict(pipeline_stages=7), dict(pipeline_stages=-1)):
+                   dict(pipeline_stages=3), dict(pipeline_stages=7), dict(pipeline_stages=-1),
+                   dict(tile_n=128), dict(tile_n=1024)):
         with pytest.raises(_lib.MoEError) as ei:
             _lib.moe_workspace_bytes(_lib.problem(256, 256, 512, 8, 2, **bad_kw))
         assert ei.value.status == _lib.MOE_ERR_UNSUPPORTED
     for good in (4, 5, 6):  # the ring depths the GEMMs are built for; sizes do not change
         assert _lib.moe_workspace_bytes(_lib.problem(256, 256, 512, 8, 2, pipeline_stages=good)) == ws
+    for good in (256, 512):
+        assert _lib.moe_workspace_bytes(_lib.problem(256, 256, 512, 8, 2, tile_n=good)) == ws
     # MXFP8 adds the quantised-operand buffers; T = 256 grows the padded rows
     mx = _lib.moe_workspace_bytes(_lib.problem(256, 256, 512, 8, 2, dtype=_lib.MOE_MXFP8))
     assert mx > ws + R * (2 * 256 + 4 * 512) * 2 - 4096

@@ -379,18 +379,26 @@ def test_empty_batch():
     assert layer.y.shape == (0, 256) and layer.grads.dx.shape == (0, 256)
     for t in (layer.grads.dw_gate, layer.grads.dw_up, layer.grads.dw_down):
         assert torch.all(t == 0)
+    # the fused dispatch + expert FFN launch on an empty batch: nothing to do,
+    # and no counter wait is left waiting
+    layer.forward_inference(empty["x"], inp["wg"], inp["wu"], inp["wd"])
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
 
 
-@pytest.mark.parametrize("stages", [4, 5, 6])
-def test_results_do_not_depend_on_the_ring_depth(stages):
+@pytest.mark.parametrize("stages,tile_n", [(4, 256), (5, 256), (6, 256), (0, 512), (0, 256)])
+def test_results_do_not_depend_on_the_ring_depth(stages, tile_n):
     """moe_problem.pipeline_stages only changes how many k-blocks the SM-pair
-    GEMMs keep in flight: the MMAs, their order and the epilogues are the
-    same, so every output equals the library's default choice bit for bit."""
+    GEMMs keep in flight, and tile_n = 512 only makes two N tiles share each
+    staged A k-block (two pair MMAs per k-step into the two halves of TMEM):
+    the MMAs of every 256-column block, their order and the epilogues are the
+    same, so every output equals the library's default choice bit for bit
+    (ragged experts, odd last 128-row items, several N tiles)."""
     shape = custom_shape(2048, 1024, 512, 16, 4, zipf_s=1.2, name="ring_depth")
     inp = to_dev(inputs.make_inputs(shape, seed=5, device="cpu"))
     ref = run_layer(shape, inp)
     layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev(),
-                     pipeline_stages=stages)
+                     pipeline_stages=stages, tile_n=tile_n)
     layer.step(inp["x"], inp["logits"], inp["bias"], inp["wg"], inp["wu"], inp["wd"], inp["dy"])
     torch.cuda.synchronize()
     assert layer.device_error() == 0
@@ -403,3 +411,18 @@ def test_results_do_not_depend_on_the_ring_depth(stages):
         a, b = getattr(layer.grads, name), getattr(ref.grads, name)
         assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b), name
+
+
+@pytest.mark.parametrize("shape", [LAYER_SHAPES[i] for i in (0, 1, 3, 4, 5, 9)], ids=lambda s: s.name)
+def test_wide_tiles_match_oracle(shape):
+    """The whole layer with 512-wide pair tiles in the token-row GEMMs, against
+    the fp64 oracle (bf16 bound), on ragged, empty-expert, T = 256 / 1024 and
+    single-expert shapes."""
+    inp = inputs.make_inputs(shape, seed=1, device="cpu")
+    d = to_dev(inp)
+    layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev(),
+                     minibatch_rows=shape.minibatch_rows, tile_n=512)
+    layer.step(d["x"], d["logits"], d["bias"], d["wg"], d["wu"], d["wd"], d["dy"])
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    _oracle_compare(shape, inp, layer)
