@@ -42,7 +42,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=None,
-                    help="workload name (default: skewed fwd+bwd) or N,H,I,E,k[,zipf][,T=..][,mxfp8]")
+                    help="workload name (default: skewed fwd+bwd) or "
+                         "N,H,I,E,k[,zipf][,T=..][,mxfp8][,fwd] (fwd: forward only)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=0,
@@ -412,17 +413,21 @@ def workload(name):
     if name in inputs.ALL:
         return inputs.ALL[name]
     f = name.split(",")
-    dtype = "bf16"
-    if f[-1] == "mxfp8":
-        dtype = f.pop()
-    T = 128
-    if f[-1].startswith("T="):
-        T = int(f.pop()[2:])
+    dtype, T, backward = "bf16", 128, True
+    while len(f) > 5 and (f[-1] in ("mxfp8", "fwd") or f[-1].startswith("T=")):
+        tok = f.pop()
+        if tok == "mxfp8":
+            dtype = tok
+        elif tok == "fwd":
+            backward = False
+        else:
+            T = int(tok[2:])
     N, H, I, E, k = (int(v) for v in f[:5])
     z = float(f[5]) if len(f) > 5 and float(f[5]) > 0 else None
     return inputs.LayerShape(f"custom_N{N}_H{H}_I{I}_E{E}_k{k}" + (f"_zipf{z}" if z else "")
-                             + f"_T{T}" + ("_mxfp8" if dtype == "mxfp8" else ""), N, H, I, E, k,
-                             zipf_s=z, minibatch_rows=T, dtype=dtype)
+                             + f"_T{T}" + ("_mxfp8" if dtype == "mxfp8" else "")
+                             + ("" if backward else "_fwd"), N, H, I, E, k,
+                             zipf_s=z, minibatch_rows=T, dtype=dtype, backward=backward)
 
 
 def run_ours(args, ws_, rank, local, shape=None, stages=None, tile_n=None):

@@ -298,9 +298,15 @@ moe_status moe_dispatch_expert_ffn(const moe_problem* p, const void* ws, const v
                                    void* ye, void* stream);
 
 /* Forward without a context (inference): dispatch, gate/up (Act only) and
- * down in one launch (moe_dispatch_expert_ffn; MOE_MXFP8: separate launches)
- * with Xe and Ye sharing one scratch buffer, then the combine; same y as
- * moe_forward.
+ * down in one persistent launch (MOE_MXFP8: separate launches), then the
+ * combine; same y as moe_forward. MOE_BF16: the dispatch fills, and the GEMMs
+ * drain, a ring of 256-row minibatch slots for Xe and Act ("ring token
+ * buffer", [Clip] key points 3-4): item p of the schedule's SM-pair items
+ * uses slot p mod S, and a slot is refilled once the GEMM that reads it has
+ * loaded it (per-item counters, bounded waits). S is set from the number of
+ * co-resident CTA pairs, so the ring holds S * 256 * (H + I) bf16 values
+ * whatever N is; a problem with fewer expert-grouped rows than the ring needs
+ * runs with Xe and Ye sharing one scratch buffer instead.
  * Uses the workspace's backward buffers as scratch for Xe/Ye and Act, so it
  * must not run between a moe_forward and its moe_backward. */
 moe_status moe_forward_inference(const moe_problem* p, const void* x, const moe_weights* w,

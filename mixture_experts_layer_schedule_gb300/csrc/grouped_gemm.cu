@@ -705,16 +705,22 @@ __device__ __forceinline__ bool wait_count(const int32_t* p, int32_t target, vol
 // accumulator acc, `commit` when it ends the tile.
 // The producer, the MMA issuer and the epilogue walk the same items.
 //  * Token-row modes: whole tiles in order on alternating accumulators.
-//  * WGRAD: the pair's tiles come alternately from the front (largest
-//    experts, long K) and the back (smallest experts, short K) of the
-//    size-ordered list, on alternating accumulators, so the MMAs of one tile
-//    overlap the epilogue (fp32 stores) of the previous. A front tile of more
-//    than kWgChunkMin k-blocks is issued in chunks of kWgChunk with one whole back
-//    tile, on the other accumulator, after each chunk, and the next front
-//    tile's first chunk comes before the next back tile: the short tiles'
-//    epilogues then run under the long tile's MMAs instead of the MMAs
-//    waiting for them.
-constexpr int kWgChunk = 24, kWgChunkMin = 48;
+//  * WGRAD: the tiles, ordered by expert size (largest first), fall into three
+//    regions by K: big tiles (more than kWgChunk k-blocks), mid tiles, and
+//    light tiles (at most kWgLight k-blocks). A light tile's MMAs are short
+//    and its epilogue (a whole fp32 tile of stores) is long, so it can only
+//    hide under another tile's MMAs: when the pair has light tiles, it issues
+//    each big tile in chunks of kWgChunk k-blocks and, after each chunk but
+//    the last, up to kWgPerSlot light tiles on the other accumulator, at the
+//    rate that spreads the pair's light tiles evenly over the chunk
+//    boundaries of its big tiles. Mid tiles follow, whole, on alternating
+//    accumulators, then any light tiles left. Every tile opens on the
+//    accumulator whose last tile committed earlier. Chunks do not change a
+//    tile's MMA order, so the results are those of whole tiles.
+//    Measured on a GB300 (skewed workload, gate/up weight gradient): 2.72-2.74
+//    ms against 2.79-2.80 for big and small tiles taken alternately; two light
+//    tiles per boundary, or chunks of 12 or 24 k-blocks, were not faster.
+constexpr int kWgChunk = 16, kWgLight = 8, kWgPerSlot = 1;
 
 struct PairItem {
   int64_t t;
@@ -722,73 +728,167 @@ struct PairItem {
   bool commit;
 };
 
+// WGRAD: this pair's share of the three tile regions (one warp computes it in
+// both CTAs of the pair before the roles start).
+struct WgSplit {
+  int64_t big_end, mid_end;  // tile index bounds of the big and mid regions
+  int64_t slots;             // chunk boundaries in this pair's big tiles
+  int64_t lights;            // this pair's light tiles
+};
+
+// K blocks of the expert at rank r of the size order (the expert as the tile
+// decode reads it).
+__device__ __forceinline__ int wg_rank_nkb(const Args& a, int r) {
+  int e = a.order[r];
+  if (e < 0 || e >= a.E) e = 0;
+  const int c = a.counts[e];
+  return c <= 0 ? 0 : (c + BK - 1) / BK;
+}
+
+// The first tile at or after t0 that pair p (of P) takes, and how many of
+// [lo, hi) it takes.
+__device__ __forceinline__ int64_t first_mine(int64_t t0, int64_t p, int64_t P) {
+  return t0 <= p ? p : p + ((t0 - p + P - 1) / P) * P;
+}
+__device__ __forceinline__ int64_t count_mine(int64_t lo, int64_t hi, int64_t p, int64_t P) {
+  const int64_t f = first_mine(lo, p, P);
+  return f < hi ? (hi - 1 - f) / P + 1 : 0;
+}
+
+__device__ __forceinline__ int warp_min_i32(int v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+__device__ __forceinline__ int64_t warp_sum_i64(int64_t v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// The regions are cut at the first rank at or below each K bound, so a rank
+// order that is not monotone (a corrupt schedule) still covers every tile once.
+__device__ void wg_split(const Args& a, int64_t p, int64_t P, int lane, WgSplit* out) {
+  const int64_t per_e = static_cast<int64_t>(a.w_mt / 2) * a.w_nt * a.n_probs;
+  int rb = a.E, rl = a.E;
+  for (int r = lane; r < a.E; r += 32)
+    if (wg_rank_nkb(a, r) <= kWgChunk) { rb = r; break; }
+  rb = warp_min_i32(rb);
+  for (int r = rb + lane; r < a.E; r += 32)
+    if (wg_rank_nkb(a, r) <= kWgLight) { rl = r; break; }
+  rl = warp_min_i32(rl);
+  int64_t slots = 0, lights = 0;
+  for (int r = lane; r < a.E; r += 32) {
+    const int64_t n = count_mine(r * per_e, (r + 1) * per_e, p, P);
+    if (r < rb) slots += n * max((wg_rank_nkb(a, r) + kWgChunk - 1) / kWgChunk - 1, 0);
+    else if (r >= rl) lights += n;
+  }
+  slots = warp_sum_i64(slots);
+  lights = warp_sum_i64(lights);
+  if (lane == 0) {
+    out->big_end = rb * per_e;
+    out->mid_end = rl * per_e;
+    out->slots = slots;
+    out->lights = lights;
+  }
+}
+
 template <int MODE>
 struct PairPlan {
-  int64_t fi, bi, half, total, stride;
-  int64_t lt;         // open front tile
-  TileInfo lti;       // its decoded tile
-  int lkb, lnk, la;   // its next k-block, k-blocks, accumulator
-  int nxt;            // accumulator of the next tile opened without a front tile open
-  bool has_l, chunked, short_next;
-  __device__ __forceinline__ PairPlan(int64_t first, int64_t stride_, int64_t total_)
-      : fi(first), bi(first), half(MODE == WGRAD ? (total_ + 1) / 2 : total_), total(total_),
-        stride(stride_), lt(0), lkb(0), lnk(0), la(0), nxt(0), has_l(false), chunked(false),
-        short_next(false) {}
+  int64_t fi, total, stride;
+  // WGRAD
+  WgSplit sp;
+  int64_t lcur, used, lit;  // next light tile, chunk boundaries passed, light tiles issued
+  int64_t lt;               // open big tile
+  TileInfo lti;             // its decoded tile
+  int lkb, lnk, la;         // its next k-block, k-blocks, accumulator
+  int last;                 // accumulator of the last committed tile
+  int pending;              // light tiles to issue at this chunk boundary
+  bool has_l;
+  __device__ __forceinline__ PairPlan(int64_t first, int64_t stride_, int64_t total_,
+                                      const WgSplit* split = nullptr)
+      : fi(first), total(total_), stride(stride_), used(0), lit(0), lt(0), lkb(0), lnk(0), la(0),
+        last(1), pending(0), has_l(false) {
+    if constexpr (MODE == WGRAD) {
+      sp = *split;
+      lcur = first_mine(sp.mid_end, first, stride_);
+    } else {
+      sp = WgSplit{0, 0, 0, 0};
+      lcur = total_;
+    }
+  }
 
-  __device__ __forceinline__ int take_acc() {
-    const int a = nxt;
-    nxt ^= 1;
-    return a;
+  // A whole tile on the accumulator whose last tile committed earlier.
+  __device__ __forceinline__ void whole(PairItem& it, TileInfo& ti, const Args& a, int64_t t,
+                                        int acc, int crank) {
+    it.t = t;
+    ti = decode_pair_tile<MODE>(a, t, crank);
+    it.acc = acc;
+    it.kb0 = 0;
+    it.kb1 = ti.nkb;
+    it.commit = true;
+    last = acc;
   }
 
   // The next item and its decoded tile (decoded once per tile).
   __device__ __forceinline__ bool next(PairItem& it, TileInfo& ti, const Args& a, int crank) {
     if constexpr (MODE != WGRAD) {
       if (fi >= total) return false;
-      it.t = fi;
+      whole(it, ti, a, fi, last ^ 1, crank);
       fi += stride;
-      ti = decode_pair_tile<MODE>(a, it.t, crank);
-      it.acc = take_acc();
-      it.kb0 = 0;
-      it.kb1 = ti.nkb;
-      it.commit = true;
       return true;
     } else {
-      const bool f_ok = fi < half, b_ok = bi < total - half;
-      if ((short_next || (!has_l && !f_ok)) && b_ok) {  // a whole back tile
-        it.t = total - 1 - bi;
-        bi += stride;
-        ti = decode_pair_tile<MODE>(a, it.t, crank);
-        it.acc = has_l ? (la ^ 1) : take_acc();
-        it.kb0 = 0;
-        it.kb1 = ti.nkb;
-        it.commit = true;
-        short_next = false;
-        return true;
+      if (pending > 0) {
+        if (lcur < total) {  // a light tile beside the open big tile
+          whole(it, ti, a, lcur, la ^ 1, crank);
+          lcur += stride;
+          ++lit;
+          --pending;
+          return true;
+        }
+        pending = 0;
       }
-      if (!has_l) {  // open the next front tile
-        if (!f_ok) return false;
+      if (!has_l && fi < sp.big_end) {  // open the next big tile
         lt = fi;
         fi += stride;
         lti = decode_pair_tile<MODE>(a, lt, crank);
         lkb = 0;
         lnk = lti.nkb;
-        la = take_acc();
-        chunked = lnk > kWgChunkMin;
+        la = last ^ 1;
         has_l = true;
       }
-      ti = lti;
-      it.t = lt;
-      it.acc = la;
-      it.kb0 = lkb;
-      it.kb1 = chunked ? min(lkb + kWgChunk, lnk) : lnk;
-      it.commit = it.kb1 == lnk;
-      lkb = it.kb1;
-      if (it.commit) has_l = false;
-      // after a chunk, or a short front tile, a back tile; after a chunked
-      // front tile's last chunk, the next front tile's first chunk
-      short_next = !(it.commit && chunked);
-      return true;
+      if (has_l) {
+        ti = lti;
+        it.t = lt;
+        it.acc = la;
+        it.kb0 = lkb;
+        it.kb1 = sp.lights > 0 ? min(lkb + kWgChunk, lnk) : lnk;
+        if (it.kb1 < it.kb0) it.kb1 = it.kb0;
+        it.commit = it.kb1 >= lnk;
+        lkb = it.kb1;
+        if (it.commit) {
+          has_l = false;
+          last = la;
+        } else if (sp.slots > 0) {
+          ++used;
+          int64_t target = (used * sp.lights + sp.slots - 1) / sp.slots;
+          if (target > sp.lights) target = sp.lights;
+          const int64_t owe = target - lit;
+          pending = owe <= 0 ? 0 : (owe < kWgPerSlot ? static_cast<int>(owe) : kWgPerSlot);
+        }
+        return true;
+      }
+      if (fi < sp.mid_end) {  // a mid tile
+        whole(it, ti, a, fi, last ^ 1, crank);
+        fi += stride;
+        return true;
+      }
+      if (lcur < total) {  // light tiles left over
+        whole(it, ti, a, lcur, last ^ 1, crank);
+        lcur += stride;
+        return true;
+      }
+      return false;
     }
   }
 };
@@ -889,6 +989,11 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
     tmem_alloc_pair(&tmem_base_slot, kTmemCols);  // one warp of each CTA, collectively
     tmem_relinquish_pair();
   }
+  const int64_t first = blockIdx.x / 2, stride = gridDim.x / 2;
+  __shared__ WgSplit wsplit;
+  if constexpr (MODE == WGRAD) {
+    if (warp == 2) wg_split(args, first, stride, lane, &wsplit);
+  }
   tc_fence_before();
   __syncthreads();
   cluster_sync();
@@ -896,7 +1001,6 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
   const uint32_t tmem_base = tmem_base_slot;
   volatile int* abortp = &abort_flag;
   const int64_t total = total_pair_tiles<MODE>(args);
-  const int64_t first = blockIdx.x / 2, stride = gridDim.x / 2;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -907,7 +1011,7 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
       bool ok = true;
       PairItem it;
       TileInfo ti;
-      for (PairPlan<MODE> plan(first, stride, total); ok && plan.next(it, ti, args, crank);) {
+      for (PairPlan<MODE> plan(first, stride, total, &wsplit); ok && plan.next(it, ti, args, crank);) {
         if constexpr (RC) {  // this CTA's dYe rows come from the side warps
           if (ti.nkb > 0 && !wait_count(args.rc_sync + 1 + ti.row0 / BM, BM, abortp, args.err)) {
             ok = false;
@@ -943,7 +1047,7 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
       bool ok = true;
       PairItem it;
       TileInfo ti;
-      for (PairPlan<MODE> plan(first, stride, total); ok && plan.next(it, ti, args, crank);) {
+      for (PairPlan<MODE> plan(first, stride, total, &wsplit); ok && plan.next(it, ti, args, crank);) {
         const int acc = it.acc;
         if (it.kb0 == 0) {  // a new tile: its accumulator's last tile has been read out
           if (!mbar_wait(&tempty_bar[acc], ((acc ? uses1 : uses0) & 1u) ^ 1u, abortp, args.err))
@@ -990,7 +1094,7 @@ __global__ void __launch_bounds__(kGemmThreads + (RC ? 32 * kRcWarps : 0), 1)
     uint32_t uses0 = 0u, uses1 = 0u;
     PairItem it;
     TileInfo ti;
-    for (PairPlan<MODE> plan(first, stride, total); plan.next(it, ti, args, crank);) {
+    for (PairPlan<MODE> plan(first, stride, total, &wsplit); plan.next(it, ti, args, crank);) {
       if (!it.commit) continue;
       const int acc = it.acc;
       if (!mbar_wait(&tfull_bar[acc], (acc ? uses1 : uses0) & 1u, abortp, args.err)) break;
@@ -1227,7 +1331,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // The arithmetic of each tile is that of the separate gate/up and down
 // launches (same MMAs in the same order, same epilogues), so the results are
 // bit-identical to dispatch + gate/up + down.
+//
+// Ring mode (the context-free forward, which keeps neither Xe nor Act): Xe
+// and Act live in a ring of `ring` minibatch slots of 256 rows, item p in
+// slot p % ring, instead of in buffers of all R rows, so the forward's
+// working set is ring * 256 * (H + I) * 2 bytes whatever N is, and stays in
+// L2. The dispatch side warps claim 8-row chunks item by item; before
+// copying into item p's slot they wait until the G gate/up units of item
+// p - ring are done (so their Xe loads have landed). Before storing item p's
+// Act, a gate/up epilogue waits until the D down units of item p - ring have
+// started their epilogues (so their Act loads have landed). ring > lag puts
+// those down units earlier in the list than the gate/up units that wait for
+// them, so every wait is still on earlier work or on the dispatch of earlier
+// items.
 constexpr int kFfDispWarps = 4;
+constexpr int kRingSpare = 4;  // ring slots beyond the lag
 
 struct FusedArgs {
   const uint4* x;            // token rows [N][H/8]
@@ -1237,10 +1355,32 @@ struct FusedArgs {
   int32_t* ticket;           // dispatch chunk ticket
   int32_t* disp_done;        // [R/128] rows dispatched per 128-row tile
   int32_t* gu_done;          // [R/128] finished gate/up epilogue-warp units per item
+  int32_t* dn_done;          // [R/128] ring mode: down epilogue-warp units started per item
+  const int32_t* ptiles;     // ring mode: the pair items (expert, row0, rows)
   int64_t A, rows;
   int E, k, hv;
   int G, D, lag;             // units per item (gate/up, down); item lag of the down units
+  int ring;                  // slots of the Xe and Act rings (0: buffers of all R rows)
 };
+
+// First row of this CTA's part of item p in the ring.
+__device__ __forceinline__ int32_t ring_row(const FusedArgs& f, int p, int crank, bool fold) {
+  return (p % f.ring) * (2 * BM) + crank * (fold ? BM / 2 : BM);
+}
+
+// A bounded wait that every lane of the warp leaves together: lane 0 polls,
+// then every lane acquires the counter itself.
+__device__ __forceinline__ bool warp_wait_count(const int32_t* p, int32_t target, volatile int* abort,
+                                                int32_t* err, int lane) {
+  int ok = 1;
+  if (lane == 0) ok = wait_count(p, target, abort, err) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) {
+    asm volatile("{\n\t.reg .b32 v;\n\tld.acquire.gpu.global.b32 v, [%0];\n\t}" ::"l"(p) : "memory");
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+  }
+  return ok != 0;
+}
 
 struct FusedUnit {
   bool valid, down;
@@ -1260,6 +1400,30 @@ __device__ __forceinline__ FusedUnit fused_unit(const FusedArgs& f, int64_t u, i
   return x;
 }
 
+// One row of the dispatch: drow = x[src_of_row[row] / k], or zeros on padding.
+__device__ __forceinline__ void copy_token_row(const FusedArgs& f, int64_t row, uint4* drow,
+                                               int lane) {
+  const int32_t as = f.src_of_row[row];
+  if (as < 0 || as >= f.A) {
+    for (int v = lane; v < f.hv; v += 32) drow[v] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const uint4* srow = f.x + static_cast<int64_t>(as / f.k) * f.hv;
+  for (int base = 0; base < f.hv; base += 256) {
+    uint4 v8[8];  // all loads of the step first: 8 in flight per lane
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int v = base + 32 * q + lane;
+      if (v < f.hv) v8[q] = __ldg(srow + v);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int v = base + 32 * q + lane;
+      if (v < f.hv) drow[v] = v8[q];
+    }
+  }
+}
+
 // Dispatch side warps: xe[row] = x[src_of_row[row] / k], padding rows 0.
 // They claim chunks from the front as fast as they can: making them wait for
 // the gate/up progress (a bounded window of items ahead, so rows are still in
@@ -1275,32 +1439,46 @@ __device__ __forceinline__ void dispatch_rows(const FusedArgs& f, int lane) {
     if (c >= n_chunks) break;
     for (int r = 0; r < kRcRows; ++r) {
       const int64_t row = static_cast<int64_t>(c) * kRcRows + r;
-      const int32_t as = f.src_of_row[row];
-      uint4* drow = f.xe + row * f.hv;
-      if (as < 0 || as >= f.A) {
-        for (int v = lane; v < f.hv; v += 32) drow[v] = make_uint4(0u, 0u, 0u, 0u);
-        continue;
-      }
-      const uint4* srow = f.x + static_cast<int64_t>(as / f.k) * f.hv;
-      for (int base = 0; base < f.hv; base += 256) {
-        uint4 v8[8];  // all loads of the step first: 8 in flight per lane
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int v = base + 32 * q + lane;
-          if (v < f.hv) v8[q] = __ldg(srow + v);
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int v = base + 32 * q + lane;
-          if (v < f.hv) drow[v] = v8[q];
-        }
-      }
+      copy_token_row(f, row, f.xe + row * f.hv, lane);
     }
     __syncwarp();
     if (lane == 0) {
       asm volatile("fence.proxy.async.global;" ::: "memory");  // rows seen by the TMA loads
       __threadfence();
       atomicAdd(f.disp_done + (static_cast<int64_t>(c) * kRcRows) / BM, kRcRows);
+    }
+  }
+}
+
+// Ring mode: the same copies into the ring, item by item (32 chunks of 8
+// rows per slot; a 128-row item fills half of its slot). Rows of a corrupt
+// item are not copied: the GEMM roles skip that item.
+__device__ __forceinline__ void dispatch_ring(const FusedArgs& f, int n_items, int lane,
+                                              volatile int* abort, int32_t* err) {
+  constexpr int kChunks = 2 * BM / kRcRows;
+  const int64_t n_chunks = static_cast<int64_t>(n_items) * kChunks;
+  int freed = -1;  // the last item whose slot this warp has seen free
+  while (true) {
+    int32_t c = 0;
+    if (lane == 0) c = atomicAdd(f.ticket, 1);
+    c = __shfl_sync(0xffffffffu, c, 0);
+    if (c >= n_chunks) break;
+    const int p = c / kChunks, q = c % kChunks;
+    const int r0 = f.ptiles[3 * p + 1], nr = f.ptiles[3 * p + 2];
+    if ((nr != BM && nr != 2 * BM) || r0 < 0 || r0 > f.rows - nr) continue;
+    if (q * kRcRows >= nr) continue;
+    if (p >= f.ring && p != freed) {
+      if (!warp_wait_count(f.gu_done + (p - f.ring), 8 * f.G, abort, err, lane)) break;
+      freed = p;
+    }
+    uint4* slot = f.xe + (static_cast<int64_t>(p % f.ring) * (2 * BM) + q * kRcRows) * f.hv;
+    for (int r = 0; r < kRcRows; ++r)
+      copy_token_row(f, static_cast<int64_t>(r0) + q * kRcRows + r, slot + r * f.hv, lane);
+    __syncwarp();
+    if (lane == 0) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // rows seen by the TMA loads
+      __threadfence();
+      atomicAdd(f.disp_done + (r0 + q * kRcRows) / BM, kRcRows);
     }
   }
 }
@@ -1370,12 +1548,13 @@ __global__ void __launch_bounds__(kGemmThreads + 32 * kFfDispWarps, 1)
       for (int64_t u = first; u < total && ok; u += stride) {
         const FusedUnit fu = fused_unit(f, u, n_items);
         if (!fu.valid) continue;
-        const TileInfo ti = fused_tile(f, gu, dn, fu, crank);
+        TileInfo ti = fused_tile(f, gu, dn, fu, crank);
         if (ti.nkb > 0) {
           const bool ready = fu.down ? wait_count(f.gu_done + fu.item, 8 * f.G, abortp, gu.err)
                                      : wait_count(f.disp_done + ti.row0 / BM, BM, abortp, gu.err);
           if (!ready) break;
         }
+        if (f.ring > 0) ti.row0 = ring_row(f, fu.item, crank, ti.fold);  // A rows: the ring slot
         for (int kb = 0; kb < ti.nkb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abortp, gu.err)) { ok = false; break; }
           uint8_t* sA = smem + stage * kPairStageBytes;
@@ -1437,7 +1616,8 @@ __global__ void __launch_bounds__(kGemmThreads + 32 * kFfDispWarps, 1)
     }
   } else if (warp >= 6) {
     // ---------------- dispatch side warps 6.. ----------------
-    dispatch_rows(f, lane);
+    if (f.ring > 0) dispatch_ring(f, n_items, lane, abortp, gu.err);
+    else dispatch_rows(f, lane);
   } else {
     // ---------------- epilogue warps 2..5 (both CTAs) ----------------
     const int quad = warp & 3;
@@ -1448,14 +1628,24 @@ __global__ void __launch_bounds__(kGemmThreads + 32 * kFfDispWarps, 1)
     for (int64_t u = first; u < total; u += stride) {
       const FusedUnit fu = fused_unit(f, u, n_items);
       if (!fu.valid) continue;
-      const TileInfo ti = fused_tile(f, gu, dn, fu, crank);
+      TileInfo ti = fused_tile(f, gu, dn, fu, crank);
       if (!mbar_wait(&tfull_bar[acc], (acc ? uses1 : uses0) & 1u, abortp, gu.err)) break;
       tc_fence_after();
+      if (f.ring > 0 && fu.down && lane == 0) {  // the tile's MMAs are done: its Act loads have landed
+        __threadfence();
+        atomicAdd(f.dn_done + fu.item, 1);
+      }
       if (ti.skip) {
         if (lane == 0) set_dev_error(gu.err, MOE_DEVERR_BAD_EXPERT);
       } else if (fu.down) {
         epilogue<DOWN, true>(mdn, dn, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
       } else {
+        if (f.ring > 0) {  // Act goes to the item's ring slot, once the slot's last reader is done
+          ti.row0 = ring_row(f, fu.item, crank, ti.fold);
+          if (fu.item >= f.ring &&
+              !warp_wait_count(f.dn_done + (fu.item - f.ring), 8 * f.D, abortp, gu.err, lane))
+            break;
+        }
         epilogue<GATE_UP, true>(mgu, gu, ti, tmem_base + acc * BN, quad, lane, stage_out, nstore);
       }
       tc_fence_before();
@@ -1887,19 +2077,71 @@ moe_status gemm_gate_up_wgrad(const Layout& L, const void* ws, const void* dg, c
   return launch_pair<WGRAD>(L, m, a, 2LL * L.E * (a.w_mt / 2) * a.w_nt, s);
 }
 
+namespace {
+void fused_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* att, int clusters) {
+  att[0].id = cudaLaunchAttributeClusterDimension;
+  att[0].val.clusterDim.x = 2;
+  att[0].val.clusterDim.y = 1;
+  att[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(kGemmThreads + 32 * kFfDispWarps);
+  cfg.dynamicSmemBytes = kPairSmemBytes;
+  cfg.attrs = att;
+  cfg.numAttrs = 1;
+}
+
+// CTA pairs of the fused forward's grid: the occupancy query's count of
+// co-resident clusters (every wait relies on all of them being resident).
+// -1 if the query fails.
+int fused_clusters() {
+  static std::once_flag once;
+  static int max_clusters = -1;
+  std::call_once(once, [] {
+    if (cudaFuncSetAttribute(fused_forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kPairSmemBytes) != cudaSuccess)
+      return;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute att[1];
+    fused_config(cfg, att, 64);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fused_forward_kernel, &cfg) == cudaSuccess && n > 0)
+      max_clusters = n;
+  });
+  return max_clusters;
+}
+
+// The down units of an item follow its gate/up units by about three waves
+// of units, so they rarely find its Act unfinished.
+int fused_lag(const Layout& L, int clusters) {
+  const int units = L.I / (BN / 2) + L.H / BN;
+  return std::max(2, (3 * clusters + units - 1) / units);
+}
+}  // namespace
+
+int fused_ring_slots(const Layout& L) {
+  const int clusters = fused_clusters();
+  return clusters > 0 ? fused_lag(L, clusters) + kRingSpare : 0;
+}
+
 moe_status gemm_fused_forward(const Layout& L, const void* ws, const void* x, const void* wg,
                               const void* wu, const void* wd, void* xe, void* g, void* u,
-                              void* act, void* ye, cudaStream_t s) {
+                              void* act, void* ye, int ring, cudaStream_t s) {
+  const int clusters = fused_clusters();
+  if (clusters <= 0) return MOE_ERR_CUDA;
+  const bool store_gu = g != nullptr && u != nullptr;
+  if (ring < 0 || (ring > 0 && (store_gu || ring <= fused_lag(L, clusters))))
+    return MOE_ERR_INVALID_ARG;
+  // rows of the Xe and Act buffers: all R, or the ring's slots
+  const int64_t xrows = ring > 0 ? static_cast<int64_t>(ring) * 2 * BM : L.R;
   Maps mg{}, md{};
-  if (!make_a_maps(&mg.a0, &mg.a0h, xe, L.H, L.R) ||
+  if (!make_a_maps(&mg.a0, &mg.a0h, xe, L.H, xrows) ||
       !make_map(&mg.b0, wg, L.H, static_cast<int64_t>(L.E) * L.I, BN / 4) ||
       !make_map(&mg.b1, wu, L.H, static_cast<int64_t>(L.E) * L.I, BN / 4) ||
-      !make_bf16_out_map(&mg.o2, act, L.I, L.R) ||
-      !make_a_maps(&md.a0, &md.a0h, act, L.I, L.R) ||
+      !make_bf16_out_map(&mg.o2, act, L.I, xrows) ||
+      !make_a_maps(&md.a0, &md.a0h, act, L.I, xrows) ||
       !make_map(&md.b0, wd, L.I, static_cast<int64_t>(L.E) * L.H, BN / 2) ||
       !make_bf16_out_map(&md.o0, ye, L.H, L.R))
     return MOE_ERR_CUDA;
-  const bool store_gu = g != nullptr && u != nullptr;
   if (store_gu && (!make_bf16_out_map(&mg.o0, g, L.I, L.R) || !make_bf16_out_map(&mg.o1, u, L.I, L.R)))
     return MOE_ERR_CUDA;
   mg.a1 = mg.a0;
@@ -1928,6 +2170,8 @@ moe_status gemm_fused_forward(const Layout& L, const void* ws, const void* x, co
   f.ticket = sync;
   f.disp_done = sync + 1;
   f.gu_done = sync + 1 + n_tiles;
+  f.dn_done = sync + 1 + 2 * n_tiles;
+  f.ptiles = at<int32_t>(ws, L.ptiles);
   f.A = L.A;
   f.rows = L.R;
   f.E = L.E;
@@ -1935,44 +2179,14 @@ moe_status gemm_fused_forward(const Layout& L, const void* ws, const void* x, co
   f.hv = L.H / 8;
   f.G = ag.n_nt;
   f.D = ad.n_nt;
-
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  static int max_clusters = 0;
-  auto config = [](cudaLaunchConfig_t& cfg, cudaLaunchAttribute* att, int clusters) {
-    att[0].id = cudaLaunchAttributeClusterDimension;
-    att[0].val.clusterDim.x = 2;
-    att[0].val.clusterDim.y = 1;
-    att[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * clusters);
-    cfg.blockDim = dim3(kGemmThreads + 32 * kFfDispWarps);
-    cfg.dynamicSmemBytes = kPairSmemBytes;
-    cfg.attrs = att;
-    cfg.numAttrs = 1;
-  };
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(fused_forward_kernel,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
-    if (attr_err != cudaSuccess) return;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute att[1];
-    config(cfg, att, 64);
-    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, fused_forward_kernel, &cfg);
-    if (attr_err == cudaSuccess && max_clusters <= 0) attr_err = cudaErrorInvalidConfiguration;
-  });
-  if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
-  // every CTA pair of the grid is resident at once (the waits rely on it):
-  // the grid is the occupancy query's cluster count, never more
-  const int clusters = max_clusters;
-  // the down units of an item follow its gate/up units by about three waves
-  // of units, so they rarely find its Act unfinished
-  f.lag = std::max(2, (3 * clusters + f.G + f.D - 1) / (f.G + f.D));
-  if (cudaMemsetAsync(sync, 0, sizeof(int32_t) * (1 + 2 * n_tiles), s) != cudaSuccess)
+  f.lag = fused_lag(L, clusters);
+  f.ring = ring;
+  if (cudaMemsetAsync(sync, 0, sizeof(int32_t) * (1 + 3 * n_tiles), s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (L.R == 0) return MOE_OK;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute att[1];
-  config(cfg, att, clusters);
+  fused_config(cfg, att, clusters);
   cfg.stream = s;
   if (cudaLaunchKernelEx(&cfg, fused_forward_kernel, mg, md, ag, ad, f) != cudaSuccess)
     return MOE_ERR_CUDA;

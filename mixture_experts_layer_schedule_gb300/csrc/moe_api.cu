@@ -66,7 +66,7 @@ moe_status make_layout(const moe_problem* p, Layout* L) {
   L->ptiles = take(sizeof(int32_t) * 3 * (R / kTileM));  // SM-pair items (at most one per tile)
   L->n_ptiles = take(sizeof(int32_t));
   L->rc_sync = take(sizeof(int32_t) * (1 + R / kTileM));
-  L->ff_sync = take(sizeof(int32_t) * (1 + 2 * (R / kTileM)));
+  L->ff_sync = take(sizeof(int32_t) * (1 + 3 * (R / kTileM)));
   L->warp_counts = take(sizeof(int32_t) * p->E * std::max<int64_t>(L->n_warps, 1));
   L->expert_order = take(sizeof(int32_t) * p->E);
   L->router_logits = take(sizeof(float) * std::max<int64_t>(p->N, 1) * p->E);
@@ -479,7 +479,8 @@ moe_status moe_dispatch_expert_ffn(const moe_problem* p, const void* ws, const v
   if ((L.N > 0 && !aligned(x, 16)) || !weights_ok(w) || !aligned(xe, 16) || !aligned(act, 16) ||
       !aligned(ye, 16) || (!no_gu && (!aligned(g, 16) || !aligned(u, 16))))
     return MOE_ERR_INVALID_ARG;
-  return gemm_fused_forward(L, ws, x, w->w_gate, w->w_up, w->w_down, xe, g, u, act, ye, S(stream));
+  return gemm_fused_forward(L, ws, x, w->w_gate, w->w_up, w->w_down, xe, g, u, act, ye, 0,
+                            S(stream));
 }
 
 moe_status moe_forward_inference(const moe_problem* p, const void* x, const moe_weights* w,
@@ -506,9 +507,21 @@ moe_status moe_forward_inference(const moe_problem* p, const void* x, const moe_
     }
     return moe_combine(p, ws, ye, topk_w, y, stream);
   }
-  // Dispatch, gate/up (Act only) and down in one launch; Xe and Ye share the
-  // scratch rows (a row group's Xe is consumed before its Ye is written).
-  MOE_TRY(moe_dispatch_expert_ffn(p, ws, x, w, ye, nullptr, nullptr, act, ye, stream));
+  // Dispatch, gate/up (Act only) and down in one launch, Xe and Act in a ring
+  // of minibatch slots carved from the Act scratch.
+  if ((L.N > 0 && !aligned(x, 16)) || !weights_ok(w)) return MOE_ERR_INVALID_ARG;
+  const int ring = fused_ring_slots(L);
+  const size_t ring_x = static_cast<size_t>(ring) * 2 * kTileM * L.H * 2;
+  const size_t ring_a = static_cast<size_t>(ring) * 2 * kTileM * L.I * 2;
+  if (ring > 0 && ring_x + ring_a <= static_cast<size_t>(L.R) * L.I * 2) {
+    char* xe = static_cast<char*>(act);
+    MOE_TRY(gemm_fused_forward(L, ws, x, w->w_gate, w->w_up, w->w_down, xe, nullptr, nullptr,
+                               xe + ring_x, ye, ring, S(stream)));
+  } else {
+    // too few rows for the ring: Xe and Ye share the scratch rows (a row
+    // group's Xe is consumed before its Ye is written)
+    MOE_TRY(moe_dispatch_expert_ffn(p, ws, x, w, ye, nullptr, nullptr, act, ye, stream));
+  }
   return moe_combine(p, ws, ye, topk_w, y, stream);
 }
 

@@ -35,7 +35,7 @@ struct Layout {
       mq_rh, ms_rh, mq_ri, ms_ri, mq_ri2, ms_ri2, mq_th, ms_th, mq_ti, ms_ti, mq_ti2, ms_ti2,
       router_logits, router_dz, router_partial,  // router: logits scratch [N,E], dz [A], tile partials
       rc_sync,  // fused reverse-combine: chunk ticket + finished rows per 128-row tile
-      ff_sync,  // fused forward: dispatch ticket, rows per 128-row tile, gate/up units per item
+      ff_sync,  // fused forward: dispatch ticket, rows per 128-row tile, gate/up and down units per item
       dyxe, dg, du, ws_bytes;
   // forward-context byte offsets
   size_t xe, g, u, act, ye, saved_bytes;
@@ -93,10 +93,15 @@ moe_status gemm_down(const Layout& L, const void* ws, const void* act, const voi
                      cudaStream_t s);
 // Dispatch + gate/up + SwiGLU + down in one persistent launch (bit-identical
 // to launch_dispatch, gemm_gate_up and gemm_down in sequence). g, u may both
-// be NULL (inference: Act only).
+// be NULL (inference: Act only). ring = 0: xe and act hold all R rows;
+// ring > 0 (g, u NULL): xe and act are rings of `ring` slots of 256 rows
+// (ring * 256 * H and ring * 256 * I bf16 values), ring from fused_ring_slots.
 moe_status gemm_fused_forward(const Layout& L, const void* ws, const void* x, const void* wg,
                               const void* wu, const void* wd, void* xe, void* g, void* u,
-                              void* act, void* ye, cudaStream_t s);
+                              void* act, void* ye, int ring, cudaStream_t s);
+// Slots of the fused forward's Xe/Act ring on this device (0 if the
+// occupancy query fails).
+int fused_ring_slots(const Layout& L);
 moe_status gemm_down_dgrad(const Layout& L, const void* ws, const void* dye, const void* g,
                            const void* u, const void* wd, void* dg, void* du, cudaStream_t s);
 // DACT with the reverse-combine fused in: dYe (written here, then read by the

@@ -154,8 +154,10 @@ class MoELayer:
         return self.y
 
     def forward_inference(self, x, wg, wu, wd, topk_w=None, stream=None, mx=None):
-        """Forward without a saved context (inference): dispatch into workspace
-        scratch, gate/up storing Act only, down, combine; same y as forward()."""
+        """Forward without a saved context (inference): dispatch, gate/up
+        storing Act only and down in one persistent launch (bf16: Xe and Act in
+        a ring of 256-row minibatch slots in workspace scratch), then the
+        combine; same y as forward()."""
         w = _lib.weights(wg, wu, wd, mx=mx.struct if mx is not None else None)
         _lib.moe_forward_inference(self.p, x, w, self.topk_w if topk_w is None else topk_w,
                                    self.y, self.ws, stream)

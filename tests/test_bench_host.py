@@ -24,6 +24,17 @@ def test_expert_loads_whole_tiles_have_no_padding():
     assert bench.expert_loads([0, 0], tile_rows=128)["padded_row_frac"] == 0.0
 
 
+def test_custom_workload_suffixes_in_any_order():
+    s = bench.workload("16384,4096,1536,128,8,1.2,fwd")
+    assert (s.N, s.H, s.I, s.E, s.k, s.zipf_s) == (16384, 4096, 1536, 128, 8, 1.2)
+    assert not s.backward and s.dtype == "bf16" and s.minibatch_rows == 128
+    s = bench.workload("300,512,768,16,4,T=256,fwd,mxfp8")
+    assert s.zipf_s is None and s.minibatch_rows == 256 and s.dtype == "mxfp8" and not s.backward
+    s = bench.workload("4096,2048,1024,64,8")
+    assert s.backward and s.zipf_s is None and s.name == "custom_N4096_H2048_I1024_E64_k8_T128"
+    assert bench.workload(None).name.startswith("skewed_fwd_bwd")
+
+
 def test_digest_is_sha256_of_the_bytes_in_order():
     a = torch.arange(1000, dtype=torch.float32)
     b = torch.arange(77, dtype=torch.int16)

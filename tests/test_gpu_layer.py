@@ -38,7 +38,11 @@ def _segments(layer):
 
 
 PHASE_SHAPES = [inputs.TINY, RAGGED, inputs.TINY.with_(name="tiny_T256", minibatch_rows=256),
-                RAGGED.with_(name="ragged_skewed_T256", minibatch_rows=256)]
+                RAGGED.with_(name="ragged_skewed_T256", minibatch_rows=256),
+                # experts of 3568, 2130 and 1098 rows (weight-gradient tiles issued in
+                # chunks, with short-K tiles of other experts between the chunks), one
+                # of 527 rows, and twelve of at most 312 (seed 0)
+                custom_shape(4096, 1024, 512, 16, 2, zipf_s=1.5, name="wgrad_chunked_and_short")]
 
 
 @pytest.mark.parametrize("shape", PHASE_SHAPES, ids=lambda s: s.name)
@@ -276,8 +280,16 @@ def test_backward_equals_phase_chain(shape, overlap):
         assert torch.equal(got, want), name
 
 
+# Shapes whose context-free forward runs Xe and Act through the ring of
+# minibatch slots, wrapping around it several times: the ring has lag + 4
+# slots, lag = max(2, ceil(3 * CTA pairs / (I / 128 + H / 256))), and needs
+# ring * 256 * (H + I) <= R * I rows of scratch (R >= N * k); with at most 76
+# CTA pairs that holds here, for about 130 and 260 pair items.
+RING_SHAPES = [custom_shape(4096, 1024, 1024, 16, 8, zipf_s=1.2, name="ring_wraps_skewed"),
+               custom_shape(8192, 2048, 1024, 32, 8, name="ring_wraps_uniform")]
+
 FUSED_SHAPES = CHAIN_SHAPES + [LAYER_SHAPES[i] for i in (2, 3, 5, 7, 8, 9)] + [
-    custom_shape(3000, 1024, 768, 16, 8, zipf_s=1.2, name="fused_skewed_odd_items")]
+    custom_shape(3000, 1024, 768, 16, 8, zipf_s=1.2, name="fused_skewed_odd_items")] + RING_SHAPES
 
 
 @pytest.mark.parametrize("inference", [False, True], ids=["training", "inference"])
@@ -287,8 +299,9 @@ def test_fused_forward_equals_phase_chain(shape, inference):
     persistent launch) followed by the combine must equal, bit for bit,
     moe_dispatch + moe_expert_gate_up + moe_expert_down + moe_combine on the
     same inputs: Xe (padding rows zero), G, U, Act, Ye and y. The context-free
-    forward (moe_forward_inference: the fused launch with Xe and Ye sharing one
-    scratch buffer) gives the same y."""
+    forward (moe_forward_inference: the fused launch with Xe and Act in a ring
+    of 256-row minibatch slots where the scratch holds one, else with Xe and
+    Ye sharing one scratch buffer) gives the same y."""
     inp = to_dev(inputs.make_inputs(shape, seed=4, device="cpu"))
     layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev(),
                      minibatch_rows=shape.minibatch_rows, allocate_grads=False)
@@ -323,6 +336,23 @@ def test_fused_forward_equals_phase_chain(shape, inference):
     rows = int(layer.schedule_tensors()["pad_offsets"][shape.E])
     for name in ("xe", "g", "u", "act", "ye"):
         assert torch.equal(got[name][:rows].view(torch.int16), ref[name][:rows].view(torch.int16)), name
+
+
+@pytest.mark.parametrize("shape", RING_SHAPES, ids=lambda s: s.name)
+def test_ring_forward_reruns_are_bitwise_identical(shape):
+    """The ring forward's slot recycling depends on timing (which CTA frees a
+    slot first); its results must not."""
+    inp = to_dev(inputs.make_inputs(shape, seed=9, device="cpu"))
+    layer = MoELayer(shape.N, shape.H, shape.I, shape.E, shape.k, device=dev(), allocate_grads=False)
+    layer.route(inp["logits"], inp["bias"])
+    layer.build_schedule()
+    ys = [layer.forward_inference(inp["x"], inp["wg"], inp["wu"], inp["wd"]).clone()
+          for _ in range(3)]
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert torch.isfinite(ys[0].float()).all()
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
 
 
 def test_fused_forward_reruns_are_bitwise_identical():
