@@ -1783,9 +1783,9 @@ moe_status launch_pair_s(const Maps& maps, const Args& args, int64_t units, cuda
 // epilogue staging buffers, pair_out_bufs):
 //  * weight gradients: 4 stages when the experts average at most 256 tokens
 //    (large batch at N = 8192: dWg + dWu 7.48 ms at 4 stages against 7.87 at
-//    6 -- the fp32 stores bound them there), else 6 (skewed workload: 2.84
-//    at 6 against 2.92 at 5 and 2.98 at 4; uniform routing 2.66 / 2.79 /
-//    2.83);
+//    6 -- the fp32 stores bound them there), else 6 (skewed workload: 2.74
+//    at 6 against 2.89 at 5 and 2.99 at 4; uniform routing 2.62 / 2.76 /
+//    2.81);
 //  * token-row GEMMs: 5 stages when the experts average at least 1024 tokens
 //    (skewed and uniform workloads: gate/up 2.27 / 2.13 ms at 5 against
 //    2.30 / 2.18 at 6, gate/up dgrad 2.26 / 2.15 against 2.29 / 2.17), else 6
@@ -1838,19 +1838,21 @@ moe_status launch_wide_s(const Maps& maps, const Args& args, int64_t units, cuda
 // Width of the token-row GEMMs' pair tiles in N: the caller's
 // moe_problem.tile_n if set, else the library's choice per shape, from
 // sweeps on a GB300 (bench.py --sweep-stages, 2070 MHz). The 512-wide tile
-// stages each A k-block once for two N tiles but keeps one accumulator, so its
-// epilogue stalls the MMAs: it pays only where K is long and the epilogue
-// light. The gate/up data gradient (K = 2 I) with experts of at least 1024
-// tokens on average: 2.11 against 2.30 ms narrow (skewed workload), 2.11
-// against 2.20 (uniform routing); at 256 tokens per expert (large batch,
-// N = 8192) 3.37 against 3.34. Not for gate/up and down (skewed -4%, uniform
-// +3%, fine-grained +10%), nor the down data gradient, whose epilogue reads G
-// and U back (+28% and +37%).
+// stages each A k-block once for two N tiles, a quarter fewer bytes through
+// L2 per flop, but keeps one accumulator, so its epilogue stalls the MMAs.
+// With experts of at least 1024 tokens on average it wins for gate/up (skewed
+// workload 2.17-2.22 against 2.29-2.32 ms narrow; uniform routing 2.21-2.29
+// against 2.23), down (1.14 against 1.17-1.18; uniform 1.12-1.14 against
+// 1.13-1.14) and the gate/up data gradient (K = 2 I: 2.09-2.11 against
+// 2.25-2.30; uniform 2.05-2.11 against 2.20-2.22). With fewer tokens the
+// epilogue weighs more: fine-grained forward (512 per expert) gate/up 0.235
+// against 0.215, large batch at N = 8192 (256) even. Never for the down data
+// gradient, whose epilogue reads G and U back (+28% and +37%).
 bool pick_wide(const Layout& L, int mode, int n_nt) {
   if (n_nt % 2 != 0) return false;
   if (L.tile_n == 256) return false;
   if (L.tile_n == 512) return true;
-  return mode == DXE && L.A >= 1024LL * L.E;
+  return mode != DACT && L.A >= 1024LL * L.E;
 }
 
 template <int MODE, bool RC = false>
