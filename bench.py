@@ -198,14 +198,14 @@ def expert_loads(counts, tile_rows=128):
 GEMM_SRC = ("mixture_experts_layer_schedule_gb300/csrc/grouped_gemm.cu",
             "mixture_experts_layer_schedule_gb300/csrc/moe_common.cuh")
 MEASURED_TRAFFIC = {
-    "src_sha256": "a07ba35e179c7e9810381dca8278d3a25c971bd948e0b74533025d27e66ebaf1",
+    "src_sha256": "77f82cf6ac992b7cce412d0585002b8e66c2dee7852f35c0bbb2ab736af31521",
     "workload": "skewed_fwd_bwd_N16384_H4096_I1536_E128_k8_zipf1.2",
-    "bytes": {"gate_up": 5.0274e9 + 1.2978e9,
-              "down": 2.0358e9 + 1.1502e9,
-              "down_dgrad": 3.9605e9 + 0.8546e9,
-              "down_wgrad": 2.4071e9 + 3.1561e9,
-              "gate_up_dgrad": 4.3469e9 + 1.1581e9,
-              "gate_up_wgrad": 4.7530e9 + 6.3776e9},
+    "bytes": {"gate_up": 5.381e9 + 1.299e9,
+              "down": 2.072e9 + 1.145e9,
+              "down_dgrad": 3.920e9 + 0.855e9,
+              "down_wgrad": 2.378e9 + 3.168e9,
+              "gate_up_dgrad": 4.762e9 + 1.156e9,
+              "gate_up_wgrad": 4.751e9 + 6.393e9},
 }
 
 def measured_traffic(workload_name, phase):
