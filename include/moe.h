@@ -255,14 +255,20 @@ moe_status moe_dispatch_mxfp8(const moe_problem* p, const void* ws, const void* 
 moe_status moe_mxfp8_forward_operands(const moe_problem* p, void* ws, moe_mxfp8_operand* xe_rows,
                                       moe_mxfp8_operand* act_rows);
 
-/* The workspace buffers holding the row forms of dG and dU (E4M3 codes
- * [R, I] with scales in the mxfp8_quantize_mma chunk layout) that the MXFP8
- * tensor-core backward quantises for the gate/up data-gradient GEMM
- * (host-only address arithmetic, no GPU work). Valid after moe_backward on the
- * FP8 tensor cores until the next call that reuses the workspace. For
- * inspecting the quantised operands (error accounting); MOE_MXFP8 only. */
+/* The workspace buffers where the MXFP8 tensor-core backward leaves dG and dU
+ * (host-only address arithmetic, no GPU work): their bf16 values (dg, du:
+ * [R, I], written by the down data-gradient GEMM) and the two MXFP8 forms of
+ * each that it quantises them into for the later GEMMs (E4M3 codes, scales in
+ * the mxfp8_quantize_mma chunk layout): the row form (dg_rows, du_rows: [R, I], K = I, read by the gate/up
+ * data-gradient GEMM) and the transposed form (dg_cols, du_cols: [I, R],
+ * K = the token axis, read by the gate/up weight-gradient GEMM). Valid after
+ * moe_backward on the FP8 tensor cores until the next call that reuses the
+ * workspace. Any output pointer but dg_rows and du_rows may be NULL (not
+ * written). For inspecting the quantised operands (error accounting, parity
+ * of the fused quantisation); MOE_MXFP8 only. */
 moe_status moe_mxfp8_backward_operands(const moe_problem* p, void* ws, moe_mxfp8_operand* dg_rows,
-                                       moe_mxfp8_operand* du_rows);
+                                       moe_mxfp8_operand* du_rows, moe_mxfp8_operand* dg_cols,
+                                       moe_mxfp8_operand* du_cols, void** dg, void** du);
 
 /* Expert gate/up GEMM with the SwiGLU epilogue ([Clip] key point 5): per
  * expert e and its rows, G = Xe Wg[e]^T, U = Xe Wu[e]^T (fp32 accumulation on

@@ -90,7 +90,7 @@ _SIGS = {
     "moe_reverse_dispatch": ([c_vp] * 5, c_i32),
     "moe_backward": ([c_vp] * 12, c_i32),
     "moe_mxfp8_forward_operands": ([c_vp] * 4, c_i32),
-    "moe_mxfp8_backward_operands": ([c_vp] * 4, c_i32),
+    "moe_mxfp8_backward_operands": ([c_vp] * 8, c_i32),
     "moe_dispatch_expert_ffn": ([c_vp] * 10, c_i32),
     "moe_dispatch_mxfp8": ([c_vp] * 7, c_i32),
     "moe_backward_overlap": ([c_vp] * 12, c_i32),
@@ -252,11 +252,16 @@ def moe_mxfp8_forward_operands(p, ws):
 
 
 def moe_mxfp8_backward_operands(p, ws):
-    """Device addresses (q, s) of dG's and dU's row-form MXFP8 operands in ws."""
-    dg, du = MXFP8Operand(), MXFP8Operand()
-    _call("moe_mxfp8_backward_operands", ctypes.byref(p), _ptr(ws), ctypes.byref(dg),
-          ctypes.byref(du))
-    return (dg.q, dg.s), (du.q, du.s)
+    """Device addresses in ws of what the MXFP8 tensor-core backward leaves for
+    dG and dU: {"dg_rows", "du_rows", "dg_cols", "du_cols"} -> (q, s) of the
+    row and transposed MXFP8 forms, {"dg", "du"} -> the bf16 [R, I] values."""
+    ops = [MXFP8Operand() for _ in range(4)]
+    dg, du = ctypes.c_void_p(), ctypes.c_void_p()
+    _call("moe_mxfp8_backward_operands", ctypes.byref(p), _ptr(ws), *(ctypes.byref(o) for o in ops),
+          ctypes.byref(dg), ctypes.byref(du))
+    out = {k: (o.q, o.s) for k, o in zip(("dg_rows", "du_rows", "dg_cols", "du_cols"), ops)}
+    out.update(dg=dg.value, du=du.value)
+    return out
 
 
 def moe_dispatch_expert_ffn(p, ws, x, w: Weights, xe, g, u, act, ye, stream=None):

@@ -422,12 +422,18 @@ moe_status moe_mxfp8_forward_operands(const moe_problem* p, void* ws, moe_mxfp8_
 }
 
 moe_status moe_mxfp8_backward_operands(const moe_problem* p, void* ws, moe_mxfp8_operand* dg_rows,
-                                       moe_mxfp8_operand* du_rows) {
+                                       moe_mxfp8_operand* du_rows, moe_mxfp8_operand* dg_cols,
+                                       moe_mxfp8_operand* du_cols, void** dg, void** du) {
   Layout L;
   MOE_TRY(prep(p, ws, &L));
   if (p->dtype != MOE_MXFP8 || !dg_rows || !du_rows) return MOE_ERR_INVALID_ARG;
-  *dg_rows = ws_operand(ws, L.mq_ri, L.ms_ri);  // written by mx_backward_gemms
+  // the buffers mx_backward_gemms passes to gemm_mx_down_dgrad
+  *dg_rows = ws_operand(ws, L.mq_ri, L.ms_ri);
   *du_rows = ws_operand(ws, L.mq_ri2, L.ms_ri2);
+  if (dg_cols) *dg_cols = ws_operand(ws, L.mq_ti, L.ms_ti);
+  if (du_cols) *du_cols = ws_operand(ws, L.mq_ti2, L.ms_ti2);
+  if (dg) *dg = at<char>(ws, L.dg);
+  if (du) *du = at<char>(ws, L.du);
   return MOE_OK;
 }
 

@@ -138,9 +138,12 @@ def test_workspace_and_context_regions_are_disjoint_and_aligned(lib, N, H, I, E,
                ("act_s", as_, R * I // 32)]
         # the backward's dG / dU row operands (dG reuses Act's buffer after the
         # forward's last reader): checked beside the tables, apart from the forward's
-        (gq, gs), (uq, us) = _lib.moe_mxfp8_backward_operands(p, base)
-        check(regions + [("dg_q", gq, R * I), ("dg_s", gs, R * I // 32), ("du_q", uq, R * I),
-                         ("du_s", us, R * I // 32)], ws_bytes)
+        ops = _lib.moe_mxfp8_backward_operands(p, base)
+        bwd = [("dg", ops["dg"], 2 * R * I), ("du", ops["du"], 2 * R * I)]
+        for name in ("dg_rows", "du_rows", "dg_cols", "du_cols"):
+            q, sc = ops[name]
+            bwd += [(name + "_q", q, R * I), (name + "_s", sc, R * I // 32)]
+        check(regions + bwd, ws_bytes)
         regions += fwd
     check(regions, ws_bytes)
     sv = _lib.SavedView()

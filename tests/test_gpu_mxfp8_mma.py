@@ -151,6 +151,47 @@ def test_fp8_forward_operands_equal_the_quantiser(shape):
                                       untile_scales(s_ref.cpu().numpy(), R, K)[:used])
 
 
+@pytest.mark.parametrize("shape", SHAPES + [custom_shape(2048, 512, 768, 16, 8, zipf_s=1.2,
+                                                       name="many_tiles_mxfp8").with_(dtype="mxfp8")],
+                         ids=lambda s: s.name)
+def test_fp8_backward_operands_equal_the_quantiser(shape):
+    """The MXFP8 backward quantises dG and dU into both forms the later GEMMs
+    read: rows along I (gate/up data gradient) and the transposed form along
+    the token axis (gate/up weight gradient). Each must equal, bit for bit,
+    mxfp8_quantize_mma of the bf16 dG and dU the down data gradient wrote, on
+    every row (token) of the used expert segments."""
+    inp = to_dev(inputs.make_inputs(shape, seed=10, device="cpu"))
+    fwd, bwd = MoELayer.prepare_mxfp8_weights(inp["wg"], inp["wu"], inp["wd"])
+    mx = MoELayer.prepare_mxfp8_mma_weights(inp["wg"], inp["wu"], inp["wd"])
+    layer = _layer(shape)
+    layer.step(inp["x"], inp["logits"], inp["bias"], *fwd, inp["dy"], bwd=bwd, mx=mx)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    R, I = layer.R, shape.I
+    used = int(layer.schedule_tensors()["pad_offsets"][shape.E])
+    ops = _lib.moe_mxfp8_backward_operands(layer.p, layer.ws)
+    for t in ("dg", "du"):
+        src = torch.as_tensor(_DevBytes(ops[t], R * I * 2), device=dev()).view(torch.bfloat16)
+        src = src.view(R, I).clone()
+        for form, tr in (("_rows", 0), ("_cols", 1)):
+            q_ref = torch.empty(R * I, dtype=torch.uint8, device=dev())
+            s_ref = torch.empty(R * I // 32, dtype=torch.uint8, device=dev())
+            _lib.mxfp8_quantize_mma(src, R, I, tr, q_ref, s_ref)
+            q_ptr, s_ptr = ops[t + form]
+            q_got = torch.as_tensor(_DevBytes(q_ptr, R * I), device=dev()).clone()
+            s_got = torch.as_tensor(_DevBytes(s_ptr, R * I // 32), device=dev()).clone()
+            torch.cuda.synchronize()
+            if tr == 0:
+                assert torch.equal(q_got.view(R, I)[:used], q_ref.view(R, I)[:used]), t + form
+                np.testing.assert_array_equal(untile_scales(s_got.cpu().numpy(), R, I)[:used],
+                                              untile_scales(s_ref.cpu().numpy(), R, I)[:used])
+            else:
+                assert torch.equal(q_got.view(I, R)[:, :used], q_ref.view(I, R)[:, :used]), t + form
+                np.testing.assert_array_equal(
+                    untile_scales(s_got.cpu().numpy(), I, R)[:, :used // 32],
+                    untile_scales(s_ref.cpu().numpy(), I, R)[:, :used // 32])
+
+
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: s.name)
 def test_fp8_forward_matches_bf16_mma_forward(shape):
     inp = to_dev(inputs.make_inputs(shape, seed=5, device="cpu"))
@@ -320,7 +361,8 @@ def test_fp8_error_budget_at_the_tiny_shape():
     ref = {gb: oracle.layer_mxfp8_trace(inp_cpu["x"], prep, ids, w, inp_cpu["dy"], gu_bf16=gb)
            for gb in (False, True)}
     slot = layer.schedule_tensors()["slot_of"].cpu().numpy().reshape(-1)
-    (gq, gs), (uq, us) = _lib.moe_mxfp8_backward_operands(layer.p, layer.ws)
+    ops = _lib.moe_mxfp8_backward_operands(layer.p, layer.ws)
+    (gq, gs), (uq, us) = ops["dg_rows"], ops["du_rows"]
     got_rows = {"dg": _decode_rows(gq, gs, layer.R, shape.I)[slot],
                 "du": _decode_rows(uq, us, layer.R, shape.I)[slot]}
     g = layer.grads
